@@ -1,0 +1,187 @@
+"""Seeded synthetic inputs for paged chunk attention.
+
+This module is the one thing the oracle tests and the CUDA path share. It draws
+random tensors and block-table permutations and nothing else: it holds none of
+the attention, paging or page-selection arithmetic.
+
+Draws use numpy's counter-based Philox generator keyed by (workload seed,
+tensor id, chunk index), so any chunk can be regenerated on its own and in any
+order. Values are drawn in fp32 and, for bf16 workloads, rounded to bf16 with
+round-to-nearest-even; the float32 arrays returned here already hold the
+rounded values, so the oracle (which widens them to fp64) and the kernels (which
+read the bf16 bit patterns) see the same numbers.
+
+Workloads follow the shapes named in "Out of the Memory Barrier" for
+Qwen2.5-7B (28 query heads, 4 KV heads, head dim 128): the pages train that
+model on one GPU (gist.science/de §4; sciencestack.ai abstract). Page size,
+chunk sizes and distributions are fixed by the workload table below; the pages
+do not state them.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field, replace
+from typing import Optional
+
+import numpy as np
+
+__all__ = [
+    "Workload", "WORKLOADS", "workload", "draw_normal", "round_bf16",
+    "bf16_bits", "chunk_q", "chunk_k", "chunk_v", "chunk_do", "block_table",
+]
+
+# Tensor ids for the Philox key; changing one changes every draw of that tensor.
+_TENSOR_ID = {"q": 1, "k": 2, "v": 3, "do": 4, "mu": 5, "perm": 6, "misc": 7}
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One synthetic workload: sequence/chunk/page geometry, heads, dtype, inputs."""
+    name: str
+    N: int                 # context length in tokens
+    C: int                 # chunk length in tokens
+    P: int                 # page size in tokens
+    Hq: int                # query heads
+    Hkv: int               # KV heads (Hq % Hkv == 0, grouped consecutively)
+    d: int                 # head dimension
+    dtype: str             # "f32" or "bf16": storage type of Q/K/V/O/dO/dQ
+    seed: int
+    table: str = "identity"    # "identity" or "perm" (seeded permutation of physical pages)
+    keys: str = "normal"       # "normal": K ~ N(0,1); "clustered": page centre N(0,2^2) + N(0,1)
+    topk: Optional[tuple] = None   # (K, n_sink, n_local) for the page-sparse variant
+    offload: bool = False          # pools in pinned host memory, pages streamed to HBM
+    extra_pages: int = 0           # physical pages beyond the sequence's need
+
+    @property
+    def g(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def n_chunks(self) -> int:
+        return (self.N + self.C - 1) // self.C
+
+    @property
+    def n_pages(self) -> int:
+        return (self.N + self.P - 1) // self.P
+
+    @property
+    def n_phys(self) -> int:
+        return self.n_pages + self.extra_pages
+
+    def chunk_range(self, c: int) -> tuple[int, int]:
+        s = c * self.C
+        return s, min(self.N, s + self.C)
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+# Seeds are 1234 + the workload's index in this table.
+WORKLOADS = {
+    # Tiny dense fp32: 2 q heads / 1 KV head, d 64, page 16, 256 tokens in 4 chunks of 64.
+    "tiny_dense_f32": Workload("tiny_dense_f32", N=256, C=64, P=16, Hq=2, Hkv=1, d=64,
+                               dtype="f32", seed=1235),
+    # Qwen2.5-7B attention shape, dense, 32K context in chunks of 4096.
+    "qwen7b_dense_32k": Workload("qwen7b_dense_32k", N=32768, C=4096, P=128, Hq=28, Hkv=4,
+                                 d=128, dtype="bf16", seed=1236),
+    # Same shape, 128K context in chunks of 8192, permuted block table.
+    "qwen7b_dense_128k_perm": Workload("qwen7b_dense_128k_perm", N=131072, C=8192, P=128,
+                                       Hq=28, Hkv=4, d=128, dtype="bf16", seed=1237,
+                                       table="perm"),
+    # Page-sparse, 256K context, clustered keys, top-64 + 1 sink + 2 local pages.
+    "qwen7b_sparse_256k": Workload("qwen7b_sparse_256k", N=262144, C=8192, P=128, Hq=28,
+                                   Hkv=4, d=128, dtype="bf16", seed=1238, table="perm",
+                                   keys="clustered", topk=(64, 1, 2)),
+    # Page-sparse at 1M context with all pages in pinned host memory.
+    "qwen7b_sparse_1m_offload": Workload("qwen7b_sparse_1m_offload", N=1048576, C=8192,
+                                         P=128, Hq=28, Hkv=4, d=128, dtype="bf16",
+                                         seed=1239, table="perm", keys="clustered",
+                                         topk=(64, 1, 2), offload=True),
+}
+
+
+def workload(name: str, **overrides) -> Workload:
+    w = WORKLOADS[name]
+    return replace(w, **overrides) if overrides else w
+
+
+def _rng(seed: int, tensor: str, chunk: int) -> np.random.Generator:
+    key = np.array([seed, (_TENSOR_ID[tensor] << 40) | chunk], dtype=np.uint64)
+    return np.random.Generator(np.random.Philox(key=key))
+
+
+def draw_normal(seed: int, tensor: str, chunk: int, shape, std: float = 1.0) -> np.ndarray:
+    """float32 N(0, std^2) draws from the (seed, tensor, chunk) Philox stream."""
+    x = _rng(seed, tensor, chunk).standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        x *= np.float32(std)
+    return x
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bf16 (ties to even); returns float32.
+
+    Inputs must be finite (the generators never produce NaN or Inf)."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    bias = ((b >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+    return ((b + bias) & np.uint32(0xFFFF0000)).view(np.float32)
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """uint16 bf16 bit patterns of float32 values that are already bf16-exact."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    if np.any(b & np.uint32(0xFFFF)):
+        raise ValueError("bf16_bits: values are not bf16-representable; call round_bf16 first")
+    return (b >> np.uint32(16)).astype(np.uint16)
+
+
+def _finish(w: Workload, x: np.ndarray) -> np.ndarray:
+    return round_bf16(x) if w.dtype == "bf16" else x
+
+
+def chunk_q(w: Workload, c: int) -> np.ndarray:
+    """Queries of chunk c, [n, Hq, d] float32 (bf16-exact for bf16 workloads)."""
+    s, e = w.chunk_range(c)
+    return _finish(w, draw_normal(w.seed, "q", c, (e - s, w.Hq, w.d)))
+
+
+def chunk_k(w: Workload, c: int) -> np.ndarray:
+    """Keys of chunk c, [n, Hkv, d].
+
+    "clustered": every (page, KV head) draws a centre ~ N(0, 2^2 I) and each
+    token adds noise ~ N(0, I), so pages differ in how well they match a query."""
+    s, e = w.chunk_range(c)
+    if w.keys == "normal":
+        return _finish(w, draw_normal(w.seed, "k", c, (e - s, w.Hkv, w.d)))
+    if w.keys != "clustered":
+        raise ValueError(w.keys)
+    if s % w.P:
+        raise ValueError("clustered keys need chunks that start on a page boundary")
+    n_pg = (e - s + w.P - 1) // w.P
+    mu = draw_normal(w.seed, "mu", c, (n_pg, w.Hkv, w.d), std=2.0)
+    eps = draw_normal(w.seed, "k", c, (e - s, w.Hkv, w.d))
+    page_of_token = np.arange(e - s) // w.P
+    return _finish(w, mu[page_of_token] + eps)
+
+
+def chunk_v(w: Workload, c: int) -> np.ndarray:
+    s, e = w.chunk_range(c)
+    return _finish(w, draw_normal(w.seed, "v", c, (e - s, w.Hkv, w.d)))
+
+
+def chunk_do(w: Workload, c: int) -> np.ndarray:
+    """Upstream gradient dL/dO of chunk c, [n, Hq, d]."""
+    s, e = w.chunk_range(c)
+    return _finish(w, draw_normal(w.seed, "do", c, (e - s, w.Hq, w.d)))
+
+
+def block_table(w: Workload) -> np.ndarray:
+    """int32 [n_pages]: physical page of each logical page.
+
+    "identity" maps page p to p; "perm" takes the first n_pages entries of a
+    seeded permutation of all n_phys physical pages."""
+    if w.table == "identity":
+        return np.arange(w.n_pages, dtype=np.int32)
+    if w.table != "perm":
+        raise ValueError(w.table)
+    perm = _rng(w.seed, "perm", 0).permutation(w.n_phys)
+    return perm[: w.n_pages].astype(np.int32)
