@@ -1,0 +1,559 @@
+// C-ABI layer of libpkv: argument validation, the page pool and block-table
+// allocator, and dispatch to the kernels. See include/pkv.h for the contract.
+//
+// The paged memory manager follows "Out of the Memory Barrier" (gist.science/de
+// §2.B; sciencestack.ai Fig. 3, Fig. 4): all page memory is allocated once, at
+// pool creation; a sequence grows by taking pages off a free list and writing
+// their indices into its block table, so appending never reallocates or copies
+// the cache, and the gradient pages share the physical index of their K/V page.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+
+static thread_local std::string g_last_error;
+
+pkv_status fail(pkv_status s, const std::string& msg) {
+    g_last_error = msg;
+    return s;
+}
+
+pkv_status cuda_fail(cudaError_t e, const char* what) {
+    std::string m = std::string(what) + ": " + cudaGetErrorName(e) + " (" +
+                    cudaGetErrorString(e) + ")";
+    return fail(e == cudaErrorMemoryAllocation ? PKV_ERR_OOM : PKV_ERR_CUDA, m);
+}
+
+// ---------------------------------------------------------------- TMA descriptors
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn(std::string* why) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    static std::string err;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || p == nullptr) {
+            err = "cuTensorMapEncodeTiled entry point not available";
+        } else {
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        }
+    });
+    if (!fn && why) *why = err;
+    return fn;
+}
+
+bool make_tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t inner,
+                  uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
+                  uint32_t box_rows, std::string* why) {
+    auto fn = encode_fn(why);
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        if (why) *why = "cuTensorMapEncodeTiled (2-D) failed with CUresult " + std::to_string(r);
+        return false;
+    }
+    return true;
+}
+
+bool make_tmap_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t d0,
+                  uint64_t d1, uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes,
+                  uint32_t b0, uint32_t b1, uint32_t b2, std::string* why) {
+    auto fn = encode_fn(why);
+    if (!fn) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    cuuint32_t box[3] = {b0, b1, b2};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        if (why) *why = "cuTensorMapEncodeTiled (3-D) failed with CUresult " + std::to_string(r);
+        return false;
+    }
+    return true;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+// ---------------------------------------------------------------- helpers
+
+static pkv_status validate_desc(const pkv_pool_desc* d) {
+    if (!d) return fail(PKV_ERR_INVALID, "pkv_pool_create: desc is NULL");
+    if (d->page_size <= 0 || d->page_size % 8)
+        return fail(PKV_ERR_INVALID, "page_size must be a positive multiple of 8");
+    if (d->n_kv_heads <= 0 || d->n_q_heads <= 0 || d->n_q_heads % d->n_kv_heads)
+        return fail(PKV_ERR_INVALID, "n_q_heads must be a positive multiple of n_kv_heads");
+    if (d->head_dim != 64 && d->head_dim != 128)
+        return fail(PKV_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (d->dtype != PKV_BF16 && d->dtype != PKV_F32)
+        return fail(PKV_ERR_INVALID, "dtype must be PKV_BF16 or PKV_F32");
+    if (d->residency < PKV_RES_DEVICE || d->residency > PKV_RES_META)
+        return fail(PKV_ERR_INVALID, "unknown residency");
+    if (d->num_phys_pages <= 0 || d->num_phys_pages > (int64_t(1) << 30))
+        return fail(PKV_ERR_INVALID, "num_phys_pages out of range");
+    if ((int64_t)d->num_phys_pages * d->n_kv_heads * d->page_size >= (int64_t(1) << 31))
+        return fail(PKV_ERR_INVALID, "pool too large: pages*Hkv*P must be < 2^31 rows");
+    return PKV_OK;
+}
+
+static bool is_device(const pkv_pool* p) { return p->desc.residency != PKV_RES_META; }
+
+// Claims pages so that the sequence covers new_len tokens. Host-only; on
+// failure nothing changes.
+static pkv_status claim_pages(pkv_seq* s, int64_t new_len) {
+    pkv_pool* p = s->pool;
+    const int64_t P = p->desc.page_size;
+    const int64_t need = (new_len + P - 1) / P;
+    const int64_t have = (int64_t)s->bt.size();
+    if (need <= have) return PKV_OK;
+    const int64_t extra = need - have;
+    if ((int64_t)p->free_list.size() < extra)
+        return fail(PKV_ERR_OOM, "page pool exhausted: need " + std::to_string(extra) +
+                                     " pages, " + std::to_string(p->free_list.size()) + " free");
+    for (int64_t i = 0; i < extra; ++i) {
+        int32_t pg = p->free_list.back();
+        p->free_list.pop_back();
+        p->in_use[pg] = 1;
+        s->bt.push_back(pg);
+        if (s->h_bt) s->h_bt[have + i] = pg;
+    }
+    return PKV_OK;
+}
+
+static void release_pages(pkv_seq* s) {
+    pkv_pool* p = s->pool;
+    // Push back in reverse so a fresh sequence gets the same pages in the same order.
+    for (auto it = s->bt.rbegin(); it != s->bt.rend(); ++it) {
+        p->in_use[*it] = 0;
+        p->free_list.push_back(*it);
+    }
+    s->bt.clear();
+    s->len = 0;
+    s->n_reserved_pages = 0;
+}
+
+// Uploads block-table entries [from, bt.size()) to the device copy on stream.
+static pkv_status upload_bt(pkv_seq* s, int64_t from, cudaStream_t st) {
+    if (!is_device(s->pool)) return PKV_OK;
+    const int64_t n = (int64_t)s->bt.size() - from;
+    if (n <= 0) return PKV_OK;
+    cudaError_t e = cudaMemcpyAsync(s->d_bt + from, s->h_bt + from, n * sizeof(int32_t),
+                                    cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "block-table upload");
+    return PKV_OK;
+}
+
+static pkv_status check_stream_device(const pkv_pool* p) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != p->device)
+        return fail(PKV_ERR_INVALID, "the current CUDA device is not the pool's device");
+    return PKV_OK;
+}
+
+// ---------------------------------------------------------------- C ABI
+
+extern "C" {
+
+const char* pkv_last_error(void) { return g_last_error.c_str(); }
+
+pkv_status pkv_check(pkv_pool* pool) {
+    if (!pool) return fail(PKV_ERR_INVALID, "pkv_check: pool is NULL");
+    if (!is_device(pool)) return PKV_OK;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_check: cudaDeviceSynchronize");
+    int h = 0;
+    e = cudaMemcpy(&h, pool->d_err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_check: read error word");
+    if (h != 0) {
+        int zero = 0;
+        cudaMemcpy(pool->d_err, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        const char* what = h == pkv::kErrWaitTimeout ? "a bounded wait expired"
+                         : h == pkv::kErrBadPage     ? "a page index was out of range"
+                         : h == pkv::kErrTmemAlloc   ? "tensor-memory allocation failed"
+                                                : "unknown device error";
+        return fail(PKV_ERR_DEVICE_FAULT, std::string("device error ") + std::to_string(h) +
+                                              ": " + what);
+    }
+    return PKV_OK;
+}
+
+pkv_status pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
+    if (!out) return fail(PKV_ERR_INVALID, "pkv_pool_create: out is NULL");
+    *out = nullptr;
+    pkv_status st = validate_desc(desc);
+    if (st != PKV_OK) return st;
+    pkv_pool* p = new pkv_pool();
+    p->desc = *desc;
+    p->elem = desc->dtype == PKV_BF16 ? 2 : 4;
+    p->page_elems = (size_t)desc->n_kv_heads * desc->page_size * desc->head_dim;
+    const int64_t np = desc->num_phys_pages;
+    p->free_list.resize(np);
+    for (int64_t i = 0; i < np; ++i) p->free_list[i] = (int32_t)(np - 1 - i);  // page 0 on top
+    p->in_use.assign(np, 0);
+    if (desc->residency == PKV_RES_META) {
+        *out = p;
+        return PKV_OK;
+    }
+    if (desc->residency == PKV_RES_PINNED_HOST) {
+        delete p;
+        return fail(PKV_ERR_UNSUPPORTED, "PINNED_HOST pools are not built yet");
+    }
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e != cudaSuccess) { delete p; return cuda_fail(e, "cudaGetDevice"); }
+    const size_t kv_bytes = p->page_elems * p->elem * np;
+    const size_t g_bytes = p->page_elems * sizeof(float) * np;
+    const size_t rep_bytes = (size_t)np * desc->n_kv_heads * desc->head_dim * sizeof(float);
+    auto cleanup = [p]() {
+        cudaFree(p->k); cudaFree(p->v); cudaFree(p->dk); cudaFree(p->dv);
+        cudaFree(p->rep); cudaFree(p->d_err);
+        delete p;
+    };
+    if ((e = cudaMalloc(&p->k, kv_bytes)) != cudaSuccess ||
+        (e = cudaMalloc(&p->v, kv_bytes)) != cudaSuccess ||
+        (e = cudaMalloc(reinterpret_cast<void**>(&p->dk), g_bytes)) != cudaSuccess ||
+        (e = cudaMalloc(reinterpret_cast<void**>(&p->dv), g_bytes)) != cudaSuccess ||
+        (e = cudaMalloc(reinterpret_cast<void**>(&p->rep), rep_bytes)) != cudaSuccess ||
+        (e = cudaMalloc(reinterpret_cast<void**>(&p->d_err), sizeof(int))) != cudaSuccess) {
+        cleanup();
+        return cuda_fail(e, "pkv_pool_create: page memory");
+    }
+    if ((e = cudaMemset(p->d_err, 0, sizeof(int))) != cudaSuccess ||
+        (e = cudaMemset(p->k, 0, kv_bytes)) != cudaSuccess ||
+        (e = cudaMemset(p->v, 0, kv_bytes)) != cudaSuccess ||
+        (e = cudaMemset(p->rep, 0, rep_bytes)) != cudaSuccess) {
+        cleanup();
+        return cuda_fail(e, "pkv_pool_create: memset");
+    }
+    if (desc->dtype == PKV_BF16 && desc->head_dim == 128 && desc->page_size == 128) {
+        std::string why;
+        const uint64_t rows = (uint64_t)np * desc->n_kv_heads * desc->page_size;
+        if (!make_tmap_2d(&p->tmap_k, p->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
+                          128, &why) ||
+            !make_tmap_2d(&p->tmap_v, p->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
+                          128, &why)) {
+            cleanup();
+            return fail(PKV_ERR_CUDA, "pkv_pool_create: " + why);
+        }
+        p->tmaps_ready = true;
+    }
+    *out = p;
+    return PKV_OK;
+}
+
+void pkv_pool_destroy(pkv_pool* p) {
+    if (!p) return;
+    std::vector<pkv_seq*> seqs = p->seqs;
+    for (pkv_seq* s : seqs) pkv_seq_free(s);
+    if (is_device(p)) {
+        cudaFree(p->k); cudaFree(p->v); cudaFree(p->dk); cudaFree(p->dv);
+        cudaFree(p->rep); cudaFree(p->d_err); cudaFree(p->scratch);
+    }
+    delete p;
+}
+
+pkv_status pkv_pool_free_pages(const pkv_pool* p, int64_t* n) {
+    if (!p || !n) return fail(PKV_ERR_INVALID, "pkv_pool_free_pages: NULL argument");
+    *n = (int64_t)p->free_list.size();
+    return PKV_OK;
+}
+
+pkv_status pkv_pool_arrays(const pkv_pool* p, void** k, void** v, float** dk, float** dv,
+                           float** rep) {
+    if (!p) return fail(PKV_ERR_INVALID, "pkv_pool_arrays: pool is NULL");
+    if (k) *k = p->k;
+    if (v) *v = p->v;
+    if (dk) *dk = p->dk;
+    if (dv) *dv = p->dv;
+    if (rep) *rep = p->rep;
+    return PKV_OK;
+}
+
+pkv_status pkv_seq_create(pkv_pool* p, pkv_seq** out) {
+    if (!p || !out) return fail(PKV_ERR_INVALID, "pkv_seq_create: NULL argument");
+    *out = nullptr;
+    pkv_seq* s = new pkv_seq();
+    s->pool = p;
+    if (is_device(p)) {
+        const size_t bytes = (size_t)p->desc.num_phys_pages * sizeof(int32_t);
+        cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&s->h_bt), bytes,
+                                      cudaHostAllocDefault);
+        if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&s->d_bt), bytes);
+        if (e != cudaSuccess) {
+            cudaFreeHost(s->h_bt);
+            delete s;
+            return cuda_fail(e, "pkv_seq_create: block table");
+        }
+    }
+    p->seqs.push_back(s);
+    *out = s;
+    return PKV_OK;
+}
+
+void pkv_seq_free(pkv_seq* s) {
+    if (!s) return;
+    release_pages(s);
+    auto& v = s->pool->seqs;
+    v.erase(std::remove(v.begin(), v.end(), s), v.end());
+    if (is_device(s->pool)) {
+        cudaFreeHost(s->h_bt);
+        cudaFree(s->d_bt);
+    }
+    delete s;
+}
+
+pkv_status pkv_seq_reset(pkv_seq* s) {
+    if (!s) return fail(PKV_ERR_INVALID, "pkv_seq_reset: seq is NULL");
+    release_pages(s);
+    return PKV_OK;
+}
+
+pkv_status pkv_seq_length(const pkv_seq* s, int64_t* len) {
+    if (!s || !len) return fail(PKV_ERR_INVALID, "pkv_seq_length: NULL argument");
+    *len = s->len;
+    return PKV_OK;
+}
+
+pkv_status pkv_seq_reserve(pkv_seq* s, int64_t n_tok) {
+    if (!s || n_tok < 0) return fail(PKV_ERR_INVALID, "pkv_seq_reserve: bad argument");
+    return claim_pages(s, s->len + n_tok);
+}
+
+pkv_status pkv_get_block_table(const pkv_seq* s, int32_t* out, int64_t cap, int64_t* n) {
+    if (!s || !n || (cap > 0 && !out))
+        return fail(PKV_ERR_INVALID, "pkv_get_block_table: bad argument");
+    *n = (int64_t)s->bt.size();
+    const int64_t m = std::min<int64_t>(cap, *n);
+    if (m > 0) std::memcpy(out, s->bt.data(), m * sizeof(int32_t));
+    return PKV_OK;
+}
+
+pkv_status pkv_set_block_table(pkv_seq* s, const int32_t* bt, int64_t n) {
+    if (!s || (n > 0 && !bt) || n < 0)
+        return fail(PKV_ERR_INVALID, "pkv_set_block_table: bad argument");
+    if (s->len != 0 || !s->bt.empty())
+        return fail(PKV_ERR_INVALID, "pkv_set_block_table: the sequence must be empty");
+    pkv_pool* p = s->pool;
+    std::vector<uint8_t> seen(p->desc.num_phys_pages, 0);
+    for (int64_t i = 0; i < n; ++i) {
+        const int32_t pg = bt[i];
+        if (pg < 0 || pg >= p->desc.num_phys_pages)
+            return fail(PKV_ERR_INVALID, "pkv_set_block_table: entry " + std::to_string(i) +
+                                             " = " + std::to_string(pg) + " out of range");
+        if (p->in_use[pg] || seen[pg])
+            return fail(PKV_ERR_INVALID, "pkv_set_block_table: page " + std::to_string(pg) +
+                                             " is not free or appears twice");
+        seen[pg] = 1;
+    }
+    // Remove the claimed pages from the free list, keeping its order otherwise.
+    std::vector<int32_t> fl;
+    fl.reserve(p->free_list.size());
+    for (int32_t pg : p->free_list)
+        if (!seen[pg]) fl.push_back(pg);
+    p->free_list.swap(fl);
+    s->bt.assign(bt, bt + n);
+    for (int64_t i = 0; i < n; ++i) p->in_use[bt[i]] = 1;
+    s->n_reserved_pages = n;
+    if (is_device(p) && n > 0) {
+        std::memcpy(s->h_bt, bt, n * sizeof(int32_t));
+        cudaError_t e = cudaMemcpy(s->d_bt, s->h_bt, n * sizeof(int32_t), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "pkv_set_block_table: upload");
+    }
+    return PKV_OK;
+}
+
+pkv_status pkv_append(pkv_seq* s, const void* k, const void* v, int64_t n_tok, void* stream) {
+    if (!s || n_tok < 0) return fail(PKV_ERR_INVALID, "pkv_append: bad argument");
+    if (n_tok == 0) return PKV_OK;
+    if (!k || !v) return fail(PKV_ERR_INVALID, "pkv_append: k or v is NULL");
+    pkv_pool* p = s->pool;
+    if (!is_device(p)) return fail(PKV_ERR_INVALID, "pkv_append: META pool holds no data");
+    pkv_status st = check_stream_device(p);
+    if (st != PKV_OK) return st;
+    const int64_t old_pages = (int64_t)s->bt.size();
+    st = claim_pages(s, s->len + n_tok);
+    if (st != PKV_OK) return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    st = upload_bt(s, old_pages, cs);
+    if (st != PKV_OK) return st;
+    AppendArgs a{};
+    a.P = p->desc.page_size; a.Hkv = p->desc.n_kv_heads; a.d = p->desc.head_dim;
+    a.dtype = p->desc.dtype;
+    a.k_in = k; a.v_in = v;
+    a.kpool = p->k; a.vpool = p->v; a.dkpool = p->dk; a.dvpool = p->dv; a.rep = p->rep;
+    a.bt = s->d_bt; a.num_phys = p->desc.num_phys_pages;
+    a.old_len = s->len; a.n_tok = n_tok; a.err = p->d_err;
+    cudaError_t e = launch_append(a, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_append: launch");
+    s->len += n_tok;
+    return PKV_OK;
+}
+
+static pkv_status attn_common(pkv_seq* s, const void* q, int64_t q_start, int64_t n_q,
+                              const pkv_sel* sel, AttnArgs* a, const char* who) {
+    if (!s || !q) return fail(PKV_ERR_INVALID, std::string(who) + ": NULL argument");
+    pkv_pool* p = s->pool;
+    if (!is_device(p)) return fail(PKV_ERR_INVALID, std::string(who) + ": META pool");
+    const int64_t P = p->desc.page_size;
+    if (n_q <= 0 || q_start < 0 || q_start % P != 0 || q_start + n_q > s->len)
+        return fail(PKV_ERR_INVALID,
+                    std::string(who) + ": need q_start % P == 0 and q_start + n_q <= length (" +
+                        std::to_string(q_start) + " + " + std::to_string(n_q) +
+                        " vs " + std::to_string(s->len) + ")");
+    pkv_status st = check_stream_device(p);
+    if (st != PKV_OK) return st;
+    *a = AttnArgs{};
+    a->P = (int)P; a->Hq = p->desc.n_q_heads; a->Hkv = p->desc.n_kv_heads;
+    a->d = p->desc.head_dim; a->dtype = p->desc.dtype;
+    a->q_start = q_start; a->n_q = n_q; a->q = q;
+    a->kpool = p->k; a->vpool = p->v; a->dkpool = p->dk; a->dvpool = p->dv;
+    a->bt = s->d_bt; a->num_phys = p->desc.num_phys_pages; a->err = p->d_err;
+    a->tmap_k = p->tmaps_ready ? &p->tmap_k : nullptr;
+    a->tmap_v = p->tmaps_ready ? &p->tmap_v : nullptr;
+    if (sel) {
+        const int64_t n_qp = (n_q + P - 1) / P;
+        if (!sel->pages || sel->kmax <= 0 || sel->n_qp != n_qp)
+            return fail(PKV_ERR_INVALID, std::string(who) + ": selection does not match chunk");
+        a->sel = sel->pages;
+        a->kmax = sel->kmax;
+    }
+    return PKV_OK;
+}
+
+static bool use_tc(const pkv_pool* p, const AttnArgs& a) {
+    return !(p->desc.flags & PKV_FLAG_SIMT_ONLY) && p->tmaps_ready && tc_supported(a);
+}
+
+pkv_status pkv_chunk_attn_fwd(pkv_seq* s, const void* q, int64_t q_start, int64_t n_q, void* o,
+                              float* lse, const pkv_sel* sel, void* stream) {
+    AttnArgs a;
+    pkv_status st = attn_common(s, q, q_start, n_q, sel, &a, "pkv_chunk_attn_fwd");
+    if (st != PKV_OK) return st;
+    if (!o || !lse) return fail(PKV_ERR_INVALID, "pkv_chunk_attn_fwd: o or lse is NULL");
+    a.o = o; a.lse = lse;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = use_tc(s->pool, a) ? launch_attn_fwd_tc(a, cs) : launch_attn_fwd_simt(a, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_chunk_attn_fwd: launch");
+    return PKV_OK;
+}
+
+static pkv_status ensure_scratch(pkv_pool* p, size_t floats) {
+    if (p->scratch_floats >= floats) return PKV_OK;
+    // Called outside kernels in flight on the old buffer only after a device sync.
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "scratch grow: sync");
+    cudaFree(p->scratch);
+    p->scratch = nullptr;
+    p->scratch_floats = 0;
+    e = cudaMalloc(reinterpret_cast<void**>(&p->scratch), floats * sizeof(float));
+    if (e != cudaSuccess) return cuda_fail(e, "scratch grow");
+    p->scratch_floats = floats;
+    return PKV_OK;
+}
+
+pkv_status pkv_chunk_attn_bwd(pkv_seq* s, const void* q, const void* o, const void* dout,
+                              const float* lse, int64_t q_start, int64_t n_q, void* dq,
+                              const pkv_sel* sel, void* stream) {
+    AttnArgs a;
+    pkv_status st = attn_common(s, q, q_start, n_q, sel, &a, "pkv_chunk_attn_bwd");
+    if (st != PKV_OK) return st;
+    if (!o || !dout || !lse || !dq)
+        return fail(PKV_ERR_INVALID, "pkv_chunk_attn_bwd: o, dout, lse or dq is NULL");
+    st = ensure_scratch(s->pool, (size_t)a.Hq * n_q);
+    if (st != PKV_OK) return st;
+    a.o_in = o; a.dout = dout; a.lse_in = lse; a.dq = dq; a.Dbuf = s->pool->scratch;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_bwd_rowdot(a, cs);
+    if (e == cudaSuccess)
+        e = use_tc(s->pool, a) ? launch_attn_bwd_tc(a, cs) : launch_attn_bwd_simt(a, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_chunk_attn_bwd: launch");
+    return PKV_OK;
+}
+
+pkv_status pkv_grad_zero(pkv_seq* s, void* stream) {
+    if (!s) return fail(PKV_ERR_INVALID, "pkv_grad_zero: seq is NULL");
+    if (!is_device(s->pool)) return fail(PKV_ERR_INVALID, "pkv_grad_zero: META pool");
+    if (s->bt.empty()) return PKV_OK;
+    cudaError_t e = launch_grad_zero(s->pool, s->d_bt, 0, (int64_t)s->bt.size(),
+                                     static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_grad_zero: launch");
+    return PKV_OK;
+}
+
+pkv_status pkv_gather(const pkv_seq* s, void* k, void* v, float* dk, float* dv, float* rep,
+                      void* stream) {
+    if (!s) return fail(PKV_ERR_INVALID, "pkv_gather: seq is NULL");
+    if (!is_device(s->pool)) return fail(PKV_ERR_INVALID, "pkv_gather: META pool");
+    if (s->len == 0) return PKV_OK;
+    cudaError_t e = launch_gather(s->pool, s->d_bt, s->len, k, v, dk, dv, rep,
+                                  static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_gather: launch");
+    return PKV_OK;
+}
+
+pkv_status pkv_page_topk(pkv_seq* s, const void* q, int64_t q_start, int64_t n_q, int32_t k,
+                         int32_t n_sink, int32_t n_local, int32_t* pages_out,
+                         int32_t* counts_out, void* stream) {
+    (void)s; (void)q; (void)q_start; (void)n_q; (void)k; (void)n_sink; (void)n_local;
+    (void)pages_out; (void)counts_out; (void)stream;
+    return fail(PKV_ERR_UNSUPPORTED, "pkv_page_topk: not built yet");
+}
+
+pkv_status pkv_prefetch(pkv_seq* s, const int32_t* pages, int64_t n, void* side) {
+    (void)s; (void)pages; (void)n; (void)side;
+    return fail(PKV_ERR_UNSUPPORTED, "pkv_prefetch: not built yet");
+}
+
+pkv_status pkv_writeback_grads(pkv_seq* s, void* side) {
+    (void)s; (void)side;
+    return fail(PKV_ERR_UNSUPPORTED, "pkv_writeback_grads: not built yet");
+}
+
+pkv_status pkv_wait(pkv_seq* s, void* main, int64_t timeout_us) {
+    (void)s; (void)main; (void)timeout_us;
+    return fail(PKV_ERR_UNSUPPORTED, "pkv_wait: not built yet");
+}
+
+pkv_status pkv_selftest_umma(int32_t mode, const void* a, const void* b, float* d, int32_t lbo,
+                             int32_t sbo) {
+    if (mode < 0 || mode > 2 || !a || !b || !d)
+        return fail(PKV_ERR_INVALID, "pkv_selftest_umma: bad argument");
+    int* d_err = nullptr;
+    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&d_err), sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_selftest_umma: alloc");
+    cudaMemset(d_err, 0, sizeof(int));
+    e = run_selftest_umma(mode, a, b, d, lbo, sbo, d_err);
+    int h = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&h, d_err, sizeof(int), cudaMemcpyDeviceToHost);
+    cudaFree(d_err);
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_selftest_umma");
+    if (h) return fail(PKV_ERR_DEVICE_FAULT, "pkv_selftest_umma: device error " + std::to_string(h));
+    return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,196 @@
+// Page writes: append (scatter a chunk's K/V into its pages, page
+// representatives, fresh-page gradient zeroing), gradient zeroing and the
+// logical-order gather used by tests and by the K/V projections' backward.
+//
+// Representatives follow "Out of the Memory Barrier" (gist.science/de §2.D:
+// relevant pages are found through per-page representative vectors): here the
+// fp32 mean of the keys a page holds, per KV head.
+//
+// All three kernels are HBM-bound copies: one CTA per (logical page, KV head),
+// 16-byte loads/stores, a row of d elements read by d*elem/16 consecutive
+// threads so that every warp touches whole 32-byte sectors.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
+    constexpr int VPR = D * (int)sizeof(T) / 16;   // 16-byte vectors per row
+    constexpr int EPV = 16 / (int)sizeof(T);       // elements per vector
+    constexpr int RSTEP = kThreads / VPR;          // rows handled per pass
+    __shared__ float red[RSTEP][D];
+
+    const int P = a.P;
+    const int64_t lp = a.old_len / P + blockIdx.x;  // logical page
+    const int h = blockIdx.y;
+    const int32_t pp = a.bt[lp];
+    if (pp < 0 || pp >= a.num_phys) {
+        report_error(a.err, kErrBadPage);
+        return;
+    }
+    const int64_t new_len = a.old_len + a.n_tok;
+    const int64_t page_start = lp * P;
+    const int tid = threadIdx.x;
+    const int vc = tid % VPR;
+    const int r0 = tid / VPR;
+    const size_t page_off = ((size_t)pp * a.Hkv + h) * (size_t)P * D;
+    T* kpage = static_cast<T*>(a.kpool) + page_off;
+    T* vpage = static_cast<T*>(a.vpool) + page_off;
+
+    float acc[EPV];
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) acc[e] = 0.f;
+
+    for (int r = r0; r < P; r += RSTEP) {
+        const int64_t pos = page_start + r;
+        uint4 kv;
+        uint4* kdst = reinterpret_cast<uint4*>(kpage + (size_t)r * D) + vc;
+        uint4* vdst = reinterpret_cast<uint4*>(vpage + (size_t)r * D) + vc;
+        if (pos >= a.old_len && pos < new_len) {
+            const size_t src = ((size_t)(pos - a.old_len) * a.Hkv + h) * D;
+            kv = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.k_in) + src) + vc);
+            const uint4 vv =
+                __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.v_in) + src) + vc);
+            *kdst = kv;
+            *vdst = vv;
+        } else if (pos < a.old_len) {
+            kv = *kdst;                               // row written by an earlier append
+        } else {
+            kv = make_uint4(0, 0, 0, 0);              // beyond the sequence: keep rows zero
+            *kdst = kv;
+            *vdst = kv;
+        }
+        if (pos < new_len) {
+            float f[EPV];
+            widen16<T>(kv, f);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) acc[e] += f[e];
+        }
+    }
+
+    // A page taken off the free list starts with zero gradient.
+    if (page_start >= a.old_len) {
+        float4* g0 = reinterpret_cast<float4*>(a.dkpool + page_off);
+        float4* g1 = reinterpret_cast<float4*>(a.dvpool + page_off);
+        const int n4 = P * D / 4;
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = tid; i < n4; i += kThreads) {
+            g0[i] = z;
+            g1[i] = z;
+        }
+    }
+
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) red[r0][vc * EPV + e] = acc[e];
+    __syncthreads();
+    if (tid < D) {
+        float sum = 0.f;
+#pragma unroll 4
+        for (int g = 0; g < RSTEP; ++g) sum += red[g][tid];
+        const int64_t valid = min64(P, new_len - page_start);
+        a.rep[((size_t)pp * a.Hkv + h) * D + tid] = sum / (float)valid;
+    }
+}
+
+__global__ void grad_zero_kernel(float* dk, float* dv, const int32_t* bt, int64_t p0, int64_t num_phys,
+                                 int Hkv, int page_floats, int* err) {
+    const int64_t lp = p0 + blockIdx.x;
+    const int32_t pp = bt[lp];
+    if (pp < 0 || pp >= num_phys) {
+        report_error(err, kErrBadPage);
+        return;
+    }
+    const size_t off = ((size_t)pp * Hkv + blockIdx.y) * page_floats;
+    float4* a = reinterpret_cast<float4*>(dk + off);
+    float4* b = reinterpret_cast<float4*>(dv + off);
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = threadIdx.x; i < page_floats / 4; i += blockDim.x) {
+        a[i] = z;
+        b[i] = z;
+    }
+}
+
+// Copies rows of one (logical page, KV head) into logical-order outputs.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) gather_kernel(const T* kpool, const T* vpool,
+        const float* dkpool, const float* dvpool, const float* reppool, const int32_t* bt,
+        int64_t num_phys, int P, int Hkv, int64_t len, T* k, T* v, float* dk, float* dv,
+        float* rep, int* err) {
+    const int64_t lp = blockIdx.x;
+    const int h = blockIdx.y;
+    const int32_t pp = bt[lp];
+    if (pp < 0 || pp >= num_phys) {
+        report_error(err, kErrBadPage);
+        return;
+    }
+    const size_t page_off = ((size_t)pp * Hkv + h) * (size_t)P * D;
+    const int rows = (int)min64(P, len - lp * P);
+    for (int i = threadIdx.x; i < rows * D; i += kThreads) {
+        const int r = i / D, c = i % D;
+        const size_t dst = ((size_t)(lp * P + r) * Hkv + h) * D + c;
+        const size_t src = page_off + (size_t)r * D + c;
+        if (k) k[dst] = kpool[src];
+        if (v) v[dst] = vpool[src];
+        if (dk) dk[dst] = dkpool[src];
+        if (dv) dv[dst] = dvpool[src];
+    }
+    if (rep && threadIdx.x < D)
+        rep[((size_t)lp * Hkv + h) * D + threadIdx.x] =
+            reppool[((size_t)pp * Hkv + h) * D + threadIdx.x];
+}
+
+template <typename T>
+cudaError_t append_dispatch_d(const AppendArgs& a, cudaStream_t s, dim3 grid) {
+    if (a.d == 128) append_kernel<T, 128><<<grid, kThreads, 0, s>>>(a);
+    else append_kernel<T, 64><<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t gather_dispatch(const pkv_pool* p, const int32_t* bt, int64_t len, void* k, void* v,
+                            float* dk, float* dv, float* rep, cudaStream_t s) {
+    const int P = p->desc.page_size, Hkv = p->desc.n_kv_heads;
+    dim3 grid((unsigned)((len + P - 1) / P), Hkv);
+#define PKV_GATHER_ARGS                                                                      \
+    static_cast<const T*>(p->k), static_cast<const T*>(p->v), p->dk, p->dv, p->rep, bt,     \
+        p->desc.num_phys_pages, P, Hkv, len, static_cast<T*>(k), static_cast<T*>(v), dk, dv, \
+        rep, p->d_err
+    if (p->desc.head_dim == 128) gather_kernel<T, 128><<<grid, kThreads, 0, s>>>(PKV_GATHER_ARGS);
+    else gather_kernel<T, 64><<<grid, kThreads, 0, s>>>(PKV_GATHER_ARGS);
+#undef PKV_GATHER_ARGS
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
+    const int64_t first = a.old_len / a.P;
+    const int64_t last = (a.old_len + a.n_tok - 1) / a.P;
+    dim3 grid((unsigned)(last - first + 1), a.Hkv);
+    return a.dtype == PKV_BF16 ? append_dispatch_d<__nv_bfloat16>(a, s, grid)
+                               : append_dispatch_d<float>(a, s, grid);
+}
+
+cudaError_t launch_grad_zero(const pkv_pool* p, const int32_t* d_bt, int64_t p0, int64_t p1,
+                             cudaStream_t s) {
+    if (p1 <= p0) return cudaSuccess;
+    dim3 grid((unsigned)(p1 - p0), p->desc.n_kv_heads);
+    grad_zero_kernel<<<grid, kThreads, 0, s>>>(p->dk, p->dv, d_bt, p0, p->desc.num_phys_pages,
+                                               p->desc.n_kv_heads,
+                                               p->desc.page_size * p->desc.head_dim, p->d_err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const pkv_pool* p, const int32_t* d_bt, int64_t len, void* k, void* v,
+                          float* dk, float* dv, float* rep, cudaStream_t s) {
+    return p->desc.dtype == PKV_BF16 ? gather_dispatch<__nv_bfloat16>(p, d_bt, len, k, v, dk, dv, rep, s)
+                                     : gather_dispatch<float>(p, d_bt, len, k, v, dk, dv, rep, s);
+}
+
+}  // namespace pkv

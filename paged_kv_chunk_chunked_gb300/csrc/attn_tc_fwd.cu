@@ -1,0 +1,364 @@
+// Tensor-core (tcgen05) paged chunk attention forward, bf16 in / fp32 accumulate.
+//
+// Computes, for one query chunk, exact causal softmax attention over every
+// key reached through the block table (dense) or over the pages selected for
+// each query page (sparse), and saves the row log-sum-exp for the backward
+// ("Out of the Memory Barrier": kernels that run forward and backward directly
+// on the paged KV cache, gist.science/de §2.B, sciencestack.ai Fig. 3; page
+// selection, gist.science/de §2.D).
+//
+// One CTA per (query tile of 128 rows = one query page, query head); key
+// tiles are whole pages (P = 128), fetched by TMA with the physical page
+// taken from the block table. Warp roles (192 threads):
+//   warp 0      TMA producer: Q once, then K/V pages into a 2-stage ring.
+//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into a double-buffered
+//               TMEM tile, then O += P_{j-1} V_{j-1} (O lives in TMEM).
+//   warps 2..5  softmax: one thread per query row; reads S_j from TMEM, keeps
+//               the running max m and sum l, writes P_j (bf16) to shared
+//               memory in the 128-byte-swizzled K-major layout, and rescales
+//               O in TMEM only when m grows by more than 2^8 (P <= 256 then,
+//               exactly representable range for bf16). Epilogue: O / l, LSE.
+// TMEM columns: S0 [0,128), S1 [128,256), O [256,384) of a 512-column block.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kTile = 128;                   // query rows = keys per tile = head dim
+constexpr int kThreads = 192;
+constexpr uint32_t kHalfBytes = 128 * 128;   // [128 rows][64 bf16] = 16 KB
+constexpr uint32_t kTileBytes = 2 * kHalfBytes;
+// Shared-memory tile offsets (bytes from a 1024-aligned base).
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kTileBytes;          // 2 stages
+constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;      // 2 stages
+constexpr uint32_t kOffP = kOffV + 2 * kTileBytes;
+constexpr uint32_t kTilesBytes = kOffP + kTileBytes;    // 192 KB
+constexpr uint32_t kSmemBytes = kTilesBytes + 1024;     // + alignment slack
+constexpr float kRescaleThreshold = 8.0f;               // log2 units
+
+struct FwdParams {
+    int Hq, Hkv;
+    int64_t q_start, n_q;
+    void* o;
+    float* lse;
+    const int32_t* bt;
+    int64_t num_phys;
+    const int32_t* sel;
+    int kmax;
+    int* err;
+};
+
+struct __align__(8) FwdBarriers {
+    uint64_t q_full;
+    uint64_t k_full[2], v_full[2], kv_empty[2];
+    uint64_t s_full[2];
+    uint64_t p_full;
+    uint64_t o_done;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int n_tiles;
+};
+
+// Number of key tiles and the logical page of tile j for this CTA.
+__device__ __forceinline__ int tile_count(const FwdParams& p, int qt, int kvh) {
+    if (!p.sel) return (int)(p.q_start / kTile) + qt + 1;
+    const int32_t* row = p.sel + ((size_t)qt * p.Hkv + kvh) * p.kmax;
+    int n = 0;
+    while (n < p.kmax && row[n] >= 0) ++n;
+    return n;
+}
+__device__ __forceinline__ int32_t tile_page(const FwdParams& p, int qt, int kvh, int j) {
+    return p.sel ? p.sel[((size_t)qt * p.Hkv + kvh) * p.kmax + j] : j;
+}
+
+// Bounded wait that ignores errors recorded elsewhere: used only to drain
+// this CTA's own copies and MMAs before it exits.
+__device__ bool drain_wait(uint64_t* bar, uint32_t parity) {
+    const uint32_t addr = tc::smem_u32(bar);
+    const uint64_t t0 = tc::globaltimer();
+    while (!tc::mbar_try_wait(addr, parity))
+        if (tc::globaltimer() - t0 > 1000000000ull) return false;
+    return true;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+              const __grid_constant__ CUtensorMap tmap_v, FwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ FwdBarriers B;
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;        // longest tiles first
+    const int h = blockIdx.y;
+    const int kvh = h / (p.Hq / p.Hkv);
+
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&B.q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(&B.k_full[s], 1);
+            tc::mbar_init(&B.v_full[s], 1);
+            tc::mbar_init(&B.kv_empty[s], 1);
+            tc::mbar_init(&B.s_full[s], 1);
+        }
+        tc::mbar_init(&B.p_full, 128);
+        tc::mbar_init(&B.o_done, 1);
+        tc::mbar_init(&B.drain, 1);
+        B.n_tiles = tile_count(p, qt, kvh);
+        tc::fence_barrier_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(&B.tmem_base, 512);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = B.tmem_base;
+    const int nt = B.n_tiles;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tc::prefetch_tmap(&tmap_q);
+            tc::prefetch_tmap(&tmap_k);
+            tc::prefetch_tmap(&tmap_v);
+            const int q_row0 = (int)(qt * kTile);
+            tc::mbar_arrive_expect_tx(&B.q_full, kTileBytes);
+            tc::tma_load_3d(smem + kOffQ, &tmap_q, &B.q_full, 0, h, q_row0);
+            tc::tma_load_3d(smem + kOffQ + kHalfBytes, &tmap_q, &B.q_full, 64, h, q_row0);
+            int issued = 0;
+            for (int j = 0; j < nt; ++j) {
+                const int st = j & 1;
+                if (j >= 2 && !tc::mbar_wait(&B.kv_empty[st], ((j >> 1) - 1) & 1, p.err)) break;
+                const int32_t lp = tile_page(p, qt, kvh, j);
+                const int32_t pp = (lp >= 0) ? p.bt[lp] : -1;
+                if (pp < 0 || pp >= p.num_phys) {
+                    report_error(p.err, kErrBadPage);
+                    break;
+                }
+                const int row = (int)(((int64_t)pp * p.Hkv + kvh) * kTile);
+                uint8_t* kdst = smem + kOffK + st * kTileBytes;
+                uint8_t* vdst = smem + kOffV + st * kTileBytes;
+                tc::mbar_arrive_expect_tx(&B.k_full[st], kTileBytes);
+                tc::tma_load_2d(kdst, &tmap_k, &B.k_full[st], 0, row);
+                tc::tma_load_2d(kdst + kHalfBytes, &tmap_k, &B.k_full[st], 64, row);
+                tc::mbar_arrive_expect_tx(&B.v_full[st], kTileBytes);
+                tc::tma_load_2d(vdst, &tmap_v, &B.v_full[st], 0, row);
+                tc::tma_load_2d(vdst + kHalfBytes, &tmap_v, &B.v_full[st], 64, row);
+                issued = j + 1;
+            }
+            // Make sure none of this CTA's copies is still landing when it exits.
+            drain_wait(&B.q_full, 0);
+            for (int j = max(0, issued - 2); j < issued; ++j) {
+                drain_wait(&B.k_full[j & 1], (j >> 1) & 1);
+                drain_wait(&B.v_full[j & 1], (j >> 1) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = tc::idesc_bf16(128, 128, false, false);       // S = Q K^T
+            const uint32_t idesc_pv = tc::idesc_bf16(128, 128, false, true);     // O += P V
+            const uint32_t sq = tc::smem_u32(smem + kOffQ);
+            const uint32_t sp = tc::smem_u32(smem + kOffP);
+            const uint32_t tmem_o = tmem + 256;
+            bool ok = tc::mbar_wait(&B.q_full, 0, p.err);
+            auto issue_pv = [&](int i) -> bool {
+                if (!tc::mbar_wait(&B.p_full, i & 1, p.err)) return false;
+                if (!tc::mbar_wait(&B.v_full[i & 1], (i >> 1) & 1, p.err)) return false;
+                tc::tc_fence_after();
+                const uint32_t sv = tc::smem_u32(smem + kOffV + (i & 1) * kTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    // A = P [128 q][128 keys] K-major; B = V [128 keys][128 d] MN-major:
+                    // 16 keys = 2 K-groups of 8 rows (1024 B apart); d spans the two
+                    // 64-column halves (16 KB apart).
+                    const uint64_t a = tc::sdesc(sp + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = tc::sdesc(sv + kk * 2048, kHalfBytes, 1024);
+                    tc::mma_bf16(tmem_o, a, b, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc::mma_commit(&B.o_done);
+                tc::mma_commit(&B.kv_empty[i & 1]);
+                return true;
+            };
+            for (int j = 0; ok && j < nt; ++j) {
+                const int st = j & 1;
+                if (!tc::mbar_wait(&B.k_full[st], (j >> 1) & 1, p.err)) { ok = false; break; }
+                tc::tc_fence_after();
+                const uint32_t sk = tc::smem_u32(smem + kOffK + st * kTileBytes);
+                const uint32_t tmem_s = tmem + st * 128;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t koff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                    tc::mma_bf16(tmem_s, tc::sdesc(sq + koff, 16, 1024), tc::sdesc(sk + koff, 16, 1024),
+                                 idesc, kk > 0 ? 1u : 0u);
+                }
+                tc::mma_commit(&B.s_full[st]);
+                if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
+            }
+            if (ok && nt > 0) issue_pv(nt - 1);
+            // Drain: nothing of ours may still run on the tensor core at exit.
+            tc::mma_commit(&B.drain);
+            drain_wait(&B.drain, 0);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax (128 threads)
+        const int quad = warp & 3;                    // TMEM lane quadrant of this warp
+        const int row = quad * 32 + lane;             // query row within the tile
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        const float sl2 = rsqrtf(128.f) * kLog2e;
+        const int64_t q_local = (int64_t)qt * kTile + row;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        uint8_t* sP = smem + kOffP;
+        for (int j = 0; j < nt; ++j) {
+            const int st = j & 1;
+            ok = tc::mbar_wait(&B.s_full[st], (j >> 1) & 1, p.err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc::tc_fence_after();
+            float x[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tc::tmem_ld32(lane_base + st * 128 + c * 32, r);
+                tc::tmem_wait_ld(r);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(r[e]) * sl2;
+            }
+            if (j == nt - 1) {                        // own page: causal mask (key col > row)
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (c > row) x[c] = -INFINITY;
+            }
+            float mx = x[0];
+#pragma unroll
+            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+            float alpha = 1.f;
+            bool rescale = false;
+            if (mx > m + kRescaleThreshold) {
+                alpha = (m == -INFINITY) ? 0.f : fast_exp2(m - mx);
+                m = mx;
+                rescale = true;
+            }
+            l *= alpha;
+            uint32_t pk[64];
+            float ls = 0.f;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float p0 = fast_exp2(x[2 * c] - m), p1 = fast_exp2(x[2 * c + 1] - m);
+                ls += p0 + p1;
+                pk[c] = pack_bf16x2(p0, p1);
+            }
+            l += ls;
+            if (j > 0) {                              // PV_{j-1} done: P buffer free, O stable
+                ok = tc::mbar_wait(&B.o_done, (j - 1) & 1, p.err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc::tc_fence_after();
+                if (__any_sync(0xffffffffu, rescale)) {
+                    const float f = rescale ? alpha : 1.f;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r[32];
+                        tc::tmem_ld32(lane_base + 256 + c * 32, r);
+                        tc::tmem_wait_ld(r);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
+                        tc::tmem_st32(lane_base + 256 + c * 32, r);
+                    }
+                    tc::tmem_wait_st();
+                }
+            }
+            // P row -> shared memory, 128-byte swizzle, keys 0..63 | 64..127 halves.
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch) {
+                uint8_t* base = sP + (ch >> 3) * kHalfBytes;
+                *reinterpret_cast<uint4*>(base + tc::sw128_offset(row, ch & 7)) =
+                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            }
+            tc::fence_proxy_async_smem();
+            tc::tc_fence_before();
+            tc::mbar_arrive(&B.p_full);
+        }
+        if (ok && nt > 0) {
+            ok = tc::mbar_wait(&B.o_done, (nt - 1) & 1, p.err);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok && nt > 0) {
+            tc::tc_fence_after();
+            const float inv = 1.f / l;
+            const bool valid = q_local < p.n_q;
+            __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + ((size_t)q_local * p.Hq + h) * kTile;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tc::tmem_ld32(lane_base + 256 + c * 32, r);
+                tc::tmem_wait_ld(r);
+                if (valid) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
+                        *reinterpret_cast<uint4*>(orow + c * 32 + v * 8) = w;
+                    }
+                }
+            }
+            if (valid) p.lse[(size_t)h * p.n_q + q_local] = (m + log2f(l)) * kLn2;
+        }
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+bool tc_supported(const AttnArgs& a) {
+    return a.dtype == PKV_BF16 && a.d == 128 && a.P == 128 && a.tmap_k && a.tmap_v &&
+           (reinterpret_cast<uintptr_t>(a.q) & 15) == 0;
+}
+
+cudaError_t launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t s) {
+    CUtensorMap tq;
+    std::string why;
+    if (!make_tmap_3d(&tq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, a.Hq, a.n_q, 256,
+                      (uint64_t)a.Hq * 256, 64, 1, 128, &why))
+        return cudaErrorInvalidValue;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    FwdParams p{};
+    p.Hq = a.Hq; p.Hkv = a.Hkv; p.q_start = a.q_start; p.n_q = a.n_q;
+    p.o = a.o; p.lse = a.lse; p.bt = a.bt; p.num_phys = a.num_phys;
+    p.sel = a.sel; p.kmax = a.kmax; p.err = a.err;
+    dim3 grid((unsigned)((a.n_q + kTile - 1) / kTile), a.Hq);
+    fwd_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, *a.tmap_k, *a.tmap_v, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
+    // The tensor-core backward is not built yet: use the CUDA-core kernels.
+    return launch_attn_bwd_simt(a, s);
+}
+
+}  // namespace pkv

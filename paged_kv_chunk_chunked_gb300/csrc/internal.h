@@ -1,0 +1,117 @@
+// Host-side structures and kernel-launcher declarations shared by the C-ABI
+// layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/pkv.h"
+
+struct pkv_pool {
+    pkv_pool_desc desc{};
+    int device = 0;
+    size_t elem = 2;                 // bytes per K/V element
+    size_t page_elems = 0;           // Hkv * P * d: one physical page of K (or V)
+    // Page memory (device for DEVICE pools, pinned host for PINNED_HOST pools).
+    void* k = nullptr;
+    void* v = nullptr;
+    float* dk = nullptr;
+    float* dv = nullptr;
+    float* rep = nullptr;            // [num_phys, Hkv, d]
+    int* d_err = nullptr;            // device error word
+    std::vector<int32_t> free_list;  // stack of free physical pages (top = back)
+    std::vector<uint8_t> in_use;     // per physical page
+    std::vector<pkv_seq*> seqs;
+    // Scratch (bwd row statistics D = rowsum(dO * O)), grown on demand.
+    float* scratch = nullptr;
+    size_t scratch_floats = 0;
+    // TMA descriptors over the K and V page pools (2-D: rows x d).
+    CUtensorMap tmap_k{}, tmap_v{};
+    bool tmaps_ready = false;
+};
+
+struct pkv_seq {
+    pkv_pool* pool = nullptr;
+    std::vector<int32_t> bt;         // host block table
+    int64_t n_reserved_pages = 0;    // pages pre-assigned by pkv_set_block_table not yet filled
+    int32_t* h_bt = nullptr;         // pinned mirror used as the copy source
+    int32_t* d_bt = nullptr;         // device block table, capacity num_phys_pages
+    int64_t len = 0;
+};
+
+namespace pkv {
+
+// Sets the thread's last-error message and returns the status.
+pkv_status fail(pkv_status s, const std::string& msg);
+pkv_status cuda_fail(cudaError_t e, const char* what);
+
+struct AppendArgs {
+    int P, Hkv, d, dtype;
+    const void* k_in;
+    const void* v_in;
+    void* kpool;
+    void* vpool;
+    float* dkpool;
+    float* dvpool;
+    float* rep;
+    const int32_t* bt;
+    int64_t num_phys;
+    int64_t old_len, n_tok;
+    int* err;
+};
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+
+// Zero the gradient rows of the given logical pages range [p0, p1).
+cudaError_t launch_grad_zero(const pkv_pool* pool, const int32_t* d_bt, int64_t p0, int64_t p1,
+                             cudaStream_t s);
+cudaError_t launch_gather(const pkv_pool* pool, const int32_t* d_bt, int64_t len, void* k,
+                          void* v, float* dk, float* dv, float* rep, cudaStream_t s);
+
+struct AttnArgs {
+    int P, Hq, Hkv, d, dtype;
+    int64_t q_start, n_q;            // keys 0 .. q_start + n_q - 1
+    const void* q;
+    const void* o_in;                // bwd: forward output
+    const void* dout;                // bwd: dL/dO
+    const float* lse_in;             // bwd: forward LSE
+    void* o;                         // fwd out
+    float* lse;                      // fwd out
+    void* dq;                        // bwd out
+    float* Dbuf;                     // bwd scratch [Hq, n_q]
+    const void* kpool;
+    const void* vpool;
+    float* dkpool;
+    float* dvpool;
+    const int32_t* bt;
+    int64_t num_phys;
+    const int32_t* sel;              // sparse: [n_qp, Hkv, kmax] or null
+    int kmax;
+    int* err;
+    const CUtensorMap* tmap_k;       // tensor-core path only
+    const CUtensorMap* tmap_v;
+};
+
+cudaError_t launch_attn_fwd_simt(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_attn_bwd_simt(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_rowdot(const AttnArgs& a, cudaStream_t s);
+
+bool tc_supported(const AttnArgs& a);
+cudaError_t launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s);
+
+// TMA descriptor helpers (driver entry point fetched through the runtime).
+bool make_tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t inner,
+                  uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
+                  uint32_t box_rows, std::string* why);
+bool make_tmap_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t d0,
+                  uint64_t d1, uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes,
+                  uint32_t b0, uint32_t b1, uint32_t b2, std::string* why);
+
+cudaError_t run_selftest_umma(int mode, const void* a, const void* b, float* d, int lbo, int sbo,
+                              int* d_err);
+
+}  // namespace pkv

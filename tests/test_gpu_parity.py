@@ -1,0 +1,120 @@
+"""GPU parity: libpkv (through its C ABI) against the CPU oracle, element by element.
+
+Tolerances (stated for this path): O and LSE max-abs <= 1e-2 with bf16 inputs,
+1e-4 with fp32; dQ, dK, dV relative Frobenius <= 2e-2 (bf16), 1e-4 (fp32).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_chunk_chunked_gb300 import binding as B
+from paged_kv_chunk_chunked_gb300 import build as pkv_build
+from paged_kv_chunk_chunked_gb300 import synth
+from paged_kv_chunk_chunked_gb300.sweep import ChunkSweep, to_device, to_numpy
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": (1e-2, 2e-2), "f32": (1e-4, 1e-4)}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    pkv_build.build()
+    B.lib()
+    torch.cuda.set_device(0)
+
+
+def _rel(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def _oracle(w):
+    n = w.n_chunks
+    qs = [synth.chunk_q(w, c) for c in range(n)]
+    ks = [synth.chunk_k(w, c) for c in range(n)]
+    vs = [synth.chunk_v(w, c) for c in range(n)]
+    dos = [synth.chunk_do(w, c) for c in range(n)]
+    bt = synth.block_table(w)
+    return oracle.chunk_recurrent_step(qs, ks, vs, dos, bt, w.P, w.n_phys), bt
+
+
+def _sweep_vs_oracle(w, flags=0):
+    sw = ChunkSweep(w, flags=flags).load_inputs()
+    try:
+        sw.run()
+        B.pkv_check(sw.pool)
+        g = sw.gather()
+        ref, bt = _oracle(w)
+        tol_abs, tol_rel = TOL[w.dtype]
+        o = np.concatenate([to_numpy(x) for x in sw.o])
+        lse = np.concatenate([to_numpy(x) for x in sw.lse], axis=1)
+        dq = np.concatenate([to_numpy(x) for x in sw.dq])
+        err = dict(
+            o=float(np.abs(o - np.concatenate(ref["o"])).max()),
+            lse=float(np.abs(lse - np.concatenate(ref["lse"], axis=1)).max()),
+            dq=_rel(dq, np.concatenate(ref["dq"])),
+            dk=_rel(to_numpy(g["dk"]), oracle.logical_rows(ref["dkpool"], bt, w.N, w.P)),
+            dv=_rel(to_numpy(g["dv"]), oracle.logical_rows(ref["dvpool"], bt, w.N, w.P)),
+        )
+        assert err["o"] <= tol_abs and err["lse"] <= tol_abs, err
+        assert err["dq"] <= tol_rel and err["dk"] <= tol_rel and err["dv"] <= tol_rel, err
+        # the pool holds exactly the appended keys/values, in logical order
+        np.testing.assert_array_equal(to_numpy(g["k"]), oracle.logical_rows(ref["kpool"], bt, w.N, w.P))
+        np.testing.assert_array_equal(to_numpy(g["v"]), oracle.logical_rows(ref["vpool"], bt, w.N, w.P))
+        rep_ref = oracle.page_representatives(oracle.logical_rows(ref["kpool"], bt, w.N, w.P), w.P)
+        np.testing.assert_allclose(to_numpy(g["rep"]), rep_ref, rtol=0, atol=1e-5)
+        return err, sw
+    finally:
+        sw.close()
+
+
+def test_tiny_dense_f32():
+    _sweep_vs_oracle(synth.workload("tiny_dense_f32"))
+
+
+def test_tiny_dense_f32_partial_last_page_and_perm():
+    _sweep_vs_oracle(synth.workload("tiny_dense_f32", N=200, table="perm", extra_pages=3))
+
+
+def test_small_dense_bf16_page16_cuda_cores():
+    _sweep_vs_oracle(synth.workload("tiny_dense_f32", dtype="bf16", Hq=4, Hkv=2, N=320, C=96,
+                                    table="perm", extra_pages=2, name="bf16_p16"))
+
+
+@pytest.mark.parametrize("N,C,Hq,Hkv", [(768, 256, 4, 2), (1024, 512, 7, 1), (700, 256, 4, 2)])
+def test_dense_bf16_page128_tensor_cores(N, C, Hq, Hkv):
+    w = synth.workload("qwen7b_dense_32k", N=N, C=C, Hq=Hq, Hkv=Hkv, table="perm",
+                       extra_pages=3, name=f"bf16_p128_{N}_{C}")
+    _sweep_vs_oracle(w)
+
+
+def test_dense_bf16_page128_cuda_cores_flag():
+    w = synth.workload("qwen7b_dense_32k", N=512, C=256, Hq=4, Hkv=2, name="bf16_p128_simt")
+    _sweep_vs_oracle(w, flags=B.PKV_FLAG_SIMT_ONLY)
+
+
+def test_permuted_block_table_gives_identical_results():
+    base = dict(N=640, C=256, Hq=4, Hkv=2, extra_pages=4)
+    outs = []
+    for table in ("identity", "perm"):
+        w = synth.workload("qwen7b_dense_32k", table=table, **base)
+        sw = ChunkSweep(w).load_inputs()
+        sw.run()
+        g = sw.gather()
+        outs.append(([to_numpy(x) for x in sw.o], [to_numpy(x) for x in sw.lse], to_numpy(g["dv"])))
+        sw.close()
+    for a, b in zip(outs[0][0] + outs[0][1], outs[1][0] + outs[1][1]):
+        np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_umma_selftest(mode):
+    g = torch.Generator().manual_seed(mode)
+    a = torch.randn((128, 64) if mode < 2 else (64, 128), generator=g).to(torch.bfloat16)
+    b = torch.randn((128, 64) if mode == 0 else (64, 128), generator=g).to(torch.bfloat16)
+    d = torch.empty((128, 128), dtype=torch.float32, device="cuda")
+    B.pkv_selftest_umma(mode, a.cuda(), b.cuda(), d)
+    af, bf = a.double(), b.double()
+    ref = af @ bf.T if mode == 0 else (af @ bf if mode == 1 else af.T @ bf)
+    np.testing.assert_allclose(d.cpu().double().numpy(), ref.numpy(), rtol=1e-5, atol=1e-4)
