@@ -99,8 +99,9 @@ WORKLOADS = {
 }
 
 
-def workload(name: str, **overrides) -> Workload:
-    w = WORKLOADS[name]
+def workload(key: str, **overrides) -> Workload:
+    """The named workload, optionally with fields replaced (e.g. a smaller N)."""
+    w = WORKLOADS[key]
     return replace(w, **overrides) if overrides else w
 
 
