@@ -1,0 +1,402 @@
+#!/usr/bin/env python
+"""Benchmark of paged chunk attention forward + backward on GB300.
+
+One step = one attention layer's whole chunk-recurrent sweep over a sequence
+("Out of the Memory Barrier", gist.science/de §2.A-B): reset the sequence,
+then for every chunk append its K/V into the paged pool and run the forward,
+then run the backward over the chunks in reverse (dQ written, dK/dV added in
+place into the paged fp32 gradient pool). Default workload: the Qwen2.5-7B
+attention shape (28 q heads, 4 KV heads, d 128), bf16, page 128, 32K tokens in
+chunks of 4096.
+
+value = algorithmic fwd+bwd FLOPs (14 * Hq * d * attended pairs; pairs =
+N(N+1)/2 for dense causal) / device time, in TFLOP/s. Prints one JSON line.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged chunk-attn fwd+bwd TFLOP/s & tokens/s/layer; % of bf16 TC peak"
+UNIT = "TFLOP/s"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--workload", default="qwen7b_dense_32k")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--flags", type=int, default=0, help="pool flags (1 = CUDA cores only)")
+    return ap.parse_args()
+
+
+def pairs_dense(N: int) -> int:
+    return N * (N + 1) // 2
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed (replicas)
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int) -> float:
+    """Max over ranks (replicas): the job's time is its slowest rank's."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ CPU oracle sample
+
+def oracle_sample(w, n_queries: int):
+    """Oracle fwd+bwd of the last chunk's last n_queries queries, one query head,
+    against every key before them. Returns (algorithmic FLOPs, seconds, desc)."""
+    import numpy as np
+    import oracle
+    from paged_kv_chunk_chunked_gb300 import synth
+    c = w.n_chunks - 1
+    s, e = w.chunk_range(c)
+    ks = np.concatenate([synth.chunk_k(w, i)[:, :1] for i in range(w.n_chunks)])
+    vs = np.concatenate([synth.chunk_v(w, i)[:, :1] for i in range(w.n_chunks)])
+    q = synth.chunk_q(w, c)[-n_queries:, :1]
+    do = synth.chunk_do(w, c)[-n_queries:, :1]
+    q0 = e - n_queries
+    t = time.perf_counter()
+    o, lse = oracle.attention_forward(q, ks[:e], vs[:e], q0)
+    oracle.attention_backward(q, ks[:e], vs[:e], o, do, lse, q0)
+    dt = time.perf_counter() - t
+    pairs = sum(q0 + i + 1 for i in range(n_queries))
+    flops = 14 * w.d * pairs
+    desc = (f"oracle fp64 fwd+bwd of the last {n_queries} queries of chunk {c}, 1 of {w.Hq} "
+            f"query heads, against all {e} earlier keys ({pairs} pairs)")
+    return flops, dt, desc
+
+
+def cpu_threads() -> int:
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ roofline traffic
+
+def traffic_for(kernel: str, source: str):
+    """dram bytes per launch from the committed ncu summary, if the kernel's
+    source is unchanged since the counters were taken; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        ent = t[kernel]
+        sha = hashlib.sha256(open(os.path.join(ROOT, source), "rb").read()).hexdigest()[:16]
+        return ent["bytes_per_launch"] if ent.get("source_sha") == sha else None
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ pkv arm
+
+def run_pkv(args, world, rank):
+    import torch
+    from paged_kv_chunk_chunked_gb300 import binding as B
+    from paged_kv_chunk_chunked_gb300 import build as pkv_build
+    from paged_kv_chunk_chunked_gb300 import synth
+    from paged_kv_chunk_chunked_gb300.sweep import ChunkSweep
+
+    if rank == 0 or world == 1:
+        pkv_build.build()
+    barrier(world)
+    B.lib()
+    w = synth.workload(args.workload)
+    sw = ChunkSweep(w, flags=args.flags).load_inputs()
+    stream = torch.cuda.current_stream()
+    n = w.n_chunks
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    fwd_ev = [[(ev(), ev()) for _ in range(n)] for _ in range(args.steps)]
+    bwd_ev = [[(ev(), ev()) for _ in range(n)] for _ in range(args.steps)]
+
+    def step(k=None):
+        """One sweep; k = timed step index (records per-call events) or None."""
+        sw.reset()
+        for c in range(n):
+            s, e = w.chunk_range(c)
+            B.pkv_append(sw.seq, sw.k[c], sw.v[c], e - s, stream)
+            if k is not None:
+                fwd_ev[k][c][0].record(stream)
+            B.pkv_chunk_attn_fwd(sw.seq, sw.q[c], s, e - s, sw.o[c], sw.lse[c], None, stream)
+            if k is not None:
+                fwd_ev[k][c][1].record(stream)
+        for c in reversed(range(n)):
+            if k is not None:
+                bwd_ev[k][c][0].record(stream)
+            sw.backward(c, stream)
+            if k is not None:
+                bwd_ev[k][c][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    B.pkv_check(sw.pool)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    t0, t1 = ev(), ev()
+    t0.record(stream)
+    for k in range(args.steps):
+        step(k)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    fwd_ms = [sum(a.elapsed_time(b) for a, b in fwd_ev[k]) for k in range(args.steps)]
+    bwd_ms = [sum(a.elapsed_time(b) for a, b in bwd_ev[k]) for k in range(args.steps)]
+    clk = clocks.stop()
+    barrier(world)
+    B.pkv_check(sw.pool)
+    ms_step = reduce_max(t0.elapsed_time(t1) / args.steps, world)
+
+    flops_fwd = 4 * w.Hq * w.d * pairs_dense(w.N)
+    flops_bwd = 10 * w.Hq * w.d * pairs_dense(w.N)
+    tflops = world * (flops_fwd + flops_bwd) / (ms_step * 1e-3) / 1e12
+    pk, pk_kind = peaks()
+    peak_tc = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
+    fwd_call = statistics.mean(fwd_ms) / n
+    bwd_call = statistics.mean(bwd_ms) / n
+    # the fwd call is one kernel launch; per-launch algorithmic FLOPs averaged over the chunks
+    fwd_ach = flops_fwd / n / (fwd_call * 1e-3) / 1e12
+    bwd_ach = flops_bwd / n / (bwd_call * 1e-3) / 1e12
+    tc_bwd = False
+    dominant = "bwd" if bwd_call > fwd_call else "fwd"
+    roof = {
+        "bound": "tensor", "unit": "TFLOP/s", "peak": peak_tc,
+        "peak_kind": f"{pk_kind} bf16_tflops_sustained (kernels timed inside a long step)",
+    }
+    if dominant == "fwd":
+        roof.update(kernel="fwd_tc_kernel", achieved=round(fwd_ach, 2),
+                    frac=round(fwd_ach / peak_tc, 4),
+                    traffic=traffic_for("fwd_tc_kernel",
+                                        "paged_kv_chunk_chunked_gb300/csrc/attn_tc_fwd.cu"))
+    else:
+        roof.update(kernel="pkv_chunk_attn_bwd (all its kernels)", achieved=round(bwd_ach, 2),
+                    frac=round(bwd_ach / peak_tc, 4), traffic=None)
+    launches_per_step = n + n + 3 * n       # append, fwd, bwd (row-dot + dQ + dK/dV)
+
+    out = {
+        "metric": METRIC, "value": round(tflops, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) Q/K/V/dO, bf16-rounded)",
+        "config": {"workload": w.name, "N": w.N, "C": w.C, "P": w.P, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "d": w.d, "block_table": w.table, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (Q, dO, O, dQ: 4 x 235 MB per step)"},
+        "tokens_per_s_per_layer": round(world * w.N / (ms_step * 1e-3), 1),
+        "pct_bf16_peak": round(100 * tflops / world / peak_tc, 2),
+        "fwd_ms_per_step": round(statistics.mean(fwd_ms), 3),
+        "bwd_ms_per_step": round(statistics.mean(bwd_ms), 3),
+        "fwd_tflops": round(fwd_ach, 2), "bwd_tflops": round(bwd_ach, 2),
+        "roofline": roof,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+
+    if not args.no_e2e:
+        out["e2e"] = run_e2e(args, w, sw, step, world)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        flops, dt, desc = oracle_sample(w, w.C)
+        out["cpu_baseline"] = {"value": round(flops / dt / 1e12, 6), "unit": UNIT,
+                               "cores": cpu_threads(), "kind": "oracle", "sample": desc,
+                               "seconds": round(dt, 2)}
+    sw.close()
+    return out
+
+
+def run_e2e(args, w, sw, step, world):
+    """Same step with inputs in pinned host memory: H2D of every chunk's Q, K,
+    V, dO and D2H of every chunk's dQ and the gathered dK, dV inside the
+    timed region."""
+    import torch
+    from paged_kv_chunk_chunked_gb300 import binding as B
+    stream = torch.cuda.current_stream()
+    host_in = [[t.cpu().pin_memory() for t in lst] for lst in (sw.q, sw.k, sw.v, sw.do)]
+    host_dq = [t.cpu().pin_memory() for t in sw.dq]
+    dk = torch.empty((w.N, w.Hkv, w.d), dtype=torch.float32, device="cuda")
+    dv = torch.empty_like(dk)
+    host_dk = torch.empty(dk.shape, dtype=torch.float32).pin_memory()
+    host_dv = torch.empty_like(host_dk).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for lst in host_in for t in lst)
+    d2h = sum(t.numel() * t.element_size() for t in host_dq) + 2 * dk.numel() * 4
+
+    def e2e_step():
+        for dst_l, src_l in zip((sw.q, sw.k, sw.v, sw.do), host_in):
+            for d_, s_ in zip(dst_l, src_l):
+                d_.copy_(s_, non_blocking=True)
+        step()
+        B.pkv_gather(sw.seq, None, None, dk, dv, None, stream)
+        for d_, s_ in zip(host_dq, sw.dq):
+            d_.copy_(s_, non_blocking=True)
+        host_dk.copy_(dk, non_blocking=True)
+        host_dv.copy_(dv, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    ms = reduce_max((time.perf_counter() - t0) * 1e3 / args.steps, world)
+    flops = 14 * w.Hq * w.d * pairs_dense(w.N)
+    return {"value": round(world * flops / (ms * 1e-3) / 1e12, 3), "unit": UNIT,
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+
+def run_reference(args, world, rank):
+    from paged_kv_chunk_chunked_gb300 import synth
+    w = synth.workload(args.workload)
+    n_q = 512
+    for _ in range(args.warmup):
+        oracle_sample(w, n_q)
+    times, flops, desc = [], 0, ""
+    for _ in range(args.steps):
+        flops, dt, desc = oracle_sample(w, n_q)
+        times.append(dt)
+    dt = statistics.mean(times)
+    val = flops / dt / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "N": w.N, "C": w.C, "P": w.P, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "d": w.d, "block_table": w.table},
+        "cpu_baseline": {"value": round(val, 6), "unit": UNIT, "cores": cpu_threads(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(val, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), rank)))
+        return 0
+    world, rank, _ = dist_setup(args)
+    out = run_pkv(args, world, rank)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
