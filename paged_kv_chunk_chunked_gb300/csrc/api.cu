@@ -256,7 +256,11 @@ pkv_status pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
         if (!make_tmap_2d(&p->tmap_k, p->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
                           128, &why) ||
             !make_tmap_2d(&p->tmap_v, p->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
-                          128, &why)) {
+                          128, &why) ||
+            !make_tmap_2d(&p->tmap_k64, p->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
+                          64, &why) ||
+            !make_tmap_2d(&p->tmap_v64, p->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
+                          64, &why)) {
             cleanup();
             return fail(PKV_ERR_CUDA, "pkv_pool_create: " + why);
         }
@@ -435,6 +439,8 @@ static pkv_status attn_common(pkv_seq* s, const void* q, int64_t q_start, int64_
     a->bt = s->d_bt; a->num_phys = p->desc.num_phys_pages; a->err = p->d_err;
     a->tmap_k = p->tmaps_ready ? &p->tmap_k : nullptr;
     a->tmap_v = p->tmaps_ready ? &p->tmap_v : nullptr;
+    a->tmap_k64 = p->tmaps_ready ? &p->tmap_k64 : nullptr;
+    a->tmap_v64 = p->tmaps_ready ? &p->tmap_v64 : nullptr;
     if (sel) {
         const int64_t n_qp = (n_q + P - 1) / P;
         if (!sel->pages || sel->kmax <= 0 || sel->n_qp != n_qp)

@@ -1,0 +1,591 @@
+// Tensor-core (tcgen05) paged chunk attention backward, bf16 in / fp32 accumulate.
+//
+// Recomputes P from the saved LSE (activation recomputation, "Out of the
+// Memory Barrier", gist.science/de §2.A) and computes, for one query chunk,
+//   dQ_i  = s sum_j P_ij (dP_ij - D_i) k_j,       dP_ij = dO_i . v_j,
+//   dK_j += s sum_{h,i} P_ij (dP_ij - D_i) q_i,   dV_j += sum_{h,i} P_ij dO_i,
+// adding dK/dV in place into the paged fp32 gradient pool (gist.science/de
+// §2.B: gradients accumulated in place; sciencestack.ai Fig. 3).
+// D_i = rowsum(dO_i * O_i) comes from the row-dot kernel run before these.
+//
+// Two kernels, so that no output needs atomics between CTAs:
+//   bwd_kv_tc_kernel  one CTA per (key page, KV head). K and V of the page stay
+//                     in shared memory; the CTA walks every 64-query tile of
+//                     the chunk that sees the page, for each of the g query
+//                     heads of the group, and accumulates dK and dV in tensor
+//                     memory. At the end it adds them into the page's gradient
+//                     rows with vectorised red.global.add.v4.f32 (the CTA owns
+//                     those rows within the call; the red keeps earlier chunks'
+//                     contributions).
+//   bwd_q_tc_kernel   one CTA per (128-query tile, query head); walks the
+//                     visible keys in half-page tiles of 64 and accumulates dQ
+//                     in tensor memory, written once as bf16.
+// Both have the forward's warp roles: warp 0 TMA producer, warp 1 single-
+// thread MMA issuer, warps 2..5 one thread per accumulator row. S and dP (or
+// their transposes) are double-buffered in tensor memory so the tensor core
+// computes tile t+1 while the softmax warps work on tile t.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace pkv {
+namespace {
+
+using tc::drain_wait;
+
+constexpr int kThreads = 192;
+constexpr uint32_t KB = 1024;
+
+struct BwdParams {
+    int Hq, Hkv;
+    int64_t q_start, n_q;
+    const float* lse;          // [Hq, n_q]
+    const float* Dbuf;         // [Hq, n_q]
+    void* dq;                  // [n_q, Hq, d] bf16
+    float* dkpool;
+    float* dvpool;
+    const int32_t* bt;
+    int64_t num_phys;
+    int* err;
+};
+
+__device__ __forceinline__ void store_row_bf16x64(uint8_t* tile, int row, const uint32_t (&w)[32]) {
+    // 64 bf16 (32 words) of one row of a [rows][64] tile with the 128-byte swizzle.
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<uint4*>(tile + tc::sw128_offset(row, ch)) =
+            make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
+}
+
+// ============================================================================ dK / dV
+
+// Shared-memory layout (offsets from a 1024-aligned base).
+constexpr uint32_t kv_K = 0;                 // [128 keys][128 d]: two 16 KB halves
+constexpr uint32_t kv_V = 32 * KB;
+constexpr uint32_t kv_Q = 64 * KB;           // 2 stages x [64 q][128 d]: two 8 KB halves
+constexpr uint32_t kv_dO = 96 * KB;          // 2 stages
+constexpr uint32_t kv_PT = 128 * KB;         // 2 buffers x [128 keys][64 q] (16 KB)
+constexpr uint32_t kv_DST = 160 * KB;        // 2 buffers
+constexpr uint32_t kv_STAT = 192 * KB;       // 2 stages x (64 lse*log2e + 64 D) floats
+constexpr uint32_t kv_SMEM = kv_STAT + 2 * 512 + 1024;
+
+struct __align__(8) KVBar {
+    uint64_t kv_full;
+    uint64_t qdo_full[2], qdo_empty[2];
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t pt_free[2];
+    uint64_t acc_done;
+    uint64_t drain;
+    uint32_t tmem_base;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                 const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                 BwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ KVBar B;
+    float* stat = reinterpret_cast<float*>(smem + kv_STAT);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int j = blockIdx.x;                        // logical key page
+    const int kvh = blockIdx.y;
+    const int g = p.Hq / p.Hkv;
+    const int64_t kfirst = (int64_t)j * 128;
+    const int n_qt = (int)((p.n_q + 63) / 64);
+    const int i0 = kfirst > p.q_start ? (int)((kfirst - p.q_start) / 64) : 0;
+    const int n_i = n_qt - i0;
+    const int T = n_i * g;                           // iterations: (head, 64-query tile)
+    const int32_t pp = p.bt[j];
+    const bool page_ok = pp >= 0 && pp < p.num_phys;
+
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&B.kv_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(&B.qdo_full[s], 32);
+            tc::mbar_init(&B.qdo_empty[s], 1);
+            tc::mbar_init(&B.s_full[s], 1);
+            tc::mbar_init(&B.p_full[s], 128);
+            tc::mbar_init(&B.pt_free[s], 1);
+        }
+        tc::mbar_init(&B.acc_done, 1);
+        tc::mbar_init(&B.drain, 1);
+        tc::fence_barrier_init();
+        if (!page_ok) report_error(p.err, kErrBadPage);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(&B.tmem_base, 512);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = B.tmem_base;
+
+    if (!page_ok) {
+        // nothing issued: fall through to the common exit
+    } else if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        const int row = (int)(((int64_t)pp * p.Hkv + kvh) * 128);
+        if (lane == 0) {
+            tc::prefetch_tmap(&tm_q);
+            tc::prefetch_tmap(&tm_do);
+            tc::mbar_arrive_expect_tx(&B.kv_full, 64 * KB);
+            tc::tma_load_2d(smem + kv_K, &tm_k, &B.kv_full, 0, row);
+            tc::tma_load_2d(smem + kv_K + 16 * KB, &tm_k, &B.kv_full, 64, row);
+            tc::tma_load_2d(smem + kv_V, &tm_v, &B.kv_full, 0, row);
+            tc::tma_load_2d(smem + kv_V + 16 * KB, &tm_v, &B.kv_full, 64, row);
+        }
+        int issued = 0;
+        for (int t = 0; t < T; ++t) {
+            const int st = t & 1;
+            if (t >= 2) {
+                bool ok = tc::mbar_wait(&B.qdo_empty[st], ((t >> 1) - 1) & 1, p.err);
+                if (!__all_sync(0xffffffffu, ok)) break;
+            }
+            const int h = kvh * g + t / n_i;
+            const int i = i0 + t % n_i;
+            // per-query statistics for this tile: log2e * LSE (+inf past the chunk) and D
+            float* sst = stat + st * 128;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int c = lane * 2 + e;
+                const int64_t q = (int64_t)i * 64 + c;
+                const bool v = q < p.n_q;
+                sst[c] = v ? p.lse[(size_t)h * p.n_q + q] * kLog2e : INFINITY;
+                sst[64 + c] = v ? p.Dbuf[(size_t)h * p.n_q + q] : 0.f;
+            }
+            if (lane == 0) {
+                uint8_t* q_dst = smem + kv_Q + st * 16 * KB;
+                uint8_t* do_dst = smem + kv_dO + st * 16 * KB;
+                tc::mbar_arrive_expect_tx(&B.qdo_full[st], 32 * KB);
+                tc::tma_load_3d(q_dst, &tm_q, &B.qdo_full[st], 0, h, i * 64);
+                tc::tma_load_3d(q_dst + 8 * KB, &tm_q, &B.qdo_full[st], 64, h, i * 64);
+                tc::tma_load_3d(do_dst, &tm_do, &B.qdo_full[st], 0, h, i * 64);
+                tc::tma_load_3d(do_dst + 8 * KB, &tm_do, &B.qdo_full[st], 64, h, i * 64);
+            } else {
+                tc::mbar_arrive(&B.qdo_full[st]);
+            }
+            issued = t + 1;
+        }
+        if (lane == 0) {
+            drain_wait(&B.kv_full, 0);
+            for (int t = max(0, issued - 2); t < issued; ++t) drain_wait(&B.qdo_full[t & 1], (t >> 1) & 1);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t id_s = tc::idesc_bf16(128, 64, false, false);    // S^T = K Q^T
+            const uint32_t id_g = tc::idesc_bf16(128, 128, false, true);    // dV += P^T dO
+            const uint32_t sK = tc::smem_u32(smem + kv_K), sV = tc::smem_u32(smem + kv_V);
+            const uint32_t t_dK = tmem + 256, t_dV = tmem + 384;
+            bool ok = tc::mbar_wait(&B.kv_full, 0, p.err);
+            auto issue_grad = [&](int t) -> bool {
+                const int b = t & 1;
+                if (!tc::mbar_wait(&B.p_full[b], (t >> 1) & 1, p.err)) return false;
+                tc::tc_fence_after();
+                const uint32_t sPT = tc::smem_u32(smem + kv_PT + b * 16 * KB);
+                const uint32_t sDST = tc::smem_u32(smem + kv_DST + b * 16 * KB);
+                const uint32_t sQ = tc::smem_u32(smem + kv_Q + b * 16 * KB);
+                const uint32_t sdO = tc::smem_u32(smem + kv_dO + b * 16 * KB);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)      // K = 64 queries, 16 per MMA
+                    tc::mma_bf16(t_dV, tc::sdesc(sPT + kk * 32, 16, 1024),
+                                 tc::sdesc(sdO + kk * 2048, 8 * KB, 1024), id_g,
+                                 (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc::mma_bf16(t_dK, tc::sdesc(sDST + kk * 32, 16, 1024),
+                                 tc::sdesc(sQ + kk * 2048, 8 * KB, 1024), id_g,
+                                 (t > 0 || kk > 0) ? 1u : 0u);
+                tc::mma_commit(&B.qdo_empty[b]);
+                tc::mma_commit(&B.pt_free[b]);
+                return true;
+            };
+            for (int t = 0; ok && t < T; ++t) {
+                const int st = t & 1;
+                if (!tc::mbar_wait(&B.qdo_full[st], (t >> 1) & 1, p.err)) { ok = false; break; }
+                tc::tc_fence_after();
+                const uint32_t sQ = tc::smem_u32(smem + kv_Q + st * 16 * KB);
+                const uint32_t sdO = tc::smem_u32(smem + kv_dO + st * 16 * KB);
+                const uint32_t t_S = tmem + st * 128, t_dP = t_S + 64;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t oa = (kk >> 2) * 16 * KB + (kk & 3) * 32;
+                    const uint32_t ob = (kk >> 2) * 8 * KB + (kk & 3) * 32;
+                    tc::mma_bf16(t_S, tc::sdesc(sK + oa, 16, 1024), tc::sdesc(sQ + ob, 16, 1024), id_s,
+                                 kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t oa = (kk >> 2) * 16 * KB + (kk & 3) * 32;
+                    const uint32_t ob = (kk >> 2) * 8 * KB + (kk & 3) * 32;
+                    tc::mma_bf16(t_dP, tc::sdesc(sV + oa, 16, 1024), tc::sdesc(sdO + ob, 16, 1024), id_s,
+                                 kk > 0 ? 1u : 0u);
+                }
+                tc::mma_commit(&B.s_full[st]);
+                if (t > 0 && !issue_grad(t - 1)) { ok = false; break; }
+            }
+            if (ok && T > 0 && issue_grad(T - 1)) tc::mma_commit(&B.acc_done);
+            tc::mma_commit(&B.drain);
+            drain_wait(&B.drain, 0);
+        }
+    } else {
+        // ---------------------------------------------------------------- softmax-grad warps
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;                      // key row of the page
+        const int64_t kpos = kfirst + r;
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        const float sl2 = rsqrtf(128.f) * kLog2e;
+        bool ok = true;
+        for (int t = 0; t < T; ++t) {
+            const int st = t & 1;
+            ok = tc::mbar_wait(&B.s_full[st], (t >> 1) & 1, p.err) &&
+                 tc::mbar_wait(&B.qdo_full[st], (t >> 1) & 1, p.err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc::tc_fence_after();
+            const int i = i0 + t % n_i;
+            const int64_t q0 = p.q_start + (int64_t)i * 64;  // position of column 0
+            const bool diag = kfirst + 127 > q0;
+            const float* sst = stat + st * 128;
+            uint32_t pw[32], dw[32];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {           // 32 query columns at a time
+                uint32_t sv[32], dv[32];
+                tc::tmem_ld32(lane_base + st * 128 + half * 32, sv);
+                tc::tmem_ld32(lane_base + st * 128 + 64 + half * 32, dv);
+                tc::tmem_wait_ld(sv);
+                tc::tmem_wait_ld(dv);
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    float pr[2], dr[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int cc = half * 32 + c + e;
+                        float pv = fast_exp2(__uint_as_float(sv[c + e]) * sl2 - sst[cc]);
+                        if (diag && kpos > q0 + cc) pv = 0.f;
+                        pr[e] = pv;
+                        dr[e] = pv * (__uint_as_float(dv[c + e]) - sst[64 + cc]);
+                    }
+                    pw[half * 16 + c / 2] = pack_bf16x2(pr[0], pr[1]);
+                    dw[half * 16 + c / 2] = pack_bf16x2(dr[0], dr[1]);
+                }
+            }
+            if (t >= 2) {
+                ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.pt_free[st], ((t >> 1) - 1) & 1, p.err));
+                if (!ok) break;
+            }
+            store_row_bf16x64(smem + kv_PT + st * 16 * KB, r, pw);
+            store_row_bf16x64(smem + kv_DST + st * 16 * KB, r, dw);
+            tc::fence_proxy_async_smem();
+            tc::tc_fence_before();
+            tc::mbar_arrive(&B.p_full[st]);
+        }
+        if (ok && T > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.acc_done, 0, p.err));
+        if (ok && T > 0) {
+            tc::tc_fence_after();
+            const bool live = kpos < p.q_start + p.n_q;
+            const size_t off = (((size_t)pp * p.Hkv + kvh) * 128 + r) * 128;
+            const float scale = rsqrtf(128.f);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t a[32];
+                tc::tmem_ld32(lane_base + 256 + c * 32, a);
+                tc::tmem_wait_ld(a);
+                if (live) {
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        red_add_v4(p.dkpool + off + c * 32 + v * 4, __uint_as_float(a[4 * v]) * scale,
+                                   __uint_as_float(a[4 * v + 1]) * scale,
+                                   __uint_as_float(a[4 * v + 2]) * scale,
+                                   __uint_as_float(a[4 * v + 3]) * scale);
+                }
+                tc::tmem_ld32(lane_base + 384 + c * 32, a);
+                tc::tmem_wait_ld(a);
+                if (live) {
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        red_add_v4(p.dvpool + off + c * 32 + v * 4, __uint_as_float(a[4 * v]),
+                                   __uint_as_float(a[4 * v + 1]), __uint_as_float(a[4 * v + 2]),
+                                   __uint_as_float(a[4 * v + 3]));
+                }
+            }
+        }
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ============================================================================ dQ
+
+constexpr uint32_t q_Q = 0;                  // [128 q][128 d]: two 16 KB halves
+constexpr uint32_t q_dO = 32 * KB;
+constexpr uint32_t q_KV = 64 * KB;           // 3 stages x (K 16 KB + V 16 KB), [64 keys][128 d]
+constexpr int q_STAGES = 3;
+constexpr uint32_t q_DS = q_KV + q_STAGES * 32 * KB;   // 2 buffers x [128 q][64 keys] (16 KB)
+constexpr uint32_t q_SMEM = q_DS + 32 * KB + 1024;
+
+struct __align__(8) QBar {
+    uint64_t q_full;
+    uint64_t kv_full[q_STAGES], kv_empty[q_STAGES];
+    uint64_t s_full[2];
+    uint64_t ds_full[2];
+    uint64_t ds_free[2];
+    uint64_t acc_done;
+    uint64_t drain;
+    uint32_t tmem_base;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                BwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ QBar B;
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;        // longest tiles first
+    const int h = blockIdx.y;
+    const int kvh = h / (p.Hq / p.Hkv);
+    const int T = 2 * ((int)(p.q_start / 128) + qt + 1);        // half-page key tiles
+
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&B.q_full, 1);
+        for (int s = 0; s < q_STAGES; ++s) {
+            tc::mbar_init(&B.kv_full[s], 1);
+            tc::mbar_init(&B.kv_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(&B.s_full[s], 1);
+            tc::mbar_init(&B.ds_full[s], 128);
+            tc::mbar_init(&B.ds_free[s], 1);
+        }
+        tc::mbar_init(&B.acc_done, 1);
+        tc::mbar_init(&B.drain, 1);
+        tc::fence_barrier_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(&B.tmem_base, 512);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = B.tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tc::prefetch_tmap(&tm_k);
+            tc::prefetch_tmap(&tm_v);
+            const int q_row0 = qt * 128;
+            tc::mbar_arrive_expect_tx(&B.q_full, 64 * KB);
+            tc::tma_load_3d(smem + q_Q, &tm_q, &B.q_full, 0, h, q_row0);
+            tc::tma_load_3d(smem + q_Q + 16 * KB, &tm_q, &B.q_full, 64, h, q_row0);
+            tc::tma_load_3d(smem + q_dO, &tm_do, &B.q_full, 0, h, q_row0);
+            tc::tma_load_3d(smem + q_dO + 16 * KB, &tm_do, &B.q_full, 64, h, q_row0);
+            int issued = 0;
+            for (int t = 0; t < T; ++t) {
+                const int st = t % q_STAGES;
+                if (t >= q_STAGES && !tc::mbar_wait(&B.kv_empty[st], ((t / q_STAGES) - 1) & 1, p.err))
+                    break;
+                const int32_t pp = p.bt[t >> 1];
+                if (pp < 0 || pp >= p.num_phys) {
+                    report_error(p.err, kErrBadPage);
+                    break;
+                }
+                const int row = (int)(((int64_t)pp * p.Hkv + kvh) * 128 + (t & 1) * 64);
+                uint8_t* kd = smem + q_KV + st * 32 * KB;
+                tc::mbar_arrive_expect_tx(&B.kv_full[st], 32 * KB);
+                tc::tma_load_2d(kd, &tm_k, &B.kv_full[st], 0, row);
+                tc::tma_load_2d(kd + 8 * KB, &tm_k, &B.kv_full[st], 64, row);
+                tc::tma_load_2d(kd + 16 * KB, &tm_v, &B.kv_full[st], 0, row);
+                tc::tma_load_2d(kd + 24 * KB, &tm_v, &B.kv_full[st], 64, row);
+                issued = t + 1;
+            }
+            drain_wait(&B.q_full, 0);
+            for (int t = max(0, issued - q_STAGES); t < issued; ++t)
+                drain_wait(&B.kv_full[t % q_STAGES], (t / q_STAGES) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t id_s = tc::idesc_bf16(128, 64, false, false);    // S = Q K^T
+            const uint32_t id_q = tc::idesc_bf16(128, 128, false, true);    // dQ += dS K
+            const uint32_t sQ = tc::smem_u32(smem + q_Q), sdO = tc::smem_u32(smem + q_dO);
+            const uint32_t t_dQ = tmem + 256;
+            bool ok = tc::mbar_wait(&B.q_full, 0, p.err);
+            auto issue_dq = [&](int t) -> bool {
+                const int b = t & 1, st = t % q_STAGES;
+                if (!tc::mbar_wait(&B.ds_full[b], (t >> 1) & 1, p.err)) return false;
+                tc::tc_fence_after();
+                const uint32_t sDS = tc::smem_u32(smem + q_DS + b * 16 * KB);
+                const uint32_t sK = tc::smem_u32(smem + q_KV + st * 32 * KB);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)      // K = 64 keys, 16 per MMA
+                    tc::mma_bf16(t_dQ, tc::sdesc(sDS + kk * 32, 16, 1024),
+                                 tc::sdesc(sK + kk * 2048, 8 * KB, 1024), id_q,
+                                 (t > 0 || kk > 0) ? 1u : 0u);
+                tc::mma_commit(&B.kv_empty[st]);
+                tc::mma_commit(&B.ds_free[b]);
+                return true;
+            };
+            for (int t = 0; ok && t < T; ++t) {
+                const int st = t % q_STAGES, sb = t & 1;
+                if (!tc::mbar_wait(&B.kv_full[st], (t / q_STAGES) & 1, p.err)) { ok = false; break; }
+                tc::tc_fence_after();
+                const uint32_t sK = tc::smem_u32(smem + q_KV + st * 32 * KB);
+                const uint32_t sV = sK + 16 * KB;
+                const uint32_t t_S = tmem + sb * 128, t_dP = t_S + 64;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t oa = (kk >> 2) * 16 * KB + (kk & 3) * 32;
+                    const uint32_t ob = (kk >> 2) * 8 * KB + (kk & 3) * 32;
+                    tc::mma_bf16(t_S, tc::sdesc(sQ + oa, 16, 1024), tc::sdesc(sK + ob, 16, 1024), id_s,
+                                 kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t oa = (kk >> 2) * 16 * KB + (kk & 3) * 32;
+                    const uint32_t ob = (kk >> 2) * 8 * KB + (kk & 3) * 32;
+                    tc::mma_bf16(t_dP, tc::sdesc(sdO + oa, 16, 1024), tc::sdesc(sV + ob, 16, 1024), id_s,
+                                 kk > 0 ? 1u : 0u);
+                }
+                tc::mma_commit(&B.s_full[sb]);
+                if (t > 0 && !issue_dq(t - 1)) { ok = false; break; }
+            }
+            if (ok && T > 0 && issue_dq(T - 1)) tc::mma_commit(&B.acc_done);
+            tc::mma_commit(&B.drain);
+            drain_wait(&B.drain, 0);
+        }
+    } else {
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;                      // query row of the tile
+        const int64_t q_local = (int64_t)qt * 128 + r;
+        const int64_t qpos = p.q_start + q_local;
+        const bool valid = q_local < p.n_q;
+        const float lse2 = valid ? p.lse[(size_t)h * p.n_q + q_local] * kLog2e : INFINITY;
+        const float Dr = valid ? p.Dbuf[(size_t)h * p.n_q + q_local] : 0.f;
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        const float sl2 = rsqrtf(128.f) * kLog2e;
+        const int64_t first_diag = p.q_start + (int64_t)qt * 128;   // first key of the own page
+        bool ok = true;
+        for (int t = 0; t < T; ++t) {
+            const int sb = t & 1;
+            ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.s_full[sb], (t >> 1) & 1, p.err));
+            if (!ok) break;
+            tc::tc_fence_after();
+            const int64_t kbase = (int64_t)(t >> 1) * 128 + (t & 1) * 64;
+            const bool diag = kbase + 63 > first_diag;
+            uint32_t dw[32];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {           // 32 key columns at a time
+                uint32_t sv[32], dv[32];
+                tc::tmem_ld32(lane_base + sb * 128 + half * 32, sv);
+                tc::tmem_ld32(lane_base + sb * 128 + 64 + half * 32, dv);
+                tc::tmem_wait_ld(sv);
+                tc::tmem_wait_ld(dv);
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    float dr[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int cc = half * 32 + c + e;
+                        float pv = fast_exp2(__uint_as_float(sv[c + e]) * sl2 - lse2);
+                        if (diag && kbase + cc > qpos) pv = 0.f;
+                        dr[e] = pv * (__uint_as_float(dv[c + e]) - Dr);
+                    }
+                    dw[half * 16 + c / 2] = pack_bf16x2(dr[0], dr[1]);
+                }
+            }
+            if (t >= 2) {
+                ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.ds_free[sb], ((t >> 1) - 1) & 1, p.err));
+                if (!ok) break;
+            }
+            store_row_bf16x64(smem + q_DS + sb * 16 * KB, r, dw);
+            tc::fence_proxy_async_smem();
+            tc::tc_fence_before();
+            tc::mbar_arrive(&B.ds_full[sb]);
+        }
+        if (ok && T > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.acc_done, 0, p.err));
+        if (ok && T > 0) {
+            tc::tc_fence_after();
+            const float scale = rsqrtf(128.f);
+            __nv_bfloat16* row = static_cast<__nv_bfloat16*>(p.dq) + ((size_t)q_local * p.Hq + h) * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t a[32];
+                tc::tmem_ld32(lane_base + 256 + c * 32, a);
+                tc::tmem_wait_ld(a);
+                if (valid) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(a[8 * v + 0]) * scale, __uint_as_float(a[8 * v + 1]) * scale);
+                        w.y = pack_bf16x2(__uint_as_float(a[8 * v + 2]) * scale, __uint_as_float(a[8 * v + 3]) * scale);
+                        w.z = pack_bf16x2(__uint_as_float(a[8 * v + 4]) * scale, __uint_as_float(a[8 * v + 5]) * scale);
+                        w.w = pack_bf16x2(__uint_as_float(a[8 * v + 6]) * scale, __uint_as_float(a[8 * v + 7]) * scale);
+                        *reinterpret_cast<uint4*>(row + c * 32 + v * 8) = w;
+                    }
+                }
+            }
+        }
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
+    if (a.sel) return launch_attn_bwd_simt(a, s);   // sparse backward: CUDA-core kernels for now
+    if ((reinterpret_cast<uintptr_t>(a.dout) & 15) || !a.tmap_k64) return cudaErrorInvalidValue;
+    CUtensorMap tq64, tdo64, tq128, tdo128;
+    std::string why;
+    const uint64_t s2 = (uint64_t)a.Hq * 256;
+    if (!make_tmap_3d(&tq64, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, a.Hq, a.n_q, 256, s2, 64, 1, 64, &why) ||
+        !make_tmap_3d(&tdo64, a.dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, a.Hq, a.n_q, 256, s2, 64, 1, 64, &why) ||
+        !make_tmap_3d(&tq128, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, a.Hq, a.n_q, 256, s2, 64, 1, 128, &why) ||
+        !make_tmap_3d(&tdo128, a.dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, a.Hq, a.n_q, 256, s2, 64, 1, 128, &why))
+        return cudaErrorInvalidValue;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(bwd_kv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kv_SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(bwd_q_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)q_SMEM);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    BwdParams p{};
+    p.Hq = a.Hq; p.Hkv = a.Hkv; p.q_start = a.q_start; p.n_q = a.n_q;
+    p.lse = a.lse_in; p.Dbuf = a.Dbuf; p.dq = a.dq; p.dkpool = a.dkpool; p.dvpool = a.dvpool;
+    p.bt = a.bt; p.num_phys = a.num_phys; p.err = a.err;
+    const int64_t n_keys = a.q_start + a.n_q;
+    dim3 g_kv((unsigned)((n_keys + 127) / 128), a.Hkv);
+    bwd_kv_tc_kernel<<<g_kv, kThreads, kv_SMEM, s>>>(tq64, tdo64, *a.tmap_k, *a.tmap_v, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dim3 g_q((unsigned)((a.n_q + 127) / 128), a.Hq);
+    bwd_q_tc_kernel<<<g_q, kThreads, q_SMEM, s>>>(tq128, tdo128, *a.tmap_k64, *a.tmap_v64, p);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -77,15 +77,7 @@ __device__ __forceinline__ int32_t tile_page(const FwdParams& p, int qt, int kvh
     return p.sel ? p.sel[((size_t)qt * p.Hkv + kvh) * p.kmax + j] : j;
 }
 
-// Bounded wait that ignores errors recorded elsewhere: used only to drain
-// this CTA's own copies and MMAs before it exits.
-__device__ bool drain_wait(uint64_t* bar, uint32_t parity) {
-    const uint32_t addr = tc::smem_u32(bar);
-    const uint64_t t0 = tc::globaltimer();
-    while (!tc::mbar_try_wait(addr, parity))
-        if (tc::globaltimer() - t0 > 1000000000ull) return false;
-    return true;
-}
+using tc::drain_wait;
 
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -354,11 +346,6 @@ cudaError_t launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t s) {
     dim3 grid((unsigned)((a.n_q + kTile - 1) / kTile), a.Hq);
     fwd_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, *a.tmap_k, *a.tmap_v, p);
     return cudaGetLastError();
-}
-
-cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
-    // The tensor-core backward is not built yet: use the CUDA-core kernels.
-    return launch_attn_bwd_simt(a, s);
 }
 
 }  // namespace pkv

@@ -29,8 +29,9 @@ struct pkv_pool {
     // Scratch (bwd row statistics D = rowsum(dO * O)), grown on demand.
     float* scratch = nullptr;
     size_t scratch_floats = 0;
-    // TMA descriptors over the K and V page pools (2-D: rows x d).
-    CUtensorMap tmap_k{}, tmap_v{};
+    // TMA descriptors over the K and V page pools (2-D: rows x d), with boxes
+    // of 64 columns x 128 rows (whole pages) and 64 x 64 (half pages).
+    CUtensorMap tmap_k{}, tmap_v{}, tmap_k64{}, tmap_v64{};
     bool tmaps_ready = false;
 };
 
@@ -91,8 +92,10 @@ struct AttnArgs {
     const int32_t* sel;              // sparse: [n_qp, Hkv, kmax] or null
     int kmax;
     int* err;
-    const CUtensorMap* tmap_k;       // tensor-core path only
+    const CUtensorMap* tmap_k;       // tensor-core path only: whole-page boxes
     const CUtensorMap* tmap_v;
+    const CUtensorMap* tmap_k64;     // half-page boxes
+    const CUtensorMap* tmap_v64;
 };
 
 cudaError_t launch_attn_fwd_simt(const AttnArgs& a, cudaStream_t s);

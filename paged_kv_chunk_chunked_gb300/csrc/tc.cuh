@@ -80,6 +80,16 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, in
     }
 }
 
+// Bounded wait (1 s) that ignores errors recorded elsewhere: used only to
+// drain a CTA's own copies and MMAs before it exits.
+static __device__ __noinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
+    const uint32_t addr = smem_u32(bar);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(addr, parity))
+        if (globaltimer() - t0 > 1000000000ull) return false;
+    return true;
+}
+
 // Generic-proxy writes to shared memory -> visible to the async proxy.
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
