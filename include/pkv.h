@@ -201,6 +201,23 @@ pkv_status pkv_chunk_attn_bwd(pkv_seq* seq, const void* q, const void* o, const 
                               const float* lse, int64_t q_start, int64_t n_q, void* dq,
                               const pkv_sel* sel, void* stream);
 
+/* pkv_chunk_attn_bwd without any allocation. Same arguments, outputs and
+ * results as pkv_chunk_attn_bwd; the paper has no counterpart: it exists for
+ * callers that cannot let the library allocate device memory at call time
+ * (a fixed memory budget, an allocator that owns all device memory, code that
+ * must not synchronize the device, loops that forbid allocation after
+ * start-up). The per-row scratch lives in one fixed array of 262144 floats
+ * (1 MiB) in the library's device image, held on every device that loads the
+ * library until exit; a call needs n_q_heads * n_q floats and is rejected
+ * with PKV_ERR_INVALID above that. The first call on a device looks up the
+ * array's device address (no allocation) and should come before any stream
+ * capture. All calls share the array: calls that overlap on the GPU race and
+ * must be serialised by the caller. Each call rewrites what it reads, so
+ * nothing needs clearing between calls. */
+pkv_status pkv_chunk_attn_bwd_noalloc(pkv_seq* seq, const void* q, const void* o,
+                                      const void* dout, const float* lse, int64_t q_start,
+                                      int64_t n_q, void* dq, const pkv_sel* sel, void* stream);
+
 /* Zeroes the gradient pages of the sequence's pages. */
 pkv_status pkv_grad_zero(pkv_seq* seq, void* stream);
 

@@ -64,6 +64,8 @@ _SIGS = {
     "pkv_append": (_ST, [_P, _P, _P, _I64, _P]),
     "pkv_chunk_attn_fwd": (_ST, [_P, _P, _I64, _I64, _P, _P, ctypes.POINTER(pkv_sel), _P]),
     "pkv_chunk_attn_bwd": (_ST, [_P, _P, _P, _P, _P, _I64, _I64, _P, ctypes.POINTER(pkv_sel), _P]),
+    "pkv_chunk_attn_bwd_noalloc": (_ST, [_P, _P, _P, _P, _P, _I64, _I64, _P,
+                                         ctypes.POINTER(pkv_sel), _P]),
     "pkv_grad_zero": (_ST, [_P, _P]),
     "pkv_gather": (_ST, [_P, _P, _P, _P, _P, _P, _P]),
     "pkv_page_topk": (_ST, [_P, _P, _I64, _I64, _I32, _I32, _I32, _P, _P, _P]),
@@ -210,6 +212,14 @@ def pkv_chunk_attn_fwd(seq, q, q_start, n_q, o, lse, sel=None, stream=None) -> N
 def pkv_chunk_attn_bwd(seq, q, o, dout, lse, q_start, n_q, dq, sel=None, stream=None) -> None:
     _check(lib().pkv_chunk_attn_bwd(seq, ptr(q), ptr(o), ptr(dout), ptr(lse), q_start, n_q,
                                     ptr(dq), _sel(sel), stream_ptr(stream)))
+
+
+def pkv_chunk_attn_bwd_noalloc(seq, q, o, dout, lse, q_start, n_q, dq, sel=None,
+                               stream=None) -> None:
+    """Same as pkv_chunk_attn_bwd, with the library's fixed device scratch instead
+    of an allocation (for callers that cannot allocate at call time)."""
+    _check(lib().pkv_chunk_attn_bwd_noalloc(seq, ptr(q), ptr(o), ptr(dout), ptr(lse), q_start,
+                                            n_q, ptr(dq), _sel(sel), stream_ptr(stream)))
 
 
 def pkv_grad_zero(seq, stream=None) -> None:
