@@ -244,11 +244,14 @@ def run_pkv(args, world, rank):
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     t0, t1 = ev(), ev()
+    B.pkv_profile_enable(True)
     t0.record(stream)
     for k in range(args.steps):
         step(k)
     t1.record(stream)
     torch.cuda.synchronize()
+    prof = B.pkv_profile_collect()
+    B.pkv_profile_enable(False)
     fwd_ms = [sum(a.elapsed_time(b) for a, b in fwd_ev[k]) for k in range(args.steps)]
     bwd_ms = [sum(a.elapsed_time(b) for a, b in bwd_ev[k]) for k in range(args.steps)]
     clk = clocks.stop()
@@ -263,24 +266,35 @@ def run_pkv(args, world, rank):
     peak_tc = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
     fwd_call = statistics.mean(fwd_ms) / n
     bwd_call = statistics.mean(bwd_ms) / n
-    # the fwd call is one kernel launch; per-launch algorithmic FLOPs averaged over the chunks
     fwd_ach = flops_fwd / n / (fwd_call * 1e-3) / 1e12
     bwd_ach = flops_bwd / n / (bwd_call * 1e-3) / 1e12
-    tc_bwd = False
-    dominant = "bwd" if bwd_call > fwd_call else "fwd"
+    # Per-kernel device time from the library's event pairs (launching stream).
+    # Algorithmic FLOPs attributed per kernel: forward 4 (S, PV); the backward's
+    # 10 split as dK/dV kernel 8 (S^T, dP^T, dV, dK) and dQ kernel 2 (dQ; its
+    # recomputed S and dP are not counted again) -- times Hq * d * pairs.
+    per_step = {"fwd_tc_kernel": 4, "bwd_kv_tc_kernel": 8, "bwd_q_tc_kernel": 2,
+                "fwd_simt": 4, "bwd_dkdv_simt": 8, "bwd_dq_simt": 2}
+    sources = {"fwd_tc_kernel": "paged_kv_chunk_chunked_gb300/csrc/attn_tc_fwd.cu",
+               "bwd_kv_tc_kernel": "paged_kv_chunk_chunked_gb300/csrc/attn_tc_bwd.cu",
+               "bwd_q_tc_kernel": "paged_kv_chunk_chunked_gb300/csrc/attn_tc_bwd.cu"}
+    total_prof = sum(v[1] for v in prof.values()) or 1.0
+    kernels = {name: {"launches": cnt, "ms_per_step": round(ms / args.steps, 3),
+                      "share": round(ms / total_prof, 4)} for name, (cnt, ms) in prof.items()}
+    dom = max(prof, key=lambda k: prof[k][1])
+    dom_cnt, dom_ms = prof[dom]
     roof = {
         "bound": "tensor", "unit": "TFLOP/s", "peak": peak_tc,
         "peak_kind": f"{pk_kind} bf16_tflops_sustained (kernels timed inside a long step)",
+        "kernel": dom,
     }
-    if dominant == "fwd":
-        roof.update(kernel="fwd_tc_kernel", achieved=round(fwd_ach, 2),
-                    frac=round(fwd_ach / peak_tc, 4),
-                    traffic=traffic_for("fwd_tc_kernel",
-                                        "paged_kv_chunk_chunked_gb300/csrc/attn_tc_fwd.cu"))
-    else:
-        roof.update(kernel="pkv_chunk_attn_bwd (all its kernels)", achieved=round(bwd_ach, 2),
-                    frac=round(bwd_ach / peak_tc, 4), traffic=None)
-    launches_per_step = n + n + 3 * n       # append, fwd, bwd (row-dot + dQ + dK/dV)
+    if dom in per_step:
+        ach = per_step[dom] * w.Hq * w.d * pairs_dense(w.N) * args.steps / (dom_ms * 1e-3) / 1e12
+        src = sources.get(dom)
+        roof.update(achieved=round(ach, 2), frac=round(ach / peak_tc, 4),
+                    flops_per_launch=per_step[dom] * w.Hq * w.d * pairs_dense(w.N) * args.steps / dom_cnt,
+                    ms_per_launch=round(dom_ms / dom_cnt, 4),
+                    traffic=traffic_for(dom, src) if src else None)
+    gpu_launches = sum(v[0] for v in prof.values())
 
     out = {
         "metric": METRIC, "value": round(tflops, 3), "unit": UNIT, "n_gpus": world,
@@ -296,7 +310,8 @@ def run_pkv(args, world, rank):
         "bwd_ms_per_step": round(statistics.mean(bwd_ms), 3),
         "fwd_tflops": round(fwd_ach, 2), "bwd_tflops": round(bwd_ach, 2),
         "roofline": roof,
-        "gpu_launches": launches_per_step * args.steps,
+        "kernels": kernels,
+        "gpu_launches": gpu_launches,
         "clocks": clk,
     }
 

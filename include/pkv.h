@@ -255,6 +255,18 @@ pkv_status pkv_prefetch(pkv_seq* seq, const int32_t* logical_pages, int64_t n, v
 pkv_status pkv_writeback_grads(pkv_seq* seq, void* side);
 pkv_status pkv_wait(pkv_seq* seq, void* main, int64_t timeout_us);
 
+/* ---------------------------------------------------------------- profiling
+ * Per-kernel device time, for benchmarks. pkv_profile_enable(1) clears old
+ * records and makes every later kernel launch record a CUDA event pair on its
+ * stream; pkv_profile_enable(0) stops recording. pkv_profile_collect waits for
+ * the recorded events, writes up to max_kernels entries in order of first
+ * launch -- names (64-byte NUL-terminated slots), summed milliseconds, launch
+ * counts -- sets *n_kernels to the number of distinct kernels, and clears the
+ * records. */
+pkv_status pkv_profile_enable(int32_t on);
+pkv_status pkv_profile_collect(int32_t max_kernels, char* names, double* total_ms,
+                               int64_t* launches, int32_t* n_kernels);
+
 /* ---------------------------------------------------------------- self-test
  * Runs one 128x128x64 bf16 tensor-core product (tcgen05, fp32 accumulator
  * in tensor memory) with the shared-memory operand layouts the attention

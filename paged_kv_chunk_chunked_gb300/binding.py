@@ -73,6 +73,8 @@ _SIGS = {
     "pkv_writeback_grads": (_ST, [_P, _P]),
     "pkv_wait": (_ST, [_P, _P, _I64]),
     "pkv_selftest_umma": (_ST, [_I32, _P, _P, _P, _I32, _I32]),
+    "pkv_profile_enable": (_ST, [_I32]),
+    "pkv_profile_collect": (_ST, [_I32, _P, _P, _P, ctypes.POINTER(_I32)]),
 }
 EXPORTED = tuple(_SIGS)
 
@@ -246,6 +248,25 @@ def pkv_writeback_grads(seq, side=None) -> None:
 
 def pkv_wait(seq, main=None, timeout_us=10_000_000) -> None:
     _check(lib().pkv_wait(seq, stream_ptr(main), timeout_us))
+
+
+def pkv_profile_enable(on: bool) -> None:
+    _check(lib().pkv_profile_enable(1 if on else 0))
+
+
+def pkv_profile_collect(max_kernels: int = 64) -> dict:
+    """{kernel name: (launches, total device ms)} since profiling was enabled."""
+    names = ctypes.create_string_buffer(64 * max_kernels)
+    ms = (ctypes.c_double * max_kernels)()
+    cnt = (ctypes.c_int64 * max_kernels)()
+    n = _I32()
+    _check(lib().pkv_profile_collect(max_kernels, ctypes.cast(names, _P), ctypes.cast(ms, _P),
+                                     ctypes.cast(cnt, _P), ctypes.byref(n)))
+    out = {}
+    for k in range(min(n.value, max_kernels)):
+        name = names.raw[64 * k: 64 * k + 64].split(b"\0", 1)[0].decode()
+        out[name] = (int(cnt[k]), float(ms[k]))
+    return out
 
 
 def pkv_selftest_umma(mode, a, b, d, lbo=0, sbo=0) -> None:

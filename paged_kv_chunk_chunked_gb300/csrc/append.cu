@@ -147,6 +147,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const T* kpool, const 
 
 template <typename T>
 cudaError_t append_dispatch_d(const AppendArgs& a, cudaStream_t s, dim3 grid) {
+    ProfScope ps("append_kernel", s);
     if (a.d == 128) append_kernel<T, 128><<<grid, kThreads, 0, s>>>(a);
     else append_kernel<T, 64><<<grid, kThreads, 0, s>>>(a);
     return cudaGetLastError();
@@ -161,6 +162,7 @@ cudaError_t gather_dispatch(const pkv_pool* p, const int32_t* bt, int64_t len, v
     static_cast<const T*>(p->k), static_cast<const T*>(p->v), p->dk, p->dv, p->rep, bt,     \
         p->desc.num_phys_pages, P, Hkv, len, static_cast<T*>(k), static_cast<T*>(v), dk, dv, \
         rep, p->d_err
+    ProfScope ps("gather_kernel", s);
     if (p->desc.head_dim == 128) gather_kernel<T, 128><<<grid, kThreads, 0, s>>>(PKV_GATHER_ARGS);
     else gather_kernel<T, 64><<<grid, kThreads, 0, s>>>(PKV_GATHER_ARGS);
 #undef PKV_GATHER_ARGS
@@ -181,6 +183,7 @@ cudaError_t launch_grad_zero(const pkv_pool* p, const int32_t* d_bt, int64_t p0,
                              cudaStream_t s) {
     if (p1 <= p0) return cudaSuccess;
     dim3 grid((unsigned)(p1 - p0), p->desc.n_kv_heads);
+    ProfScope ps("grad_zero_kernel", s);
     grad_zero_kernel<<<grid, kThreads, 0, s>>>(p->dk, p->dv, d_bt, p0, p->desc.num_phys_pages,
                                                p->desc.n_kv_heads,
                                                p->desc.page_size * p->desc.head_dim, p->d_err);

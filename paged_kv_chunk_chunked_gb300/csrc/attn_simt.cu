@@ -309,6 +309,7 @@ __global__ void rowdot_kernel(AttnArgs a) {
 template <typename T, int D>
 cudaError_t fwd_launch(const AttnArgs& a, cudaStream_t s) {
     dim3 grid((unsigned)((a.n_q + BM - 1) / BM), a.Hq);
+    ProfScope ps("fwd_simt", s);
     fwd_simt<T, D><<<grid, NT, 0, s>>>(a);
     return cudaGetLastError();
 }
@@ -316,11 +317,15 @@ cudaError_t fwd_launch(const AttnArgs& a, cudaStream_t s) {
 template <typename T, int D>
 cudaError_t bwd_launch(const AttnArgs& a, cudaStream_t s) {
     dim3 g1((unsigned)((a.n_q + BM - 1) / BM), a.Hq);
-    bwd_dq_simt<T, D><<<g1, NT, 0, s>>>(a);
+    {
+        ProfScope ps("bwd_dq_simt", s);
+        bwd_dq_simt<T, D><<<g1, NT, 0, s>>>(a);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t n_keys = a.q_start + a.n_q;
     dim3 g2((unsigned)((n_keys + BN - 1) / BN), a.Hkv);
+    ProfScope ps("bwd_dkdv_simt", s);
     bwd_dkdv_simt<T, D><<<g2, NT, 0, s>>>(a);
     return cudaGetLastError();
 }
@@ -346,6 +351,7 @@ cudaError_t launch_bwd_rowdot(const AttnArgs& a, cudaStream_t s) {
     const int vpr = a.d * (a.dtype == PKV_BF16 ? 2 : 4) / 16;
     const int threads = 256;
     const int64_t blocks = (rows * vpr + threads - 1) / threads;
+    ProfScope ps("rowdot_kernel", s);
     if (a.dtype == PKV_BF16) {
         if (a.d == 128) rowdot_kernel<__nv_bfloat16, 128><<<(unsigned)blocks, threads, 0, s>>>(a);
         else rowdot_kernel<__nv_bfloat16, 64><<<(unsigned)blocks, threads, 0, s>>>(a);

@@ -580,10 +580,14 @@ cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
     p.bt = a.bt; p.num_phys = a.num_phys; p.err = a.err;
     const int64_t n_keys = a.q_start + a.n_q;
     dim3 g_kv((unsigned)((n_keys + 127) / 128), a.Hkv);
-    bwd_kv_tc_kernel<<<g_kv, kThreads, kv_SMEM, s>>>(tq64, tdo64, *a.tmap_k, *a.tmap_v, p);
+    {
+        ProfScope ps("bwd_kv_tc_kernel", s);
+        bwd_kv_tc_kernel<<<g_kv, kThreads, kv_SMEM, s>>>(tq64, tdo64, *a.tmap_k, *a.tmap_v, p);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dim3 g_q((unsigned)((a.n_q + 127) / 128), a.Hq);
+    ProfScope ps("bwd_q_tc_kernel", s);
     bwd_q_tc_kernel<<<g_q, kThreads, q_SMEM, s>>>(tq128, tdo128, *a.tmap_k64, *a.tmap_v64, p);
     return cudaGetLastError();
 }

@@ -344,6 +344,7 @@ cudaError_t launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t s) {
     p.o = a.o; p.lse = a.lse; p.bt = a.bt; p.num_phys = a.num_phys;
     p.sel = a.sel; p.kmax = a.kmax; p.err = a.err;
     dim3 grid((unsigned)((a.n_q + kTile - 1) / kTile), a.Hq);
+    ProfScope ps("fwd_tc_kernel", s);
     fwd_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, *a.tmap_k, *a.tmap_v, p);
     return cudaGetLastError();
 }

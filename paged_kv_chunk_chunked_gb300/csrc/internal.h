@@ -46,6 +46,19 @@ struct pkv_seq {
 
 namespace pkv {
 
+// Brackets one kernel launch with CUDA events on its stream while profiling
+// is enabled (pkv_profile_enable); a no-op otherwise.
+struct ProfScope {
+    ProfScope(const char* name, cudaStream_t s);
+    ~ProfScope();
+    ProfScope(const ProfScope&) = delete;
+    ProfScope& operator=(const ProfScope&) = delete;
+    const char* name;
+    cudaStream_t s;
+    cudaEvent_t a = nullptr, b = nullptr;
+    bool active = false;
+};
+
 // Sets the thread's last-error message and returns the status.
 pkv_status fail(pkv_status s, const std::string& msg);
 pkv_status cuda_fail(cudaError_t e, const char* what);
