@@ -276,7 +276,7 @@ void pkv_pool_destroy(pkv_pool* p) {
     for (pkv_seq* s : seqs) pkv_seq_free(s);
     if (is_device(p)) {
         cudaFree(p->k); cudaFree(p->v); cudaFree(p->dk); cudaFree(p->dv);
-        cudaFree(p->rep); cudaFree(p->d_err); cudaFree(p->scratch);
+        cudaFree(p->rep); cudaFree(p->d_err); cudaFree(p->scratch); cudaFree(p->sel_scratch);
     }
     delete p;
 }
@@ -525,9 +525,38 @@ pkv_status pkv_gather(const pkv_seq* s, void* k, void* v, float* dk, float* dv, 
 pkv_status pkv_page_topk(pkv_seq* s, const void* q, int64_t q_start, int64_t n_q, int32_t k,
                          int32_t n_sink, int32_t n_local, int32_t* pages_out,
                          int32_t* counts_out, void* stream) {
-    (void)s; (void)q; (void)q_start; (void)n_q; (void)k; (void)n_sink; (void)n_local;
-    (void)pages_out; (void)counts_out; (void)stream;
-    return fail(PKV_ERR_UNSUPPORTED, "pkv_page_topk: not built yet");
+    if (!s || !q || !pages_out) return fail(PKV_ERR_INVALID, "pkv_page_topk: NULL argument");
+    pkv_pool* p = s->pool;
+    if (!is_device(p)) return fail(PKV_ERR_INVALID, "pkv_page_topk: META pool");
+    const int64_t P = p->desc.page_size;
+    if (n_q <= 0 || q_start < 0 || q_start % P != 0 || q_start + n_q > s->len)
+        return fail(PKV_ERR_INVALID, "pkv_page_topk: need q_start % P == 0 and q_start + n_q <= length");
+    if (k < 0 || n_sink < 0 || n_local < 1)
+        return fail(PKV_ERR_INVALID, "pkv_page_topk: need k >= 0, n_sink >= 0, n_local >= 1 "
+                                     "(the query page itself is always visible)");
+    const int64_t n_qp = (n_q + P - 1) / P;
+    const int64_t last_qpg = q_start / P + n_qp - 1;
+    if (last_qpg - n_local - n_sink + 1 > page_topk_max_candidates())
+        return fail(PKV_ERR_UNSUPPORTED, "pkv_page_topk: more than " +
+                                             std::to_string(page_topk_max_candidates()) +
+                                             " candidate pages");
+    pkv_status st = check_stream_device(p);
+    if (st != PKV_OK) return st;
+    const size_t need = (size_t)n_qp * p->desc.n_kv_heads * p->desc.head_dim;
+    if (p->sel_scratch_floats < need) {
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "pkv_page_topk: sync");
+        cudaFree(p->sel_scratch);
+        p->sel_scratch = nullptr;
+        p->sel_scratch_floats = 0;
+        e = cudaMalloc(reinterpret_cast<void**>(&p->sel_scratch), need * sizeof(float));
+        if (e != cudaSuccess) return cuda_fail(e, "pkv_page_topk: scratch");
+        p->sel_scratch_floats = need;
+    }
+    cudaError_t e = launch_page_topk(p, s->d_bt, q, q_start, n_q, k, n_sink, n_local, pages_out,
+                                     counts_out, p->sel_scratch, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_page_topk: launch");
+    return PKV_OK;
 }
 
 pkv_status pkv_prefetch(pkv_seq* s, const int32_t* pages, int64_t n, void* side) {

@@ -49,8 +49,20 @@ struct BwdParams {
     float* dvpool;
     const int32_t* bt;
     int64_t num_phys;
+    const int32_t* sel;        // sparse: [n_qp, Hkv, kmax] selected pages, or null
+    int kmax;
     int* err;
 };
+
+constexpr int kMaxSelQp = 256;   // query pages per chunk the sparse dK/dV kernel can list
+
+// Number of listed pages of (query page qp, KV head kvh): ascending, -1 padded.
+__device__ __forceinline__ int sel_count(const BwdParams& p, int qp, int kvh) {
+    const int32_t* row = p.sel + ((size_t)qp * p.Hkv + kvh) * p.kmax;
+    int n = 0;
+    while (n < p.kmax && row[n] >= 0) ++n;
+    return n;
+}
 
 __device__ __forceinline__ void store_row_bf16x64(uint8_t* tile, int row, const uint32_t (&w)[32]) {
     // 64 bf16 (32 words) of one row of a [rows][64] tile with the 128-byte swizzle.
@@ -81,6 +93,9 @@ struct __align__(8) KVBar {
     uint64_t acc_done;
     uint64_t drain;
     uint32_t tmem_base;
+    int n_i;                         // 64-query tiles per head
+    int16_t tiles[2 * kMaxSelQp];    // sparse: the tiles, ascending
+    uint8_t sel_flag[kMaxSelQp];
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -100,10 +115,34 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int64_t kfirst = (int64_t)j * 128;
     const int n_qt = (int)((p.n_q + 63) / 64);
     const int i0 = kfirst > p.q_start ? (int)((kfirst - p.q_start) / 64) : 0;
-    const int n_i = n_qt - i0;
-    const int T = n_i * g;                           // iterations: (head, 64-query tile)
     const int32_t pp = p.bt[j];
     const bool page_ok = pp >= 0 && pp < p.num_phys;
+    // Query tiles that see this page: dense, every tile from i0 on; sparse, the
+    // two 64-query halves of every query page whose selection lists page j.
+    if (p.sel) {
+        const int n_qp = (int)((p.n_q + 127) / 128);
+        for (int qp = threadIdx.x; qp < n_qp; qp += kThreads) {
+            const int32_t* srow = p.sel + ((size_t)qp * p.Hkv + kvh) * p.kmax;
+            uint8_t f = 0;
+            for (int e = 0; e < p.kmax; ++e) {
+                const int32_t x = srow[e];
+                if (x == j) { f = 1; break; }
+                if (x < 0 || x > j) break;
+            }
+            B.sel_flag[qp] = f;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int n = 0;
+            for (int qp = 0; qp < n_qp; ++qp)
+                if (B.sel_flag[qp])
+                    for (int hf = 0; hf < 2; ++hf)
+                        if (2 * qp + hf < n_qt) B.tiles[n++] = (int16_t)(2 * qp + hf);
+            B.n_i = n;
+        }
+    } else if (threadIdx.x == 0) {
+        B.n_i = n_qt - i0;
+    }
 
     if (threadIdx.x == 0) {
         tc::mbar_init(&B.kv_full, 1);
@@ -127,8 +166,11 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = B.tmem_base;
+    const int n_i = B.n_i;
+    const int T = n_i * g;                           // iterations: (head, 64-query tile)
+    auto tile_of = [&](int t) -> int { return p.sel ? (int)B.tiles[t % n_i] : i0 + t % n_i; };
 
-    if (!page_ok) {
+    if (!page_ok || T == 0) {
         // nothing issued: fall through to the common exit
     } else if (warp == 0) {
         // ---------------------------------------------------------------- producer
@@ -150,7 +192,7 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (!__all_sync(0xffffffffu, ok)) break;
             }
             const int h = kvh * g + t / n_i;
-            const int i = i0 + t % n_i;
+            const int i = tile_of(t);
             // per-query statistics for this tile: log2e * LSE (+inf past the chunk) and D
             float* sst = stat + st * 128;
 #pragma unroll
@@ -251,7 +293,7 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc::tc_fence_after();
-            const int i = i0 + t % n_i;
+            const int i = tile_of(t);
             const int64_t q0 = p.q_start + (int64_t)i * 64;  // position of column 0
             const bool diag = kfirst + 127 > q0;
             const float* sst = stat + st * 128;
@@ -361,7 +403,10 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;        // longest tiles first
     const int h = blockIdx.y;
     const int kvh = h / (p.Hq / p.Hkv);
-    const int T = 2 * ((int)(p.q_start / 128) + qt + 1);        // half-page key tiles
+    // Half-page key tiles: two per visible page (dense: pages 0..own; sparse: listed pages).
+    const int T = 2 * (p.sel ? sel_count(p, qt, kvh) : (int)(p.q_start / 128) + qt + 1);
+    const int32_t* sel_row = p.sel ? p.sel + ((size_t)qt * p.Hkv + kvh) * p.kmax : nullptr;
+    auto page_of = [&](int t) -> int32_t { return sel_row ? sel_row[t >> 1] : (t >> 1); };
 
     if (threadIdx.x == 0) {
         tc::mbar_init(&B.q_full, 1);
@@ -402,7 +447,8 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const int st = t % q_STAGES;
                 if (t >= q_STAGES && !tc::mbar_wait(&B.kv_empty[st], ((t / q_STAGES) - 1) & 1, p.err))
                     break;
-                const int32_t pp = p.bt[t >> 1];
+                const int32_t lp = page_of(t);
+                const int32_t pp = lp >= 0 ? p.bt[lp] : -1;
                 if (pp < 0 || pp >= p.num_phys) {
                     report_error(p.err, kErrBadPage);
                     break;
@@ -487,7 +533,7 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.s_full[sb], (t >> 1) & 1, p.err));
             if (!ok) break;
             tc::tc_fence_after();
-            const int64_t kbase = (int64_t)(t >> 1) * 128 + (t & 1) * 64;
+            const int64_t kbase = (int64_t)page_of(t) * 128 + (t & 1) * 64;
             const bool diag = kbase + 63 > first_diag;
             uint32_t dw[32];
 #pragma unroll
@@ -555,7 +601,8 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 }  // namespace
 
 cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
-    if (a.sel) return launch_attn_bwd_simt(a, s);   // sparse backward: CUDA-core kernels for now
+    // The sparse dK/dV kernel lists the selecting query pages in shared memory.
+    if (a.sel && (a.n_q + 127) / 128 > kMaxSelQp) return launch_attn_bwd_simt(a, s);
     if ((reinterpret_cast<uintptr_t>(a.dout) & 15) || !a.tmap_k64) return cudaErrorInvalidValue;
     CUtensorMap tq64, tdo64, tq128, tdo128;
     std::string why;
@@ -578,6 +625,7 @@ cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
     p.Hq = a.Hq; p.Hkv = a.Hkv; p.q_start = a.q_start; p.n_q = a.n_q;
     p.lse = a.lse_in; p.Dbuf = a.Dbuf; p.dq = a.dq; p.dkpool = a.dkpool; p.dvpool = a.dvpool;
     p.bt = a.bt; p.num_phys = a.num_phys; p.err = a.err;
+    p.sel = a.sel; p.kmax = a.kmax;
     const int64_t n_keys = a.q_start + a.n_q;
     dim3 g_kv((unsigned)((n_keys + 127) / 128), a.Hkv);
     {

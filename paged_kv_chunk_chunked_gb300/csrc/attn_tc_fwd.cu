@@ -247,8 +247,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
                 const float p0 = fast_exp2(x[2 * c] - m), p1 = fast_exp2(x[2 * c + 1] - m);
-                ls += p0 + p1;
                 pk[c] = pack_bf16x2(p0, p1);
+                // Normalise by the sum of the bf16 weights the tensor core multiplies, so
+                // O is a convex combination of values whatever the rounding of P.
+                ls += bf16lo(pk[c]) + bf16hi(pk[c]);
             }
             l += ls;
             if (j > 0) {                              // PV_{j-1} done: P buffer free, O stable

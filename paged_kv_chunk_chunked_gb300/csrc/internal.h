@@ -29,6 +29,9 @@ struct pkv_pool {
     // Scratch (bwd row statistics D = rowsum(dO * O)), grown on demand.
     float* scratch = nullptr;
     size_t scratch_floats = 0;
+    // Scratch of the page selection (page queries qbar [n_qp, Hkv, d]).
+    float* sel_scratch = nullptr;
+    size_t sel_scratch_floats = 0;
     // TMA descriptors over the K and V page pools (2-D: rows x d), with boxes
     // of 64 columns x 128 rows (whole pages) and 64 x 64 (half pages).
     CUtensorMap tmap_k{}, tmap_v{}, tmap_k64{}, tmap_v64{};
@@ -114,6 +117,11 @@ struct AttnArgs {
 cudaError_t launch_attn_fwd_simt(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_attn_bwd_simt(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_rowdot(const AttnArgs& a, cudaStream_t s);
+
+cudaError_t launch_page_topk(const pkv_pool* p, const int32_t* d_bt, const void* q,
+                             int64_t q_start, int64_t n_q, int K, int n_sink, int n_local,
+                             int32_t* out, int32_t* counts, float* qbar, cudaStream_t s);
+int64_t page_topk_max_candidates();
 
 bool tc_supported(const AttnArgs& a);
 cudaError_t launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t s);

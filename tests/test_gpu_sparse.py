@@ -1,0 +1,186 @@
+"""GPU parity of the page-sparse path against the oracle, through the C ABI.
+
+- pkv_page_topk: selected page sets equal the oracle's, except where a differing
+  page's oracle score lies within 1e-5 of the K-th score (ties in fp32 vs fp64);
+- sparse forward/backward: given the oracle's selection, O and LSE within
+  max-abs 1e-2 (bf16) / 1e-4 (fp32), dQ/dK/dV within relative Frobenius
+  2e-2 / 1e-4;
+- the whole sparse sweep with the GPU's own selection.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_chunk_chunked_gb300 import binding as B
+from paged_kv_chunk_chunked_gb300 import build as pkv_build
+from paged_kv_chunk_chunked_gb300 import synth
+from paged_kv_chunk_chunked_gb300.sweep import ChunkSweep, to_numpy
+
+pytestmark = pytest.mark.gpu
+TOL = {"bf16": (1e-2, 2e-2), "f32": (1e-4, 1e-4)}
+TIE = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    pkv_build.build()
+    B.lib()
+    torch.cuda.set_device(0)
+
+
+def _rel(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def _w(**kw):
+    base = dict(N=2048, C=1024, P=128, Hq=4, Hkv=2, d=128, dtype="bf16", table="perm",
+                keys="clustered", extra_pages=3, topk=(3, 1, 2))
+    base.update(kw)
+    return synth.workload("qwen7b_sparse_256k", **base)
+
+
+def _inputs(w):
+    n = w.n_chunks
+    return ([synth.chunk_q(w, c) for c in range(n)], [synth.chunk_k(w, c) for c in range(n)],
+            [synth.chunk_v(w, c) for c in range(n)], [synth.chunk_do(w, c) for c in range(n)])
+
+
+def _check_selection(sel_gpu, q, q_start, k_logical, P, K, n_sink, n_local):
+    """Compare against the oracle with the tie rule; returns the number of tie mismatches."""
+    lists, padded = oracle.chunk_selection(q, q_start, k_logical, P, K, n_sink, n_local)
+    qbar = oracle.query_page_means(q, P, k_logical.shape[1])
+    rep = oracle.page_representatives(k_logical[: q_start + q.shape[0]], P)
+    ties = 0
+    for i in range(len(lists)):
+        for h in range(len(lists[0])):
+            got = [int(x) for x in sel_gpu[i, h] if x >= 0]
+            assert got == sorted(set(got)), (i, h, got)
+            want = lists[i][h]
+            if got == want:
+                continue
+            qpg = q_start // P + i
+            cand = np.arange(n_sink, qpg - n_local + 1)
+            scores = rep[cand, h] @ qbar[i, h]
+            kth = np.sort(scores)[::-1][min(K, len(cand)) - 1]
+            for pg in set(got) ^ set(want):
+                assert n_sink <= pg <= qpg - n_local, (i, h, pg)
+                assert abs(rep[pg, h] @ qbar[i, h] - kth) <= TIE, (i, h, pg, got, want)
+            ties += 1
+    return ties
+
+
+@pytest.mark.parametrize("dtype,P,d,K", [("bf16", 128, 128, 3), ("f32", 16, 64, 5),
+                                         ("bf16", 128, 128, 64)])
+def test_page_topk_matches_oracle(dtype, P, d, K):
+    w = _w(dtype=dtype, P=P, d=d, N=2048 if P == 128 else 512, C=1024 if P == 128 else 256,
+           topk=(K, 1, 2))
+    qs, ks, vs, _ = _inputs(w)
+    sw = ChunkSweep(w).load_inputs()
+    try:
+        sw.reset()
+        k_all = np.concatenate(ks)
+        for c in range(w.n_chunks):
+            s, e = w.chunk_range(c)
+            B.pkv_append(sw.seq, sw.k[c], sw.v[c], e - s)
+            n_qp = (e - s + w.P - 1) // w.P
+            sel = torch.full((n_qp, w.Hkv, K + 3), 7, dtype=torch.int32, device="cuda")
+            cnt = torch.zeros((n_qp, w.Hkv), dtype=torch.int32, device="cuda")
+            B.pkv_page_topk(sw.seq, sw.q[c], s, e - s, K, 1, 2, sel, cnt)
+            torch.cuda.synchronize()
+            B.pkv_check(sw.pool)
+            got = sel.cpu().numpy()
+            _check_selection(got, qs[c], s, k_all, w.P, K, 1, 2)
+            np.testing.assert_array_equal(cnt.cpu().numpy(), (got >= 0).sum(-1))
+    finally:
+        sw.close()
+
+
+def _sparse_sweep(w, use_oracle_selection: bool, flags=0):
+    K, ns, nl = w.topk
+    qs, ks, vs, dos = _inputs(w)
+    bt = synth.block_table(w)
+    ref = oracle.chunk_recurrent_step(qs, ks, vs, dos, bt, w.P, w.n_phys, topk=w.topk)
+    sw = ChunkSweep(w, flags=flags).load_inputs()
+    try:
+        sw.reset()
+        sels = []
+        k_all = np.concatenate(ks)
+        for c in range(w.n_chunks):
+            s, e = w.chunk_range(c)
+            B.pkv_append(sw.seq, sw.k[c], sw.v[c], e - s)
+            n_qp = (e - s + w.P - 1) // w.P
+            if use_oracle_selection:
+                sel = torch.from_numpy(ref["sel"][c]).cuda()
+            else:
+                sel = torch.empty((n_qp, w.Hkv, K + ns + nl), dtype=torch.int32, device="cuda")
+                B.pkv_page_topk(sw.seq, sw.q[c], s, e - s, K, ns, nl, sel)
+                torch.cuda.synchronize()
+                assert _check_selection(sel.cpu().numpy(), qs[c], s, k_all, w.P, K, ns, nl) == 0
+            sels.append(sel)
+            B.pkv_chunk_attn_fwd(sw.seq, sw.q[c], s, e - s, sw.o[c], sw.lse[c], sels[c])
+        for c in reversed(range(w.n_chunks)):
+            sw.backward(c, sel=sels[c])
+        B.pkv_check(sw.pool)
+        g = sw.gather()
+        tol_abs, tol_rel = TOL[w.dtype]
+        o = np.concatenate([to_numpy(x) for x in sw.o])
+        lse = np.concatenate([to_numpy(x) for x in sw.lse], axis=1)
+        err = dict(
+            o=float(np.abs(o - np.concatenate(ref["o"])).max()),
+            lse=float(np.abs(lse - np.concatenate(ref["lse"], axis=1)).max()),
+            dq=_rel(np.concatenate([to_numpy(x) for x in sw.dq]), np.concatenate(ref["dq"])),
+            dk=_rel(to_numpy(g["dk"]), oracle.logical_rows(ref["dkpool"], bt, w.N, w.P)),
+            dv=_rel(to_numpy(g["dv"]), oracle.logical_rows(ref["dvpool"], bt, w.N, w.P)),
+        )
+        assert err["o"] <= tol_abs and err["lse"] <= tol_abs, err
+        assert max(err["dq"], err["dk"], err["dv"]) <= tol_rel, err
+        return err
+    finally:
+        sw.close()
+
+
+def test_sparse_attention_tensor_cores_oracle_selection():
+    _sparse_sweep(_w(), use_oracle_selection=True)
+
+
+def test_sparse_attention_tensor_cores_partial_chunk():
+    _sparse_sweep(_w(N=1900, C=1024), use_oracle_selection=True)
+
+
+def test_sparse_attention_cuda_cores_oracle_selection():
+    _sparse_sweep(_w(dtype="f32", P=16, d=64, N=512, C=256, topk=(5, 1, 2)),
+                  use_oracle_selection=True)
+
+
+def test_sparse_attention_bf16_cuda_cores_flag():
+    _sparse_sweep(_w(), use_oracle_selection=True, flags=B.PKV_FLAG_SIMT_ONLY)
+
+
+def test_sparse_sweep_with_gpu_selection():
+    _sparse_sweep(_w(N=3072, C=1024, topk=(4, 1, 2)), use_oracle_selection=False)
+
+
+def test_sparse_with_all_pages_equals_dense_on_gpu():
+    """K >= every candidate: the sparse kernels reproduce the dense ones."""
+    w = _w(N=1024, C=512, keys="normal", topk=(64, 1, 2))
+    sw = ChunkSweep(w).load_inputs()
+    try:
+        sw.run()
+        dense = ([to_numpy(x).copy() for x in sw.o], to_numpy(sw.gather()["dk"]).copy())
+        sw.reset()
+        sels = []
+        for c in range(w.n_chunks):
+            s, e = w.chunk_range(c)
+            B.pkv_append(sw.seq, sw.k[c], sw.v[c], e - s)
+            sel = torch.empty(((e - s) // w.P, w.Hkv, 67), dtype=torch.int32, device="cuda")
+            B.pkv_page_topk(sw.seq, sw.q[c], s, e - s, 64, 1, 2, sel)
+            sels.append(sel)
+            B.pkv_chunk_attn_fwd(sw.seq, sw.q[c], s, e - s, sw.o[c], sw.lse[c], sel)
+        for c in reversed(range(w.n_chunks)):
+            sw.backward(c, sel=sels[c])
+        for a, b in zip(dense[0], [to_numpy(x) for x in sw.o]):
+            np.testing.assert_array_equal(a, b)
+        assert _rel(to_numpy(sw.gather()["dk"]), dense[1]) < 1e-6
+    finally:
+        sw.close()
