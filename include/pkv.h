@@ -244,14 +244,33 @@ pkv_status pkv_page_topk(pkv_seq* seq, const void* q, int64_t q_start, int64_t n
                          int32_t* counts_out, void* stream);
 
 /* ---------------------------------------------------------------- host offload (a7)
- * For PINNED_HOST pools: the K/V and gradient pages live in pinned host
- * memory; n_device_slots page slots live in HBM. pkv_prefetch stages the
- * listed logical pages (NULL = all pages) into slots on `side`, recording an
- * event; attention calls on the main stream then read the slots.
- * pkv_writeback_grads adds the slots' gradients back into the host gradient
- * pages on `side`. pkv_wait makes `main` wait for the side stream's last
- * recorded event, polling at most timeout_us (PKV_ERR_TIMEOUT after that). */
-pkv_status pkv_prefetch(pkv_seq* seq, const int32_t* logical_pages, int64_t n, void* side);
+ * For PINNED_HOST pools the K/V pages and their fp32 gradient pages live in
+ * mapped pinned host memory (appends write them there; pkv_gather and
+ * pkv_grad_zero work on them) and the pool owns n_device_slots page slots in
+ * HBM; page representatives stay in HBM. Attention calls on such a pool read
+ * the slots, so the pages a call needs must be staged first. One sequence
+ * of the pool uses the slots at a time (one pool per layer to prefetch layer
+ * l+1 while layer l computes).
+ *
+ * pkv_prefetch: on stream `side`, after the sequence's last append or
+ * attention call (an internal event), stages the logical pages listed in
+ * device int32 logical_pages[0..n) -- duplicates and -1 entries are ignored,
+ * so a selection array from pkv_page_topk can be passed flattened -- or every
+ * page of the sequence if logical_pages is NULL (n = 0). Pages get slots in
+ * ascending page order; what = PKV_STAGE_KV copies K and V, PKV_STAGE_GRADS
+ * copies dK and dV (or both). Staged pages beyond the slot count are not
+ * staged and record PKV_ERR_DEVICE_FAULT for pkv_check. Kernels copy the pages
+ * over the host link; nothing is allocated and the host does not wait.
+ * pkv_writeback_grads: on `side`, after the sequence's last attention call,
+ * copies the staged slots' dK/dV back into the host gradient pages.
+ * pkv_wait: makes stream `main` wait (on the GPU) for the sequence's last
+ * prefetch or writeback; with timeout_us > 0 the host first polls for its
+ * completion and returns PKV_ERR_TIMEOUT, enqueuing nothing, after
+ * timeout_us microseconds. */
+#define PKV_STAGE_KV 1
+#define PKV_STAGE_GRADS 2
+pkv_status pkv_prefetch(pkv_seq* seq, const int32_t* logical_pages, int64_t n, int32_t what,
+                        void* side);
 pkv_status pkv_writeback_grads(pkv_seq* seq, void* side);
 pkv_status pkv_wait(pkv_seq* seq, void* main, int64_t timeout_us);
 

@@ -21,6 +21,7 @@ STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID", 2: "PKV_ERR_OOM", 3: "PKV_ERR
 PKV_BF16, PKV_F32 = 0, 1
 PKV_RES_DEVICE, PKV_RES_PINNED_HOST, PKV_RES_META = 0, 1, 2
 PKV_FLAG_SIMT_ONLY = 1
+PKV_STAGE_KV, PKV_STAGE_GRADS = 1, 2
 
 
 class PkvError(RuntimeError):
@@ -69,7 +70,7 @@ _SIGS = {
     "pkv_grad_zero": (_ST, [_P, _P]),
     "pkv_gather": (_ST, [_P, _P, _P, _P, _P, _P, _P]),
     "pkv_page_topk": (_ST, [_P, _P, _I64, _I64, _I32, _I32, _I32, _P, _P, _P]),
-    "pkv_prefetch": (_ST, [_P, _P, _I64, _P]),
+    "pkv_prefetch": (_ST, [_P, _P, _I64, _I32, _P]),
     "pkv_writeback_grads": (_ST, [_P, _P]),
     "pkv_wait": (_ST, [_P, _P, _I64]),
     "pkv_selftest_umma": (_ST, [_I32, _P, _P, _P, _I32, _I32]),
@@ -238,8 +239,9 @@ def pkv_page_topk(seq, q, q_start, n_q, k, n_sink, n_local, pages_out, counts_ou
                                ptr(counts_out), stream_ptr(stream)))
 
 
-def pkv_prefetch(seq, logical_pages, n, side=None) -> None:
-    _check(lib().pkv_prefetch(seq, ptr(logical_pages), n, stream_ptr(side)))
+def pkv_prefetch(seq, logical_pages=None, n=0, what=3, side=None) -> None:
+    """what: PKV_STAGE_KV (1) | PKV_STAGE_GRADS (2)."""
+    _check(lib().pkv_prefetch(seq, ptr(logical_pages), n, what, stream_ptr(side)))
 
 
 def pkv_writeback_grads(seq, side=None) -> None:

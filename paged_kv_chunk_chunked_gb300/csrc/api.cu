@@ -11,11 +11,13 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <chrono>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <thread>
 #include <vector>
 
 #include "common.cuh"
@@ -196,6 +198,7 @@ pkv_status pkv_check(pkv_pool* pool) {
         const char* what = h == pkv::kErrWaitTimeout ? "a bounded wait expired"
                          : h == pkv::kErrBadPage     ? "a page index was out of range"
                          : h == pkv::kErrTmemAlloc   ? "tensor-memory allocation failed"
+                         : h == pkv::kErrSlots       ? "more pages staged than device slots"
                                                 : "unknown device error";
         return fail(PKV_ERR_DEVICE_FAULT, std::string("device error ") + std::to_string(h) +
                                               ": " + what);
@@ -220,46 +223,75 @@ pkv_status pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
         *out = p;
         return PKV_OK;
     }
-    if (desc->residency == PKV_RES_PINNED_HOST) {
-        delete p;
-        return fail(PKV_ERR_UNSUPPORTED, "PINNED_HOST pools are not built yet");
-    }
+    const bool host = desc->residency == PKV_RES_PINNED_HOST;
+    if (host && (desc->n_device_slots <= 0 || desc->n_device_slots > np))
+        { delete p; return fail(PKV_ERR_INVALID, "PINNED_HOST pools need 0 < n_device_slots <= num_phys_pages"); }
     cudaError_t e = cudaGetDevice(&p->device);
     if (e != cudaSuccess) { delete p; return cuda_fail(e, "cudaGetDevice"); }
     const size_t kv_bytes = p->page_elems * p->elem * np;
     const size_t g_bytes = p->page_elems * sizeof(float) * np;
     const size_t rep_bytes = (size_t)np * desc->n_kv_heads * desc->head_dim * sizeof(float);
-    auto cleanup = [p]() {
-        cudaFree(p->k); cudaFree(p->v); cudaFree(p->dk); cudaFree(p->dv);
+    auto cleanup = [p, host]() {
+        if (host) {
+            cudaFreeHost(p->k); cudaFreeHost(p->v); cudaFreeHost(p->dk); cudaFreeHost(p->dv);
+            cudaFree(p->kslot); cudaFree(p->vslot); cudaFree(p->dkslot); cudaFree(p->dvslot);
+        } else {
+            cudaFree(p->k); cudaFree(p->v); cudaFree(p->dk); cudaFree(p->dv);
+        }
         cudaFree(p->rep); cudaFree(p->d_err);
         delete p;
     };
-    if ((e = cudaMalloc(&p->k, kv_bytes)) != cudaSuccess ||
-        (e = cudaMalloc(&p->v, kv_bytes)) != cudaSuccess ||
-        (e = cudaMalloc(reinterpret_cast<void**>(&p->dk), g_bytes)) != cudaSuccess ||
-        (e = cudaMalloc(reinterpret_cast<void**>(&p->dv), g_bytes)) != cudaSuccess ||
-        (e = cudaMalloc(reinterpret_cast<void**>(&p->rep), rep_bytes)) != cudaSuccess ||
-        (e = cudaMalloc(reinterpret_cast<void**>(&p->d_err), sizeof(int))) != cudaSuccess) {
+    if (host) {
+        // Pages in mapped pinned host memory (reachable by kernels over the
+        // host link); slots and representatives in HBM.
+        const unsigned fl = cudaHostAllocMapped | cudaHostAllocPortable;
+        p->n_slots = desc->n_device_slots;
+        const size_t skv = p->page_elems * p->elem * p->n_slots;
+        const size_t sg = p->page_elems * sizeof(float) * p->n_slots;
+        if ((e = cudaHostAlloc(&p->k, kv_bytes, fl)) != cudaSuccess ||
+            (e = cudaHostAlloc(&p->v, kv_bytes, fl)) != cudaSuccess ||
+            (e = cudaHostAlloc(reinterpret_cast<void**>(&p->dk), g_bytes, fl)) != cudaSuccess ||
+            (e = cudaHostAlloc(reinterpret_cast<void**>(&p->dv), g_bytes, fl)) != cudaSuccess ||
+            (e = cudaMalloc(&p->kslot, skv)) != cudaSuccess ||
+            (e = cudaMalloc(&p->vslot, skv)) != cudaSuccess ||
+            (e = cudaMalloc(reinterpret_cast<void**>(&p->dkslot), sg)) != cudaSuccess ||
+            (e = cudaMalloc(reinterpret_cast<void**>(&p->dvslot), sg)) != cudaSuccess ||
+            (e = cudaMalloc(reinterpret_cast<void**>(&p->rep), rep_bytes)) != cudaSuccess ||
+            (e = cudaMalloc(reinterpret_cast<void**>(&p->d_err), sizeof(int))) != cudaSuccess) {
+            cleanup();
+            return cuda_fail(e, "pkv_pool_create: pinned pages / slots");
+        }
+        std::memset(p->k, 0, kv_bytes);
+        std::memset(p->v, 0, kv_bytes);
+    } else if ((e = cudaMalloc(&p->k, kv_bytes)) != cudaSuccess ||
+               (e = cudaMalloc(&p->v, kv_bytes)) != cudaSuccess ||
+               (e = cudaMalloc(reinterpret_cast<void**>(&p->dk), g_bytes)) != cudaSuccess ||
+               (e = cudaMalloc(reinterpret_cast<void**>(&p->dv), g_bytes)) != cudaSuccess ||
+               (e = cudaMalloc(reinterpret_cast<void**>(&p->rep), rep_bytes)) != cudaSuccess ||
+               (e = cudaMalloc(reinterpret_cast<void**>(&p->d_err), sizeof(int))) != cudaSuccess) {
         cleanup();
         return cuda_fail(e, "pkv_pool_create: page memory");
     }
     if ((e = cudaMemset(p->d_err, 0, sizeof(int))) != cudaSuccess ||
-        (e = cudaMemset(p->k, 0, kv_bytes)) != cudaSuccess ||
-        (e = cudaMemset(p->v, 0, kv_bytes)) != cudaSuccess ||
+        (!host && (e = cudaMemset(p->k, 0, kv_bytes)) != cudaSuccess) ||
+        (!host && (e = cudaMemset(p->v, 0, kv_bytes)) != cudaSuccess) ||
         (e = cudaMemset(p->rep, 0, rep_bytes)) != cudaSuccess) {
         cleanup();
         return cuda_fail(e, "pkv_pool_create: memset");
     }
     if (desc->dtype == PKV_BF16 && desc->head_dim == 128 && desc->page_size == 128) {
+        // The tensor-core kernels read K/V by TMA: the pool in HBM, or the slots.
         std::string why;
-        const uint64_t rows = (uint64_t)np * desc->n_kv_heads * desc->page_size;
-        if (!make_tmap_2d(&p->tmap_k, p->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
+        void* kb = host ? p->kslot : p->k;
+        void* vb = host ? p->vslot : p->v;
+        const uint64_t rows = (uint64_t)(host ? p->n_slots : np) * desc->n_kv_heads * desc->page_size;
+        if (!make_tmap_2d(&p->tmap_k, kb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
                           128, &why) ||
-            !make_tmap_2d(&p->tmap_v, p->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
+            !make_tmap_2d(&p->tmap_v, vb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
                           128, &why) ||
-            !make_tmap_2d(&p->tmap_k64, p->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
+            !make_tmap_2d(&p->tmap_k64, kb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
                           64, &why) ||
-            !make_tmap_2d(&p->tmap_v64, p->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
+            !make_tmap_2d(&p->tmap_v64, vb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
                           64, &why)) {
             cleanup();
             return fail(PKV_ERR_CUDA, "pkv_pool_create: " + why);
@@ -274,8 +306,13 @@ void pkv_pool_destroy(pkv_pool* p) {
     if (!p) return;
     std::vector<pkv_seq*> seqs = p->seqs;
     for (pkv_seq* s : seqs) pkv_seq_free(s);
-    if (is_device(p)) {
+    if (p->desc.residency == PKV_RES_PINNED_HOST) {
+        cudaFreeHost(p->k); cudaFreeHost(p->v); cudaFreeHost(p->dk); cudaFreeHost(p->dv);
+        cudaFree(p->kslot); cudaFree(p->vslot); cudaFree(p->dkslot); cudaFree(p->dvslot);
+    } else if (is_device(p)) {
         cudaFree(p->k); cudaFree(p->v); cudaFree(p->dk); cudaFree(p->dv);
+    }
+    if (is_device(p)) {
         cudaFree(p->rep); cudaFree(p->d_err); cudaFree(p->scratch); cudaFree(p->sel_scratch);
     }
     delete p;
@@ -308,8 +345,20 @@ pkv_status pkv_seq_create(pkv_pool* p, pkv_seq** out) {
         cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&s->h_bt), bytes,
                                       cudaHostAllocDefault);
         if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&s->d_bt), bytes);
+        if (e == cudaSuccess && p->desc.residency == PKV_RES_PINNED_HOST) {
+            e = cudaMalloc(reinterpret_cast<void**>(&s->d_slot_of), bytes);
+            if (e == cudaSuccess) e = cudaMemset(s->d_slot_of, 0xff, bytes);   // all -1
+            if (e == cudaSuccess)
+                e = cudaMalloc(reinterpret_cast<void**>(&s->d_slot_page), p->n_slots * sizeof(int32_t));
+            if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&s->d_flags), bytes + sizeof(int32_t));
+            if (e == cudaSuccess) e = cudaMemset(s->d_flags, 0, bytes + sizeof(int32_t));
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->staged, cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->used, cudaEventDisableTiming);
+        }
         if (e != cudaSuccess) {
             cudaFreeHost(s->h_bt);
+            cudaFree(s->d_bt); cudaFree(s->d_slot_of); cudaFree(s->d_slot_page); cudaFree(s->d_flags);
+            if (s->staged) cudaEventDestroy(s->staged);
             delete s;
             return cuda_fail(e, "pkv_seq_create: block table");
         }
@@ -327,6 +376,9 @@ void pkv_seq_free(pkv_seq* s) {
     if (is_device(s->pool)) {
         cudaFreeHost(s->h_bt);
         cudaFree(s->d_bt);
+        cudaFree(s->d_slot_of); cudaFree(s->d_slot_page); cudaFree(s->d_flags);
+        if (s->staged) cudaEventDestroy(s->staged);
+        if (s->used) cudaEventDestroy(s->used);
     }
     delete s;
 }
@@ -413,6 +465,7 @@ pkv_status pkv_append(pkv_seq* s, const void* k, const void* v, int64_t n_tok, v
     a.bt = s->d_bt; a.num_phys = p->desc.num_phys_pages;
     a.old_len = s->len; a.n_tok = n_tok; a.err = p->d_err;
     cudaError_t e = launch_append(a, cs);
+    if (e == cudaSuccess && s->used) e = cudaEventRecord(s->used, cs);
     if (e != cudaSuccess) return cuda_fail(e, "pkv_append: launch");
     s->len += n_tok;
     return PKV_OK;
@@ -435,8 +488,15 @@ static pkv_status attn_common(pkv_seq* s, const void* q, int64_t q_start, int64_
     a->P = (int)P; a->Hq = p->desc.n_q_heads; a->Hkv = p->desc.n_kv_heads;
     a->d = p->desc.head_dim; a->dtype = p->desc.dtype;
     a->q_start = q_start; a->n_q = n_q; a->q = q;
-    a->kpool = p->k; a->vpool = p->v; a->dkpool = p->dk; a->dvpool = p->dv;
-    a->bt = s->d_bt; a->num_phys = p->desc.num_phys_pages; a->err = p->d_err;
+    if (p->desc.residency == PKV_RES_PINNED_HOST) {
+        // Attention reads the device slots through the logical-page -> slot table.
+        a->kpool = p->kslot; a->vpool = p->vslot; a->dkpool = p->dkslot; a->dvpool = p->dvslot;
+        a->bt = s->d_slot_of; a->num_phys = p->n_slots;
+    } else {
+        a->kpool = p->k; a->vpool = p->v; a->dkpool = p->dk; a->dvpool = p->dv;
+        a->bt = s->d_bt; a->num_phys = p->desc.num_phys_pages;
+    }
+    a->err = p->d_err;
     a->tmap_k = p->tmaps_ready ? &p->tmap_k : nullptr;
     a->tmap_v = p->tmaps_ready ? &p->tmap_v : nullptr;
     a->tmap_k64 = p->tmaps_ready ? &p->tmap_k64 : nullptr;
@@ -464,6 +524,7 @@ pkv_status pkv_chunk_attn_fwd(pkv_seq* s, const void* q, int64_t q_start, int64_
     a.o = o; a.lse = lse;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e = use_tc(s->pool, a) ? launch_attn_fwd_tc(a, cs) : launch_attn_fwd_simt(a, cs);
+    if (e == cudaSuccess && s->used) e = cudaEventRecord(s->used, cs);
     if (e != cudaSuccess) return cuda_fail(e, "pkv_chunk_attn_fwd: launch");
     return PKV_OK;
 }
@@ -497,6 +558,7 @@ pkv_status pkv_chunk_attn_bwd(pkv_seq* s, const void* q, const void* o, const vo
     cudaError_t e = launch_bwd_rowdot(a, cs);
     if (e == cudaSuccess)
         e = use_tc(s->pool, a) ? launch_attn_bwd_tc(a, cs) : launch_attn_bwd_simt(a, cs);
+    if (e == cudaSuccess && s->used) e = cudaEventRecord(s->used, cs);
     if (e != cudaSuccess) return cuda_fail(e, "pkv_chunk_attn_bwd: launch");
     return PKV_OK;
 }
@@ -559,19 +621,63 @@ pkv_status pkv_page_topk(pkv_seq* s, const void* q, int64_t q_start, int64_t n_q
     return PKV_OK;
 }
 
-pkv_status pkv_prefetch(pkv_seq* s, const int32_t* pages, int64_t n, void* side) {
-    (void)s; (void)pages; (void)n; (void)side;
-    return fail(PKV_ERR_UNSUPPORTED, "pkv_prefetch: not built yet");
+static pkv_status host_pool_check(pkv_seq* s, const char* who) {
+    if (!s) return fail(PKV_ERR_INVALID, std::string(who) + ": seq is NULL");
+    if (s->pool->desc.residency != PKV_RES_PINNED_HOST)
+        return fail(PKV_ERR_INVALID, std::string(who) + ": the pool is not PINNED_HOST");
+    return check_stream_device(s->pool);
+}
+
+pkv_status pkv_prefetch(pkv_seq* s, const int32_t* pages, int64_t n, int32_t what, void* side) {
+    pkv_status st = host_pool_check(s, "pkv_prefetch");
+    if (st != PKV_OK) return st;
+    if (n < 0 || (n > 0 && !pages) || !(what & (PKV_STAGE_KV | PKV_STAGE_GRADS)) ||
+        (what & ~(PKV_STAGE_KV | PKV_STAGE_GRADS)))
+        return fail(PKV_ERR_INVALID, "pkv_prefetch: bad pages/n/what");
+    if (s->bt.empty()) return PKV_OK;
+    cudaStream_t cs = static_cast<cudaStream_t>(side);
+    // Slots are rewritten: wait for the last append/attention call on this sequence.
+    cudaError_t e = cudaStreamWaitEvent(cs, s->used, 0);
+    if (e == cudaSuccess) e = launch_stage_plan(s, n > 0 ? pages : nullptr, n, cs);
+    if (e == cudaSuccess) e = launch_stage_copy(s, what, cs);
+    if (e == cudaSuccess) e = cudaEventRecord(s->staged, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_prefetch");
+    return PKV_OK;
 }
 
 pkv_status pkv_writeback_grads(pkv_seq* s, void* side) {
-    (void)s; (void)side;
-    return fail(PKV_ERR_UNSUPPORTED, "pkv_writeback_grads: not built yet");
+    pkv_status st = host_pool_check(s, "pkv_writeback_grads");
+    if (st != PKV_OK) return st;
+    if (s->bt.empty()) return PKV_OK;
+    cudaStream_t cs = static_cast<cudaStream_t>(side);
+    cudaError_t e = cudaStreamWaitEvent(cs, s->used, 0);
+    if (e == cudaSuccess) e = launch_stage_writeback(s, cs);
+    if (e == cudaSuccess) e = cudaEventRecord(s->staged, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_writeback_grads");
+    return PKV_OK;
 }
 
 pkv_status pkv_wait(pkv_seq* s, void* main, int64_t timeout_us) {
-    (void)s; (void)main; (void)timeout_us;
-    return fail(PKV_ERR_UNSUPPORTED, "pkv_wait: not built yet");
+    pkv_status st = host_pool_check(s, "pkv_wait");
+    if (st != PKV_OK) return st;
+    if (timeout_us > 0) {
+        // Bounded host poll: never blocks longer than timeout_us.
+        const auto t0 = std::chrono::steady_clock::now();
+        for (;;) {
+            cudaError_t q = cudaEventQuery(s->staged);
+            if (q == cudaSuccess) break;
+            if (q != cudaErrorNotReady) return cuda_fail(q, "pkv_wait: event");
+            const auto us = std::chrono::duration_cast<std::chrono::microseconds>(
+                                std::chrono::steady_clock::now() - t0).count();
+            if (us > timeout_us)
+                return fail(PKV_ERR_TIMEOUT, "pkv_wait: staging not complete after " +
+                                                 std::to_string(timeout_us) + " us");
+            std::this_thread::sleep_for(std::chrono::microseconds(20));
+        }
+    }
+    cudaError_t e = cudaStreamWaitEvent(static_cast<cudaStream_t>(main), s->staged, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_wait");
+    return PKV_OK;
 }
 
 pkv_status pkv_selftest_umma(int32_t mode, const void* a, const void* b, float* d, int32_t lbo,

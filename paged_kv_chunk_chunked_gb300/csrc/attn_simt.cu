@@ -222,6 +222,13 @@ __global__ void __launch_bounds__(NT) bwd_dkdv_simt(AttnArgs a) {
     const int64_t lp = kp0 / a.P;
     const int r = threadIdx.x / 8, sub = threadIdx.x % 8;   // r = key row
     const float scale = rsqrtf((float)D);
+    if (a.sel) {
+        // Sparse: a page no query page of the chunk selected contributes nothing
+        // (and, in a staged pool, need not be in a slot).
+        bool used = false;
+        for (int64_t qp = 0; qp * a.P < a.n_q && !used; ++qp) used = page_selected(a, qp, kvh, lp);
+        if (!used) return;
+    }
     if (!load_keys<T, D>(Ks, Vs, a, kp0, kvh)) return;
     float dk[E], dv[E];
 #pragma unroll

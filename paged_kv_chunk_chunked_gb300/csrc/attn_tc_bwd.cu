@@ -156,7 +156,8 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         tc::mbar_init(&B.acc_done, 1);
         tc::mbar_init(&B.drain, 1);
         tc::fence_barrier_init();
-        if (!page_ok) report_error(p.err, kErrBadPage);
+        // A page no query tile uses needs no valid slot (sparse, staged pools).
+        if (!page_ok && B.n_i > 0) report_error(p.err, kErrBadPage);
     }
     if (warp == 1) {
         tc::tmem_alloc(&B.tmem_base, 512);

@@ -14,6 +14,7 @@ enum DeviceError : int {
     kErrWaitTimeout = 1,     // a bounded mbarrier / flag wait expired
     kErrBadPage = 2,         // a block-table or selection entry out of range
     kErrTmemAlloc = 3,       // tensor-memory allocation returned an unusable address
+    kErrSlots = 4,           // more pages requested for staging than device slots
 };
 
 __device__ __forceinline__ void report_error(int* err, int code) {

@@ -33,9 +33,17 @@ struct pkv_pool {
     float* sel_scratch = nullptr;
     size_t sel_scratch_floats = 0;
     // TMA descriptors over the K and V page pools (2-D: rows x d), with boxes
-    // of 64 columns x 128 rows (whole pages) and 64 x 64 (half pages).
+    // of 64 columns x 128 rows (whole pages) and 64 x 64 (half pages). For a
+    // PINNED_HOST pool they describe the device slots.
     CUtensorMap tmap_k{}, tmap_v{}, tmap_k64{}, tmap_v64{};
     bool tmaps_ready = false;
+    // PINNED_HOST pools: k/v/dk/dv above are mapped pinned host pages; the
+    // attention kernels read these device slots instead.
+    int64_t n_slots = 0;
+    void* kslot = nullptr;
+    void* vslot = nullptr;
+    float* dkslot = nullptr;
+    float* dvslot = nullptr;
 };
 
 struct pkv_seq {
@@ -45,6 +53,12 @@ struct pkv_seq {
     int32_t* h_bt = nullptr;         // pinned mirror used as the copy source
     int32_t* d_bt = nullptr;         // device block table, capacity num_phys_pages
     int64_t len = 0;
+    // PINNED_HOST pools: staging state (device), capacity num_phys_pages.
+    int32_t* d_slot_of = nullptr;    // logical page -> device slot, or -1
+    int32_t* d_slot_page = nullptr;  // device slot -> logical page [n_slots]
+    int32_t* d_flags = nullptr;      // planning scratch [num_phys_pages + 1]
+    cudaEvent_t staged = nullptr;    // last event recorded on the side stream
+    cudaEvent_t used = nullptr;      // last append/attention call on the sequence's slots
 };
 
 namespace pkv {
@@ -122,6 +136,11 @@ cudaError_t launch_page_topk(const pkv_pool* p, const int32_t* d_bt, const void*
                              int64_t q_start, int64_t n_q, int K, int n_sink, int n_local,
                              int32_t* out, int32_t* counts, float* qbar, cudaStream_t s);
 int64_t page_topk_max_candidates();
+
+// Host offload (stream.cu).
+cudaError_t launch_stage_plan(const pkv_seq* s, const int32_t* pages, int64_t n, cudaStream_t st);
+cudaError_t launch_stage_copy(const pkv_seq* s, int what, cudaStream_t st);
+cudaError_t launch_stage_writeback(const pkv_seq* s, cudaStream_t st);
 
 bool tc_supported(const AttnArgs& a);
 cudaError_t launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t s);

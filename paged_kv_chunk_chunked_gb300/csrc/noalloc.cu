@@ -94,8 +94,14 @@ extern "C" pkv_status pkv_chunk_attn_bwd_noalloc(pkv_seq* s, const void* q, cons
     a.P = (int)P; a.Hq = p->desc.n_q_heads; a.Hkv = p->desc.n_kv_heads;
     a.d = p->desc.head_dim; a.dtype = p->desc.dtype;
     a.q_start = q_start; a.n_q = n_q; a.q = q;
-    a.kpool = p->k; a.vpool = p->v; a.dkpool = p->dk; a.dvpool = p->dv;
-    a.bt = s->d_bt; a.num_phys = p->desc.num_phys_pages; a.err = p->d_err;
+    if (p->desc.residency == PKV_RES_PINNED_HOST) {      // staged pages: read the slots
+        a.kpool = p->kslot; a.vpool = p->vslot; a.dkpool = p->dkslot; a.dvpool = p->dvslot;
+        a.bt = s->d_slot_of; a.num_phys = p->n_slots;
+    } else {
+        a.kpool = p->k; a.vpool = p->v; a.dkpool = p->dk; a.dvpool = p->dv;
+        a.bt = s->d_bt; a.num_phys = p->desc.num_phys_pages;
+    }
+    a.err = p->d_err;
     a.tmap_k = p->tmaps_ready ? &p->tmap_k : nullptr;
     a.tmap_v = p->tmaps_ready ? &p->tmap_v : nullptr;
     a.tmap_k64 = p->tmaps_ready ? &p->tmap_k64 : nullptr;

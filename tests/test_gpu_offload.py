@@ -1,0 +1,147 @@
+"""GPU tests of the pinned-host page streamer (PINNED_HOST pools), through the C ABI.
+
+The K/V pages and their fp32 gradient pages live in mapped pinned host memory;
+per chunk the selected (or all) pages are staged into HBM slots on a side
+stream, attention runs on the slots on the main stream, and the gradients are
+written back. Results must match the oracle within the parity tolerances.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_chunk_chunked_gb300 import binding as B
+from paged_kv_chunk_chunked_gb300 import build as pkv_build
+from paged_kv_chunk_chunked_gb300 import synth
+from paged_kv_chunk_chunked_gb300.sweep import to_device, to_numpy
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    pkv_build.build()
+    B.lib()
+    torch.cuda.set_device(0)
+
+
+def _rel(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def _offloaded_sweep(w, n_slots, sparse: bool):
+    K, ns, nl = w.topk
+    n = w.n_chunks
+    qs = [synth.chunk_q(w, c) for c in range(n)]
+    ks = [synth.chunk_k(w, c) for c in range(n)]
+    vs = [synth.chunk_v(w, c) for c in range(n)]
+    dos = [synth.chunk_do(w, c) for c in range(n)]
+    bt = synth.block_table(w)
+    ref = oracle.chunk_recurrent_step(qs, ks, vs, dos, bt, w.P, w.n_phys,
+                                      topk=w.topk if sparse else None)
+    pool = B.pkv_pool_create(w.P, w.Hkv, w.Hq, w.d, B.PKV_BF16, w.n_phys,
+                             residency=B.PKV_RES_PINNED_HOST, n_device_slots=n_slots)
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    try:
+        seq = B.pkv_seq_create(pool)
+        B.pkv_set_block_table(seq, bt)
+        dq_, o_, lse_, sels = [], [], [], []
+        dev = lambda x: to_device(x, "bf16")
+        q = [dev(x) for x in qs]; k = [dev(x) for x in ks]; v = [dev(x) for x in vs]
+        do = [dev(x) for x in dos]
+        for c in range(n):
+            s, e = w.chunk_range(c)
+            B.pkv_append(seq, k[c], v[c], e - s, main)
+            o_.append(torch.empty_like(q[c]))
+            lse_.append(torch.empty((w.Hq, e - s), dtype=torch.float32, device="cuda"))
+            dq_.append(torch.empty_like(q[c]))
+            sel = None
+            if sparse:
+                sel = torch.empty(((e - s + w.P - 1) // w.P, w.Hkv, K + ns + nl), dtype=torch.int32,
+                                  device="cuda")
+                B.pkv_page_topk(seq, q[c], s, e - s, K, ns, nl, sel, None, main)
+            sels.append(sel)
+            B.pkv_prefetch(seq, sel, 0 if sel is None else sel.numel(), B.PKV_STAGE_KV, side)
+            B.pkv_wait(seq, main, 0)
+            B.pkv_chunk_attn_fwd(seq, q[c], s, e - s, o_[c], lse_[c], sel, main)
+        for c in reversed(range(n)):
+            s, e = w.chunk_range(c)
+            sel = sels[c]
+            B.pkv_prefetch(seq, sel, 0 if sel is None else sel.numel(),
+                           B.PKV_STAGE_KV | B.PKV_STAGE_GRADS, side)
+            B.pkv_wait(seq, main, 0)
+            B.pkv_chunk_attn_bwd(seq, q[c], o_[c], do[c], lse_[c], s, e - s, dq_[c], sel, main)
+            B.pkv_writeback_grads(seq, side)
+        B.pkv_wait(seq, main, 5_000_000)            # bounded host wait, then GPU-side wait
+        dk = torch.empty((w.N, w.Hkv, w.d), dtype=torch.float32, device="cuda")
+        dv = torch.empty_like(dk)
+        kk = torch.empty((w.N, w.Hkv, w.d), dtype=torch.bfloat16, device="cuda")
+        B.pkv_gather(seq, kk, None, dk, dv, None, main)
+        torch.cuda.synchronize()
+        B.pkv_check(pool)
+        np.testing.assert_array_equal(to_numpy(kk), np.concatenate(ks))
+        o = np.concatenate([to_numpy(x) for x in o_])
+        lse = np.concatenate([to_numpy(x) for x in lse_], axis=1)
+        err = dict(
+            o=float(np.abs(o - np.concatenate(ref["o"])).max()),
+            lse=float(np.abs(lse - np.concatenate(ref["lse"], axis=1)).max()),
+            dq=_rel(np.concatenate([to_numpy(x) for x in dq_]), np.concatenate(ref["dq"])),
+            dk=_rel(to_numpy(dk), oracle.logical_rows(ref["dkpool"], bt, w.N, w.P)),
+            dv=_rel(to_numpy(dv), oracle.logical_rows(ref["dvpool"], bt, w.N, w.P)),
+        )
+        assert err["o"] <= 1e-2 and err["lse"] <= 1e-2, err
+        assert max(err["dq"], err["dk"], err["dv"]) <= 2e-2, err
+        return err
+    finally:
+        B.pkv_pool_destroy(pool)
+
+
+def _w(**kw):
+    base = dict(N=3072, C=1024, P=128, Hq=4, Hkv=2, d=128, dtype="bf16", table="perm",
+                keys="clustered", extra_pages=5, topk=(3, 1, 2), offload=True)
+    base.update(kw)
+    return synth.workload("qwen7b_sparse_1m_offload", **base)
+
+
+def test_offloaded_sparse_sweep_matches_oracle():
+    # 24 pages; a chunk stages only the union of its selections (at most 24 pages)
+    _offloaded_sweep(_w(), n_slots=24, sparse=True)
+
+
+def test_offloaded_dense_sweep_matches_oracle():
+    w = _w(N=2048, keys="normal")
+    _offloaded_sweep(w, n_slots=w.n_pages, sparse=False)
+
+
+def test_staging_more_pages_than_slots_is_reported():
+    w = _w(N=1024, C=1024)
+    pool = B.pkv_pool_create(w.P, w.Hkv, w.Hq, w.d, B.PKV_BF16, w.n_phys,
+                             residency=B.PKV_RES_PINNED_HOST, n_device_slots=3)
+    try:
+        seq = B.pkv_seq_create(pool)
+        kv = to_device(synth.chunk_k(w, 0), "bf16")
+        B.pkv_append(seq, kv, kv, w.N)
+        B.pkv_prefetch(seq, None, 0, B.PKV_STAGE_KV, None)   # 8 pages into 3 slots
+        with pytest.raises(B.PkvError) as e:
+            B.pkv_check(pool)
+        assert e.value.status == B.PKV_ERR_DEVICE_FAULT and "slots" in str(e.value)
+        B.pkv_check(pool)                                   # the error word was cleared
+        with pytest.raises(B.PkvError) as e:
+            B.pkv_prefetch(seq, None, 0, 8, None)           # unknown staging flag
+        assert e.value.status == B.PKV_ERR_INVALID
+    finally:
+        B.pkv_pool_destroy(pool)
+
+
+def test_offload_calls_reject_device_pools():
+    pool = B.pkv_pool_create(128, 1, 2, 128, B.PKV_BF16, 4)
+    try:
+        seq = B.pkv_seq_create(pool)
+        for f in (lambda: B.pkv_prefetch(seq), lambda: B.pkv_writeback_grads(seq),
+                  lambda: B.pkv_wait(seq)):
+            with pytest.raises(B.PkvError) as e:
+                f()
+            assert e.value.status == B.PKV_ERR_INVALID
+    finally:
+        B.pkv_pool_destroy(pool)
