@@ -36,7 +36,8 @@ namespace {
 
 using tc::drain_wait;
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;     // warp 0 TMA, warp 1 MMA, warps 2..9 two softmax warpgroups
+constexpr int kSoftmaxThreads = 256;
 constexpr uint32_t KB = 1024;
 
 struct BwdParams {
@@ -64,32 +65,36 @@ __device__ __forceinline__ int sel_count(const BwdParams& p, int qp, int kvh) {
     return n;
 }
 
-__device__ __forceinline__ void store_row_bf16x64(uint8_t* tile, int row, const uint32_t (&w)[32]) {
-    // 64 bf16 (32 words) of one row of a [rows][64] tile with the 128-byte swizzle.
+
+// 32 bf16 (16 words) of one row: chunks [4 half, 4 half + 4) of a 128-byte-swizzled row.
+__device__ __forceinline__ void store_row_half(uint8_t* tile, int row, int half, const uint32_t (&w)[16]) {
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch)
-        *reinterpret_cast<uint4*>(tile + tc::sw128_offset(row, ch)) =
+    for (int ch = 0; ch < 4; ++ch)
+        *reinterpret_cast<uint4*>(tile + tc::sw128_offset(row, half * 4 + ch)) =
             make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
 }
 
 // ============================================================================ dK / dV
 
 // Shared-memory layout (offsets from a 1024-aligned base).
+// Q/dO stage for tile t+1 is the one tile t-2 used: the load has a full
+// iteration of slack behind the gradient products of tile t-1.
+constexpr int kv_STAGES = 3;
 constexpr uint32_t kv_K = 0;                 // [128 keys][128 d]: two 16 KB halves
 constexpr uint32_t kv_V = 32 * KB;
-constexpr uint32_t kv_Q = 64 * KB;           // 2 stages x [64 q][128 d]: two 8 KB halves
-constexpr uint32_t kv_dO = 96 * KB;          // 2 stages
-constexpr uint32_t kv_PT = 128 * KB;         // 2 buffers x [128 keys][64 q] (16 KB)
-constexpr uint32_t kv_DST = 160 * KB;        // 2 buffers
-constexpr uint32_t kv_STAT = 192 * KB;       // 2 stages x (64 lse*log2e + 64 D) floats
-constexpr uint32_t kv_SMEM = kv_STAT + 2 * 512 + 1024;
+constexpr uint32_t kv_Q = 64 * KB;           // stages x [64 q][128 d]: two 8 KB halves
+constexpr uint32_t kv_dO = kv_Q + kv_STAGES * 16 * KB;
+constexpr uint32_t kv_PT = kv_dO + kv_STAGES * 16 * KB;   // [128 keys][64 q] (16 KB)
+constexpr uint32_t kv_DST = kv_PT + 16 * KB;
+constexpr uint32_t kv_STAT = kv_DST + 16 * KB;   // stages x (64 lse*log2e + 64 D) floats
+constexpr uint32_t kv_SMEM = kv_STAT + kv_STAGES * 512 + 1024;
 
 struct __align__(8) KVBar {
     uint64_t kv_full;
-    uint64_t qdo_full[2], qdo_empty[2];
+    uint64_t qdo_full[kv_STAGES], qdo_empty[kv_STAGES];
     uint64_t s_full[2];
     uint64_t p_full[2];
-    uint64_t pt_free[2];
+    uint64_t pt_free;
     uint64_t acc_done;
     uint64_t drain;
     uint32_t tmem_base;
@@ -146,13 +151,15 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     if (threadIdx.x == 0) {
         tc::mbar_init(&B.kv_full, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kv_STAGES; ++s) {
             tc::mbar_init(&B.qdo_full[s], 32);
             tc::mbar_init(&B.qdo_empty[s], 1);
-            tc::mbar_init(&B.s_full[s], 1);
-            tc::mbar_init(&B.p_full[s], 128);
-            tc::mbar_init(&B.pt_free[s], 1);
         }
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(&B.s_full[s], 1);
+            tc::mbar_init(&B.p_full[s], kSoftmaxThreads);
+        }
+        tc::mbar_init(&B.pt_free, 1);
         tc::mbar_init(&B.acc_done, 1);
         tc::mbar_init(&B.drain, 1);
         tc::fence_barrier_init();
@@ -187,9 +194,9 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         int issued = 0;
         for (int t = 0; t < T; ++t) {
-            const int st = t & 1;
-            if (t >= 2) {
-                bool ok = tc::mbar_wait(&B.qdo_empty[st], ((t >> 1) - 1) & 1, p.err);
+            const int st = t % kv_STAGES;
+            if (t >= kv_STAGES) {
+                bool ok = tc::mbar_wait(&B.qdo_empty[st], ((t / kv_STAGES) - 1) & 1, p.err);
                 if (!__all_sync(0xffffffffu, ok)) break;
             }
             const int h = kvh * g + t / n_i;
@@ -219,7 +226,8 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         if (lane == 0) {
             drain_wait(&B.kv_full, 0);
-            for (int t = max(0, issued - 2); t < issued; ++t) drain_wait(&B.qdo_full[t & 1], (t >> 1) & 1);
+            for (int t = max(0, issued - kv_STAGES); t < issued; ++t)
+                drain_wait(&B.qdo_full[t % kv_STAGES], (t / kv_STAGES) & 1);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
@@ -229,14 +237,14 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const uint32_t sK = tc::smem_u32(smem + kv_K), sV = tc::smem_u32(smem + kv_V);
             const uint32_t t_dK = tmem + 256, t_dV = tmem + 384;
             bool ok = tc::mbar_wait(&B.kv_full, 0, p.err);
+            const uint32_t sPT = tc::smem_u32(smem + kv_PT);
+            const uint32_t sDST = tc::smem_u32(smem + kv_DST);
             auto issue_grad = [&](int t) -> bool {
-                const int b = t & 1;
-                if (!tc::mbar_wait(&B.p_full[b], (t >> 1) & 1, p.err)) return false;
+                const int st = t % kv_STAGES;
+                if (!tc::mbar_wait(&B.p_full[t & 1], (t >> 1) & 1, p.err)) return false;
                 tc::tc_fence_after();
-                const uint32_t sPT = tc::smem_u32(smem + kv_PT + b * 16 * KB);
-                const uint32_t sDST = tc::smem_u32(smem + kv_DST + b * 16 * KB);
-                const uint32_t sQ = tc::smem_u32(smem + kv_Q + b * 16 * KB);
-                const uint32_t sdO = tc::smem_u32(smem + kv_dO + b * 16 * KB);
+                const uint32_t sQ = tc::smem_u32(smem + kv_Q + st * 16 * KB);
+                const uint32_t sdO = tc::smem_u32(smem + kv_dO + st * 16 * KB);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)      // K = 64 queries, 16 per MMA
                     tc::mma_bf16(t_dV, tc::sdesc(sPT + kk * 32, 16, 1024),
@@ -247,17 +255,17 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     tc::mma_bf16(t_dK, tc::sdesc(sDST + kk * 32, 16, 1024),
                                  tc::sdesc(sQ + kk * 2048, 8 * KB, 1024), id_g,
                                  (t > 0 || kk > 0) ? 1u : 0u);
-                tc::mma_commit(&B.qdo_empty[b]);
-                tc::mma_commit(&B.pt_free[b]);
+                tc::mma_commit(&B.qdo_empty[st]);
+                tc::mma_commit(&B.pt_free);
                 return true;
             };
             for (int t = 0; ok && t < T; ++t) {
-                const int st = t & 1;
-                if (!tc::mbar_wait(&B.qdo_full[st], (t >> 1) & 1, p.err)) { ok = false; break; }
+                const int st = t % kv_STAGES;
+                if (!tc::mbar_wait(&B.qdo_full[st], (t / kv_STAGES) & 1, p.err)) { ok = false; break; }
                 tc::tc_fence_after();
                 const uint32_t sQ = tc::smem_u32(smem + kv_Q + st * 16 * KB);
                 const uint32_t sdO = tc::smem_u32(smem + kv_dO + st * 16 * KB);
-                const uint32_t t_S = tmem + st * 128, t_dP = t_S + 64;
+                const uint32_t t_S = tmem + (t & 1) * 128, t_dP = t_S + 64;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t oa = (kk >> 2) * 16 * KB + (kk & 3) * 32;
@@ -272,7 +280,7 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     tc::mma_bf16(t_dP, tc::sdesc(sV + oa, 16, 1024), tc::sdesc(sdO + ob, 16, 1024), id_s,
                                  kk > 0 ? 1u : 0u);
                 }
-                tc::mma_commit(&B.s_full[st]);
+                tc::mma_commit(&B.s_full[t & 1]);
                 if (t > 0 && !issue_grad(t - 1)) { ok = false; break; }
             }
             if (ok && T > 0 && issue_grad(T - 1)) tc::mma_commit(&B.acc_done);
@@ -281,6 +289,9 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
     } else {
         // ---------------------------------------------------------------- softmax-grad warps
+        // Two warpgroups: warpgroup wg handles query columns [32 wg, 32 wg + 32)
+        // of every key row (TMEM lane quadrant = warp % 4).
+        const int wg = (warp - 2) >> 2;
         const int quad = warp & 3;
         const int r = quad * 32 + lane;                      // key row of the page
         const int64_t kpos = kfirst + r;
@@ -288,76 +299,79 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const float sl2 = rsqrtf(128.f) * kLog2e;
         bool ok = true;
         for (int t = 0; t < T; ++t) {
-            const int st = t & 1;
-            ok = tc::mbar_wait(&B.s_full[st], (t >> 1) & 1, p.err) &&
-                 tc::mbar_wait(&B.qdo_full[st], (t >> 1) & 1, p.err);
+            const int sb = t & 1, st = t % kv_STAGES;
+            ok = tc::mbar_wait(&B.s_full[sb], (t >> 1) & 1, p.err) &&
+                 tc::mbar_wait(&B.qdo_full[st], (t / kv_STAGES) & 1, p.err);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc::tc_fence_after();
             const int i = tile_of(t);
-            const int64_t q0 = p.q_start + (int64_t)i * 64;  // position of column 0
-            const bool diag = kfirst + 127 > q0;
-            const float* sst = stat + st * 128;
-            uint32_t pw[32], dw[32];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {           // 32 query columns at a time
-                uint32_t sv[32], dv[32];
-                tc::tmem_ld32(lane_base + st * 128 + half * 32, sv);
-                tc::tmem_ld32(lane_base + st * 128 + 64 + half * 32, dv);
-                tc::tmem_wait_ld(sv);
-                tc::tmem_wait_ld(dv);
+            const int64_t q0 = p.q_start + (int64_t)i * 64 + wg * 32;   // position of my column 0
+            const float* sst = stat + st * 128 + wg * 32;
+            uint32_t sv[32], dv[32];
+            tc::tmem_ld32(lane_base + sb * 128 + wg * 32, sv);
+            tc::tmem_ld32(lane_base + sb * 128 + 64 + wg * 32, dv);
+            tc::tmem_wait_ld(sv);
+            tc::tmem_wait_ld(dv);
+            uint32_t pw[16], dw[16];
+            if (kfirst + 127 > q0) {                         // crosses the diagonal: mask
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
                     float pr[2], dr[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const int cc = half * 32 + c + e;
-                        float pv = fast_exp2(__uint_as_float(sv[c + e]) * sl2 - sst[cc]);
-                        if (diag && kpos > q0 + cc) pv = 0.f;
+                        float pv = fast_exp2(fmaf(__uint_as_float(sv[c + e]), sl2, -sst[c + e]));
+                        if (kpos > q0 + c + e) pv = 0.f;
                         pr[e] = pv;
-                        dr[e] = pv * (__uint_as_float(dv[c + e]) - sst[64 + cc]);
+                        dr[e] = pv * (__uint_as_float(dv[c + e]) - sst[64 + c + e]);
                     }
-                    pw[half * 16 + c / 2] = pack_bf16x2(pr[0], pr[1]);
-                    dw[half * 16 + c / 2] = pack_bf16x2(dr[0], dr[1]);
+                    pw[c / 2] = pack_bf16x2(pr[0], pr[1]);
+                    dw[c / 2] = pack_bf16x2(dr[0], dr[1]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    float pr[2], dr[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        pr[e] = fast_exp2(fmaf(__uint_as_float(sv[c + e]), sl2, -sst[c + e]));
+                        dr[e] = pr[e] * (__uint_as_float(dv[c + e]) - sst[64 + c + e]);
+                    }
+                    pw[c / 2] = pack_bf16x2(pr[0], pr[1]);
+                    dw[c / 2] = pack_bf16x2(dr[0], dr[1]);
                 }
             }
-            if (t >= 2) {
-                ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.pt_free[st], ((t >> 1) - 1) & 1, p.err));
+            if (t >= 1) {                                    // gradient products of t-1 done
+                ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.pt_free, (t - 1) & 1, p.err));
                 if (!ok) break;
             }
-            store_row_bf16x64(smem + kv_PT + st * 16 * KB, r, pw);
-            store_row_bf16x64(smem + kv_DST + st * 16 * KB, r, dw);
+            store_row_half(smem + kv_PT, r, wg, pw);
+            store_row_half(smem + kv_DST, r, wg, dw);
             tc::fence_proxy_async_smem();
             tc::tc_fence_before();
-            tc::mbar_arrive(&B.p_full[st]);
+            tc::mbar_arrive(&B.p_full[sb]);
         }
         if (ok && T > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.acc_done, 0, p.err));
         if (ok && T > 0) {
+            // Warpgroup 0 adds dK (scaled), warpgroup 1 adds dV.
             tc::tc_fence_after();
             const bool live = kpos < p.q_start + p.n_q;
             const size_t off = (((size_t)pp * p.Hkv + kvh) * 128 + r) * 128;
-            const float scale = rsqrtf(128.f);
+            const float scale = wg == 0 ? rsqrtf(128.f) : 1.f;
+            float* dst = (wg == 0 ? p.dkpool : p.dvpool) + off;
+            const uint32_t col = wg == 0 ? 256 : 384;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t a[32];
-                tc::tmem_ld32(lane_base + 256 + c * 32, a);
+                tc::tmem_ld32(lane_base + col + c * 32, a);
                 tc::tmem_wait_ld(a);
                 if (live) {
 #pragma unroll
                     for (int v = 0; v < 8; ++v)
-                        red_add_v4(p.dkpool + off + c * 32 + v * 4, __uint_as_float(a[4 * v]) * scale,
+                        red_add_v4(dst + c * 32 + v * 4, __uint_as_float(a[4 * v]) * scale,
                                    __uint_as_float(a[4 * v + 1]) * scale,
                                    __uint_as_float(a[4 * v + 2]) * scale,
                                    __uint_as_float(a[4 * v + 3]) * scale);
-                }
-                tc::tmem_ld32(lane_base + 384 + c * 32, a);
-                tc::tmem_wait_ld(a);
-                if (live) {
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        red_add_v4(p.dvpool + off + c * 32 + v * 4, __uint_as_float(a[4 * v]),
-                                   __uint_as_float(a[4 * v + 1]), __uint_as_float(a[4 * v + 2]),
-                                   __uint_as_float(a[4 * v + 3]));
                 }
             }
         }
@@ -376,7 +390,7 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 constexpr uint32_t q_Q = 0;                  // [128 q][128 d]: two 16 KB halves
 constexpr uint32_t q_dO = 32 * KB;
 constexpr uint32_t q_KV = 64 * KB;           // 3 stages x (K 16 KB + V 16 KB), [64 keys][128 d]
-constexpr int q_STAGES = 3;
+constexpr int q_STAGES = 4;      // the stage for tile t+1 was freed by dQ of tile t-3
 constexpr uint32_t q_DS = q_KV + q_STAGES * 32 * KB;   // 2 buffers x [128 q][64 keys] (16 KB)
 constexpr uint32_t q_SMEM = q_DS + 32 * KB + 1024;
 
@@ -417,7 +431,7 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         for (int s = 0; s < 2; ++s) {
             tc::mbar_init(&B.s_full[s], 1);
-            tc::mbar_init(&B.ds_full[s], 128);
+            tc::mbar_init(&B.ds_full[s], kSoftmaxThreads);
             tc::mbar_init(&B.ds_free[s], 1);
         }
         tc::mbar_init(&B.acc_done, 1);
@@ -518,6 +532,9 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             drain_wait(&B.drain, 0);
         }
     } else {
+        // Two warpgroups: warpgroup wg handles key columns [32 wg, 32 wg + 32) of
+        // every query row, and dQ columns [64 wg, 64 wg + 64) in the epilogue.
+        const int wg = (warp - 2) >> 2;
         const int quad = warp & 3;
         const int r = quad * 32 + lane;                      // query row of the tile
         const int64_t q_local = (int64_t)qt * 128 + r;
@@ -534,34 +551,42 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.s_full[sb], (t >> 1) & 1, p.err));
             if (!ok) break;
             tc::tc_fence_after();
-            const int64_t kbase = (int64_t)page_of(t) * 128 + (t & 1) * 64;
-            const bool diag = kbase + 63 > first_diag;
-            uint32_t dw[32];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {           // 32 key columns at a time
-                uint32_t sv[32], dv[32];
-                tc::tmem_ld32(lane_base + sb * 128 + half * 32, sv);
-                tc::tmem_ld32(lane_base + sb * 128 + 64 + half * 32, dv);
-                tc::tmem_wait_ld(sv);
-                tc::tmem_wait_ld(dv);
+            const int64_t kbase = (int64_t)page_of(t) * 128 + (t & 1) * 64 + wg * 32;
+            uint32_t sv[32], dv[32];
+            tc::tmem_ld32(lane_base + sb * 128 + wg * 32, sv);
+            tc::tmem_ld32(lane_base + sb * 128 + 64 + wg * 32, dv);
+            tc::tmem_wait_ld(sv);
+            tc::tmem_wait_ld(dv);
+            uint32_t dw[16];
+            if (kbase + 31 > first_diag) {                   // crosses the diagonal: mask
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
                     float dr[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const int cc = half * 32 + c + e;
-                        float pv = fast_exp2(__uint_as_float(sv[c + e]) * sl2 - lse2);
-                        if (diag && kbase + cc > qpos) pv = 0.f;
+                        float pv = fast_exp2(fmaf(__uint_as_float(sv[c + e]), sl2, -lse2));
+                        if (kbase + c + e > qpos) pv = 0.f;
                         dr[e] = pv * (__uint_as_float(dv[c + e]) - Dr);
                     }
-                    dw[half * 16 + c / 2] = pack_bf16x2(dr[0], dr[1]);
+                    dw[c / 2] = pack_bf16x2(dr[0], dr[1]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    float dr[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float pv = fast_exp2(fmaf(__uint_as_float(sv[c + e]), sl2, -lse2));
+                        dr[e] = pv * (__uint_as_float(dv[c + e]) - Dr);
+                    }
+                    dw[c / 2] = pack_bf16x2(dr[0], dr[1]);
                 }
             }
             if (t >= 2) {
                 ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.ds_free[sb], ((t >> 1) - 1) & 1, p.err));
                 if (!ok) break;
             }
-            store_row_bf16x64(smem + q_DS + sb * 16 * KB, r, dw);
+            store_row_half(smem + q_DS + sb * 16 * KB, r, wg, dw);
             tc::fence_proxy_async_smem();
             tc::tc_fence_before();
             tc::mbar_arrive(&B.ds_full[sb]);
@@ -572,7 +597,7 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const float scale = rsqrtf(128.f);
             __nv_bfloat16* row = static_cast<__nv_bfloat16*>(p.dq) + ((size_t)q_local * p.Hq + h) * 128;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
                 uint32_t a[32];
                 tc::tmem_ld32(lane_base + 256 + c * 32, a);
                 tc::tmem_wait_ld(a);

@@ -34,11 +34,14 @@ constexpr int kThreads = 192;
 constexpr uint32_t kHalfBytes = 128 * 128;   // [128 rows][64 bf16] = 16 KB
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;
 // Shared-memory tile offsets (bytes from a 1024-aligned base).
+// K and V have separate rings: a K stage is free as soon as S_j completes, so
+// K loads run kKStages - 1 tiles ahead; a V stage is free after PV_j.
+constexpr int kKStages = 3, kVStages = 2;
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTileBytes;          // 2 stages
-constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;      // 2 stages
-constexpr uint32_t kOffP = kOffV + 2 * kTileBytes;
-constexpr uint32_t kTilesBytes = kOffP + kTileBytes;    // 192 KB
+constexpr uint32_t kOffK = kOffQ + kTileBytes;
+constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
+constexpr uint32_t kOffP = kOffV + kVStages * kTileBytes;
+constexpr uint32_t kTilesBytes = kOffP + kTileBytes;    // 224 KB
 constexpr uint32_t kSmemBytes = kTilesBytes + 1024;     // + alignment slack
 constexpr float kRescaleThreshold = 8.0f;               // log2 units
 
@@ -56,7 +59,7 @@ struct FwdParams {
 
 struct __align__(8) FwdBarriers {
     uint64_t q_full;
-    uint64_t k_full[2], v_full[2], kv_empty[2];
+    uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
     uint64_t s_full[2];
     uint64_t p_full;
     uint64_t o_done;
@@ -94,12 +97,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
 
     if (threadIdx.x == 0) {
         tc::mbar_init(&B.q_full, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kKStages; ++s) {
             tc::mbar_init(&B.k_full[s], 1);
-            tc::mbar_init(&B.v_full[s], 1);
-            tc::mbar_init(&B.kv_empty[s], 1);
-            tc::mbar_init(&B.s_full[s], 1);
+            tc::mbar_init(&B.k_empty[s], 1);
         }
+        for (int s = 0; s < kVStages; ++s) {
+            tc::mbar_init(&B.v_full[s], 1);
+            tc::mbar_init(&B.v_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) tc::mbar_init(&B.s_full[s], 1);
         tc::mbar_init(&B.p_full, 128);
         tc::mbar_init(&B.o_done, 1);
         tc::mbar_init(&B.drain, 1);
@@ -118,18 +124,29 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tc::prefetch_tmap(&tmap_q);
-            tc::prefetch_tmap(&tmap_k);
-            tc::prefetch_tmap(&tmap_v);
-            const int q_row0 = (int)(qt * kTile);
-            tc::mbar_arrive_expect_tx(&B.q_full, kTileBytes);
-            tc::tma_load_3d(smem + kOffQ, &tmap_q, &B.q_full, 0, h, q_row0);
-            tc::tma_load_3d(smem + kOffQ + kHalfBytes, &tmap_q, &B.q_full, 64, h, q_row0);
+        // Lane 0 streams Q then the K ring; lane 1 streams the V ring, so a K load
+        // never waits behind a V stage that is still in use.
+        if (lane < 2) {
+            const bool is_k = lane == 0;
+            const int nst = is_k ? kKStages : kVStages;
+            uint64_t* full = is_k ? B.k_full : B.v_full;
+            uint64_t* empty = is_k ? B.k_empty : B.v_empty;
+            const CUtensorMap* tm = is_k ? &tmap_k : &tmap_v;
+            uint8_t* base = smem + (is_k ? kOffK : kOffV);
+            if (is_k) {
+                tc::prefetch_tmap(&tmap_q);
+                tc::prefetch_tmap(&tmap_k);
+                const int q_row0 = (int)(qt * kTile);
+                tc::mbar_arrive_expect_tx(&B.q_full, kTileBytes);
+                tc::tma_load_3d(smem + kOffQ, &tmap_q, &B.q_full, 0, h, q_row0);
+                tc::tma_load_3d(smem + kOffQ + kHalfBytes, &tmap_q, &B.q_full, 64, h, q_row0);
+            } else {
+                tc::prefetch_tmap(&tmap_v);
+            }
             int issued = 0;
             for (int j = 0; j < nt; ++j) {
-                const int st = j & 1;
-                if (j >= 2 && !tc::mbar_wait(&B.kv_empty[st], ((j >> 1) - 1) & 1, p.err)) break;
+                const int st = j % nst;
+                if (j >= nst && !tc::mbar_wait(&empty[st], ((j / nst) - 1) & 1, p.err)) break;
                 const int32_t lp = tile_page(p, qt, kvh, j);
                 const int32_t pp = (lp >= 0) ? p.bt[lp] : -1;
                 if (pp < 0 || pp >= p.num_phys) {
@@ -137,22 +154,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
                     break;
                 }
                 const int row = (int)(((int64_t)pp * p.Hkv + kvh) * kTile);
-                uint8_t* kdst = smem + kOffK + st * kTileBytes;
-                uint8_t* vdst = smem + kOffV + st * kTileBytes;
-                tc::mbar_arrive_expect_tx(&B.k_full[st], kTileBytes);
-                tc::tma_load_2d(kdst, &tmap_k, &B.k_full[st], 0, row);
-                tc::tma_load_2d(kdst + kHalfBytes, &tmap_k, &B.k_full[st], 64, row);
-                tc::mbar_arrive_expect_tx(&B.v_full[st], kTileBytes);
-                tc::tma_load_2d(vdst, &tmap_v, &B.v_full[st], 0, row);
-                tc::tma_load_2d(vdst + kHalfBytes, &tmap_v, &B.v_full[st], 64, row);
+                uint8_t* dst = base + st * kTileBytes;
+                tc::mbar_arrive_expect_tx(&full[st], kTileBytes);
+                tc::tma_load_2d(dst, tm, &full[st], 0, row);
+                tc::tma_load_2d(dst + kHalfBytes, tm, &full[st], 64, row);
                 issued = j + 1;
             }
             // Make sure none of this CTA's copies is still landing when it exits.
-            drain_wait(&B.q_full, 0);
-            for (int j = max(0, issued - 2); j < issued; ++j) {
-                drain_wait(&B.k_full[j & 1], (j >> 1) & 1);
-                drain_wait(&B.v_full[j & 1], (j >> 1) & 1);
-            }
+            if (is_k) drain_wait(&B.q_full, 0);
+            for (int j = max(0, issued - nst); j < issued; ++j) drain_wait(&full[j % nst], (j / nst) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -165,9 +175,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
             bool ok = tc::mbar_wait(&B.q_full, 0, p.err);
             auto issue_pv = [&](int i) -> bool {
                 if (!tc::mbar_wait(&B.p_full, i & 1, p.err)) return false;
-                if (!tc::mbar_wait(&B.v_full[i & 1], (i >> 1) & 1, p.err)) return false;
+                if (!tc::mbar_wait(&B.v_full[i % kVStages], (i / kVStages) & 1, p.err)) return false;
                 tc::tc_fence_after();
-                const uint32_t sv = tc::smem_u32(smem + kOffV + (i & 1) * kTileBytes);
+                const uint32_t sv = tc::smem_u32(smem + kOffV + (i % kVStages) * kTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     // A = P [128 q][128 keys] K-major; B = V [128 keys][128 d] MN-major:
@@ -178,22 +188,23 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
                     tc::mma_bf16(tmem_o, a, b, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc::mma_commit(&B.o_done);
-                tc::mma_commit(&B.kv_empty[i & 1]);
+                tc::mma_commit(&B.v_empty[i % kVStages]);
                 return true;
             };
             for (int j = 0; ok && j < nt; ++j) {
-                const int st = j & 1;
-                if (!tc::mbar_wait(&B.k_full[st], (j >> 1) & 1, p.err)) { ok = false; break; }
+                const int ks = j % kKStages;
+                if (!tc::mbar_wait(&B.k_full[ks], (j / kKStages) & 1, p.err)) { ok = false; break; }
                 tc::tc_fence_after();
-                const uint32_t sk = tc::smem_u32(smem + kOffK + st * kTileBytes);
-                const uint32_t tmem_s = tmem + st * 128;
+                const uint32_t sk = tc::smem_u32(smem + kOffK + ks * kTileBytes);
+                const uint32_t tmem_s = tmem + (j & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t koff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
                     tc::mma_bf16(tmem_s, tc::sdesc(sq + koff, 16, 1024), tc::sdesc(sk + koff, 16, 1024),
                                  idesc, kk > 0 ? 1u : 0u);
                 }
-                tc::mma_commit(&B.s_full[st]);
+                tc::mma_commit(&B.s_full[j & 1]);
+                tc::mma_commit(&B.k_empty[ks]);
                 if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
             }
             if (ok && nt > 0) issue_pv(nt - 1);
@@ -217,6 +228,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc::tc_fence_after();
+            // Raw logits q.k; the scale is folded into the exp2 argument below.
             float x[128];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -224,16 +236,25 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
                 tc::tmem_ld32(lane_base + st * 128 + c * 32, r);
                 tc::tmem_wait_ld(r);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(r[e]) * sl2;
+                for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(r[e]);
             }
             if (j == nt - 1) {                        // own page: causal mask (key col > row)
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
                     if (c > row) x[c] = -INFINITY;
             }
-            float mx = x[0];
+            // Row max with 8 independent chains (a single chain of 128 dependent
+            // max operations would dominate the tile's latency).
+            float mpart[8];
 #pragma unroll
-            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+            for (int k = 0; k < 8; ++k) mpart[k] = x[k];
+#pragma unroll
+            for (int c = 8; c < 128; ++c) mpart[c & 7] = fmaxf(mpart[c & 7], x[c]);
+#pragma unroll
+            for (int k = 4; k > 0; k >>= 1)
+#pragma unroll
+                for (int i = 0; i < k; ++i) mpart[i] = fmaxf(mpart[i], mpart[i + k]);
+            const float mx = mpart[0] * sl2;          // scaled, log2 units
             float alpha = 1.f;
             bool rescale = false;
             if (mx > m + kRescaleThreshold) {
@@ -243,16 +264,24 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
             }
             l *= alpha;
             uint32_t pk[64];
-            float ls = 0.f;
+            float lpart[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) lpart[k] = 0.f;
+            const float neg_m = -m;
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
-                const float p0 = fast_exp2(x[2 * c] - m), p1 = fast_exp2(x[2 * c + 1] - m);
+                const float p0 = fast_exp2(fmaf(x[2 * c], sl2, neg_m));
+                const float p1 = fast_exp2(fmaf(x[2 * c + 1], sl2, neg_m));
                 pk[c] = pack_bf16x2(p0, p1);
                 // Normalise by the sum of the bf16 weights the tensor core multiplies, so
                 // O is a convex combination of values whatever the rounding of P.
-                ls += bf16lo(pk[c]) + bf16hi(pk[c]);
+                lpart[c & 7] += bf16lo(pk[c]) + bf16hi(pk[c]);
             }
-            l += ls;
+#pragma unroll
+            for (int k = 4; k > 0; k >>= 1)
+#pragma unroll
+                for (int i = 0; i < k; ++i) lpart[i] += lpart[i + k];
+            l += lpart[0];
             if (j > 0) {                              // PV_{j-1} done: P buffer free, O stable
                 ok = tc::mbar_wait(&B.o_done, (j - 1) & 1, p.err);
                 ok = __all_sync(0xffffffffu, ok);
