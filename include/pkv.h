@@ -118,7 +118,8 @@ pkv_status pkv_check(pkv_pool* pool);
  * creation, once: appends never allocate device memory. */
 
 /* Creates a pool on the current CUDA device. Validates desc; PKV_ERR_OOM if
- * the page memory cannot be allocated. *out is NULL on failure. */
+ * the page memory cannot be allocated. *out is NULL on failure. Synchronous
+ * (synchronizes the device): the pool is fully initialised on return. */
 pkv_status pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out);
 
 /* Frees everything the pool owns, including its sequences. NULL-safe.
@@ -136,7 +137,8 @@ pkv_status pkv_pool_arrays(const pkv_pool* pool, void** k, void** v, float** dk,
 
 /* ---------------------------------------------------------------- sequences */
 
-/* A sequence (one layer's KV of one sample) with an empty block table. */
+/* A sequence (one layer's KV of one sample) with an empty block table.
+ * Synchronous (synchronizes the device). */
 pkv_status pkv_seq_create(pkv_pool* pool, pkv_seq** out);
 
 /* Returns the sequence's pages to the free list and frees it. NULL-safe.
@@ -252,8 +254,10 @@ pkv_status pkv_page_topk(pkv_seq* seq, const void* q, int64_t q_start, int64_t n
  * of the pool uses the slots at a time (one pool per layer to prefetch layer
  * l+1 while layer l computes).
  *
- * pkv_prefetch: on stream `side`, after the sequence's last append or
- * attention call (an internal event), stages the logical pages listed in
+ * pkv_prefetch: on stream `side`, after the sequence's last append, page
+ * selection or attention call (an internal event; a page list produced by
+ * anything else must already be ordered before `side`), stages the logical
+ * pages listed in
  * device int32 logical_pages[0..n) -- duplicates and -1 entries are ignored,
  * so a selection array from pkv_page_topk can be passed flattened -- or every
  * page of the sequence if logical_pages is NULL (n = 0). Pages get slots in

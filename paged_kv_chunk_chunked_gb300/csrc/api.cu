@@ -298,6 +298,12 @@ pkv_status pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
         }
         p->tmaps_ready = true;
     }
+    // Pool creation is synchronous: the memsets above are complete before any
+    // stream, blocking or not, uses the pool.
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) {
+        cleanup();
+        return cuda_fail(e, "pkv_pool_create: sync");
+    }
     *out = p;
     return PKV_OK;
 }
@@ -355,6 +361,9 @@ pkv_status pkv_seq_create(pkv_pool* p, pkv_seq** out) {
             if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->staged, cudaEventDisableTiming);
             if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->used, cudaEventDisableTiming);
         }
+        // The initialisation above must be complete before any stream (including a
+        // non-blocking side stream) touches the sequence.
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
         if (e != cudaSuccess) {
             cudaFreeHost(s->h_bt);
             cudaFree(s->d_bt); cudaFree(s->d_slot_of); cudaFree(s->d_slot_page); cudaFree(s->d_flags);
@@ -617,6 +626,8 @@ pkv_status pkv_page_topk(pkv_seq* s, const void* q, int64_t q_start, int64_t n_q
     }
     cudaError_t e = launch_page_topk(p, s->d_bt, q, q_start, n_q, k, n_sink, n_local, pages_out,
                                      counts_out, p->sel_scratch, static_cast<cudaStream_t>(stream));
+    // A later pkv_prefetch of this selection must wait for it.
+    if (e == cudaSuccess && s->used) e = cudaEventRecord(s->used, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "pkv_page_topk: launch");
     return PKV_OK;
 }

@@ -192,37 +192,53 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tc::tma_load_2d(smem + kv_V, &tm_v, &B.kv_full, 0, row);
             tc::tma_load_2d(smem + kv_V + 16 * KB, &tm_v, &B.kv_full, 64, row);
         }
-        int issued = 0;
-        for (int t = 0; t < T; ++t) {
-            const int st = t % kv_STAGES;
-            if (t >= kv_STAGES) {
-                bool ok = tc::mbar_wait(&B.qdo_empty[st], ((t / kv_STAGES) - 1) & 1, p.err);
-                if (!__all_sync(0xffffffffu, ok)) break;
-            }
+        // Per-query statistics of tile t (log2e * LSE, +inf past the chunk, and D),
+        // two columns per lane; loaded one tile ahead so their latency overlaps
+        // the wait for the next free stage.
+        auto load_stats = [&](int t, float (&s)[4]) {
+            if (t >= T) return;
             const int h = kvh * g + t / n_i;
             const int i = tile_of(t);
-            // per-query statistics for this tile: log2e * LSE (+inf past the chunk) and D
-            float* sst = stat + st * 128;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const int c = lane * 2 + e;
-                const int64_t q = (int64_t)i * 64 + c;
+                const int64_t q = (int64_t)i * 64 + lane * 2 + e;
                 const bool v = q < p.n_q;
-                sst[c] = v ? p.lse[(size_t)h * p.n_q + q] * kLog2e : INFINITY;
-                sst[64 + c] = v ? p.Dbuf[(size_t)h * p.n_q + q] : 0.f;
+                s[e] = v ? __ldg(p.lse + (size_t)h * p.n_q + q) * kLog2e : INFINITY;
+                s[2 + e] = v ? __ldg(p.Dbuf + (size_t)h * p.n_q + q) : 0.f;
             }
+        };
+        int issued = 0;
+        auto step = [&](int t, const float (&use)[4], float (&fill)[4]) -> bool {
+            const int st = t % kv_STAGES;
+            if (t >= kv_STAGES &&
+                !__all_sync(0xffffffffu, tc::mbar_wait(&B.qdo_empty[st], ((t / kv_STAGES) - 1) & 1, p.err)))
+                return false;
             if (lane == 0) {
+                const int h = kvh * g + t / n_i;
+                const int i = tile_of(t);
                 uint8_t* q_dst = smem + kv_Q + st * 16 * KB;
                 uint8_t* do_dst = smem + kv_dO + st * 16 * KB;
-                tc::mbar_arrive_expect_tx(&B.qdo_full[st], 32 * KB);
+                tc::mbar_expect_tx(&B.qdo_full[st], 32 * KB);
                 tc::tma_load_3d(q_dst, &tm_q, &B.qdo_full[st], 0, h, i * 64);
                 tc::tma_load_3d(q_dst + 8 * KB, &tm_q, &B.qdo_full[st], 64, h, i * 64);
                 tc::tma_load_3d(do_dst, &tm_do, &B.qdo_full[st], 0, h, i * 64);
                 tc::tma_load_3d(do_dst + 8 * KB, &tm_do, &B.qdo_full[st], 64, h, i * 64);
-            } else {
-                tc::mbar_arrive(&B.qdo_full[st]);
             }
+            load_stats(t + 1, fill);
+            float* sst = stat + st * 128;
+            sst[lane * 2] = use[0];
+            sst[lane * 2 + 1] = use[1];
+            sst[64 + lane * 2] = use[2];
+            sst[64 + lane * 2 + 1] = use[3];
+            tc::mbar_arrive(&B.qdo_full[st]);           // 32 arrivals + the tx bytes
             issued = t + 1;
+            return true;
+        };
+        float sa[4], sb[4];
+        load_stats(0, sa);
+        for (int t = 0; t < T; t += 2) {
+            if (!step(t, sa, sb)) break;
+            if (t + 1 < T && !step(t + 1, sb, sa)) break;
         }
         if (lane == 0) {
             drain_wait(&B.kv_full, 0);
@@ -448,6 +464,7 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t tmem = B.tmem_base;
 
     if (warp == 0) {
+        // Whole-warp producer: page indices arrive 32 at a time (PageBatch); lane 0 copies.
         if (lane == 0) {
             tc::prefetch_tmap(&tm_k);
             tc::prefetch_tmap(&tm_v);
@@ -457,17 +474,22 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tc::tma_load_3d(smem + q_Q + 16 * KB, &tm_q, &B.q_full, 64, h, q_row0);
             tc::tma_load_3d(smem + q_dO, &tm_do, &B.q_full, 0, h, q_row0);
             tc::tma_load_3d(smem + q_dO + 16 * KB, &tm_do, &B.q_full, 64, h, q_row0);
-            int issued = 0;
-            for (int t = 0; t < T; ++t) {
-                const int st = t % q_STAGES;
-                if (t >= q_STAGES && !tc::mbar_wait(&B.kv_empty[st], ((t / q_STAGES) - 1) & 1, p.err))
-                    break;
-                const int32_t lp = page_of(t);
-                const int32_t pp = lp >= 0 ? p.bt[lp] : -1;
-                if (pp < 0 || pp >= p.num_phys) {
-                    report_error(p.err, kErrBadPage);
-                    break;
-                }
+        }
+        tc::PageBatch pages;
+        pages.init(p.bt, sel_row, T / 2, lane);
+        int issued = 0;
+        int32_t pp = -1;
+        for (int t = 0; t < T; ++t) {
+            const int st = t % q_STAGES;
+            if (t >= q_STAGES &&
+                !__all_sync(0xffffffffu, tc::mbar_wait(&B.kv_empty[st], ((t / q_STAGES) - 1) & 1, p.err)))
+                break;
+            if ((t & 1) == 0) pp = pages.get(t >> 1);
+            if (pp < 0 || pp >= p.num_phys) {
+                if (lane == 0) report_error(p.err, kErrBadPage);
+                break;
+            }
+            if (lane == 0) {
                 const int row = (int)(((int64_t)pp * p.Hkv + kvh) * 128 + (t & 1) * 64);
                 uint8_t* kd = smem + q_KV + st * 32 * KB;
                 tc::mbar_arrive_expect_tx(&B.kv_full[st], 32 * KB);
@@ -475,8 +497,10 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tc::tma_load_2d(kd + 8 * KB, &tm_k, &B.kv_full[st], 64, row);
                 tc::tma_load_2d(kd + 16 * KB, &tm_v, &B.kv_full[st], 0, row);
                 tc::tma_load_2d(kd + 24 * KB, &tm_v, &B.kv_full[st], 64, row);
-                issued = t + 1;
             }
+            issued = t + 1;
+        }
+        if (lane == 0) {
             drain_wait(&B.q_full, 0);
             for (int t = max(0, issued - q_STAGES); t < issued; ++t)
                 drain_wait(&B.kv_full[t % q_STAGES], (t / q_STAGES) & 1);

@@ -9,8 +9,9 @@
 //
 // One CTA per (query tile of 128 rows = one query page, query head); key
 // tiles are whole pages (P = 128), fetched by TMA with the physical page
-// taken from the block table. Warp roles (192 threads):
-//   warp 0      TMA producer: Q once, then K/V pages into a 2-stage ring.
+// taken from the block table. Warp roles (224 threads):
+//   warp 0      TMA producer: Q once, then K pages into a 3-stage ring.
+//   warp 6      TMA producer: V pages into a 2-stage ring.
 //   warp 1      MMA issuer (one thread): S_j = Q K_j^T into a double-buffered
 //               TMEM tile, then O += P_{j-1} V_{j-1} (O lives in TMEM).
 //   warps 2..5  softmax: one thread per query row; reads S_j from TMEM, keeps
@@ -30,7 +31,7 @@ namespace pkv {
 namespace {
 
 constexpr int kTile = 128;                   // query rows = keys per tile = head dim
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr uint32_t kHalfBytes = 128 * 128;   // [128 rows][64 bf16] = 16 KB
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;
 // Shared-memory tile offsets (bytes from a 1024-aligned base).
@@ -82,6 +83,55 @@ __device__ __forceinline__ int32_t tile_page(const FwdParams& p, int qt, int kvh
 
 using tc::drain_wait;
 
+// One producer warp: streams the K ring (and Q first) or the V ring. The whole
+// warp walks the tiles (page indices come 32 at a time from a PageBatch);
+// lane 0 issues the copies. A K load never waits behind a V stage in use.
+__device__ __forceinline__ void produce_ring(const FwdParams& p, uint8_t* smem, FwdBarriers& B,
+                                             const CUtensorMap& tmap_q, const CUtensorMap& tmap,
+                                             bool is_k, int qt, int h, int kvh, int nt, int lane) {
+    const int nst = is_k ? kKStages : kVStages;
+    uint64_t* full = is_k ? B.k_full : B.v_full;
+    uint64_t* empty = is_k ? B.k_empty : B.v_empty;
+    uint8_t* base = smem + (is_k ? kOffK : kOffV);
+    if (lane == 0) {
+        tc::prefetch_tmap(&tmap);
+        if (is_k) {
+            tc::prefetch_tmap(&tmap_q);
+            const int q_row0 = qt * kTile;
+            tc::mbar_arrive_expect_tx(&B.q_full, kTileBytes);
+            tc::tma_load_3d(smem + kOffQ, &tmap_q, &B.q_full, 0, h, q_row0);
+            tc::tma_load_3d(smem + kOffQ + kHalfBytes, &tmap_q, &B.q_full, 64, h, q_row0);
+        }
+    }
+    tc::PageBatch pages;
+    pages.init(p.bt, p.sel ? p.sel + ((size_t)qt * p.Hkv + kvh) * p.kmax : nullptr, nt, lane);
+    int issued = 0;
+    for (int j = 0; j < nt; ++j) {
+        const int st = j % nst;
+        if (j >= nst &&
+            !__all_sync(0xffffffffu, tc::mbar_wait(&empty[st], ((j / nst) - 1) & 1, p.err)))
+            break;
+        const int32_t pp = pages.get(j);
+        if (pp < 0 || pp >= p.num_phys) {
+            if (lane == 0) report_error(p.err, kErrBadPage);
+            break;
+        }
+        if (lane == 0) {
+            const int row = (int)(((int64_t)pp * p.Hkv + kvh) * kTile);
+            uint8_t* dst = base + st * kTileBytes;
+            tc::mbar_arrive_expect_tx(&full[st], kTileBytes);
+            tc::tma_load_2d(dst, &tmap, &full[st], 0, row);
+            tc::tma_load_2d(dst + kHalfBytes, &tmap, &full[st], 64, row);
+        }
+        issued = j + 1;
+    }
+    // Make sure none of this CTA's copies is still landing when it exits.
+    if (lane == 0) {
+        if (is_k) drain_wait(&B.q_full, 0);
+        for (int j = max(0, issued - nst); j < issued; ++j) drain_wait(&full[j % nst], (j / nst) & 1);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
               const __grid_constant__ CUtensorMap tmap_v, FwdParams p) {
@@ -123,47 +173,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     const int nt = B.n_tiles;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        // Lane 0 streams Q then the K ring; lane 1 streams the V ring, so a K load
-        // never waits behind a V stage that is still in use.
-        if (lane < 2) {
-            const bool is_k = lane == 0;
-            const int nst = is_k ? kKStages : kVStages;
-            uint64_t* full = is_k ? B.k_full : B.v_full;
-            uint64_t* empty = is_k ? B.k_empty : B.v_empty;
-            const CUtensorMap* tm = is_k ? &tmap_k : &tmap_v;
-            uint8_t* base = smem + (is_k ? kOffK : kOffV);
-            if (is_k) {
-                tc::prefetch_tmap(&tmap_q);
-                tc::prefetch_tmap(&tmap_k);
-                const int q_row0 = (int)(qt * kTile);
-                tc::mbar_arrive_expect_tx(&B.q_full, kTileBytes);
-                tc::tma_load_3d(smem + kOffQ, &tmap_q, &B.q_full, 0, h, q_row0);
-                tc::tma_load_3d(smem + kOffQ + kHalfBytes, &tmap_q, &B.q_full, 64, h, q_row0);
-            } else {
-                tc::prefetch_tmap(&tmap_v);
-            }
-            int issued = 0;
-            for (int j = 0; j < nt; ++j) {
-                const int st = j % nst;
-                if (j >= nst && !tc::mbar_wait(&empty[st], ((j / nst) - 1) & 1, p.err)) break;
-                const int32_t lp = tile_page(p, qt, kvh, j);
-                const int32_t pp = (lp >= 0) ? p.bt[lp] : -1;
-                if (pp < 0 || pp >= p.num_phys) {
-                    report_error(p.err, kErrBadPage);
-                    break;
-                }
-                const int row = (int)(((int64_t)pp * p.Hkv + kvh) * kTile);
-                uint8_t* dst = base + st * kTileBytes;
-                tc::mbar_arrive_expect_tx(&full[st], kTileBytes);
-                tc::tma_load_2d(dst, tm, &full[st], 0, row);
-                tc::tma_load_2d(dst + kHalfBytes, tm, &full[st], 64, row);
-                issued = j + 1;
-            }
-            // Make sure none of this CTA's copies is still landing when it exits.
-            if (is_k) drain_wait(&B.q_full, 0);
-            for (int j = max(0, issued - nst); j < issued; ++j) drain_wait(&full[j % nst], (j / nst) & 1);
-        }
+        // ------------------------------------------------------------ Q + K producer
+        produce_ring(p, smem, B, tmap_q, tmap_k, true, qt, h, kvh, nt, lane);
+    } else if (warp == kThreads / 32 - 1) {
+        // ------------------------------------------------------------ V producer
+        produce_ring(p, smem, B, tmap_q, tmap_v, false, qt, h, kvh, nt, lane);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {

@@ -44,6 +44,12 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");
 }
 
+// Raises the barrier's expected transaction bytes without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;"
+                 :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                  :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
@@ -120,6 +126,40 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
            "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
+
+// ------------------------------------------------------------------ page index stream
+
+// Warp-cooperative stream of physical page indices for a CTA's tiles 0..n-1:
+// tile j reads logical page sel[j] (or j when sel is null) through the block
+// table. Lane l loads the entry of tile base + l, 32 tiles per coalesced load,
+// one batch ahead, so the block-table reads never sit in front of a TMA
+// issue. Every lane of the warp calls get() with the same j, j = 0, 1, 2, ...
+struct PageBatch {
+    const int32_t* bt;
+    const int32_t* sel;
+    int n;
+    int lane;
+    int32_t cur, nxt;
+
+    __device__ __forceinline__ int32_t load(int base) const {
+        const int j = base + lane;
+        if (j >= n) return -1;
+        const int32_t lp = sel ? sel[j] : j;
+        return lp >= 0 ? bt[lp] : -1;
+    }
+    __device__ __forceinline__ void init(const int32_t* bt_, const int32_t* sel_, int n_, int lane_) {
+        bt = bt_; sel = sel_; n = n_; lane = lane_;
+        cur = load(0);
+        nxt = load(32);
+    }
+    __device__ __forceinline__ int32_t get(int j) {
+        if (j > 0 && (j & 31) == 0) {
+            cur = nxt;
+            nxt = load(j + 32);
+        }
+        return __shfl_sync(0xffffffffu, cur, j & 31);
+    }
+};
 
 // ------------------------------------------------------------------ tensor memory
 
