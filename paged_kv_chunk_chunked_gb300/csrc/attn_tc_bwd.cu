@@ -247,62 +247,73 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t id_s = tc::idesc_bf16(128, 64, false, false);    // S^T = K Q^T
-            const uint32_t id_g = tc::idesc_bf16(128, 128, false, true);    // dV += P^T dO
-            const uint32_t sK = tc::smem_u32(smem + kv_K), sV = tc::smem_u32(smem + kv_V);
-            const uint32_t t_dK = tmem + 256, t_dV = tmem + 384;
-            bool ok = tc::mbar_wait(&B.kv_full, 0, p.err);
-            const uint32_t sPT = tc::smem_u32(smem + kv_PT);
-            const uint32_t sDST = tc::smem_u32(smem + kv_DST);
-            auto issue_grad = [&](int t) -> bool {
-                const int st = t % kv_STAGES;
-                if (!tc::mbar_wait(&B.p_full[t & 1], (t >> 1) & 1, p.err)) return false;
-                tc::tc_fence_after();
-                const uint32_t sQ = tc::smem_u32(smem + kv_Q + st * 16 * KB);
-                const uint32_t sdO = tc::smem_u32(smem + kv_dO + st * 16 * KB);
+        // Whole warp runs the loop (warp-uniform descriptors); the elected lane issues.
+        const bool leader = tc::elect_one_sync();
+        const uint32_t id_s = tc::idesc_bf16(128, 64, false, false);    // S^T = K Q^T
+        const uint32_t id_g = tc::idesc_bf16(128, 128, false, true);    // dV += P^T dO
+        const uint32_t t_dK = tmem + 256, t_dV = tmem + 384;
+        bool ok = tc::warp_wait(&B.kv_full, 0, p.err);
+        // Base descriptors; each MMA advances them by a compile-time offset.
+        const uint64_t dK0 = tc::sdesc(tc::smem_u32(smem + kv_K), 16, 1024);
+        const uint64_t dV0 = tc::sdesc(tc::smem_u32(smem + kv_V), 16, 1024);
+        const uint64_t dPT0 = tc::sdesc(tc::smem_u32(smem + kv_PT), 16, 1024);
+        const uint64_t dDST0 = tc::sdesc(tc::smem_u32(smem + kv_DST), 16, 1024);
+        const uint64_t dQk0 = tc::sdesc(tc::smem_u32(smem + kv_Q), 16, 1024);        // K-major
+        const uint64_t ddOk0 = tc::sdesc(tc::smem_u32(smem + kv_dO), 16, 1024);
+        const uint64_t dQm0 = tc::sdesc(tc::smem_u32(smem + kv_Q), 8 * KB, 1024);    // MN-major
+        const uint64_t ddOm0 = tc::sdesc(tc::smem_u32(smem + kv_dO), 8 * KB, 1024);
+        auto issue_grad = [&](int t) -> bool {
+            const int st = t % kv_STAGES;
+            if (!tc::warp_wait(&B.p_full[t & 1], (t >> 1) & 1, p.err)) return false;
+            tc::tc_fence_after();
+            const uint32_t so = st * 16 * KB;
+            if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)      // K = 64 queries, 16 per MMA
-                    tc::mma_bf16(t_dV, tc::sdesc(sPT + kk * 32, 16, 1024),
-                                 tc::sdesc(sdO + kk * 2048, 8 * KB, 1024), id_g,
-                                 (t > 0 || kk > 0) ? 1u : 0u);
+                    tc::mma_bf16(t_dV, tc::sdesc_at(dPT0, kk * 32), tc::sdesc_at(ddOm0, so + kk * 2048),
+                                 id_g, (t > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    tc::mma_bf16(t_dK, tc::sdesc(sDST + kk * 32, 16, 1024),
-                                 tc::sdesc(sQ + kk * 2048, 8 * KB, 1024), id_g,
-                                 (t > 0 || kk > 0) ? 1u : 0u);
+                    tc::mma_bf16(t_dK, tc::sdesc_at(dDST0, kk * 32), tc::sdesc_at(dQm0, so + kk * 2048),
+                                 id_g, (t > 0 || kk > 0) ? 1u : 0u);
                 tc::mma_commit(&B.qdo_empty[st]);
                 tc::mma_commit(&B.pt_free);
-                return true;
-            };
-            for (int t = 0; ok && t < T; ++t) {
-                const int st = t % kv_STAGES;
-                if (!tc::mbar_wait(&B.qdo_full[st], (t / kv_STAGES) & 1, p.err)) { ok = false; break; }
-                tc::tc_fence_after();
-                const uint32_t sQ = tc::smem_u32(smem + kv_Q + st * 16 * KB);
-                const uint32_t sdO = tc::smem_u32(smem + kv_dO + st * 16 * KB);
-                const uint32_t t_S = tmem + (t & 1) * 128, t_dP = t_S + 64;
+            }
+            __syncwarp();
+            return true;
+        };
+        for (int t = 0; ok && t < T; ++t) {
+            const int st = t % kv_STAGES;
+            if (!tc::warp_wait(&B.qdo_full[st], (t / kv_STAGES) & 1, p.err)) { ok = false; break; }
+            tc::tc_fence_after();
+            const uint32_t so = st * 16 * KB;
+            const uint32_t t_S = tmem + (t & 1) * 128, t_dP = t_S + 64;
+            if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t oa = (kk >> 2) * 16 * KB + (kk & 3) * 32;
                     const uint32_t ob = (kk >> 2) * 8 * KB + (kk & 3) * 32;
-                    tc::mma_bf16(t_S, tc::sdesc(sK + oa, 16, 1024), tc::sdesc(sQ + ob, 16, 1024), id_s,
+                    tc::mma_bf16(t_S, tc::sdesc_at(dK0, oa), tc::sdesc_at(dQk0, so + ob), id_s,
                                  kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t oa = (kk >> 2) * 16 * KB + (kk & 3) * 32;
                     const uint32_t ob = (kk >> 2) * 8 * KB + (kk & 3) * 32;
-                    tc::mma_bf16(t_dP, tc::sdesc(sV + oa, 16, 1024), tc::sdesc(sdO + ob, 16, 1024), id_s,
+                    tc::mma_bf16(t_dP, tc::sdesc_at(dV0, oa), tc::sdesc_at(ddOk0, so + ob), id_s,
                                  kk > 0 ? 1u : 0u);
                 }
                 tc::mma_commit(&B.s_full[t & 1]);
-                if (t > 0 && !issue_grad(t - 1)) { ok = false; break; }
             }
-            if (ok && T > 0 && issue_grad(T - 1)) tc::mma_commit(&B.acc_done);
+            __syncwarp();
+            if (t > 0 && !issue_grad(t - 1)) { ok = false; break; }
+        }
+        if (ok && T > 0 && issue_grad(T - 1) && leader) tc::mma_commit(&B.acc_done);
+        if (leader) {
             tc::mma_commit(&B.drain);
             drain_wait(&B.drain, 0);
         }
+        __syncwarp();
     } else {
         // ---------------------------------------------------------------- softmax-grad warps
         // Two warpgroups: warpgroup wg handles query columns [32 wg, 32 wg + 32)
@@ -506,55 +517,66 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 drain_wait(&B.kv_full[t % q_STAGES], (t / q_STAGES) & 1);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t id_s = tc::idesc_bf16(128, 64, false, false);    // S = Q K^T
-            const uint32_t id_q = tc::idesc_bf16(128, 128, false, true);    // dQ += dS K
-            const uint32_t sQ = tc::smem_u32(smem + q_Q), sdO = tc::smem_u32(smem + q_dO);
-            const uint32_t t_dQ = tmem + 256;
-            bool ok = tc::mbar_wait(&B.q_full, 0, p.err);
-            auto issue_dq = [&](int t) -> bool {
-                const int b = t & 1, st = t % q_STAGES;
-                if (!tc::mbar_wait(&B.ds_full[b], (t >> 1) & 1, p.err)) return false;
-                tc::tc_fence_after();
-                const uint32_t sDS = tc::smem_u32(smem + q_DS + b * 16 * KB);
-                const uint32_t sK = tc::smem_u32(smem + q_KV + st * 32 * KB);
+        // Whole warp runs the loop (warp-uniform descriptors); the elected lane issues.
+        const bool leader = tc::elect_one_sync();
+        const uint32_t id_s = tc::idesc_bf16(128, 64, false, false);    // S = Q K^T
+        const uint32_t id_q = tc::idesc_bf16(128, 128, false, true);    // dQ += dS K
+        const uint32_t t_dQ = tmem + 256;
+        bool ok = tc::warp_wait(&B.q_full, 0, p.err);
+        // Base descriptors; each MMA advances them by a compile-time offset.
+        const uint64_t dQ0 = tc::sdesc(tc::smem_u32(smem + q_Q), 16, 1024);
+        const uint64_t ddO0 = tc::sdesc(tc::smem_u32(smem + q_dO), 16, 1024);
+        const uint64_t dDS0 = tc::sdesc(tc::smem_u32(smem + q_DS), 16, 1024);
+        const uint64_t dKVk0 = tc::sdesc(tc::smem_u32(smem + q_KV), 16, 1024);       // K-major
+        const uint64_t dKm0 = tc::sdesc(tc::smem_u32(smem + q_KV), 8 * KB, 1024);    // MN-major
+        auto issue_dq = [&](int t) -> bool {
+            const int b = t & 1, st = t % q_STAGES;
+            if (!tc::warp_wait(&B.ds_full[b], (t >> 1) & 1, p.err)) return false;
+            tc::tc_fence_after();
+            const uint32_t sb_off = b * 16 * KB, st_off = st * 32 * KB;
+            if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)      // K = 64 keys, 16 per MMA
-                    tc::mma_bf16(t_dQ, tc::sdesc(sDS + kk * 32, 16, 1024),
-                                 tc::sdesc(sK + kk * 2048, 8 * KB, 1024), id_q,
-                                 (t > 0 || kk > 0) ? 1u : 0u);
+                    tc::mma_bf16(t_dQ, tc::sdesc_at(dDS0, sb_off + kk * 32),
+                                 tc::sdesc_at(dKm0, st_off + kk * 2048), id_q, (t > 0 || kk > 0) ? 1u : 0u);
                 tc::mma_commit(&B.kv_empty[st]);
                 tc::mma_commit(&B.ds_free[b]);
-                return true;
-            };
-            for (int t = 0; ok && t < T; ++t) {
-                const int st = t % q_STAGES, sb = t & 1;
-                if (!tc::mbar_wait(&B.kv_full[st], (t / q_STAGES) & 1, p.err)) { ok = false; break; }
-                tc::tc_fence_after();
-                const uint32_t sK = tc::smem_u32(smem + q_KV + st * 32 * KB);
-                const uint32_t sV = sK + 16 * KB;
-                const uint32_t t_S = tmem + sb * 128, t_dP = t_S + 64;
+            }
+            __syncwarp();
+            return true;
+        };
+        for (int t = 0; ok && t < T; ++t) {
+            const int st = t % q_STAGES, sb = t & 1;
+            if (!tc::warp_wait(&B.kv_full[st], (t / q_STAGES) & 1, p.err)) { ok = false; break; }
+            tc::tc_fence_after();
+            const uint32_t st_off = st * 32 * KB;
+            const uint32_t t_S = tmem + sb * 128, t_dP = t_S + 64;
+            if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t oa = (kk >> 2) * 16 * KB + (kk & 3) * 32;
                     const uint32_t ob = (kk >> 2) * 8 * KB + (kk & 3) * 32;
-                    tc::mma_bf16(t_S, tc::sdesc(sQ + oa, 16, 1024), tc::sdesc(sK + ob, 16, 1024), id_s,
+                    tc::mma_bf16(t_S, tc::sdesc_at(dQ0, oa), tc::sdesc_at(dKVk0, st_off + ob), id_s,
                                  kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t oa = (kk >> 2) * 16 * KB + (kk & 3) * 32;
                     const uint32_t ob = (kk >> 2) * 8 * KB + (kk & 3) * 32;
-                    tc::mma_bf16(t_dP, tc::sdesc(sdO + oa, 16, 1024), tc::sdesc(sV + ob, 16, 1024), id_s,
-                                 kk > 0 ? 1u : 0u);
+                    tc::mma_bf16(t_dP, tc::sdesc_at(ddO0, oa), tc::sdesc_at(dKVk0, st_off + 16 * KB + ob),
+                                 id_s, kk > 0 ? 1u : 0u);
                 }
                 tc::mma_commit(&B.s_full[sb]);
-                if (t > 0 && !issue_dq(t - 1)) { ok = false; break; }
             }
-            if (ok && T > 0 && issue_dq(T - 1)) tc::mma_commit(&B.acc_done);
+            __syncwarp();
+            if (t > 0 && !issue_dq(t - 1)) { ok = false; break; }
+        }
+        if (ok && T > 0 && issue_dq(T - 1) && leader) tc::mma_commit(&B.acc_done);
+        if (leader) {
             tc::mma_commit(&B.drain);
             drain_wait(&B.drain, 0);
         }
+        __syncwarp();
     } else {
         // Two warpgroups: warpgroup wg handles key columns [32 wg, 32 wg + 32) of
         // every query row, and dQ columns [64 wg, 64 wg + 64) in the epilogue.

@@ -180,52 +180,62 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         produce_ring(p, smem, B, tmap_q, tmap_v, false, qt, h, kvh, nt, lane);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = tc::idesc_bf16(128, 128, false, false);       // S = Q K^T
-            const uint32_t idesc_pv = tc::idesc_bf16(128, 128, false, true);     // O += P V
-            const uint32_t sq = tc::smem_u32(smem + kOffQ);
-            const uint32_t sp = tc::smem_u32(smem + kOffP);
-            const uint32_t tmem_o = tmem + 256;
-            bool ok = tc::mbar_wait(&B.q_full, 0, p.err);
-            auto issue_pv = [&](int i) -> bool {
-                if (!tc::mbar_wait(&B.p_full, i & 1, p.err)) return false;
-                if (!tc::mbar_wait(&B.v_full[i % kVStages], (i / kVStages) & 1, p.err)) return false;
-                tc::tc_fence_after();
-                const uint32_t sv = tc::smem_u32(smem + kOffV + (i % kVStages) * kTileBytes);
+        // The whole warp runs the loop (warp-uniform descriptors); one elected
+        // lane issues the tcgen05 instructions and commits.
+        const bool leader = tc::elect_one_sync();
+        const uint32_t idesc = tc::idesc_bf16(128, 128, false, false);       // S = Q K^T
+        const uint32_t idesc_pv = tc::idesc_bf16(128, 128, false, true);     // O += P V
+        // Base descriptors; each MMA advances them by a compile-time offset.
+        const uint64_t dq0 = tc::sdesc(tc::smem_u32(smem + kOffQ), 16, 1024);
+        const uint64_t dp0 = tc::sdesc(tc::smem_u32(smem + kOffP), 16, 1024);
+        const uint32_t tmem_o = tmem + 256;
+        bool ok = tc::warp_wait(&B.q_full, 0, p.err);
+        auto issue_pv = [&](int i) -> bool {
+            if (!tc::warp_wait(&B.p_full, i & 1, p.err)) return false;
+            if (!tc::warp_wait(&B.v_full[i % kVStages], (i / kVStages) & 1, p.err)) return false;
+            tc::tc_fence_after();
+            // A = P [128 q][128 keys] K-major; B = V [128 keys][128 d] MN-major:
+            // 16 keys = 2 K-groups of 8 rows (1024 B apart); d spans the two
+            // 64-column halves (16 KB apart).
+            const uint64_t b0 = tc::sdesc(tc::smem_u32(smem + kOffV + (i % kVStages) * kTileBytes),
+                                          kHalfBytes, 1024);
+            if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    // A = P [128 q][128 keys] K-major; B = V [128 keys][128 d] MN-major:
-                    // 16 keys = 2 K-groups of 8 rows (1024 B apart); d spans the two
-                    // 64-column halves (16 KB apart).
-                    const uint64_t a = tc::sdesc(sp + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = tc::sdesc(sv + kk * 2048, kHalfBytes, 1024);
-                    tc::mma_bf16(tmem_o, a, b, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < 8; ++kk)
+                    tc::mma_bf16(tmem_o, tc::sdesc_at(dp0, (kk >> 2) * kHalfBytes + (kk & 3) * 32),
+                                 tc::sdesc_at(b0, kk * 2048), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
                 tc::mma_commit(&B.o_done);
                 tc::mma_commit(&B.v_empty[i % kVStages]);
-                return true;
-            };
-            for (int j = 0; ok && j < nt; ++j) {
-                const int ks = j % kKStages;
-                if (!tc::mbar_wait(&B.k_full[ks], (j / kKStages) & 1, p.err)) { ok = false; break; }
-                tc::tc_fence_after();
-                const uint32_t sk = tc::smem_u32(smem + kOffK + ks * kTileBytes);
-                const uint32_t tmem_s = tmem + (j & 1) * 128;
+            }
+            __syncwarp();
+            return true;
+        };
+        for (int j = 0; ok && j < nt; ++j) {
+            const int ks = j % kKStages;
+            if (!tc::warp_wait(&B.k_full[ks], (j / kKStages) & 1, p.err)) { ok = false; break; }
+            tc::tc_fence_after();
+            const uint64_t dk0 = tc::sdesc(tc::smem_u32(smem + kOffK + ks * kTileBytes), 16, 1024);
+            const uint32_t tmem_s = tmem + (j & 1) * 128;
+            if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t koff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                    tc::mma_bf16(tmem_s, tc::sdesc(sq + koff, 16, 1024), tc::sdesc(sk + koff, 16, 1024),
-                                 idesc, kk > 0 ? 1u : 0u);
+                    tc::mma_bf16(tmem_s, tc::sdesc_at(dq0, koff), tc::sdesc_at(dk0, koff), idesc,
+                                 kk > 0 ? 1u : 0u);
                 }
                 tc::mma_commit(&B.s_full[j & 1]);
                 tc::mma_commit(&B.k_empty[ks]);
-                if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
             }
-            if (ok && nt > 0) issue_pv(nt - 1);
-            // Drain: nothing of ours may still run on the tensor core at exit.
+            __syncwarp();
+            if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
+        }
+        if (ok && nt > 0) issue_pv(nt - 1);
+        // Drain: nothing of ours may still run on the tensor core at exit.
+        if (leader) {
             tc::mma_commit(&B.drain);
             drain_wait(&B.drain, 0);
         }
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax (128 threads)
         const int quad = warp & 3;                    // TMEM lane quadrant of this warp

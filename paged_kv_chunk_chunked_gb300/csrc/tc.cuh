@@ -68,8 +68,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
 // Waits for the phase with the given parity to complete. Returns false (and
 // records kErrWaitTimeout once) when the wait gives up: after kWaitTimeoutNs,
 // or at once when *err already holds an error from any CTA.
-static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
-    const uint32_t addr = smem_u32(bar);
+// The polling loop of mbar_wait, out of line: it only runs when the phase is
+// not complete yet, and keeps the bounded-wait bookkeeping off the fast path.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t addr, uint32_t parity, int* err) {
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(addr, parity)) return true;
@@ -84,6 +85,19 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, in
             }
         }
     }
+}
+
+// A phase that has already completed costs one inlined try_wait (a call into
+// the slow path costs hundreds of cycles in these register-heavy kernels).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+    const uint32_t addr = smem_u32(bar);
+    if (mbar_try_wait(addr, parity)) return true;
+    return mbar_wait_slow(addr, parity, err);
+}
+
+// mbar_wait by every lane of a warp, with a warp-uniform result.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* err) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
 }
 
 // Bounded wait (1 s) that ignores errors recorded elsewhere: used only to
@@ -239,6 +253,11 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
     return d;
 }
 
+// The same descriptor with its start address advanced by `bytes` (a multiple
+// of 16). The start field holds address >> 4 in its low 14 bits; every tile
+// lies inside the 256 KB shared window, so the add never carries out.
+__device__ __forceinline__ uint64_t sdesc_at(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
 // Instruction descriptor for kind::f16 with bf16 A/B and an fp32 accumulator:
 // D format (bits 4-5) = f32, A/B format (bits 7-9, 10-12) = bf16, A/B major
 // (bits 15, 16; 1 = MN-major), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
@@ -246,6 +265,19 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
     return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
            (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Elects one lane of the (converged) warp; true in exactly that lane. The MMA
+// warps run their whole issue loop warp-wide, so descriptors and addresses are
+// warp-uniform values, and only the elected lane issues tcgen05 instructions.
+__device__ __forceinline__ bool elect_one_sync() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .b32 r;\n\t.reg .pred p;\n\t"
+        "elect.sync r|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
 }
 
 // D[tmem] (+)= A[smem] . B[smem]^T, one CTA, issued by a single thread.
