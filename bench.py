@@ -43,6 +43,10 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--flags", type=int, default=0, help="pool flags (1 = CUDA cores only)")
+    ap.add_argument("--offload-chunks", type=int, default=8,
+                    help="offload workload: chunks measured at the end of the sequence")
+    ap.add_argument("--slots", type=int, default=0,
+                    help="offload workload: device page slots (0 = the context's page count)")
     return ap.parse_args()
 
 
@@ -395,6 +399,231 @@ def run_reference(args, world, rank):
     }
 
 
+# ------------------------------------------------------------------ page-sparse workloads
+
+def sparse_pairs(sel_host, P: int, g: int) -> int:
+    """Attended (query, key) pairs of one chunk for all query heads, from its
+    selection [n_qp, Hkv, kmax]: P*P per listed earlier page, P(P+1)/2 for the
+    query page itself (causal), times the g query heads of each KV head."""
+    import numpy as np
+    listed = (sel_host >= 0).sum(axis=-1)                   # [n_qp, Hkv]
+    return int(g * ((listed - 1) * P * P + P * (P + 1) // 2).sum())
+
+
+def run_sparse(args, world, rank):
+    """Page-sparse chunk sweep: per chunk append, page top-K, sparse forward;
+    then the sparse backward over the chunks in reverse. Also times the dense
+    sweep of the same context once for the sparse/dense speedup."""
+    import torch
+    from paged_kv_chunk_chunked_gb300 import binding as B
+    from paged_kv_chunk_chunked_gb300 import build as pkv_build
+    from paged_kv_chunk_chunked_gb300 import synth
+    from paged_kv_chunk_chunked_gb300.sweep import ChunkSweep
+
+    pkv_build.build()
+    B.lib()
+    w = synth.workload(args.workload)
+    K, ns, nl = w.topk
+    sw = ChunkSweep(w, flags=args.flags).load_inputs()
+    stream = torch.cuda.current_stream()
+    n = w.n_chunks
+    sels = [torch.empty(((e - s + w.P - 1) // w.P, w.Hkv, K + ns + nl), dtype=torch.int32,
+                        device="cuda") for s, e in (w.chunk_range(c) for c in range(n))]
+
+    def step(sparse=True):
+        sw.reset()
+        for c in range(n):
+            s, e = w.chunk_range(c)
+            B.pkv_append(sw.seq, sw.k[c], sw.v[c], e - s, stream)
+            if sparse:
+                B.pkv_page_topk(sw.seq, sw.q[c], s, e - s, K, ns, nl, sels[c], None, stream)
+            B.pkv_chunk_attn_fwd(sw.seq, sw.q[c], s, e - s, sw.o[c], sw.lse[c],
+                                 sels[c] if sparse else None, stream)
+        for c in reversed(range(n)):
+            sw.backward(c, stream, sel=sels[c] if sparse else None)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    B.pkv_check(sw.pool)
+    pairs = sum(sparse_pairs(x.cpu().numpy(), w.P, w.g) for x in sels)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    t0, t1 = ev(), ev()
+    B.pkv_profile_enable(True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    prof = B.pkv_profile_collect()
+    B.pkv_profile_enable(False)
+    clk = clocks.stop()
+    B.pkv_check(sw.pool)
+    ms = t0.elapsed_time(t1) / args.steps
+    # the dense sweep of the same context, once, for the speedup of page sparsity
+    step(sparse=False)
+    torch.cuda.synchronize()
+    d0, d1 = ev(), ev()
+    d0.record(stream)
+    step(sparse=False)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    dense_ms = d0.elapsed_time(d1)
+    flops = 14 * w.d * pairs
+    tflops = flops / (ms * 1e-3) / 1e12
+    pk, pk_kind = peaks()
+    peak_tc = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
+    kernels = {k: {"launches": c, "ms_per_step": round(t / args.steps, 3)} for k, (c, t) in prof.items()}
+    # page selection: the page-query kernel reads the chunk's Q once (HBM-bound)
+    q_bytes = w.C * w.Hq * w.d * 2
+    qb_cnt, qb_ms = prof.get("qbar_kernel", (1, float("nan")))
+    qbar_gbs = q_bytes * qb_cnt / (qb_ms * 1e-3) / 1e9
+    sel_cnt, sel_ms = prof.get("select_kernel", (1, float("nan")))
+    return {
+        "metric": METRIC, "value": round(tflops, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded clustered keys, N(0,1) Q/V/dO, bf16-rounded)",
+        "config": {"workload": w.name, "N": w.N, "C": w.C, "P": w.P, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "d": w.d, "topk": list(w.topk), "block_table": w.table,
+                   "flops": "14*d*attended pairs (from the selections)"},
+        "attended_pairs_per_step": pairs,
+        "dense_pairs": w.Hq * pairs_dense(w.N),
+        "tokens_per_s_per_layer": round(w.N / (ms * 1e-3), 1),
+        "pct_bf16_peak": round(100 * tflops / peak_tc, 2),
+        "dense_ms_per_step": round(dense_ms, 3),
+        "sparse_speedup_vs_dense": round(dense_ms / ms, 2),
+        "roofline": {"bound": "hbm", "kernel": "qbar_kernel", "unit": "GB/s",
+                     "achieved": round(qbar_gbs, 1), "peak": pk["hbm_gbs"],
+                     "frac": round(qbar_gbs / pk["hbm_gbs"], 4),
+                     "bytes_per_launch": q_bytes, "peak_kind": f"{pk_kind} hbm_gbs",
+                     "traffic": None},
+        "select_kernel_us_per_launch": round(1e3 * sel_ms / sel_cnt, 2),
+        "kernels": kernels, "gpu_launches": sum(v[0] for v in prof.values()),
+        "clocks": clk,
+    }
+
+
+def run_offload(args, world, rank):
+    """Pinned-host offload of the 1M-token page-sparse workload. All 128 chunks'
+    K/V are appended into pinned host pages; the measured step is the sparse
+    forward + backward of the last `--offload-chunks` chunks, each staging its
+    selected pages (K/V, then K/V + gradients) into HBM slots on a side stream
+    and writing the gradients back. The same step on a device-resident pool
+    gives the staging overhead."""
+    import numpy as np
+    import torch
+    from paged_kv_chunk_chunked_gb300 import binding as B
+    from paged_kv_chunk_chunked_gb300 import build as pkv_build
+    from paged_kv_chunk_chunked_gb300 import synth
+    from paged_kv_chunk_chunked_gb300.sweep import to_device
+
+    pkv_build.build()
+    B.lib()
+    w = synth.workload(args.workload)
+    K, ns, nl = w.topk
+    n = w.n_chunks
+    meas = list(range(n - args.offload_chunks, n))
+    main_s = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    bt = synth.block_table(w)
+    if args.slots <= 0:
+        args.slots = w.n_pages
+    res = {}
+    for mode in ("pinned_host", "device"):
+        host = mode == "pinned_host"
+        pool = B.pkv_pool_create(w.P, w.Hkv, w.Hq, w.d, B.PKV_BF16, w.n_phys,
+                                 residency=B.PKV_RES_PINNED_HOST if host else B.PKV_RES_DEVICE,
+                                 n_device_slots=args.slots if host else 0)
+        seq = B.pkv_seq_create(pool)
+        q = {c: to_device(synth.chunk_q(w, c), "bf16") for c in meas}
+        do = {c: to_device(synth.chunk_do(w, c), "bf16") for c in meas}
+        o = {c: torch.empty_like(q[c]) for c in meas}
+        dq = {c: torch.empty_like(q[c]) for c in meas}
+        lse = {c: torch.empty((w.Hq, w.C), dtype=torch.float32, device="cuda") for c in meas}
+        sel = {c: torch.empty((w.C // w.P, w.Hkv, K + ns + nl), dtype=torch.int32, device="cuda")
+               for c in meas}
+
+        def fill():
+            B.pkv_seq_reset(seq)
+            B.pkv_set_block_table(seq, bt)
+            for c in range(n):
+                s, e = w.chunk_range(c)
+                k = to_device(synth.chunk_k(w, c), "bf16")
+                v = to_device(synth.chunk_v(w, c), "bf16")
+                B.pkv_append(seq, k, v, e - s, main_s)
+            torch.cuda.synchronize()
+
+        def step():
+            staged = 0
+            for c in meas:
+                s, e = w.chunk_range(c)
+                B.pkv_page_topk(seq, q[c], s, e - s, K, ns, nl, sel[c], None, main_s)
+                if host:
+                    B.pkv_prefetch(seq, sel[c], sel[c].numel(), B.PKV_STAGE_KV, side)
+                    B.pkv_wait(seq, main_s, 0)
+                B.pkv_chunk_attn_fwd(seq, q[c], s, e - s, o[c], lse[c], sel[c], main_s)
+            for c in reversed(meas):
+                s, e = w.chunk_range(c)
+                if host:
+                    B.pkv_prefetch(seq, sel[c], sel[c].numel(), B.PKV_STAGE_KV | B.PKV_STAGE_GRADS, side)
+                    B.pkv_wait(seq, main_s, 0)
+                B.pkv_chunk_attn_bwd(seq, q[c], o[c], do[c], lse[c], s, e - s, dq[c], sel[c], main_s)
+                if host:
+                    B.pkv_writeback_grads(seq, side)
+            if host:
+                B.pkv_wait(seq, main_s, 0)
+
+        fill()
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        B.pkv_check(pool)
+        # pages staged per chunk (union of the selection), for the byte count
+        staged_pages = 0
+        for c in meas:
+            u = np.unique(sel[c].cpu().numpy())
+            staged_pages += int((u >= 0).sum())
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        B.pkv_profile_enable(True)
+        ev0.record(main_s)
+        for _ in range(args.steps):
+            step()
+        ev1.record(main_s)
+        torch.cuda.synchronize()
+        prof = B.pkv_profile_collect()
+        B.pkv_profile_enable(False)
+        B.pkv_check(pool)
+        res[mode] = dict(ms=ev0.elapsed_time(ev1) / args.steps, prof=prof, staged_pages=staged_pages)
+        B.pkv_pool_destroy(pool)
+        del q, do, o, dq, lse, sel
+        torch.cuda.empty_cache()
+    hp = res["pinned_host"]
+    page_head_kv = w.Hkv * w.P * w.d * 2 * 2          # K + V of one page, all KV heads
+    page_head_g = w.Hkv * w.P * w.d * 4 * 2           # dK + dV
+    # per step: fwd stages K/V; bwd stages K/V + grads and writes grads back
+    bytes_moved = hp["staged_pages"] * (page_head_kv + (page_head_kv + page_head_g) + page_head_g)
+    copy_cnt, copy_ms = hp["prof"].get("stage_copy_kernel", (0, 0.0))
+    wb_cnt, wb_ms = hp["prof"].get("stage_writeback_kernel", (0, 0.0))
+    link_gbs = bytes_moved * args.steps / ((copy_ms + wb_ms) * 1e-3) / 1e9 if copy_ms else None
+    overhead = hp["ms"] / res["device"]["ms"] - 1.0
+    return {
+        "metric": "page-sparse offload step: staged pages over the host link, overhead vs HBM-resident",
+        "value": round(overhead * 100, 2), "unit": "% step-time overhead", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": False,
+        "ms_per_step_pinned_host": round(hp["ms"], 3), "ms_per_step_device": round(res["device"]["ms"], 3),
+        "config": {"workload": w.name, "N": w.N, "C": w.C, "P": w.P, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "d": w.d, "topk": list(w.topk), "measured_chunks": meas, "device_slots": args.slots},
+        "staged_pages_per_step": hp["staged_pages"], "bytes_moved_per_step": bytes_moved,
+        "link_gbs_in_copy_kernels": round(link_gbs, 1) if link_gbs else None,
+        "kernels_pinned_host": {k: {"launches": c, "ms_per_step": round(t / args.steps, 3)}
+                                for k, (c, t) in hp["prof"].items()},
+        "data": "synthetic (seeded clustered keys)",
+    }
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -404,7 +633,14 @@ def main():
         print(json.dumps(run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), rank)))
         return 0
     world, rank, _ = dist_setup(args)
-    out = run_pkv(args, world, rank)
+    from paged_kv_chunk_chunked_gb300 import synth
+    wl = synth.workload(args.workload)
+    if wl.offload:
+        out = run_offload(args, world, rank)
+    elif wl.topk:
+        out = run_sparse(args, world, rank)
+    else:
+        out = run_pkv(args, world, rank)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -30,7 +30,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kQbarThreads = 256;
+constexpr int kQbarThreads = 512;
 constexpr int kSelThreads = 1024;
 constexpr int kMaxCand = 16384;           // sort buffer: 128 KB of 64-bit keys
 
@@ -49,11 +49,28 @@ __global__ void __launch_bounds__(kQbarThreads) qbar_kernel(const T* q, int64_t 
     float acc[EPV];
 #pragma unroll
     for (int e = 0; e < EPV; ++e) acc[e] = 0.f;
-    for (int r = r0; r < rows; r += RSTEP) {
+    auto row_ptr = [&](int r) {
         const int t = r / g, hh = r % g;
-        const uint4 u = __ldg(reinterpret_cast<const uint4*>(q + ((t0 + t) * Hq + h * g + hh) * D) + vc);
+        return reinterpret_cast<const uint4*>(q + ((t0 + t) * Hq + h * g + hh) * D) + vc;
+    };
+    // Eight independent 16-byte loads in flight per thread before any is used.
+    constexpr int U = 8;
+    int r = r0;
+    for (; r + (U - 1) * RSTEP < rows; r += U * RSTEP) {
+        uint4 u[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) u[k] = __ldg(row_ptr(r + k * RSTEP));
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            float f[EPV];
+            widen16<T>(u[k], f);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) acc[e] += f[e];
+        }
+    }
+    for (; r < rows; r += RSTEP) {
         float f[EPV];
-        widen16<T>(u, f);
+        widen16<T>(__ldg(row_ptr(r)), f);
 #pragma unroll
         for (int e = 0; e < EPV; ++e) acc[e] += f[e];
     }
