@@ -298,6 +298,8 @@ pkv_status pkv_profile_collect(int32_t max_kernels, char* names, double* total_m
  *   mode 0: a [128(M), 64(K)], b [128(N), 64(K)]  (both K-major): d = a . b^T
  *   mode 1: a [128(M), 64(K)], b [64(K), 128(N)]  (B MN-major):   d = a . b
  *   mode 2: a [64(K), 128(M)], b [64(K), 128(N)]  (both MN-major): d = a^T . b
+ *   mode 3: a [128(M), 64(K)] placed in tensor memory, b [64(K), 128(N)]
+ *           (B MN-major): d = a . b
  * lbo/sbo override the MN-major descriptor byte offsets (0 = library
  * default). PKV_ERR_DEVICE_FAULT if a bounded wait expired. */
 pkv_status pkv_selftest_umma(int32_t mode, const void* a, const void* b, float* d,

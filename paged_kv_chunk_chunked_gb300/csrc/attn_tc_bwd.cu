@@ -20,10 +20,12 @@
 //   bwd_q_tc_kernel   one CTA per (128-query tile, query head); walks the
 //                     visible keys in half-page tiles of 64 and accumulates dQ
 //                     in tensor memory, written once as bf16.
-// Both have the forward's warp roles: warp 0 TMA producer, warp 1 single-
-// thread MMA issuer, warps 2..5 one thread per accumulator row. S and dP (or
-// their transposes) are double-buffered in tensor memory so the tensor core
-// computes tile t+1 while the softmax warps work on tile t.
+// Both have the forward's warp roles: warp 0 TMA producer, warp 1 MMA issuer
+// (elected lane), then two softmax warpgroups, one thread per accumulator row.
+// In the dK/dV kernel S^T and dP^T are double-buffered in tensor memory and
+// both warpgroups split each tile's columns; in the dQ kernel three S/dP tiles
+// are in flight and the warpgroups take alternate tiles, so the tensor core
+// computes tiles t+1 and t+2 while a warpgroup works on tile t.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -66,35 +68,32 @@ __device__ __forceinline__ int sel_count(const BwdParams& p, int qp, int kvh) {
 }
 
 
-// 32 bf16 (16 words) of one row: chunks [4 half, 4 half + 4) of a 128-byte-swizzled row.
-__device__ __forceinline__ void store_row_half(uint8_t* tile, int row, int half, const uint32_t (&w)[16]) {
-#pragma unroll
-    for (int ch = 0; ch < 4; ++ch)
-        *reinterpret_cast<uint4*>(tile + tc::sw128_offset(row, half * 4 + ch)) =
-            make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
-}
-
 // ============================================================================ dK / dV
 
 // Shared-memory layout (offsets from a 1024-aligned base).
-// Q/dO stage for tile t+1 is the one tile t-2 used: the load has a full
-// iteration of slack behind the gradient products of tile t-1.
-constexpr int kv_STAGES = 3;
+// Q/dO stage for tile t+1 is the one tile t-3 used: the load has two
+// iterations of slack behind the gradient products of tile t-2.
+// P^T and dS^T never touch shared memory: the softmax warps write them (bf16)
+// into tensor memory over the S^T / dP^T columns they have just read, and the
+// gradient MMAs take their A operand from there.
+constexpr int kv_STAGES = 4;
 constexpr uint32_t kv_K = 0;                 // [128 keys][128 d]: two 16 KB halves
 constexpr uint32_t kv_V = 32 * KB;
 constexpr uint32_t kv_Q = 64 * KB;           // stages x [64 q][128 d]: two 8 KB halves
 constexpr uint32_t kv_dO = kv_Q + kv_STAGES * 16 * KB;
-constexpr uint32_t kv_PT = kv_dO + kv_STAGES * 16 * KB;   // [128 keys][64 q] (16 KB)
-constexpr uint32_t kv_DST = kv_PT + 16 * KB;
-constexpr uint32_t kv_STAT = kv_DST + 16 * KB;   // stages x (64 lse*log2e + 64 D) floats
+constexpr uint32_t kv_STAT = kv_dO + kv_STAGES * 16 * KB;   // stages x (64 lse*log2e + 64 D) floats
 constexpr uint32_t kv_SMEM = kv_STAT + kv_STAGES * 512 + 1024;
+
+// Tensor-memory column of the bf16 operand for queries [16 kk, 16 kk + 16) of
+// a tile (kk = 0..3): warpgroup wg packs its 32 queries into the first 16 of
+// the 32 fp32 columns it read, so the halves sit at column offsets 0 and 32.
+__device__ __forceinline__ uint32_t kv_pk_col(int kk) { return (kk >> 1) * 32 + (kk & 1) * 8; }
 
 struct __align__(8) KVBar {
     uint64_t kv_full;
     uint64_t qdo_full[kv_STAGES], qdo_empty[kv_STAGES];
     uint64_t s_full[2];
     uint64_t p_full[2];
-    uint64_t pt_free;
     uint64_t acc_done;
     uint64_t drain;
     uint32_t tmem_base;
@@ -159,7 +158,6 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tc::mbar_init(&B.s_full[s], 1);
             tc::mbar_init(&B.p_full[s], kSoftmaxThreads);
         }
-        tc::mbar_init(&B.pt_free, 1);
         tc::mbar_init(&B.acc_done, 1);
         tc::mbar_init(&B.drain, 1);
         tc::fence_barrier_init();
@@ -256,28 +254,29 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // Base descriptors; each MMA advances them by a compile-time offset.
         const uint64_t dK0 = tc::sdesc(tc::smem_u32(smem + kv_K), 16, 1024);
         const uint64_t dV0 = tc::sdesc(tc::smem_u32(smem + kv_V), 16, 1024);
-        const uint64_t dPT0 = tc::sdesc(tc::smem_u32(smem + kv_PT), 16, 1024);
-        const uint64_t dDST0 = tc::sdesc(tc::smem_u32(smem + kv_DST), 16, 1024);
         const uint64_t dQk0 = tc::sdesc(tc::smem_u32(smem + kv_Q), 16, 1024);        // K-major
         const uint64_t ddOk0 = tc::sdesc(tc::smem_u32(smem + kv_dO), 16, 1024);
         const uint64_t dQm0 = tc::sdesc(tc::smem_u32(smem + kv_Q), 8 * KB, 1024);    // MN-major
         const uint64_t ddOm0 = tc::sdesc(tc::smem_u32(smem + kv_dO), 8 * KB, 1024);
+        // P^T(t) and dS^T(t) sit in tensor memory over S^T(t) / dP^T(t); the
+        // tensor core runs MMAs in issue order, so S^T(t+2), issued after these,
+        // cannot overwrite them before they are read.
         auto issue_grad = [&](int t) -> bool {
             const int st = t % kv_STAGES;
             if (!tc::warp_wait(&B.p_full[t & 1], (t >> 1) & 1, p.err)) return false;
             tc::tc_fence_after();
             const uint32_t so = st * 16 * KB;
+            const uint32_t t_P = tmem + (t & 1) * 128, t_dS = t_P + 64;
             if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)      // K = 64 queries, 16 per MMA
-                    tc::mma_bf16(t_dV, tc::sdesc_at(dPT0, kk * 32), tc::sdesc_at(ddOm0, so + kk * 2048),
-                                 id_g, (t > 0 || kk > 0) ? 1u : 0u);
+                    tc::mma_bf16_ts(t_dV, t_P + kv_pk_col(kk), tc::sdesc_at(ddOm0, so + kk * 2048),
+                                    id_g, (t > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    tc::mma_bf16(t_dK, tc::sdesc_at(dDST0, kk * 32), tc::sdesc_at(dQm0, so + kk * 2048),
-                                 id_g, (t > 0 || kk > 0) ? 1u : 0u);
+                    tc::mma_bf16_ts(t_dK, t_dS + kv_pk_col(kk), tc::sdesc_at(dQm0, so + kk * 2048),
+                                    id_g, (t > 0 || kk > 0) ? 1u : 0u);
                 tc::mma_commit(&B.qdo_empty[st]);
-                tc::mma_commit(&B.pt_free);
             }
             __syncwarp();
             return true;
@@ -368,13 +367,10 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     dw[c / 2] = pack_bf16x2(dr[0], dr[1]);
                 }
             }
-            if (t >= 1) {                                    // gradient products of t-1 done
-                ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.pt_free, (t - 1) & 1, p.err));
-                if (!ok) break;
-            }
-            store_row_half(smem + kv_PT, r, wg, pw);
-            store_row_half(smem + kv_DST, r, wg, dw);
-            tc::fence_proxy_async_smem();
+            // Over the columns this thread has just read (its own lane).
+            tc::tmem_st16(lane_base + sb * 128 + wg * 32, pw);
+            tc::tmem_st16(lane_base + sb * 128 + 64 + wg * 32, dw);
+            tc::tmem_wait_st();
             tc::tc_fence_before();
             tc::mbar_arrive(&B.p_full[sb]);
         }
@@ -414,19 +410,28 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
 // ============================================================================ dQ
 
+// K and V of a 64-key tile travel in separate rings: V is free once dP is
+// computed, K only after dQ, so K needs the deeper ring. S/dP of three tiles
+// live in tensor memory at once; the two softmax warpgroups take alternate
+// tiles, so each has two tiles' worth of tensor-core time to turn S/dP into dS.
+// dS (bf16) goes back into tensor memory over the S columns it came from, and
+// the dQ MMA reads its A operand there: no shared-memory traffic for dS.
+constexpr int q_KST = 6;
+constexpr int q_VST = 4;
+constexpr int q_NS = 3;                      // S/dP buffers in TMEM (128 columns each)
 constexpr uint32_t q_Q = 0;                  // [128 q][128 d]: two 16 KB halves
 constexpr uint32_t q_dO = 32 * KB;
-constexpr uint32_t q_KV = 64 * KB;           // 3 stages x (K 16 KB + V 16 KB), [64 keys][128 d]
-constexpr int q_STAGES = 4;      // the stage for tile t+1 was freed by dQ of tile t-3
-constexpr uint32_t q_DS = q_KV + q_STAGES * 32 * KB;   // 2 buffers x [128 q][64 keys] (16 KB)
-constexpr uint32_t q_SMEM = q_DS + 32 * KB + 1024;
+constexpr uint32_t q_K = 64 * KB;            // stages x [64 keys][128 d]: two 8 KB halves
+constexpr uint32_t q_V = q_K + q_KST * 16 * KB;
+constexpr uint32_t q_SMEM = q_V + q_VST * 16 * KB + 1024;
+constexpr uint32_t q_TDQ = q_NS * 128;       // dQ accumulator columns [384, 512)
 
 struct __align__(8) QBar {
     uint64_t q_full;
-    uint64_t kv_full[q_STAGES], kv_empty[q_STAGES];
-    uint64_t s_full[2];
+    uint64_t k_full[q_KST], k_empty[q_KST];
+    uint64_t v_full[q_VST], v_empty[q_VST];
+    uint64_t s_full[q_NS];
     uint64_t ds_full[2];
-    uint64_t ds_free[2];
     uint64_t acc_done;
     uint64_t drain;
     uint32_t tmem_base;
@@ -452,15 +457,16 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     if (threadIdx.x == 0) {
         tc::mbar_init(&B.q_full, 1);
-        for (int s = 0; s < q_STAGES; ++s) {
-            tc::mbar_init(&B.kv_full[s], 1);
-            tc::mbar_init(&B.kv_empty[s], 1);
+        for (int s = 0; s < q_KST; ++s) {
+            tc::mbar_init(&B.k_full[s], 1);
+            tc::mbar_init(&B.k_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            tc::mbar_init(&B.s_full[s], 1);
-            tc::mbar_init(&B.ds_full[s], kSoftmaxThreads);
-            tc::mbar_init(&B.ds_free[s], 1);
+        for (int s = 0; s < q_VST; ++s) {
+            tc::mbar_init(&B.v_full[s], 1);
+            tc::mbar_init(&B.v_empty[s], 1);
         }
+        for (int s = 0; s < q_NS; ++s) tc::mbar_init(&B.s_full[s], 1);
+        for (int s = 0; s < 2; ++s) tc::mbar_init(&B.ds_full[s], 128);
         tc::mbar_init(&B.acc_done, 1);
         tc::mbar_init(&B.drain, 1);
         tc::fence_barrier_init();
@@ -488,98 +494,119 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         tc::PageBatch pages;
         pages.init(p.bt, sel_row, T / 2, lane);
-        int issued = 0;
+        int k_issued = 0, v_issued = 0;
         int32_t pp = -1;
         for (int t = 0; t < T; ++t) {
-            const int st = t % q_STAGES;
-            if (t >= q_STAGES &&
-                !__all_sync(0xffffffffu, tc::mbar_wait(&B.kv_empty[st], ((t / q_STAGES) - 1) & 1, p.err)))
+            const int ks = t % q_KST, vs = t % q_VST;
+            if (t >= q_KST &&
+                !__all_sync(0xffffffffu, tc::mbar_wait(&B.k_empty[ks], ((t / q_KST) - 1) & 1, p.err)))
                 break;
             if ((t & 1) == 0) pp = pages.get(t >> 1);
             if (pp < 0 || pp >= p.num_phys) {
                 if (lane == 0) report_error(p.err, kErrBadPage);
                 break;
             }
+            const int row = (int)(((int64_t)pp * p.Hkv + kvh) * 128 + (t & 1) * 64);
             if (lane == 0) {
-                const int row = (int)(((int64_t)pp * p.Hkv + kvh) * 128 + (t & 1) * 64);
-                uint8_t* kd = smem + q_KV + st * 32 * KB;
-                tc::mbar_arrive_expect_tx(&B.kv_full[st], 32 * KB);
-                tc::tma_load_2d(kd, &tm_k, &B.kv_full[st], 0, row);
-                tc::tma_load_2d(kd + 8 * KB, &tm_k, &B.kv_full[st], 64, row);
-                tc::tma_load_2d(kd + 16 * KB, &tm_v, &B.kv_full[st], 0, row);
-                tc::tma_load_2d(kd + 24 * KB, &tm_v, &B.kv_full[st], 64, row);
+                uint8_t* kd = smem + q_K + ks * 16 * KB;
+                tc::mbar_arrive_expect_tx(&B.k_full[ks], 16 * KB);
+                tc::tma_load_2d(kd, &tm_k, &B.k_full[ks], 0, row);
+                tc::tma_load_2d(kd + 8 * KB, &tm_k, &B.k_full[ks], 64, row);
             }
-            issued = t + 1;
+            k_issued = t + 1;
+            if (t >= q_VST &&
+                !__all_sync(0xffffffffu, tc::mbar_wait(&B.v_empty[vs], ((t / q_VST) - 1) & 1, p.err)))
+                break;
+            if (lane == 0) {
+                uint8_t* vd = smem + q_V + vs * 16 * KB;
+                tc::mbar_arrive_expect_tx(&B.v_full[vs], 16 * KB);
+                tc::tma_load_2d(vd, &tm_v, &B.v_full[vs], 0, row);
+                tc::tma_load_2d(vd + 8 * KB, &tm_v, &B.v_full[vs], 64, row);
+            }
+            v_issued = t + 1;
         }
         if (lane == 0) {
             drain_wait(&B.q_full, 0);
-            for (int t = max(0, issued - q_STAGES); t < issued; ++t)
-                drain_wait(&B.kv_full[t % q_STAGES], (t / q_STAGES) & 1);
+            for (int t = max(0, k_issued - q_KST); t < k_issued; ++t)
+                drain_wait(&B.k_full[t % q_KST], (t / q_KST) & 1);
+            for (int t = max(0, v_issued - q_VST); t < v_issued; ++t)
+                drain_wait(&B.v_full[t % q_VST], (t / q_VST) & 1);
         }
     } else if (warp == 1) {
         // Whole warp runs the loop (warp-uniform descriptors); the elected lane issues.
+        // Tensor-core order: S/dP(t+2) ahead of dQ(t), so dS(t) has the time of
+        // S/dP(t+1), dQ(t-1) and S/dP(t+2) to arrive.
         const bool leader = tc::elect_one_sync();
         const uint32_t id_s = tc::idesc_bf16(128, 64, false, false);    // S = Q K^T
         const uint32_t id_q = tc::idesc_bf16(128, 128, false, true);    // dQ += dS K
-        const uint32_t t_dQ = tmem + 256;
+        const uint32_t t_dQ = tmem + q_TDQ;
         bool ok = tc::warp_wait(&B.q_full, 0, p.err);
         // Base descriptors; each MMA advances them by a compile-time offset.
         const uint64_t dQ0 = tc::sdesc(tc::smem_u32(smem + q_Q), 16, 1024);
         const uint64_t ddO0 = tc::sdesc(tc::smem_u32(smem + q_dO), 16, 1024);
-        const uint64_t dDS0 = tc::sdesc(tc::smem_u32(smem + q_DS), 16, 1024);
-        const uint64_t dKVk0 = tc::sdesc(tc::smem_u32(smem + q_KV), 16, 1024);       // K-major
-        const uint64_t dKm0 = tc::sdesc(tc::smem_u32(smem + q_KV), 8 * KB, 1024);    // MN-major
-        auto issue_dq = [&](int t) -> bool {
-            const int b = t & 1, st = t % q_STAGES;
-            if (!tc::warp_wait(&B.ds_full[b], (t >> 1) & 1, p.err)) return false;
+        const uint64_t dKk0 = tc::sdesc(tc::smem_u32(smem + q_K), 16, 1024);       // K-major
+        const uint64_t dVk0 = tc::sdesc(tc::smem_u32(smem + q_V), 16, 1024);
+        const uint64_t dKm0 = tc::sdesc(tc::smem_u32(smem + q_K), 8 * KB, 1024);   // MN-major
+        auto issue_s = [&](int t) -> bool {
+            const int ks = t % q_KST, vs = t % q_VST, sb = t % q_NS;
+            if (!tc::warp_wait(&B.k_full[ks], (t / q_KST) & 1, p.err)) return false;
+            if (!tc::warp_wait(&B.v_full[vs], (t / q_VST) & 1, p.err)) return false;
             tc::tc_fence_after();
-            const uint32_t sb_off = b * 16 * KB, st_off = st * 32 * KB;
-            if (leader) {
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)      // K = 64 keys, 16 per MMA
-                    tc::mma_bf16(t_dQ, tc::sdesc_at(dDS0, sb_off + kk * 32),
-                                 tc::sdesc_at(dKm0, st_off + kk * 2048), id_q, (t > 0 || kk > 0) ? 1u : 0u);
-                tc::mma_commit(&B.kv_empty[st]);
-                tc::mma_commit(&B.ds_free[b]);
-            }
-            __syncwarp();
-            return true;
-        };
-        for (int t = 0; ok && t < T; ++t) {
-            const int st = t % q_STAGES, sb = t & 1;
-            if (!tc::warp_wait(&B.kv_full[st], (t / q_STAGES) & 1, p.err)) { ok = false; break; }
-            tc::tc_fence_after();
-            const uint32_t st_off = st * 32 * KB;
+            const uint32_t k_off = ks * 16 * KB, v_off = vs * 16 * KB;
             const uint32_t t_S = tmem + sb * 128, t_dP = t_S + 64;
             if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t oa = (kk >> 2) * 16 * KB + (kk & 3) * 32;
                     const uint32_t ob = (kk >> 2) * 8 * KB + (kk & 3) * 32;
-                    tc::mma_bf16(t_S, tc::sdesc_at(dQ0, oa), tc::sdesc_at(dKVk0, st_off + ob), id_s,
+                    tc::mma_bf16(t_S, tc::sdesc_at(dQ0, oa), tc::sdesc_at(dKk0, k_off + ob), id_s,
                                  kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t oa = (kk >> 2) * 16 * KB + (kk & 3) * 32;
                     const uint32_t ob = (kk >> 2) * 8 * KB + (kk & 3) * 32;
-                    tc::mma_bf16(t_dP, tc::sdesc_at(ddO0, oa), tc::sdesc_at(dKVk0, st_off + 16 * KB + ob),
-                                 id_s, kk > 0 ? 1u : 0u);
+                    tc::mma_bf16(t_dP, tc::sdesc_at(ddO0, oa), tc::sdesc_at(dVk0, v_off + ob), id_s,
+                                 kk > 0 ? 1u : 0u);
                 }
                 tc::mma_commit(&B.s_full[sb]);
+                tc::mma_commit(&B.v_empty[vs]);
             }
             __syncwarp();
-            if (t > 0 && !issue_dq(t - 1)) { ok = false; break; }
+            return true;
+        };
+        // dS(t) sits over S(t); S(t+3) reuses those columns but is issued after
+        // dQ(t), and the tensor core runs MMAs in issue order.
+        auto issue_dq = [&](int t) -> bool {
+            const int ks = t % q_KST;
+            if (!tc::warp_wait(&B.ds_full[t & 1], (t >> 1) & 1, p.err)) return false;
+            tc::tc_fence_after();
+            const uint32_t t_dS = tmem + (t % q_NS) * 128, k_off = ks * 16 * KB;
+            if (leader) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)      // K = 64 keys, 16 per MMA (8 columns)
+                    tc::mma_bf16_ts(t_dQ, t_dS + kk * 8, tc::sdesc_at(dKm0, k_off + kk * 2048), id_q,
+                                    (t > 0 || kk > 0) ? 1u : 0u);
+                tc::mma_commit(&B.k_empty[ks]);
+            }
+            __syncwarp();
+            return true;
+        };
+        if (ok && T > 0) ok = issue_s(0);
+        if (ok && T > 1) ok = issue_s(1);
+        for (int t = 0; ok && t < T; ++t) {
+            if (t + 2 < T && !issue_s(t + 2)) { ok = false; break; }
+            if (!issue_dq(t)) { ok = false; break; }
         }
-        if (ok && T > 0 && issue_dq(T - 1) && leader) tc::mma_commit(&B.acc_done);
+        if (ok && T > 0 && leader) tc::mma_commit(&B.acc_done);
         if (leader) {
             tc::mma_commit(&B.drain);
             drain_wait(&B.drain, 0);
         }
         __syncwarp();
     } else {
-        // Two warpgroups: warpgroup wg handles key columns [32 wg, 32 wg + 32) of
-        // every query row, and dQ columns [64 wg, 64 wg + 64) in the epilogue.
+        // Warpgroup wg owns the key tiles t = wg, wg + 2, ... (all 64 columns of
+        // each) and, in the epilogue, dQ columns [64 wg, 64 wg + 64).
         const int wg = (warp - 2) >> 2;
         const int quad = warp & 3;
         const int r = quad * 32 + lane;                      // query row of the tile
@@ -592,50 +619,46 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const float sl2 = rsqrtf(128.f) * kLog2e;
         const int64_t first_diag = p.q_start + (int64_t)qt * 128;   // first key of the own page
         bool ok = true;
-        for (int t = 0; t < T; ++t) {
-            const int sb = t & 1;
-            ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.s_full[sb], (t >> 1) & 1, p.err));
+        for (int t = wg; t < T; t += 2) {
+            const int sb = t % q_NS;
+            ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.s_full[sb], (t / q_NS) & 1, p.err));
             if (!ok) break;
             tc::tc_fence_after();
-            const int64_t kbase = (int64_t)page_of(t) * 128 + (t & 1) * 64 + wg * 32;
-            uint32_t sv[32], dv[32];
-            tc::tmem_ld32(lane_base + sb * 128 + wg * 32, sv);
-            tc::tmem_ld32(lane_base + sb * 128 + 64 + wg * 32, dv);
-            tc::tmem_wait_ld(sv);
-            tc::tmem_wait_ld(dv);
-            uint32_t dw[16];
-            if (kbase + 31 > first_diag) {                   // crosses the diagonal: mask
+            const int64_t kbase = (int64_t)page_of(t) * 128 + (t & 1) * 64;
+            uint32_t s0[32], s1[32], d0[32], d1[32];
+            tc::tmem_ld32(lane_base + sb * 128, s0);
+            tc::tmem_ld32(lane_base + sb * 128 + 32, s1);
+            tc::tmem_ld32(lane_base + sb * 128 + 64, d0);
+            tc::tmem_ld32(lane_base + sb * 128 + 96, d1);
+            tc::tmem_wait_ld(s0);
+            tc::tmem_wait_ld(s1);
+            tc::tmem_wait_ld(d0);
+            tc::tmem_wait_ld(d1);
+            uint32_t dw[32];
+            auto grad_half = [&](const uint32_t (&sv)[32], const uint32_t (&dv)[32], int c0, bool mask) {
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
                     float dr[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         float pv = fast_exp2(fmaf(__uint_as_float(sv[c + e]), sl2, -lse2));
-                        if (kbase + c + e > qpos) pv = 0.f;
+                        if (mask && kbase + c0 + c + e > qpos) pv = 0.f;
                         dr[e] = pv * (__uint_as_float(dv[c + e]) - Dr);
                     }
-                    dw[c / 2] = pack_bf16x2(dr[0], dr[1]);
+                    dw[(c0 + c) / 2] = pack_bf16x2(dr[0], dr[1]);
                 }
+            };
+            if (kbase + 63 > first_diag) {                   // crosses the diagonal: mask
+                grad_half(s0, d0, 0, true);
+                grad_half(s1, d1, 32, true);
             } else {
-#pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    float dr[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float pv = fast_exp2(fmaf(__uint_as_float(sv[c + e]), sl2, -lse2));
-                        dr[e] = pv * (__uint_as_float(dv[c + e]) - Dr);
-                    }
-                    dw[c / 2] = pack_bf16x2(dr[0], dr[1]);
-                }
+                grad_half(s0, d0, 0, false);
+                grad_half(s1, d1, 32, false);
             }
-            if (t >= 2) {
-                ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.ds_free[sb], ((t >> 1) - 1) & 1, p.err));
-                if (!ok) break;
-            }
-            store_row_half(smem + q_DS + sb * 16 * KB, r, wg, dw);
-            tc::fence_proxy_async_smem();
+            tc::tmem_st32(lane_base + sb * 128, dw);         // over this lane's S columns
+            tc::tmem_wait_st();
             tc::tc_fence_before();
-            tc::mbar_arrive(&B.ds_full[sb]);
+            tc::mbar_arrive(&B.ds_full[wg]);
         }
         if (ok && T > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.acc_done, 0, p.err));
         if (ok && T > 0) {
@@ -645,7 +668,7 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
                 uint32_t a[32];
-                tc::tmem_ld32(lane_base + 256 + c * 32, a);
+                tc::tmem_ld32(lane_base + q_TDQ + c * 32, a);
                 tc::tmem_wait_ld(a);
                 if (valid) {
 #pragma unroll

@@ -2,6 +2,8 @@
 // on: 128-byte-swizzled shared-memory tiles described by tcgen05 matrix
 // descriptors, K-major and MN-major, bf16 in, fp32 accumulate in tensor
 // memory, read back with tcgen05.ld. One CTA, one 128x128x64 product.
+// Mode 3 takes A from tensor memory instead (written by the threads with
+// tcgen05.st, row i in lane i, two bf16 per column) and B MN-major.
 //
 // Operands are staged into shared memory by the threads (the same byte
 // layout a 128-byte-swizzle TMA load produces), inside a 200 KB dynamic
@@ -42,7 +44,7 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(int mode, const __nv
     if (mode == 2) {                    // A stored [K=64][M=128]: two 64-wide M halves
         stage_sw128(sA, a, 64, 128, 0);
         stage_sw128(sA + 8192, a, 64, 128, 64);
-    } else {                            // A stored [M=128][K=64]
+    } else if (mode != 3) {             // A stored [M=128][K=64]
         stage_sw128(sA, a, 128, 64, 0);
     }
     if (mode >= 1) {                    // B stored [K=64][N=128]
@@ -57,13 +59,29 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(int mode, const __nv
         tc::fence_barrier_init();
     }
     if (warp == 0) {
-        tc::tmem_alloc(&tmem_base, 128);
+        tc::tmem_alloc(&tmem_base, 256);
         tc::tmem_relinquish();
     }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = tmem_base;
+    const uint32_t t_A = tmem + 128;    // mode 3: A in columns [128, 160)
+    if (mode == 3) {
+        // Thread i owns row i (lane i): 64 bf16 -> 32 columns, lower k in the low half.
+        const int row = threadIdx.x;
+        uint32_t w[32];
+        for (int c = 0; c < 32; ++c) {
+            const uint32_t lo = __bfloat16_as_ushort(a[(size_t)row * 64 + 2 * c]);
+            const uint32_t hi = __bfloat16_as_ushort(a[(size_t)row * 64 + 2 * c + 1]);
+            w[c] = lo | (hi << 16);
+        }
+        tc::tmem_st32(t_A + ((uint32_t)(warp * 32) << 16), w);
+        tc::tmem_wait_st();
+        tc::tc_fence_before();
+        __syncthreads();
+        tc::tc_fence_after();
+    }
 
     const uint32_t mn_lbo = lbo ? (uint32_t)lbo : 8192u;
     const uint32_t mn_sbo = sbo ? (uint32_t)sbo : 1024u;
@@ -75,7 +93,10 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(int mode, const __nv
                                           : tc::sdesc(a0 + kk * 32, 16, 1024);
             const uint64_t bd = mode >= 1 ? tc::sdesc(b0 + kk * 2048, mn_lbo, mn_sbo)
                                           : tc::sdesc(b0 + kk * 32, 16, 1024);
-            tc::mma_bf16(tmem, ad, bd, idesc, kk > 0);
+            if (mode == 3)
+                tc::mma_bf16_ts(tmem, t_A + kk * 8, bd, idesc, kk > 0);
+            else
+                tc::mma_bf16(tmem, ad, bd, idesc, kk > 0);
         }
         tc::mma_commit(&bar);
     }
@@ -93,7 +114,7 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(int mode, const __nv
     }
     tc::tc_fence_before();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem, 128);
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
 }  // namespace

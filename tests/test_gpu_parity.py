@@ -108,13 +108,13 @@ def test_permuted_block_table_gives_identical_results():
         np.testing.assert_array_equal(a, b)
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
 def test_umma_selftest(mode):
     g = torch.Generator().manual_seed(mode)
-    a = torch.randn((128, 64) if mode < 2 else (64, 128), generator=g).to(torch.bfloat16)
+    a = torch.randn((64, 128) if mode == 2 else (128, 64), generator=g).to(torch.bfloat16)
     b = torch.randn((128, 64) if mode == 0 else (64, 128), generator=g).to(torch.bfloat16)
     d = torch.empty((128, 128), dtype=torch.float32, device="cuda")
     B.pkv_selftest_umma(mode, a.cuda(), b.cuda(), d)
     af, bf = a.double(), b.double()
-    ref = af @ bf.T if mode == 0 else (af @ bf if mode == 1 else af.T @ bf)
+    ref = af @ bf.T if mode == 0 else (af.T @ bf if mode == 2 else af @ bf)
     np.testing.assert_allclose(d.cpu().double().numpy(), ref.numpy(), rtol=1e-5, atol=1e-4)
