@@ -410,27 +410,27 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
 // ============================================================================ dQ
 
-// K and V of a 64-key tile travel in separate rings: V is free once dP is
-// computed, K only after dQ, so K needs the deeper ring. S/dP of three tiles
-// live in tensor memory at once; the two softmax warpgroups take alternate
-// tiles, so each has two tiles' worth of tensor-core time to turn S/dP into dS.
-// dS (bf16) goes back into tensor memory over the S columns it came from, and
-// the dQ MMA reads its A operand there: no shared-memory traffic for dS.
-constexpr int q_KST = 6;
-constexpr int q_VST = 4;
-constexpr int q_NS = 3;                      // S/dP buffers in TMEM (128 columns each)
+// Whole-page key tiles (128 keys): S = Q K^T and dP = dO V^T are N = 128 MMAs
+// into one buffer. The softmax warps release it as soon as they have read it
+// (s_free), so S/dP of tile t+1 overlaps their work on tile t; dS (bf16) goes
+// to one of two tensor-memory buffers, read there as the A operand of
+// dQ += dS K. Tensor-core order: S/dP(t+1) ahead of dQ(t).
+// K and V travel in separate rings: V is free once dP is computed, K only after dQ.
+constexpr int q_KST = 3;
+constexpr int q_VST = 2;
 constexpr uint32_t q_Q = 0;                  // [128 q][128 d]: two 16 KB halves
 constexpr uint32_t q_dO = 32 * KB;
-constexpr uint32_t q_K = 64 * KB;            // stages x [64 keys][128 d]: two 8 KB halves
-constexpr uint32_t q_V = q_K + q_KST * 16 * KB;
-constexpr uint32_t q_SMEM = q_V + q_VST * 16 * KB + 1024;
-constexpr uint32_t q_TDQ = q_NS * 128;       // dQ accumulator columns [384, 512)
+constexpr uint32_t q_K = 64 * KB;            // stages x [128 keys][128 d]: two 16 KB halves
+constexpr uint32_t q_V = q_K + q_KST * 32 * KB;
+constexpr uint32_t q_SMEM = q_V + q_VST * 32 * KB + 1024;
+// Tensor-memory columns.
+constexpr uint32_t q_TS = 0, q_TDP = 128, q_TDQ = 256, q_TDS = 384;   // dS: 2 x 64 columns
 
 struct __align__(8) QBar {
     uint64_t q_full;
     uint64_t k_full[q_KST], k_empty[q_KST];
     uint64_t v_full[q_VST], v_empty[q_VST];
-    uint64_t s_full[q_NS];
+    uint64_t s_full, s_free;
     uint64_t ds_full[2];
     uint64_t acc_done;
     uint64_t drain;
@@ -450,10 +450,9 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;        // longest tiles first
     const int h = blockIdx.y;
     const int kvh = h / (p.Hq / p.Hkv);
-    // Half-page key tiles: two per visible page (dense: pages 0..own; sparse: listed pages).
-    const int T = 2 * (p.sel ? sel_count(p, qt, kvh) : (int)(p.q_start / 128) + qt + 1);
+    // Key tiles = visible pages (dense: pages 0..own; sparse: the listed pages).
+    const int T = p.sel ? sel_count(p, qt, kvh) : (int)(p.q_start / 128) + qt + 1;
     const int32_t* sel_row = p.sel ? p.sel + ((size_t)qt * p.Hkv + kvh) * p.kmax : nullptr;
-    auto page_of = [&](int t) -> int32_t { return sel_row ? sel_row[t >> 1] : (t >> 1); };
 
     if (threadIdx.x == 0) {
         tc::mbar_init(&B.q_full, 1);
@@ -465,8 +464,9 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tc::mbar_init(&B.v_full[s], 1);
             tc::mbar_init(&B.v_empty[s], 1);
         }
-        for (int s = 0; s < q_NS; ++s) tc::mbar_init(&B.s_full[s], 1);
-        for (int s = 0; s < 2; ++s) tc::mbar_init(&B.ds_full[s], 128);
+        tc::mbar_init(&B.s_full, 1);
+        tc::mbar_init(&B.s_free, kSoftmaxThreads);
+        for (int s = 0; s < 2; ++s) tc::mbar_init(&B.ds_full[s], kSoftmaxThreads);
         tc::mbar_init(&B.acc_done, 1);
         tc::mbar_init(&B.drain, 1);
         tc::fence_barrier_init();
@@ -493,35 +493,34 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tc::tma_load_3d(smem + q_dO + 16 * KB, &tm_do, &B.q_full, 64, h, q_row0);
         }
         tc::PageBatch pages;
-        pages.init(p.bt, sel_row, T / 2, lane);
+        pages.init(p.bt, sel_row, T, lane);
         int k_issued = 0, v_issued = 0;
-        int32_t pp = -1;
         for (int t = 0; t < T; ++t) {
             const int ks = t % q_KST, vs = t % q_VST;
             if (t >= q_KST &&
                 !__all_sync(0xffffffffu, tc::mbar_wait(&B.k_empty[ks], ((t / q_KST) - 1) & 1, p.err)))
                 break;
-            if ((t & 1) == 0) pp = pages.get(t >> 1);
+            const int32_t pp = pages.get(t);
             if (pp < 0 || pp >= p.num_phys) {
                 if (lane == 0) report_error(p.err, kErrBadPage);
                 break;
             }
-            const int row = (int)(((int64_t)pp * p.Hkv + kvh) * 128 + (t & 1) * 64);
+            const int row = (int)(((int64_t)pp * p.Hkv + kvh) * 128);
             if (lane == 0) {
-                uint8_t* kd = smem + q_K + ks * 16 * KB;
-                tc::mbar_arrive_expect_tx(&B.k_full[ks], 16 * KB);
+                uint8_t* kd = smem + q_K + ks * 32 * KB;
+                tc::mbar_arrive_expect_tx(&B.k_full[ks], 32 * KB);
                 tc::tma_load_2d(kd, &tm_k, &B.k_full[ks], 0, row);
-                tc::tma_load_2d(kd + 8 * KB, &tm_k, &B.k_full[ks], 64, row);
+                tc::tma_load_2d(kd + 16 * KB, &tm_k, &B.k_full[ks], 64, row);
             }
             k_issued = t + 1;
             if (t >= q_VST &&
                 !__all_sync(0xffffffffu, tc::mbar_wait(&B.v_empty[vs], ((t / q_VST) - 1) & 1, p.err)))
                 break;
             if (lane == 0) {
-                uint8_t* vd = smem + q_V + vs * 16 * KB;
-                tc::mbar_arrive_expect_tx(&B.v_full[vs], 16 * KB);
+                uint8_t* vd = smem + q_V + vs * 32 * KB;
+                tc::mbar_arrive_expect_tx(&B.v_full[vs], 32 * KB);
                 tc::tma_load_2d(vd, &tm_v, &B.v_full[vs], 0, row);
-                tc::tma_load_2d(vd + 8 * KB, &tm_v, &B.v_full[vs], 64, row);
+                tc::tma_load_2d(vd + 16 * KB, &tm_v, &B.v_full[vs], 64, row);
             }
             v_issued = t + 1;
         }
@@ -534,57 +533,53 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
     } else if (warp == 1) {
         // Whole warp runs the loop (warp-uniform descriptors); the elected lane issues.
-        // Tensor-core order: S/dP(t+2) ahead of dQ(t), so dS(t) has the time of
-        // S/dP(t+1), dQ(t-1) and S/dP(t+2) to arrive.
         const bool leader = tc::elect_one_sync();
-        const uint32_t id_s = tc::idesc_bf16(128, 64, false, false);    // S = Q K^T
+        const uint32_t id_s = tc::idesc_bf16(128, 128, false, false);   // S = Q K^T
         const uint32_t id_q = tc::idesc_bf16(128, 128, false, true);    // dQ += dS K
-        const uint32_t t_dQ = tmem + q_TDQ;
+        const uint32_t t_S = tmem + q_TS, t_dP = tmem + q_TDP, t_dQ = tmem + q_TDQ;
         bool ok = tc::warp_wait(&B.q_full, 0, p.err);
         // Base descriptors; each MMA advances them by a compile-time offset.
         const uint64_t dQ0 = tc::sdesc(tc::smem_u32(smem + q_Q), 16, 1024);
         const uint64_t ddO0 = tc::sdesc(tc::smem_u32(smem + q_dO), 16, 1024);
         const uint64_t dKk0 = tc::sdesc(tc::smem_u32(smem + q_K), 16, 1024);       // K-major
         const uint64_t dVk0 = tc::sdesc(tc::smem_u32(smem + q_V), 16, 1024);
-        const uint64_t dKm0 = tc::sdesc(tc::smem_u32(smem + q_K), 8 * KB, 1024);   // MN-major
+        const uint64_t dKm0 = tc::sdesc(tc::smem_u32(smem + q_K), 16 * KB, 1024);  // MN-major
         auto issue_s = [&](int t) -> bool {
-            const int ks = t % q_KST, vs = t % q_VST, sb = t % q_NS;
+            const int ks = t % q_KST, vs = t % q_VST;
             if (!tc::warp_wait(&B.k_full[ks], (t / q_KST) & 1, p.err)) return false;
             if (!tc::warp_wait(&B.v_full[vs], (t / q_VST) & 1, p.err)) return false;
+            if (t > 0 && !tc::warp_wait(&B.s_free, (t - 1) & 1, p.err)) return false;
             tc::tc_fence_after();
-            const uint32_t k_off = ks * 16 * KB, v_off = vs * 16 * KB;
-            const uint32_t t_S = tmem + sb * 128, t_dP = t_S + 64;
+            const uint32_t k_off = ks * 32 * KB, v_off = vs * 32 * KB;
             if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t oa = (kk >> 2) * 16 * KB + (kk & 3) * 32;
-                    const uint32_t ob = (kk >> 2) * 8 * KB + (kk & 3) * 32;
-                    tc::mma_bf16(t_S, tc::sdesc_at(dQ0, oa), tc::sdesc_at(dKk0, k_off + ob), id_s,
+                for (int kk = 0; kk < 8; ++kk) {    // K = d = 128, 16 per MMA
+                    const uint32_t o = (kk >> 2) * 16 * KB + (kk & 3) * 32;
+                    tc::mma_bf16(t_S, tc::sdesc_at(dQ0, o), tc::sdesc_at(dKk0, k_off + o), id_s,
                                  kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t oa = (kk >> 2) * 16 * KB + (kk & 3) * 32;
-                    const uint32_t ob = (kk >> 2) * 8 * KB + (kk & 3) * 32;
-                    tc::mma_bf16(t_dP, tc::sdesc_at(ddO0, oa), tc::sdesc_at(dVk0, v_off + ob), id_s,
+                    const uint32_t o = (kk >> 2) * 16 * KB + (kk & 3) * 32;
+                    tc::mma_bf16(t_dP, tc::sdesc_at(ddO0, o), tc::sdesc_at(dVk0, v_off + o), id_s,
                                  kk > 0 ? 1u : 0u);
                 }
-                tc::mma_commit(&B.s_full[sb]);
+                tc::mma_commit(&B.s_full);
                 tc::mma_commit(&B.v_empty[vs]);
             }
             __syncwarp();
             return true;
         };
-        // dS(t) sits over S(t); S(t+3) reuses those columns but is issued after
-        // dQ(t), and the tensor core runs MMAs in issue order.
+        // dS(t) is in buffer t & 1; softmax(t + 2) rewrites it only after S(t + 2),
+        // which the tensor core runs after dQ(t) (MMAs execute in issue order).
         auto issue_dq = [&](int t) -> bool {
             const int ks = t % q_KST;
             if (!tc::warp_wait(&B.ds_full[t & 1], (t >> 1) & 1, p.err)) return false;
             tc::tc_fence_after();
-            const uint32_t t_dS = tmem + (t % q_NS) * 128, k_off = ks * 16 * KB;
+            const uint32_t t_dS = tmem + q_TDS + (t & 1) * 64, k_off = ks * 32 * KB;
             if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)      // K = 64 keys, 16 per MMA (8 columns)
+                for (int kk = 0; kk < 8; ++kk)      // K = 128 keys, 16 per MMA (8 columns)
                     tc::mma_bf16_ts(t_dQ, t_dS + kk * 8, tc::sdesc_at(dKm0, k_off + kk * 2048), id_q,
                                     (t > 0 || kk > 0) ? 1u : 0u);
                 tc::mma_commit(&B.k_empty[ks]);
@@ -593,9 +588,8 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             return true;
         };
         if (ok && T > 0) ok = issue_s(0);
-        if (ok && T > 1) ok = issue_s(1);
         for (int t = 0; ok && t < T; ++t) {
-            if (t + 2 < T && !issue_s(t + 2)) { ok = false; break; }
+            if (t + 1 < T && !issue_s(t + 1)) { ok = false; break; }
             if (!issue_dq(t)) { ok = false; break; }
         }
         if (ok && T > 0 && leader) tc::mma_commit(&B.acc_done);
@@ -605,8 +599,8 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         __syncwarp();
     } else {
-        // Warpgroup wg owns the key tiles t = wg, wg + 2, ... (all 64 columns of
-        // each) and, in the epilogue, dQ columns [64 wg, 64 wg + 64).
+        // Two warpgroups: warpgroup wg handles keys [64 wg, 64 wg + 64) of every
+        // tile, and dQ columns [64 wg, 64 wg + 64) in the epilogue.
         const int wg = (warp - 2) >> 2;
         const int quad = warp & 3;
         const int r = quad * 32 + lane;                      // query row of the tile
@@ -619,21 +613,22 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const float sl2 = rsqrtf(128.f) * kLog2e;
         const int64_t first_diag = p.q_start + (int64_t)qt * 128;   // first key of the own page
         bool ok = true;
-        for (int t = wg; t < T; t += 2) {
-            const int sb = t % q_NS;
-            ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.s_full[sb], (t / q_NS) & 1, p.err));
+        for (int t = 0; t < T; ++t) {
+            ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.s_full, t & 1, p.err));
             if (!ok) break;
             tc::tc_fence_after();
-            const int64_t kbase = (int64_t)page_of(t) * 128 + (t & 1) * 64;
+            const int64_t kbase = (int64_t)(sel_row ? sel_row[t] : t) * 128 + wg * 64;
             uint32_t s0[32], s1[32], d0[32], d1[32];
-            tc::tmem_ld32(lane_base + sb * 128, s0);
-            tc::tmem_ld32(lane_base + sb * 128 + 32, s1);
-            tc::tmem_ld32(lane_base + sb * 128 + 64, d0);
-            tc::tmem_ld32(lane_base + sb * 128 + 96, d1);
+            tc::tmem_ld32(lane_base + q_TS + wg * 64, s0);
+            tc::tmem_ld32(lane_base + q_TS + wg * 64 + 32, s1);
+            tc::tmem_ld32(lane_base + q_TDP + wg * 64, d0);
+            tc::tmem_ld32(lane_base + q_TDP + wg * 64 + 32, d1);
             tc::tmem_wait_ld(s0);
             tc::tmem_wait_ld(s1);
             tc::tmem_wait_ld(d0);
             tc::tmem_wait_ld(d1);
+            tc::tc_fence_before();
+            tc::mbar_arrive(&B.s_free);                      // S/dP buffer may be overwritten
             uint32_t dw[32];
             auto grad_half = [&](const uint32_t (&sv)[32], const uint32_t (&dv)[32], int c0, bool mask) {
 #pragma unroll
@@ -655,10 +650,10 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 grad_half(s0, d0, 0, false);
                 grad_half(s1, d1, 32, false);
             }
-            tc::tmem_st32(lane_base + sb * 128, dw);         // over this lane's S columns
+            tc::tmem_st32(lane_base + q_TDS + (t & 1) * 64 + wg * 32, dw);
             tc::tmem_wait_st();
             tc::tc_fence_before();
-            tc::mbar_arrive(&B.ds_full[wg]);
+            tc::mbar_arrive(&B.ds_full[t & 1]);
         }
         if (ok && T > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.acc_done, 0, p.err));
         if (ok && T > 0) {
@@ -698,7 +693,7 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
     // The sparse dK/dV kernel lists the selecting query pages in shared memory.
     if (a.sel && (a.n_q + 127) / 128 > kMaxSelQp) return launch_attn_bwd_simt(a, s);
-    if ((reinterpret_cast<uintptr_t>(a.dout) & 15) || !a.tmap_k64) return cudaErrorInvalidValue;
+    if ((reinterpret_cast<uintptr_t>(a.dout) & 15) || !a.tmap_k) return cudaErrorInvalidValue;
     CUtensorMap tq64, tdo64, tq128, tdo128;
     std::string why;
     const uint64_t s2 = (uint64_t)a.Hq * 256;
@@ -731,7 +726,7 @@ cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     dim3 g_q((unsigned)((a.n_q + 127) / 128), a.Hq);
     ProfScope ps("bwd_q_tc_kernel", s);
-    bwd_q_tc_kernel<<<g_q, kThreads, q_SMEM, s>>>(tq128, tdo128, *a.tmap_k64, *a.tmap_v64, p);
+    bwd_q_tc_kernel<<<g_q, kThreads, q_SMEM, s>>>(tq128, tdo128, *a.tmap_k, *a.tmap_v, p);
     return cudaGetLastError();
 }
 
