@@ -9,17 +9,23 @@
 //
 // One CTA per (query tile of 128 rows = one query page, query head); key
 // tiles are whole pages (P = 128), fetched by TMA with the physical page
-// taken from the block table. Warp roles (224 threads):
-//   warp 0      TMA producer: Q once, then K pages into a 3-stage ring.
-//   warp 6      TMA producer: V pages into a 2-stage ring.
-//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into a double-buffered
-//               TMEM tile, then O += P_{j-1} V_{j-1} (O lives in TMEM).
-//   warps 2..5  softmax: one thread per query row; reads S_j from TMEM, keeps
-//               the running max m and sum l, writes P_j (bf16) to shared
-//               memory in the 128-byte-swizzled K-major layout, and rescales
-//               O in TMEM only when m grows by more than 2^8 (P <= 256 then,
-//               exactly representable range for bf16). Epilogue: O / l, LSE.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256,384) of a 512-column block.
+// taken from the block table. Both MMAs take their A operand from tensor
+// memory (an A operand in shared memory costs the tensor core a fixed ~33
+// cycles per instruction on top of the math): Q is placed there once, and
+// P overwrites the S columns it came from. Warp roles (352 threads):
+//   warp 0       TMA producer: K pages into a 3-stage ring.
+//   warp 10      TMA producer: V pages into a 3-stage ring.
+//   warp 1       MMA issuer (elected lane): S_j = Q K_j^T into a double-
+//                buffered TMEM tile, then O += P_{j-1} V_{j-1} (O in TMEM).
+//   warps 2..9   softmax, two warpgroups: thread (wg, row) owns keys
+//                [64 wg, 64 wg + 64) of query row `row` in every tile. The two
+//                partial row maxima meet through shared memory (an mbarrier
+//                per tile parity); the running max m is shared, the sums l are
+//                kept per warpgroup and added at the end. O is rescaled in TMEM
+//                only when m grows by more than 2^8 (P <= 256 then, exactly
+//                representable range for bf16), each warpgroup its own half
+//                of the columns. Epilogue: O / l, LSE.
+// TMEM columns: S0 [0,128), S1 [128,256), O [256,384), Q [384,448).
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -31,24 +37,25 @@ namespace pkv {
 namespace {
 
 constexpr int kTile = 128;                   // query rows = keys per tile = head dim
-constexpr int kThreads = 224;
+constexpr int kThreads = 352;
+constexpr int kSoftmaxThreads = 256;
 constexpr uint32_t kHalfBytes = 128 * 128;   // [128 rows][64 bf16] = 16 KB
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;
 // Shared-memory tile offsets (bytes from a 1024-aligned base).
 // K and V have separate rings: a K stage is free as soon as S_j completes, so
 // K loads run kKStages - 1 tiles ahead; a V stage is free after PV_j.
-constexpr int kKStages = 3, kVStages = 2;
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTileBytes;
+constexpr int kKStages = 3, kVStages = 3;
+constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
-constexpr uint32_t kOffP = kOffV + kVStages * kTileBytes;
-constexpr uint32_t kTilesBytes = kOffP + kTileBytes;    // 224 KB
-constexpr uint32_t kSmemBytes = kTilesBytes + 1024;     // + alignment slack
-constexpr float kRescaleThreshold = 8.0f;               // log2 units
+constexpr uint32_t kTilesBytes = kOffV + kVStages * kTileBytes;   // 192 KB
+constexpr uint32_t kSmemBytes = kTilesBytes + 1024;               // + alignment slack
+constexpr float kRescaleThreshold = 8.0f;                         // log2 units
+constexpr uint32_t kColO = 256, kColQ = 384;
 
 struct FwdParams {
     int Hq, Hkv;
     int64_t q_start, n_q;
+    const void* q;
     void* o;
     float* lse;
     const int32_t* bt;
@@ -59,17 +66,19 @@ struct FwdParams {
 };
 
 struct __align__(8) FwdBarriers {
-    uint64_t q_full;
+    uint64_t q_full;                 // Q in TMEM (256 softmax arrivals)
     uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
     uint64_t s_full[2];
     uint64_t p_full;
     uint64_t o_done;
+    uint64_t xchg[2];                // row-statistics exchange, by tile parity
     uint64_t drain;
     uint32_t tmem_base;
     int n_tiles;
+    float red[2][2][kTile];          // [parity][warpgroup][row]
 };
 
-// Number of key tiles and the logical page of tile j for this CTA.
+// Number of key tiles for this CTA.
 __device__ __forceinline__ int tile_count(const FwdParams& p, int qt, int kvh) {
     if (!p.sel) return (int)(p.q_start / kTile) + qt + 1;
     const int32_t* row = p.sel + ((size_t)qt * p.Hkv + kvh) * p.kmax;
@@ -77,32 +86,24 @@ __device__ __forceinline__ int tile_count(const FwdParams& p, int qt, int kvh) {
     while (n < p.kmax && row[n] >= 0) ++n;
     return n;
 }
-__device__ __forceinline__ int32_t tile_page(const FwdParams& p, int qt, int kvh, int j) {
-    return p.sel ? p.sel[((size_t)qt * p.Hkv + kvh) * p.kmax + j] : j;
-}
+
+// Tensor-memory column (within an S buffer) of P for keys [16 kk, 16 kk + 16):
+// warpgroup wg packs its 64 keys into the first 32 of the 64 columns it read.
+__device__ __forceinline__ uint32_t p_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
 using tc::drain_wait;
 
-// One producer warp: streams the K ring (and Q first) or the V ring. The whole
-// warp walks the tiles (page indices come 32 at a time from a PageBatch);
-// lane 0 issues the copies. A K load never waits behind a V stage in use.
+// One producer warp: streams the K ring or the V ring. The whole warp walks
+// the tiles (page indices come 32 at a time from a PageBatch); lane 0 issues
+// the copies. A K load never waits behind a V stage in use.
 __device__ __forceinline__ void produce_ring(const FwdParams& p, uint8_t* smem, FwdBarriers& B,
-                                             const CUtensorMap& tmap_q, const CUtensorMap& tmap,
-                                             bool is_k, int qt, int h, int kvh, int nt, int lane) {
+                                             const CUtensorMap& tmap, bool is_k, int qt, int kvh,
+                                             int nt, int lane) {
     const int nst = is_k ? kKStages : kVStages;
     uint64_t* full = is_k ? B.k_full : B.v_full;
     uint64_t* empty = is_k ? B.k_empty : B.v_empty;
     uint8_t* base = smem + (is_k ? kOffK : kOffV);
-    if (lane == 0) {
-        tc::prefetch_tmap(&tmap);
-        if (is_k) {
-            tc::prefetch_tmap(&tmap_q);
-            const int q_row0 = qt * kTile;
-            tc::mbar_arrive_expect_tx(&B.q_full, kTileBytes);
-            tc::tma_load_3d(smem + kOffQ, &tmap_q, &B.q_full, 0, h, q_row0);
-            tc::tma_load_3d(smem + kOffQ + kHalfBytes, &tmap_q, &B.q_full, 64, h, q_row0);
-        }
-    }
+    if (lane == 0) tc::prefetch_tmap(&tmap);
     tc::PageBatch pages;
     pages.init(p.bt, p.sel ? p.sel + ((size_t)qt * p.Hkv + kvh) * p.kmax : nullptr, nt, lane);
     int issued = 0;
@@ -126,15 +127,13 @@ __device__ __forceinline__ void produce_ring(const FwdParams& p, uint8_t* smem, 
         issued = j + 1;
     }
     // Make sure none of this CTA's copies is still landing when it exits.
-    if (lane == 0) {
-        if (is_k) drain_wait(&B.q_full, 0);
+    if (lane == 0)
         for (int j = max(0, issued - nst); j < issued; ++j) drain_wait(&full[j % nst], (j / nst) & 1);
-    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-              const __grid_constant__ CUtensorMap tmap_v, FwdParams p) {
+fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+              FwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -146,7 +145,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     const int kvh = h / (p.Hq / p.Hkv);
 
     if (threadIdx.x == 0) {
-        tc::mbar_init(&B.q_full, 1);
+        tc::mbar_init(&B.q_full, kSoftmaxThreads);
         for (int s = 0; s < kKStages; ++s) {
             tc::mbar_init(&B.k_full[s], 1);
             tc::mbar_init(&B.k_empty[s], 1);
@@ -155,8 +154,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
             tc::mbar_init(&B.v_full[s], 1);
             tc::mbar_init(&B.v_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) tc::mbar_init(&B.s_full[s], 1);
-        tc::mbar_init(&B.p_full, 128);
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(&B.s_full[s], 1);
+            tc::mbar_init(&B.xchg[s], kSoftmaxThreads);
+        }
+        tc::mbar_init(&B.p_full, kSoftmaxThreads);
         tc::mbar_init(&B.o_done, 1);
         tc::mbar_init(&B.drain, 1);
         B.n_tiles = tile_count(p, qt, kvh);
@@ -173,11 +175,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     const int nt = B.n_tiles;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ Q + K producer
-        produce_ring(p, smem, B, tmap_q, tmap_k, true, qt, h, kvh, nt, lane);
+        // ------------------------------------------------------------ K producer
+        produce_ring(p, smem, B, tmap_k, true, qt, kvh, nt, lane);
     } else if (warp == kThreads / 32 - 1) {
         // ------------------------------------------------------------ V producer
-        produce_ring(p, smem, B, tmap_q, tmap_v, false, qt, h, kvh, nt, lane);
+        produce_ring(p, smem, B, tmap_v, false, qt, kvh, nt, lane);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // The whole warp runs the loop (warp-uniform descriptors); one elected
@@ -185,27 +187,27 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         const bool leader = tc::elect_one_sync();
         const uint32_t idesc = tc::idesc_bf16(128, 128, false, false);       // S = Q K^T
         const uint32_t idesc_pv = tc::idesc_bf16(128, 128, false, true);     // O += P V
-        // Base descriptors; each MMA advances them by a compile-time offset.
-        const uint64_t dq0 = tc::sdesc(tc::smem_u32(smem + kOffQ), 16, 1024);
-        const uint64_t dp0 = tc::sdesc(tc::smem_u32(smem + kOffP), 16, 1024);
-        const uint32_t tmem_o = tmem + 256;
+        const uint32_t tmem_o = tmem + kColO, tmem_q = tmem + kColQ;
+        const uint64_t dk0 = tc::sdesc(tc::smem_u32(smem + kOffK), 16, 1024);            // K-major
+        const uint64_t dv0 = tc::sdesc(tc::smem_u32(smem + kOffV), kHalfBytes, 1024);    // MN-major
         bool ok = tc::warp_wait(&B.q_full, 0, p.err);
+        // P_i sits over S_i in TMEM; S_{i+2} reuses those columns but is issued
+        // after PV_i, and the tensor core runs MMAs in issue order.
         auto issue_pv = [&](int i) -> bool {
+            const int vs = i % kVStages;
             if (!tc::warp_wait(&B.p_full, i & 1, p.err)) return false;
-            if (!tc::warp_wait(&B.v_full[i % kVStages], (i / kVStages) & 1, p.err)) return false;
+            if (!tc::warp_wait(&B.v_full[vs], (i / kVStages) & 1, p.err)) return false;
             tc::tc_fence_after();
-            // A = P [128 q][128 keys] K-major; B = V [128 keys][128 d] MN-major:
-            // 16 keys = 2 K-groups of 8 rows (1024 B apart); d spans the two
-            // 64-column halves (16 KB apart).
-            const uint64_t b0 = tc::sdesc(tc::smem_u32(smem + kOffV + (i % kVStages) * kTileBytes),
-                                          kHalfBytes, 1024);
+            // B = V [128 keys][128 d] MN-major: 16 keys = 2 K-groups of 8 rows
+            // (1024 B apart); d spans the two 64-column halves (16 KB apart).
+            const uint32_t tmem_p = tmem + (i & 1) * 128;
             if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc::mma_bf16(tmem_o, tc::sdesc_at(dp0, (kk >> 2) * kHalfBytes + (kk & 3) * 32),
-                                 tc::sdesc_at(b0, kk * 2048), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+                    tc::mma_bf16_ts(tmem_o, tmem_p + p_col(kk), tc::sdesc_at(dv0, vs * kTileBytes + kk * 2048),
+                                    idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
                 tc::mma_commit(&B.o_done);
-                tc::mma_commit(&B.v_empty[i % kVStages]);
+                tc::mma_commit(&B.v_empty[vs]);
             }
             __syncwarp();
             return true;
@@ -214,14 +216,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
             const int ks = j % kKStages;
             if (!tc::warp_wait(&B.k_full[ks], (j / kKStages) & 1, p.err)) { ok = false; break; }
             tc::tc_fence_after();
-            const uint64_t dk0 = tc::sdesc(tc::smem_u32(smem + kOffK + ks * kTileBytes), 16, 1024);
             const uint32_t tmem_s = tmem + (j & 1) * 128;
             if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
+                for (int kk = 0; kk < 8; ++kk) {    // K = d: 16 per MMA, 8 TMEM columns of Q
                     const uint32_t koff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                    tc::mma_bf16(tmem_s, tc::sdesc_at(dq0, koff), tc::sdesc_at(dk0, koff), idesc,
-                                 kk > 0 ? 1u : 0u);
+                    tc::mma_bf16_ts(tmem_s, tmem_q + kk * 8, tc::sdesc_at(dk0, ks * kTileBytes + koff),
+                                    idesc, kk > 0 ? 1u : 0u);
                 }
                 tc::mma_commit(&B.s_full[j & 1]);
                 tc::mma_commit(&B.k_empty[ks]);
@@ -237,48 +238,74 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ softmax (128 threads)
+        // ------------------------------------------------------------ softmax (256 threads)
+        const int wg = (warp - 2) >> 2;
         const int quad = warp & 3;                    // TMEM lane quadrant of this warp
         const int row = quad * 32 + lane;             // query row within the tile
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         const float sl2 = rsqrtf(128.f) * kLog2e;
         const int64_t q_local = (int64_t)qt * kTile + row;
+        const bool valid = q_local < p.n_q;
+        {
+            // Q row, head dims [64 wg, 64 wg + 64) -> TMEM columns kColQ + 32 wg ..
+            uint32_t w[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) w[e] = 0u;          // rows past the chunk: Q = 0
+            if (valid) {
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    static_cast<const __nv_bfloat16*>(p.q) + ((size_t)q_local * p.Hq + h) * kTile + wg * 64);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    const uint4 u = __ldg(src + v);
+                    w[4 * v] = u.x; w[4 * v + 1] = u.y; w[4 * v + 2] = u.z; w[4 * v + 3] = u.w;
+                }
+            }
+            tc::tmem_st32(lane_base + kColQ + wg * 32, w);
+            tc::tmem_wait_st();
+            tc::tc_fence_before();
+            tc::mbar_arrive(&B.q_full);
+        }
         float m = -INFINITY, l = 0.f;
         bool ok = true;
-        uint8_t* sP = smem + kOffP;
         for (int j = 0; j < nt; ++j) {
             const int st = j & 1;
-            ok = tc::mbar_wait(&B.s_full[st], (j >> 1) & 1, p.err);
-            ok = __all_sync(0xffffffffu, ok);
+            ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.s_full[st], (j >> 1) & 1, p.err));
             if (!ok) break;
             tc::tc_fence_after();
-            // Raw logits q.k; the scale is folded into the exp2 argument below.
-            float x[128];
+            // Raw logits q.k of my 64 keys; the scale is folded into the exp2 argument.
+            float x[64];
+            {
+                uint32_t r0[32], r1[32];
+                tc::tmem_ld32(lane_base + st * 128 + wg * 64, r0);
+                tc::tmem_ld32(lane_base + st * 128 + wg * 64 + 32, r1);
+                tc::tmem_wait_ld(r0);
+                tc::tmem_wait_ld(r1);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tc::tmem_ld32(lane_base + st * 128 + c * 32, r);
-                tc::tmem_wait_ld(r);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(r[e]);
+                for (int e = 0; e < 32; ++e) {
+                    x[e] = __uint_as_float(r0[e]);
+                    x[32 + e] = __uint_as_float(r1[e]);
+                }
             }
             if (j == nt - 1) {                        // own page: causal mask (key col > row)
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (c > row) x[c] = -INFINITY;
+                for (int c = 0; c < 64; ++c)
+                    if (wg * 64 + c > row) x[c] = -INFINITY;
             }
-            // Row max with 8 independent chains (a single chain of 128 dependent
-            // max operations would dominate the tile's latency).
+            // Row max with 8 independent chains, then the other warpgroup's half.
             float mpart[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) mpart[k] = x[k];
 #pragma unroll
-            for (int c = 8; c < 128; ++c) mpart[c & 7] = fmaxf(mpart[c & 7], x[c]);
+            for (int c = 8; c < 64; ++c) mpart[c & 7] = fmaxf(mpart[c & 7], x[c]);
 #pragma unroll
             for (int k = 4; k > 0; k >>= 1)
 #pragma unroll
                 for (int i = 0; i < k; ++i) mpart[i] = fmaxf(mpart[i], mpart[i + k]);
-            const float mx = mpart[0] * sl2;          // scaled, log2 units
+            B.red[st][wg][row] = mpart[0];
+            tc::mbar_arrive(&B.xchg[st]);             // release: the partial max is visible
+            ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.xchg[st], (j >> 1) & 1, p.err));
+            if (!ok) break;
+            const float mx = fmaxf(mpart[0], B.red[st][wg ^ 1][row]) * sl2;   // scaled, log2 units
             float alpha = 1.f;
             bool rescale = false;
             if (mx > m + kRescaleThreshold) {
@@ -287,13 +314,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
                 rescale = true;
             }
             l *= alpha;
-            uint32_t pk[64];
+            uint32_t pk[32];
             float lpart[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) lpart[k] = 0.f;
             const float neg_m = -m;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
+            for (int c = 0; c < 32; ++c) {
                 const float p0 = fast_exp2(fmaf(x[2 * c], sl2, neg_m));
                 const float p1 = fast_exp2(fmaf(x[2 * c + 1], sl2, neg_m));
                 pk[c] = pack_bf16x2(p0, p1);
@@ -306,49 +333,45 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
 #pragma unroll
                 for (int i = 0; i < k; ++i) lpart[i] += lpart[i + k];
             l += lpart[0];
-            if (j > 0) {                              // PV_{j-1} done: P buffer free, O stable
-                ok = tc::mbar_wait(&B.o_done, (j - 1) & 1, p.err);
-                ok = __all_sync(0xffffffffu, ok);
+            if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+                // PV_{j-1} must be done before O is touched (PV_j waits for this tile's P).
+                ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.o_done, (j - 1) & 1, p.err));
                 if (!ok) break;
                 tc::tc_fence_after();
-                if (__any_sync(0xffffffffu, rescale)) {
-                    const float f = rescale ? alpha : 1.f;
+                const float f = rescale ? alpha : 1.f;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t r[32];
-                        tc::tmem_ld32(lane_base + 256 + c * 32, r);
-                        tc::tmem_wait_ld(r);
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t r[32];
+                    tc::tmem_ld32(lane_base + kColO + wg * 64 + c * 32, r);
+                    tc::tmem_wait_ld(r);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
-                        tc::tmem_st32(lane_base + 256 + c * 32, r);
-                    }
-                    tc::tmem_wait_st();
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
+                    tc::tmem_st32(lane_base + kColO + wg * 64 + c * 32, r);
                 }
             }
-            // P row -> shared memory, 128-byte swizzle, keys 0..63 | 64..127 halves.
-#pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
-                uint8_t* base = sP + (ch >> 3) * kHalfBytes;
-                *reinterpret_cast<uint4*>(base + tc::sw128_offset(row, ch & 7)) =
-                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-            }
-            tc::fence_proxy_async_smem();
+            // P over the first 32 of the 64 S columns this thread read.
+            tc::tmem_st32(lane_base + st * 128 + wg * 64, pk);
+            tc::tmem_wait_st();
             tc::tc_fence_before();
             tc::mbar_arrive(&B.p_full);
         }
         if (ok && nt > 0) {
-            ok = tc::mbar_wait(&B.o_done, (nt - 1) & 1, p.err);
-            ok = __all_sync(0xffffffffu, ok);
+            // Row sum = both warpgroups' partial sums (same running max).
+            const int sx = nt & 1;
+            B.red[sx][wg][row] = l;
+            tc::mbar_arrive(&B.xchg[sx]);
+            ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.xchg[sx], (nt >> 1) & 1, p.err));
+            if (ok) l += B.red[sx][wg ^ 1][row];
         }
+        if (ok && nt > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.o_done, (nt - 1) & 1, p.err));
         if (ok && nt > 0) {
             tc::tc_fence_after();
             const float inv = 1.f / l;
-            const bool valid = q_local < p.n_q;
             __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + ((size_t)q_local * p.Hq + h) * kTile;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
                 uint32_t r[32];
-                tc::tmem_ld32(lane_base + 256 + c * 32, r);
+                tc::tmem_ld32(lane_base + kColO + c * 32, r);
                 tc::tmem_wait_ld(r);
                 if (valid) {
 #pragma unroll
@@ -362,7 +385,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
                     }
                 }
             }
-            if (valid) p.lse[(size_t)h * p.n_q + q_local] = (m + log2f(l)) * kLn2;
+            if (valid && wg == 0) p.lse[(size_t)h * p.n_q + q_local] = (m + log2f(l)) * kLn2;
         }
     }
 
@@ -382,11 +405,6 @@ bool tc_supported(const AttnArgs& a) {
 }
 
 cudaError_t launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t s) {
-    CUtensorMap tq;
-    std::string why;
-    if (!make_tmap_3d(&tq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, a.Hq, a.n_q, 256,
-                      (uint64_t)a.Hq * 256, 64, 1, 128, &why))
-        return cudaErrorInvalidValue;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -396,11 +414,11 @@ cudaError_t launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t s) {
     }
     FwdParams p{};
     p.Hq = a.Hq; p.Hkv = a.Hkv; p.q_start = a.q_start; p.n_q = a.n_q;
-    p.o = a.o; p.lse = a.lse; p.bt = a.bt; p.num_phys = a.num_phys;
+    p.q = a.q; p.o = a.o; p.lse = a.lse; p.bt = a.bt; p.num_phys = a.num_phys;
     p.sel = a.sel; p.kmax = a.kmax; p.err = a.err;
     dim3 grid((unsigned)((a.n_q + kTile - 1) / kTile), a.Hq);
     ProfScope ps("fwd_tc_kernel", s);
-    fwd_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, *a.tmap_k, *a.tmap_v, p);
+    fwd_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(*a.tmap_k, *a.tmap_v, p);
     return cudaGetLastError();
 }
 
