@@ -9,8 +9,8 @@
 // D_i = rowsum(dO_i * O_i) comes from the row-dot kernel run before these.
 //
 // Two kernels, so that no output needs atomics between CTAs:
-//   bwd_kv_tc_kernel  one CTA per (key page, KV head). K and V of the page stay
-//                     in shared memory; the CTA walks every 64-query tile of
+//   bwd_kv_tc_kernel  one CTA per (key page, KV head). K of the page stays in
+//                     tensor memory, V in shared memory; the CTA walks every 64-query tile of
 //                     the chunk that sees the page, for each of the g query
 //                     heads of the group, and accumulates dK and dV in tensor
 //                     memory. At the end it adds them into the page's gradient
@@ -21,13 +21,17 @@
 //                     visible keys in half-page tiles of 64 and accumulates dQ
 //                     in tensor memory, written once as bf16.
 // Both have the forward's warp roles: warp 0 TMA producer, warp 1 MMA issuer
-// (elected lane), then two softmax warpgroups, one thread per accumulator row.
-// In the dK/dV kernel S^T and dP^T are double-buffered in tensor memory and
-// both warpgroups split each tile's columns; in the dQ kernel three S/dP tiles
-// are in flight and the warpgroups take alternate tiles, so the tensor core
-// computes tiles t+1 and t+2 while a warpgroup works on tile t.
+// (elected lane), then two softmax warpgroups, one thread per accumulator row,
+// that split each tile's columns. The S/dP (or S^T/dP^T) buffer is released
+// as soon as the softmax warps have read it, so the tensor core computes tile
+// t+1 while they work on tile t. Wherever tensor memory has room, the MMAs take
+// their A operand from it rather than from shared memory (an A operand in
+// shared memory costs the tensor core ~33 extra cycles per instruction on this
+// part): K, P^T and dS^T in the dK/dV kernel, Q and dS in the dQ kernel.
 #include <cuda_bf16.h>
 #include <math.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "internal.h"
@@ -45,6 +49,8 @@ constexpr uint32_t KB = 1024;
 struct BwdParams {
     int Hq, Hkv;
     int64_t q_start, n_q;
+    const void* q;             // [n_q, Hq, d] bf16
+    const void* kpool;         // [pages, Hkv, 128, d] bf16 (the tensor maps' base)
     const float* lse;          // [Hq, n_q]
     const float* Dbuf;         // [Hq, n_q]
     void* dq;                  // [n_q, Hq, d] bf16
@@ -73,27 +79,29 @@ __device__ __forceinline__ int sel_count(const BwdParams& p, int qp, int kvh) {
 // Shared-memory layout (offsets from a 1024-aligned base).
 // Q/dO stage for tile t+1 is the one tile t-3 used: the load has two
 // iterations of slack behind the gradient products of tile t-2.
-// P^T and dS^T never touch shared memory: the softmax warps write them (bf16)
-// into tensor memory over the S^T / dP^T columns they have just read, and the
-// gradient MMAs take their A operand from there.
+// Every A operand except V lives in tensor memory: K (placed once by the
+// softmax warps, the A of every S^T MMA), P^T and dS^T (written by the softmax
+// warps, the A of the dV and dK MMAs). S^T/dP^T are single-buffered and
+// released as soon as the softmax warps have read them (s_free), so S^T(t+1)
+// overlaps their work on tile t; P^T/dS^T are rewritten once the gradient
+// MMAs of the previous tile have read them (p_free).
 constexpr int kv_STAGES = 4;
-constexpr uint32_t kv_K = 0;                 // [128 keys][128 d]: two 16 KB halves
-constexpr uint32_t kv_V = 32 * KB;
-constexpr uint32_t kv_Q = 64 * KB;           // stages x [64 q][128 d]: two 8 KB halves
+constexpr uint32_t kv_V = 0;                 // [128 keys][128 d]: two 16 KB halves
+constexpr uint32_t kv_Q = 32 * KB;           // stages x [64 q][128 d]: two 8 KB halves
 constexpr uint32_t kv_dO = kv_Q + kv_STAGES * 16 * KB;
 constexpr uint32_t kv_STAT = kv_dO + kv_STAGES * 16 * KB;   // stages x (64 lse*log2e + 64 D) floats
 constexpr uint32_t kv_SMEM = kv_STAT + kv_STAGES * 512 + 1024;
-
-// Tensor-memory column of the bf16 operand for queries [16 kk, 16 kk + 16) of
-// a tile (kk = 0..3): warpgroup wg packs its 32 queries into the first 16 of
-// the 32 fp32 columns it read, so the halves sit at column offsets 0 and 32.
-__device__ __forceinline__ uint32_t kv_pk_col(int kk) { return (kk >> 1) * 32 + (kk & 1) * 8; }
+// Tensor-memory columns: S^T, dP^T (64 fp32 each), P^T, dS^T (64 bf16 = 32
+// each), K (128 bf16 = 64), dK, dV accumulators (128 fp32 each).
+constexpr uint32_t kv_TS = 0, kv_TDP = 64, kv_TP = 128, kv_TDS = 160, kv_TK = 192, kv_TDK = 256,
+                   kv_TDV = 384;
 
 struct __align__(8) KVBar {
     uint64_t kv_full;
     uint64_t qdo_full[kv_STAGES], qdo_empty[kv_STAGES];
-    uint64_t s_full[2];
-    uint64_t p_full[2];
+    uint64_t k_tmem;                 // K in TMEM (softmax threads)
+    uint64_t s_full, s_free;
+    uint64_t p_full, p_free;
     uint64_t acc_done;
     uint64_t drain;
     uint32_t tmem_base;
@@ -104,8 +112,7 @@ struct __align__(8) KVBar {
 
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-                 const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                 BwdParams p) {
+                 const __grid_constant__ CUtensorMap tm_v, BwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -154,10 +161,11 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tc::mbar_init(&B.qdo_full[s], 32);
             tc::mbar_init(&B.qdo_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            tc::mbar_init(&B.s_full[s], 1);
-            tc::mbar_init(&B.p_full[s], kSoftmaxThreads);
-        }
+        tc::mbar_init(&B.k_tmem, kSoftmaxThreads);
+        tc::mbar_init(&B.s_full, 1);
+        tc::mbar_init(&B.s_free, kSoftmaxThreads);
+        tc::mbar_init(&B.p_full, kSoftmaxThreads);
+        tc::mbar_init(&B.p_free, 1);
         tc::mbar_init(&B.acc_done, 1);
         tc::mbar_init(&B.drain, 1);
         tc::fence_barrier_init();
@@ -173,8 +181,17 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tc::tc_fence_after();
     const uint32_t tmem = B.tmem_base;
     const int n_i = B.n_i;
-    const int T = n_i * g;                           // iterations: (head, 64-query tile)
-    auto tile_of = [&](int t) -> int { return p.sel ? (int)B.tiles[t % n_i] : i0 + t % n_i; };
+    // Iterations (head, 64-query tile), t = head * n_i + tile; blockIdx.z takes
+    // the share [t_base, t_base + T) of them (the gradient epilogue adds, so
+    // any partition of the iterations gives the same sums).
+    const int t_all = n_i * g;
+    const int t_base = (int)(((int64_t)t_all * blockIdx.z) / gridDim.z);
+    const int T = (int)(((int64_t)t_all * (blockIdx.z + 1)) / gridDim.z) - t_base;
+    auto tile_of = [&](int t) -> int {
+        const int u = (t_base + t) % n_i;
+        return p.sel ? (int)B.tiles[u] : i0 + u;
+    };
+    auto head_of = [&](int t) -> int { return kvh * g + (t_base + t) / n_i; };
 
     if (!page_ok || T == 0) {
         // nothing issued: fall through to the common exit
@@ -184,9 +201,7 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (lane == 0) {
             tc::prefetch_tmap(&tm_q);
             tc::prefetch_tmap(&tm_do);
-            tc::mbar_arrive_expect_tx(&B.kv_full, 64 * KB);
-            tc::tma_load_2d(smem + kv_K, &tm_k, &B.kv_full, 0, row);
-            tc::tma_load_2d(smem + kv_K + 16 * KB, &tm_k, &B.kv_full, 64, row);
+            tc::mbar_arrive_expect_tx(&B.kv_full, 32 * KB);
             tc::tma_load_2d(smem + kv_V, &tm_v, &B.kv_full, 0, row);
             tc::tma_load_2d(smem + kv_V + 16 * KB, &tm_v, &B.kv_full, 64, row);
         }
@@ -195,7 +210,7 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // the wait for the next free stage.
         auto load_stats = [&](int t, float (&s)[4]) {
             if (t >= T) return;
-            const int h = kvh * g + t / n_i;
+            const int h = head_of(t);
             const int i = tile_of(t);
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -212,7 +227,7 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 !__all_sync(0xffffffffu, tc::mbar_wait(&B.qdo_empty[st], ((t / kv_STAGES) - 1) & 1, p.err)))
                 return false;
             if (lane == 0) {
-                const int h = kvh * g + t / n_i;
+                const int h = head_of(t);
                 const int i = tile_of(t);
                 uint8_t* q_dst = smem + kv_Q + st * 16 * KB;
                 uint8_t* do_dst = smem + kv_dO + st * 16 * KB;
@@ -249,51 +264,27 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const bool leader = tc::elect_one_sync();
         const uint32_t id_s = tc::idesc_bf16(128, 64, false, false);    // S^T = K Q^T
         const uint32_t id_g = tc::idesc_bf16(128, 128, false, true);    // dV += P^T dO
-        const uint32_t t_dK = tmem + 256, t_dV = tmem + 384;
-        bool ok = tc::warp_wait(&B.kv_full, 0, p.err);
+        const uint32_t t_dK = tmem + kv_TDK, t_dV = tmem + kv_TDV;
+        const uint32_t t_S = tmem + kv_TS, t_dP = tmem + kv_TDP, t_K = tmem + kv_TK;
+        bool ok = tc::warp_wait(&B.kv_full, 0, p.err) && tc::warp_wait(&B.k_tmem, 0, p.err);
         // Base descriptors; each MMA advances them by a compile-time offset.
-        const uint64_t dK0 = tc::sdesc(tc::smem_u32(smem + kv_K), 16, 1024);
         const uint64_t dV0 = tc::sdesc(tc::smem_u32(smem + kv_V), 16, 1024);
         const uint64_t dQk0 = tc::sdesc(tc::smem_u32(smem + kv_Q), 16, 1024);        // K-major
         const uint64_t ddOk0 = tc::sdesc(tc::smem_u32(smem + kv_dO), 16, 1024);
         const uint64_t dQm0 = tc::sdesc(tc::smem_u32(smem + kv_Q), 8 * KB, 1024);    // MN-major
         const uint64_t ddOm0 = tc::sdesc(tc::smem_u32(smem + kv_dO), 8 * KB, 1024);
-        // P^T(t) and dS^T(t) sit in tensor memory over S^T(t) / dP^T(t); the
-        // tensor core runs MMAs in issue order, so S^T(t+2), issued after these,
-        // cannot overwrite them before they are read.
-        auto issue_grad = [&](int t) -> bool {
+        // Tensor-core order: S^T/dP^T(t+1) ahead of the gradient products of t.
+        auto issue_s = [&](int t) -> bool {
             const int st = t % kv_STAGES;
-            if (!tc::warp_wait(&B.p_full[t & 1], (t >> 1) & 1, p.err)) return false;
+            if (!tc::warp_wait(&B.qdo_full[st], (t / kv_STAGES) & 1, p.err)) return false;
+            if (t > 0 && !tc::warp_wait(&B.s_free, (t - 1) & 1, p.err)) return false;
             tc::tc_fence_after();
             const uint32_t so = st * 16 * KB;
-            const uint32_t t_P = tmem + (t & 1) * 128, t_dS = t_P + 64;
             if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)      // K = 64 queries, 16 per MMA
-                    tc::mma_bf16_ts(t_dV, t_P + kv_pk_col(kk), tc::sdesc_at(ddOm0, so + kk * 2048),
-                                    id_g, (t > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    tc::mma_bf16_ts(t_dK, t_dS + kv_pk_col(kk), tc::sdesc_at(dQm0, so + kk * 2048),
-                                    id_g, (t > 0 || kk > 0) ? 1u : 0u);
-                tc::mma_commit(&B.qdo_empty[st]);
-            }
-            __syncwarp();
-            return true;
-        };
-        for (int t = 0; ok && t < T; ++t) {
-            const int st = t % kv_STAGES;
-            if (!tc::warp_wait(&B.qdo_full[st], (t / kv_STAGES) & 1, p.err)) { ok = false; break; }
-            tc::tc_fence_after();
-            const uint32_t so = st * 16 * KB;
-            const uint32_t t_S = tmem + (t & 1) * 128, t_dP = t_S + 64;
-            if (leader) {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t oa = (kk >> 2) * 16 * KB + (kk & 3) * 32;
+                for (int kk = 0; kk < 8; ++kk) {    // K = d: 16 per MMA (8 columns of K)
                     const uint32_t ob = (kk >> 2) * 8 * KB + (kk & 3) * 32;
-                    tc::mma_bf16(t_S, tc::sdesc_at(dK0, oa), tc::sdesc_at(dQk0, so + ob), id_s,
-                                 kk > 0 ? 1u : 0u);
+                    tc::mma_bf16_ts(t_S, t_K + kk * 8, tc::sdesc_at(dQk0, so + ob), id_s, kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
@@ -302,12 +293,37 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     tc::mma_bf16(t_dP, tc::sdesc_at(dV0, oa), tc::sdesc_at(ddOk0, so + ob), id_s,
                                  kk > 0 ? 1u : 0u);
                 }
-                tc::mma_commit(&B.s_full[t & 1]);
+                tc::mma_commit(&B.s_full);
             }
             __syncwarp();
-            if (t > 0 && !issue_grad(t - 1)) { ok = false; break; }
+            return true;
+        };
+        auto issue_grad = [&](int t) -> bool {
+            const int st = t % kv_STAGES;
+            if (!tc::warp_wait(&B.p_full, t & 1, p.err)) return false;
+            tc::tc_fence_after();
+            const uint32_t so = st * 16 * KB;
+            if (leader) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)      // K = 64 queries, 16 per MMA (8 columns)
+                    tc::mma_bf16_ts(t_dV, tmem + kv_TP + kk * 8, tc::sdesc_at(ddOm0, so + kk * 2048),
+                                    id_g, (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc::mma_bf16_ts(t_dK, tmem + kv_TDS + kk * 8, tc::sdesc_at(dQm0, so + kk * 2048),
+                                    id_g, (t > 0 || kk > 0) ? 1u : 0u);
+                tc::mma_commit(&B.qdo_empty[st]);
+                tc::mma_commit(&B.p_free);
+            }
+            __syncwarp();
+            return true;
+        };
+        if (ok) ok = issue_s(0);
+        for (int t = 0; ok && t < T; ++t) {
+            if (t + 1 < T && !issue_s(t + 1)) { ok = false; break; }
+            if (!issue_grad(t)) { ok = false; break; }
         }
-        if (ok && T > 0 && issue_grad(T - 1) && leader) tc::mma_commit(&B.acc_done);
+        if (ok && leader) tc::mma_commit(&B.acc_done);
         if (leader) {
             tc::mma_commit(&B.drain);
             drain_wait(&B.drain, 0);
@@ -323,10 +339,25 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int64_t kpos = kfirst + r;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         const float sl2 = rsqrtf(128.f) * kLog2e;
+        {
+            // K row r, head dims [64 wg, 64 wg + 64) -> TMEM columns kv_TK + 32 wg ..
+            const uint4* src = reinterpret_cast<const uint4*>(
+                static_cast<const __nv_bfloat16*>(p.kpool) + (((size_t)pp * p.Hkv + kvh) * 128 + r) * 128 + wg * 64);
+            uint32_t w[32];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const uint4 u = __ldg(src + v);
+                w[4 * v] = u.x; w[4 * v + 1] = u.y; w[4 * v + 2] = u.z; w[4 * v + 3] = u.w;
+            }
+            tc::tmem_st32(lane_base + kv_TK + wg * 32, w);
+            tc::tmem_wait_st();
+            tc::tc_fence_before();
+            tc::mbar_arrive(&B.k_tmem);
+        }
         bool ok = true;
         for (int t = 0; t < T; ++t) {
-            const int sb = t & 1, st = t % kv_STAGES;
-            ok = tc::mbar_wait(&B.s_full[sb], (t >> 1) & 1, p.err) &&
+            const int st = t % kv_STAGES;
+            ok = tc::mbar_wait(&B.s_full, t & 1, p.err) &&
                  tc::mbar_wait(&B.qdo_full[st], (t / kv_STAGES) & 1, p.err);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
@@ -335,10 +366,12 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int64_t q0 = p.q_start + (int64_t)i * 64 + wg * 32;   // position of my column 0
             const float* sst = stat + st * 128 + wg * 32;
             uint32_t sv[32], dv[32];
-            tc::tmem_ld32(lane_base + sb * 128 + wg * 32, sv);
-            tc::tmem_ld32(lane_base + sb * 128 + 64 + wg * 32, dv);
+            tc::tmem_ld32(lane_base + kv_TS + wg * 32, sv);
+            tc::tmem_ld32(lane_base + kv_TDP + wg * 32, dv);
             tc::tmem_wait_ld(sv);
             tc::tmem_wait_ld(dv);
+            tc::tc_fence_before();
+            tc::mbar_arrive(&B.s_free);                      // S^T/dP^T may be overwritten
             uint32_t pw[16], dw[16];
             if (kfirst + 127 > q0) {                         // crosses the diagonal: mask
 #pragma unroll
@@ -367,12 +400,15 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     dw[c / 2] = pack_bf16x2(dr[0], dr[1]);
                 }
             }
-            // Over the columns this thread has just read (its own lane).
-            tc::tmem_st16(lane_base + sb * 128 + wg * 32, pw);
-            tc::tmem_st16(lane_base + sb * 128 + 64 + wg * 32, dw);
+            if (t > 0) {                                     // gradient MMAs of t-1 have read P^T/dS^T
+                ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.p_free, (t - 1) & 1, p.err));
+                if (!ok) break;
+            }
+            tc::tmem_st16(lane_base + kv_TP + wg * 16, pw);
+            tc::tmem_st16(lane_base + kv_TDS + wg * 16, dw);
             tc::tmem_wait_st();
             tc::tc_fence_before();
-            tc::mbar_arrive(&B.p_full[sb]);
+            tc::mbar_arrive(&B.p_full);
         }
         if (ok && T > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.acc_done, 0, p.err));
         if (ok && T > 0) {
@@ -382,7 +418,7 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const size_t off = (((size_t)pp * p.Hkv + kvh) * 128 + r) * 128;
             const float scale = wg == 0 ? rsqrtf(128.f) : 1.f;
             float* dst = (wg == 0 ? p.dkpool : p.dvpool) + off;
-            const uint32_t col = wg == 0 ? 256 : 384;
+            const uint32_t col = wg == 0 ? kv_TDK : kv_TDV;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t a[32];
@@ -413,34 +449,34 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 // Whole-page key tiles (128 keys): S = Q K^T and dP = dO V^T are N = 128 MMAs
 // into one buffer. The softmax warps release it as soon as they have read it
 // (s_free), so S/dP of tile t+1 overlaps their work on tile t; dS (bf16) goes
-// to one of two tensor-memory buffers, read there as the A operand of
-// dQ += dS K. Tensor-core order: S/dP(t+1) ahead of dQ(t).
+// to tensor memory, read there as the A operand of dQ += dS K (ds_free: dQ of
+// the previous tile has read it). Q, the A operand of every S MMA, is placed in
+// tensor memory once. Tensor-core order: S/dP(t+1) ahead of dQ(t).
 // K and V travel in separate rings: V is free once dP is computed, K only after dQ.
-constexpr int q_KST = 3;
+constexpr int q_KST = 4;
 constexpr int q_VST = 2;
-constexpr uint32_t q_Q = 0;                  // [128 q][128 d]: two 16 KB halves
-constexpr uint32_t q_dO = 32 * KB;
-constexpr uint32_t q_K = 64 * KB;            // stages x [128 keys][128 d]: two 16 KB halves
+constexpr uint32_t q_dO = 0;                 // [128 q][128 d]: two 16 KB halves
+constexpr uint32_t q_K = 32 * KB;            // stages x [128 keys][128 d]: two 16 KB halves
 constexpr uint32_t q_V = q_K + q_KST * 32 * KB;
 constexpr uint32_t q_SMEM = q_V + q_VST * 32 * KB + 1024;
 // Tensor-memory columns.
-constexpr uint32_t q_TS = 0, q_TDP = 128, q_TDQ = 256, q_TDS = 384;   // dS: 2 x 64 columns
+constexpr uint32_t q_TS = 0, q_TDP = 128, q_TDQ = 256, q_TDS = 384, q_TQ = 448;
 
 struct __align__(8) QBar {
     uint64_t q_full;
     uint64_t k_full[q_KST], k_empty[q_KST];
     uint64_t v_full[q_VST], v_empty[q_VST];
+    uint64_t q_tmem;                 // Q in TMEM (softmax threads)
     uint64_t s_full, s_free;
-    uint64_t ds_full[2];
+    uint64_t ds_full, ds_free;
     uint64_t acc_done;
     uint64_t drain;
     uint32_t tmem_base;
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
-bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                BwdParams p) {
+bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, BwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -464,9 +500,11 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tc::mbar_init(&B.v_full[s], 1);
             tc::mbar_init(&B.v_empty[s], 1);
         }
+        tc::mbar_init(&B.q_tmem, kSoftmaxThreads);
         tc::mbar_init(&B.s_full, 1);
         tc::mbar_init(&B.s_free, kSoftmaxThreads);
-        for (int s = 0; s < 2; ++s) tc::mbar_init(&B.ds_full[s], kSoftmaxThreads);
+        tc::mbar_init(&B.ds_full, kSoftmaxThreads);
+        tc::mbar_init(&B.ds_free, 1);
         tc::mbar_init(&B.acc_done, 1);
         tc::mbar_init(&B.drain, 1);
         tc::fence_barrier_init();
@@ -486,9 +524,7 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tc::prefetch_tmap(&tm_k);
             tc::prefetch_tmap(&tm_v);
             const int q_row0 = qt * 128;
-            tc::mbar_arrive_expect_tx(&B.q_full, 64 * KB);
-            tc::tma_load_3d(smem + q_Q, &tm_q, &B.q_full, 0, h, q_row0);
-            tc::tma_load_3d(smem + q_Q + 16 * KB, &tm_q, &B.q_full, 64, h, q_row0);
+            tc::mbar_arrive_expect_tx(&B.q_full, 32 * KB);
             tc::tma_load_3d(smem + q_dO, &tm_do, &B.q_full, 0, h, q_row0);
             tc::tma_load_3d(smem + q_dO + 16 * KB, &tm_do, &B.q_full, 64, h, q_row0);
         }
@@ -536,10 +572,9 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const bool leader = tc::elect_one_sync();
         const uint32_t id_s = tc::idesc_bf16(128, 128, false, false);   // S = Q K^T
         const uint32_t id_q = tc::idesc_bf16(128, 128, false, true);    // dQ += dS K
-        const uint32_t t_S = tmem + q_TS, t_dP = tmem + q_TDP, t_dQ = tmem + q_TDQ;
-        bool ok = tc::warp_wait(&B.q_full, 0, p.err);
+        const uint32_t t_S = tmem + q_TS, t_dP = tmem + q_TDP, t_dQ = tmem + q_TDQ, t_Q = tmem + q_TQ;
+        bool ok = tc::warp_wait(&B.q_full, 0, p.err) && tc::warp_wait(&B.q_tmem, 0, p.err);
         // Base descriptors; each MMA advances them by a compile-time offset.
-        const uint64_t dQ0 = tc::sdesc(tc::smem_u32(smem + q_Q), 16, 1024);
         const uint64_t ddO0 = tc::sdesc(tc::smem_u32(smem + q_dO), 16, 1024);
         const uint64_t dKk0 = tc::sdesc(tc::smem_u32(smem + q_K), 16, 1024);       // K-major
         const uint64_t dVk0 = tc::sdesc(tc::smem_u32(smem + q_V), 16, 1024);
@@ -553,10 +588,9 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const uint32_t k_off = ks * 32 * KB, v_off = vs * 32 * KB;
             if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {    // K = d = 128, 16 per MMA
+                for (int kk = 0; kk < 8; ++kk) {    // K = d = 128, 16 per MMA (8 columns of Q)
                     const uint32_t o = (kk >> 2) * 16 * KB + (kk & 3) * 32;
-                    tc::mma_bf16(t_S, tc::sdesc_at(dQ0, o), tc::sdesc_at(dKk0, k_off + o), id_s,
-                                 kk > 0 ? 1u : 0u);
+                    tc::mma_bf16_ts(t_S, t_Q + kk * 8, tc::sdesc_at(dKk0, k_off + o), id_s, kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
@@ -570,19 +604,18 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             __syncwarp();
             return true;
         };
-        // dS(t) is in buffer t & 1; softmax(t + 2) rewrites it only after S(t + 2),
-        // which the tensor core runs after dQ(t) (MMAs execute in issue order).
         auto issue_dq = [&](int t) -> bool {
             const int ks = t % q_KST;
-            if (!tc::warp_wait(&B.ds_full[t & 1], (t >> 1) & 1, p.err)) return false;
+            if (!tc::warp_wait(&B.ds_full, t & 1, p.err)) return false;
             tc::tc_fence_after();
-            const uint32_t t_dS = tmem + q_TDS + (t & 1) * 64, k_off = ks * 32 * KB;
+            const uint32_t t_dS = tmem + q_TDS, k_off = ks * 32 * KB;
             if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)      // K = 128 keys, 16 per MMA (8 columns)
                     tc::mma_bf16_ts(t_dQ, t_dS + kk * 8, tc::sdesc_at(dKm0, k_off + kk * 2048), id_q,
                                     (t > 0 || kk > 0) ? 1u : 0u);
                 tc::mma_commit(&B.k_empty[ks]);
+                tc::mma_commit(&B.ds_free);
             }
             __syncwarp();
             return true;
@@ -612,6 +645,25 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         const float sl2 = rsqrtf(128.f) * kLog2e;
         const int64_t first_diag = p.q_start + (int64_t)qt * 128;   // first key of the own page
+        {
+            // Q row, head dims [64 wg, 64 wg + 64) -> TMEM columns q_TQ + 32 wg ..
+            uint32_t w[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) w[e] = 0u;          // rows past the chunk: Q = 0
+            if (valid) {
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    static_cast<const __nv_bfloat16*>(p.q) + ((size_t)q_local * p.Hq + h) * 128 + wg * 64);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    const uint4 u = __ldg(src + v);
+                    w[4 * v] = u.x; w[4 * v + 1] = u.y; w[4 * v + 2] = u.z; w[4 * v + 3] = u.w;
+                }
+            }
+            tc::tmem_st32(lane_base + q_TQ + wg * 32, w);
+            tc::tmem_wait_st();
+            tc::tc_fence_before();
+            tc::mbar_arrive(&B.q_tmem);
+        }
         bool ok = true;
         for (int t = 0; t < T; ++t) {
             ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.s_full, t & 1, p.err));
@@ -650,10 +702,14 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 grad_half(s0, d0, 0, false);
                 grad_half(s1, d1, 32, false);
             }
-            tc::tmem_st32(lane_base + q_TDS + (t & 1) * 64 + wg * 32, dw);
+            if (t > 0) {                                     // dQ(t - 1) has read dS(t - 1)
+                ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.ds_free, (t - 1) & 1, p.err));
+                if (!ok) break;
+            }
+            tc::tmem_st32(lane_base + q_TDS + wg * 32, dw);
             tc::tmem_wait_st();
             tc::tc_fence_before();
-            tc::mbar_arrive(&B.ds_full[t & 1]);
+            tc::mbar_arrive(&B.ds_full);
         }
         if (ok && T > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.acc_done, 0, p.err));
         if (ok && T > 0) {
@@ -694,12 +750,11 @@ cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
     // The sparse dK/dV kernel lists the selecting query pages in shared memory.
     if (a.sel && (a.n_q + 127) / 128 > kMaxSelQp) return launch_attn_bwd_simt(a, s);
     if ((reinterpret_cast<uintptr_t>(a.dout) & 15) || !a.tmap_k) return cudaErrorInvalidValue;
-    CUtensorMap tq64, tdo64, tq128, tdo128;
+    CUtensorMap tq64, tdo64, tdo128;
     std::string why;
     const uint64_t s2 = (uint64_t)a.Hq * 256;
     if (!make_tmap_3d(&tq64, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, a.Hq, a.n_q, 256, s2, 64, 1, 64, &why) ||
         !make_tmap_3d(&tdo64, a.dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, a.Hq, a.n_q, 256, s2, 64, 1, 64, &why) ||
-        !make_tmap_3d(&tq128, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, a.Hq, a.n_q, 256, s2, 64, 1, 128, &why) ||
         !make_tmap_3d(&tdo128, a.dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, a.Hq, a.n_q, 256, s2, 64, 1, 128, &why))
         return cudaErrorInvalidValue;
     static bool attr = false;
@@ -712,21 +767,29 @@ cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
         attr = true;
     }
     BwdParams p{};
-    p.Hq = a.Hq; p.Hkv = a.Hkv; p.q_start = a.q_start; p.n_q = a.n_q;
+    p.Hq = a.Hq; p.Hkv = a.Hkv; p.q_start = a.q_start; p.n_q = a.n_q; p.q = a.q; p.kpool = a.kpool;
     p.lse = a.lse_in; p.Dbuf = a.Dbuf; p.dq = a.dq; p.dkpool = a.dkpool; p.dvpool = a.dvpool;
     p.bt = a.bt; p.num_phys = a.num_phys; p.err = a.err;
     p.sel = a.sel; p.kmax = a.kmax;
     const int64_t n_keys = a.q_start + a.n_q;
-    dim3 g_kv((unsigned)((n_keys + 127) / 128), a.Hkv);
+    // Small grids (early chunks) leave SMs idle behind a few long CTAs: split
+    // each CTA's iterations over gridDim.z so that there are >= ~16 waves.
+    int dev = 0, sm_count = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
+    sm_count = std::max(sm_count, 1);
+    const int64_t n_cta = ((n_keys + 127) / 128) * a.Hkv;
+    const int splits = (int)std::min<int64_t>(4, std::max<int64_t>(1, (16 * (int64_t)sm_count + n_cta - 1) / n_cta));
+    dim3 g_kv((unsigned)((n_keys + 127) / 128), a.Hkv, splits);
     {
         ProfScope ps("bwd_kv_tc_kernel", s);
-        bwd_kv_tc_kernel<<<g_kv, kThreads, kv_SMEM, s>>>(tq64, tdo64, *a.tmap_k, *a.tmap_v, p);
+        bwd_kv_tc_kernel<<<g_kv, kThreads, kv_SMEM, s>>>(tq64, tdo64, *a.tmap_v, p);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dim3 g_q((unsigned)((a.n_q + 127) / 128), a.Hq);
     ProfScope ps("bwd_q_tc_kernel", s);
-    bwd_q_tc_kernel<<<g_q, kThreads, q_SMEM, s>>>(tq128, tdo128, *a.tmap_k, *a.tmap_v, p);
+    bwd_q_tc_kernel<<<g_q, kThreads, q_SMEM, s>>>(tdo128, *a.tmap_k, *a.tmap_v, p);
     return cudaGetLastError();
 }
 
