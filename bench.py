@@ -145,6 +145,14 @@ def reduce_max(x: float, world: int) -> float:
     return float(t.item())
 
 
+def replica_rate(units_per_rank: float, ms_local: float, world: int):
+    """Whole-job rate over `world` independent replicas: every rank processes
+    units_per_rank per step; the job's step time is the slowest rank's.
+    Returns (units per second summed over ranks, max ms per step)."""
+    ms = reduce_max(ms_local, world)
+    return world * units_per_rank / (ms * 1e-3), ms
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -261,11 +269,10 @@ def run_pkv(args, world, rank):
     clk = clocks.stop()
     barrier(world)
     B.pkv_check(sw.pool)
-    ms_step = reduce_max(t0.elapsed_time(t1) / args.steps, world)
-
     flops_fwd = 4 * w.Hq * w.d * pairs_dense(w.N)
     flops_bwd = 10 * w.Hq * w.d * pairs_dense(w.N)
-    tflops = world * (flops_fwd + flops_bwd) / (ms_step * 1e-3) / 1e12
+    flops_s, ms_step = replica_rate(flops_fwd + flops_bwd, t0.elapsed_time(t1) / args.steps, world)
+    tflops = flops_s / 1e12
     pk, pk_kind = peaks()
     peak_tc = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
     fwd_call = statistics.mean(fwd_ms) / n
@@ -365,9 +372,9 @@ def run_e2e(args, w, sw, step, world):
     for _ in range(args.steps):
         e2e_step()
     torch.cuda.synchronize()
-    ms = reduce_max((time.perf_counter() - t0) * 1e3 / args.steps, world)
     flops = 14 * w.Hq * w.d * pairs_dense(w.N)
-    return {"value": round(world * flops / (ms * 1e-3) / 1e12, 3), "unit": UNIT,
+    flops_s, ms = replica_rate(flops, (time.perf_counter() - t0) * 1e3 / args.steps, world)
+    return {"value": round(flops_s / 1e12, 3), "unit": UNIT,
             "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
@@ -472,7 +479,8 @@ def run_sparse(args, world, rank):
     torch.cuda.synchronize()
     dense_ms = d0.elapsed_time(d1)
     flops = 14 * w.d * pairs
-    tflops = flops / (ms * 1e-3) / 1e12
+    flops_s, ms = replica_rate(flops, ms, world)
+    tflops = flops_s / 1e12
     pk, pk_kind = peaks()
     peak_tc = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
     kernels = {k: {"launches": c, "ms_per_step": round(t / args.steps, 3)} for k, (c, t) in prof.items()}
