@@ -42,7 +42,12 @@ namespace {
 
 using tc::drain_wait;
 
-constexpr int kThreads = 320;     // warp 0 TMA, warp 1 MMA, warps 2..9 two softmax warpgroups
+// Warp 0 TMA; warp 1 issues the S/dP (or S^T/dP^T) MMAs; warps 2..9 two softmax
+// warpgroups; warp 10 issues the MMAs that consume their output (dK/dV or dQ).
+// An MMA issue blocks its thread for about the MMA's run time, so a single
+// issuer would hold S(t+1) back behind the products of tile t.
+constexpr int kThreads = 352;
+constexpr int kWarpG = 10;
 constexpr int kSoftmaxThreads = 256;
 constexpr uint32_t KB = 1024;
 
@@ -103,7 +108,7 @@ struct __align__(8) KVBar {
     uint64_t s_full, s_free;
     uint64_t p_full, p_free;
     uint64_t acc_done;
-    uint64_t drain;
+    uint64_t drain[2];
     uint32_t tmem_base;
     int n_i;                         // 64-query tiles per head
     int16_t tiles[2 * kMaxSelQp];    // sparse: the tiles, ascending
@@ -167,7 +172,8 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         tc::mbar_init(&B.p_full, kSoftmaxThreads);
         tc::mbar_init(&B.p_free, 1);
         tc::mbar_init(&B.acc_done, 1);
-        tc::mbar_init(&B.drain, 1);
+        tc::mbar_init(&B.drain[0], 1);
+        tc::mbar_init(&B.drain[1], 1);
         tc::fence_barrier_init();
         // A page no query tile uses needs no valid slot (sparse, staged pools).
         if (!page_ok && B.n_i > 0) report_error(p.err, kErrBadPage);
@@ -258,22 +264,22 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             for (int t = max(0, issued - kv_STAGES); t < issued; ++t)
                 drain_wait(&B.qdo_full[t % kv_STAGES], (t / kv_STAGES) & 1);
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
-        // Whole warp runs the loop (warp-uniform descriptors); the elected lane issues.
+    } else if (warp == 1 || warp == kWarpG) {
+        // ---------------------------------------------------------------- MMA issuers
+        // Warp 1: S^T/dP^T(t); warp kWarpG: dV/dK(t). Each whole warp runs its
+        // loop (warp-uniform descriptors); the elected lane issues.
         const bool leader = tc::elect_one_sync();
         const uint32_t id_s = tc::idesc_bf16(128, 64, false, false);    // S^T = K Q^T
         const uint32_t id_g = tc::idesc_bf16(128, 128, false, true);    // dV += P^T dO
         const uint32_t t_dK = tmem + kv_TDK, t_dV = tmem + kv_TDV;
         const uint32_t t_S = tmem + kv_TS, t_dP = tmem + kv_TDP, t_K = tmem + kv_TK;
-        bool ok = tc::warp_wait(&B.kv_full, 0, p.err) && tc::warp_wait(&B.k_tmem, 0, p.err);
+        bool ok = true;
         // Base descriptors; each MMA advances them by a compile-time offset.
         const uint64_t dV0 = tc::sdesc(tc::smem_u32(smem + kv_V), 16, 1024);
         const uint64_t dQk0 = tc::sdesc(tc::smem_u32(smem + kv_Q), 16, 1024);        // K-major
         const uint64_t ddOk0 = tc::sdesc(tc::smem_u32(smem + kv_dO), 16, 1024);
         const uint64_t dQm0 = tc::sdesc(tc::smem_u32(smem + kv_Q), 8 * KB, 1024);    // MN-major
         const uint64_t ddOm0 = tc::sdesc(tc::smem_u32(smem + kv_dO), 8 * KB, 1024);
-        // Tensor-core order: S^T/dP^T(t+1) ahead of the gradient products of t.
         auto issue_s = [&](int t) -> bool {
             const int st = t % kv_STAGES;
             if (!tc::warp_wait(&B.qdo_full[st], (t / kv_STAGES) & 1, p.err)) return false;
@@ -318,15 +324,19 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             __syncwarp();
             return true;
         };
-        if (ok) ok = issue_s(0);
-        for (int t = 0; ok && t < T; ++t) {
-            if (t + 1 < T && !issue_s(t + 1)) { ok = false; break; }
-            if (!issue_grad(t)) { ok = false; break; }
+        // The Q/dO stage of tile t is released by the gradient products of t,
+        // which start only after the softmax has seen S^T(t) complete.
+        const int role = warp == 1 ? 0 : 1;
+        if (role == 0) {
+            ok = tc::warp_wait(&B.kv_full, 0, p.err) && tc::warp_wait(&B.k_tmem, 0, p.err);
+            for (int t = 0; ok && t < T; ++t) ok = issue_s(t);
+        } else {
+            for (int t = 0; ok && t < T; ++t) ok = issue_grad(t);
+            if (ok && leader) tc::mma_commit(&B.acc_done);
         }
-        if (ok && leader) tc::mma_commit(&B.acc_done);
         if (leader) {
-            tc::mma_commit(&B.drain);
-            drain_wait(&B.drain, 0);
+            tc::mma_commit(&B.drain[role]);
+            drain_wait(&B.drain[role], 0);
         }
         __syncwarp();
     } else {
@@ -470,7 +480,7 @@ struct __align__(8) QBar {
     uint64_t s_full, s_free;
     uint64_t ds_full, ds_free;
     uint64_t acc_done;
-    uint64_t drain;
+    uint64_t drain[2];
     uint32_t tmem_base;
 };
 
@@ -506,7 +516,8 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant
         tc::mbar_init(&B.ds_full, kSoftmaxThreads);
         tc::mbar_init(&B.ds_free, 1);
         tc::mbar_init(&B.acc_done, 1);
-        tc::mbar_init(&B.drain, 1);
+        tc::mbar_init(&B.drain[0], 1);
+        tc::mbar_init(&B.drain[1], 1);
         tc::fence_barrier_init();
     }
     if (warp == 1) {
@@ -567,13 +578,14 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant
             for (int t = max(0, v_issued - q_VST); t < v_issued; ++t)
                 drain_wait(&B.v_full[t % q_VST], (t / q_VST) & 1);
         }
-    } else if (warp == 1) {
-        // Whole warp runs the loop (warp-uniform descriptors); the elected lane issues.
+    } else if (warp == 1 || warp == kWarpG) {
+        // Warp 1: S/dP(t); warp kWarpG: dQ(t). Each whole warp runs its loop
+        // (warp-uniform descriptors); the elected lane issues.
         const bool leader = tc::elect_one_sync();
         const uint32_t id_s = tc::idesc_bf16(128, 128, false, false);   // S = Q K^T
         const uint32_t id_q = tc::idesc_bf16(128, 128, false, true);    // dQ += dS K
         const uint32_t t_S = tmem + q_TS, t_dP = tmem + q_TDP, t_dQ = tmem + q_TDQ, t_Q = tmem + q_TQ;
-        bool ok = tc::warp_wait(&B.q_full, 0, p.err) && tc::warp_wait(&B.q_tmem, 0, p.err);
+        bool ok = true;
         // Base descriptors; each MMA advances them by a compile-time offset.
         const uint64_t ddO0 = tc::sdesc(tc::smem_u32(smem + q_dO), 16, 1024);
         const uint64_t dKk0 = tc::sdesc(tc::smem_u32(smem + q_K), 16, 1024);       // K-major
@@ -620,15 +632,19 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant
             __syncwarp();
             return true;
         };
-        if (ok && T > 0) ok = issue_s(0);
-        for (int t = 0; ok && t < T; ++t) {
-            if (t + 1 < T && !issue_s(t + 1)) { ok = false; break; }
-            if (!issue_dq(t)) { ok = false; break; }
+        // K(t) is released by dQ(t), which starts only after the softmax has
+        // seen S(t) complete, so S(t) has read K(t) by then too.
+        const int role = warp == 1 ? 0 : 1;
+        if (role == 0) {
+            ok = tc::warp_wait(&B.q_full, 0, p.err) && tc::warp_wait(&B.q_tmem, 0, p.err);
+            for (int t = 0; ok && t < T; ++t) ok = issue_s(t);
+        } else {
+            for (int t = 0; ok && t < T; ++t) ok = issue_dq(t);
+            if (ok && T > 0 && leader) tc::mma_commit(&B.acc_done);
         }
-        if (ok && T > 0 && leader) tc::mma_commit(&B.acc_done);
         if (leader) {
-            tc::mma_commit(&B.drain);
-            drain_wait(&B.drain, 0);
+            tc::mma_commit(&B.drain[role]);
+            drain_wait(&B.drain[role], 0);
         }
         __syncwarp();
     } else {

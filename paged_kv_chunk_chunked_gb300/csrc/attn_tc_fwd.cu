@@ -14,18 +14,20 @@
 // cycles per instruction on top of the math): Q is placed there once, and
 // P overwrites the S columns it came from. Warp roles (352 threads):
 //   warp 0       TMA producer: K pages into a 3-stage ring.
-//   warp 10      TMA producer: V pages into a 3-stage ring.
+//   warp 10      TMA producer: V pages into a 2-stage ring. Each V stage
+//                carries a constant third 64-column block whose first column
+//                is 1, so the PV MMA (N = 144) also accumulates the row sum
+//                l = sum_j P_ij of exactly the bf16 weights it multiplies.
 //   warp 1       MMA issuer (elected lane): S_j = Q K_j^T into a double-
 //                buffered TMEM tile, then O += P_{j-1} V_{j-1} (O in TMEM).
 //   warps 2..9   softmax, two warpgroups: thread (wg, row) owns keys
 //                [64 wg, 64 wg + 64) of query row `row` in every tile. The two
 //                partial row maxima meet through shared memory (an mbarrier
-//                per tile parity); the running max m is shared, the sums l are
-//                kept per warpgroup and added at the end. O is rescaled in TMEM
-//                only when m grows by more than 2^8 (P <= 256 then, exactly
-//                representable range for bf16), each warpgroup its own half
-//                of the columns. Epilogue: O / l, LSE.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256,384), Q [384,448).
+//                per tile parity). O (with l) is rescaled in TMEM only when m
+//                grows by more than 2^8 (P <= 256 then, exactly representable
+//                range for bf16), each warpgroup its own half of the columns.
+//                Epilogue: O / l, LSE.
+// TMEM columns: S0 [0,128), S1 [128,256), O [256,384), l 384, Q [400,464).
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -44,13 +46,14 @@ constexpr uint32_t kTileBytes = 2 * kHalfBytes;
 // Shared-memory tile offsets (bytes from a 1024-aligned base).
 // K and V have separate rings: a K stage is free as soon as S_j completes, so
 // K loads run kKStages - 1 tiles ahead; a V stage is free after PV_j.
-constexpr int kKStages = 3, kVStages = 3;
+constexpr int kKStages = 3, kVStages = 2;
+constexpr uint32_t kVStageBytes = kTileBytes + kHalfBytes;        // V + the ones block
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
-constexpr uint32_t kTilesBytes = kOffV + kVStages * kTileBytes;   // 192 KB
+constexpr uint32_t kTilesBytes = kOffV + kVStages * kVStageBytes; // 192 KB
 constexpr uint32_t kSmemBytes = kTilesBytes + 1024;               // + alignment slack
 constexpr float kRescaleThreshold = 8.0f;                         // log2 units
-constexpr uint32_t kColO = 256, kColQ = 384;
+constexpr uint32_t kColO = 256, kColL = kColO + 128, kColQ = 400;
 
 struct FwdParams {
     int Hq, Hkv;
@@ -119,7 +122,7 @@ __device__ __forceinline__ void produce_ring(const FwdParams& p, uint8_t* smem, 
         }
         if (lane == 0) {
             const int row = (int)(((int64_t)pp * p.Hkv + kvh) * kTile);
-            uint8_t* dst = base + st * kTileBytes;
+            uint8_t* dst = base + st * (is_k ? kTileBytes : kVStageBytes);
             tc::mbar_arrive_expect_tx(&full[st], kTileBytes);
             tc::tma_load_2d(dst, &tmap, &full[st], 0, row);
             tc::tma_load_2d(dst + kHalfBytes, &tmap, &full[st], 64, row);
@@ -144,6 +147,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
     const int h = blockIdx.y;
     const int kvh = h / (p.Hq / p.Hkv);
 
+    // The ones block of each V stage: row r holds 1 in column 0, zeros elsewhere
+    // (128-byte swizzle: column 0 sits in 16-byte chunk r & 7 of the row).
+    for (int i = threadIdx.x; i < kVStages * 128 * 8; i += kThreads) {
+        const int st = i / 1024, r = (i / 8) % 128, ch = i % 8;
+        uint8_t* blk = smem + kOffV + st * kVStageBytes + kTileBytes;
+        *reinterpret_cast<uint4*>(blk + tc::sw128_offset(r, ch)) =
+            make_uint4(ch == 0 ? 0x3f80u : 0u, 0u, 0u, 0u);
+    }
+    tc::fence_proxy_async_smem();
     if (threadIdx.x == 0) {
         tc::mbar_init(&B.q_full, kSoftmaxThreads);
         for (int s = 0; s < kKStages; ++s) {
@@ -186,7 +198,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
         // lane issues the tcgen05 instructions and commits.
         const bool leader = tc::elect_one_sync();
         const uint32_t idesc = tc::idesc_bf16(128, 128, false, false);       // S = Q K^T
-        const uint32_t idesc_pv = tc::idesc_bf16(128, 128, false, true);     // O += P V
+        const uint32_t idesc_pv = tc::idesc_bf16(128, 144, false, true);     // [O l] += P [V 1]
         const uint32_t tmem_o = tmem + kColO, tmem_q = tmem + kColQ;
         const uint64_t dk0 = tc::sdesc(tc::smem_u32(smem + kOffK), 16, 1024);            // K-major
         const uint64_t dv0 = tc::sdesc(tc::smem_u32(smem + kOffV), kHalfBytes, 1024);    // MN-major
@@ -198,13 +210,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
             if (!tc::warp_wait(&B.p_full, i & 1, p.err)) return false;
             if (!tc::warp_wait(&B.v_full[vs], (i / kVStages) & 1, p.err)) return false;
             tc::tc_fence_after();
-            // B = V [128 keys][128 d] MN-major: 16 keys = 2 K-groups of 8 rows
-            // (1024 B apart); d spans the two 64-column halves (16 KB apart).
+            // B = [V 1] [128 keys][144] MN-major: 16 keys = 2 K-groups of 8 rows
+            // (1024 B apart); columns span three 64-column blocks 16 KB apart
+            // (V's two halves, then the ones block).
             const uint32_t tmem_p = tmem + (i & 1) * 128;
             if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc::mma_bf16_ts(tmem_o, tmem_p + p_col(kk), tc::sdesc_at(dv0, vs * kTileBytes + kk * 2048),
+                    tc::mma_bf16_ts(tmem_o, tmem_p + p_col(kk), tc::sdesc_at(dv0, vs * kVStageBytes + kk * 2048),
                                     idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
                 tc::mma_commit(&B.o_done);
                 tc::mma_commit(&B.v_empty[vs]);
@@ -265,7 +278,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
             tc::tc_fence_before();
             tc::mbar_arrive(&B.q_full);
         }
-        float m = -INFINITY, l = 0.f;
+        float m = -INFINITY;
         bool ok = true;
         for (int j = 0; j < nt; ++j) {
             const int st = j & 1;
@@ -313,26 +326,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
                 m = mx;
                 rescale = true;
             }
-            l *= alpha;
             uint32_t pk[32];
-            float lpart[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) lpart[k] = 0.f;
             const float neg_m = -m;
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
                 const float p0 = fast_exp2(fmaf(x[2 * c], sl2, neg_m));
                 const float p1 = fast_exp2(fmaf(x[2 * c + 1], sl2, neg_m));
                 pk[c] = pack_bf16x2(p0, p1);
-                // Normalise by the sum of the bf16 weights the tensor core multiplies, so
-                // O is a convex combination of values whatever the rounding of P.
-                lpart[c & 7] += bf16lo(pk[c]) + bf16hi(pk[c]);
             }
-#pragma unroll
-            for (int k = 4; k > 0; k >>= 1)
-#pragma unroll
-                for (int i = 0; i < k; ++i) lpart[i] += lpart[i + k];
-            l += lpart[0];
             if (j > 0 && __any_sync(0xffffffffu, rescale)) {
                 // PV_{j-1} must be done before O is touched (PV_j waits for this tile's P).
                 ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.o_done, (j - 1) & 1, p.err));
@@ -348,6 +349,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
                     for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
                     tc::tmem_st32(lane_base + kColO + wg * 64 + c * 32, r);
                 }
+                if (wg == 1)                          // and the row sum l
+                    tc::tmem_st1(lane_base + kColL,
+                                 __float_as_uint(__uint_as_float(tc::tmem_ld1(lane_base + kColL)) * f));
             }
             // P over the first 32 of the 64 S columns this thread read.
             tc::tmem_st32(lane_base + st * 128 + wg * 64, pk);
@@ -355,17 +359,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
             tc::tc_fence_before();
             tc::mbar_arrive(&B.p_full);
         }
-        if (ok && nt > 0) {
-            // Row sum = both warpgroups' partial sums (same running max).
-            const int sx = nt & 1;
-            B.red[sx][wg][row] = l;
-            tc::mbar_arrive(&B.xchg[sx]);
-            ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.xchg[sx], (nt >> 1) & 1, p.err));
-            if (ok) l += B.red[sx][wg ^ 1][row];
-        }
         if (ok && nt > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.o_done, (nt - 1) & 1, p.err));
         if (ok && nt > 0) {
             tc::tc_fence_after();
+            // Normalise by the sum of the bf16 weights the tensor core multiplied, so
+            // O is a convex combination of values whatever the rounding of P.
+            const float l = __uint_as_float(tc::tmem_ld1(lane_base + kColL));
             const float inv = 1.f / l;
             __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + ((size_t)q_local * p.Hq + h) * kTile;
 #pragma unroll
