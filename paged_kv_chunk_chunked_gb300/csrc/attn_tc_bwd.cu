@@ -65,6 +65,7 @@ struct BwdParams {
     int64_t num_phys;
     const int32_t* sel;        // sparse: [n_qp, Hkv, kmax] selected pages, or null
     int kmax;
+    int kv_splits;             // dK/dV kernel: CTAs per (page, KV head)
     int* err;
 };
 
@@ -125,7 +126,11 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     float* stat = reinterpret_cast<float*>(smem + kv_STAT);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int j = blockIdx.x;                        // logical key page
+    // blockIdx.x = page * splits + split: the CTAs that share a page run side
+    // by side, so their gradient additions meet in L2 rather than in DRAM.
+    const int n_split = (int)p.kv_splits;
+    const int j = (int)blockIdx.x / n_split;         // logical key page
+    const int split = (int)blockIdx.x % n_split;
     const int kvh = blockIdx.y;
     const int g = p.Hq / p.Hkv;
     const int64_t kfirst = (int64_t)j * 128;
@@ -187,12 +192,12 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tc::tc_fence_after();
     const uint32_t tmem = B.tmem_base;
     const int n_i = B.n_i;
-    // Iterations (head, 64-query tile), t = head * n_i + tile; blockIdx.z takes
-    // the share [t_base, t_base + T) of them (the gradient epilogue adds, so
-    // any partition of the iterations gives the same sums).
+    // Iterations (head, 64-query tile), t = head * n_i + tile; split takes the
+    // share [t_base, t_base + T) of them (the gradient epilogue adds, so any
+    // partition of the iterations gives the same sums).
     const int t_all = n_i * g;
-    const int t_base = (int)(((int64_t)t_all * blockIdx.z) / gridDim.z);
-    const int T = (int)(((int64_t)t_all * (blockIdx.z + 1)) / gridDim.z) - t_base;
+    const int t_base = (int)(((int64_t)t_all * split) / n_split);
+    const int T = (int)(((int64_t)t_all * (split + 1)) / n_split) - t_base;
     auto tile_of = [&](int t) -> int {
         const int u = (t_base + t) % n_i;
         return p.sel ? (int)B.tiles[u] : i0 + u;
@@ -789,14 +794,16 @@ cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
     p.sel = a.sel; p.kmax = a.kmax;
     const int64_t n_keys = a.q_start + a.n_q;
     // Small grids (early chunks) leave SMs idle behind a few long CTAs: split
-    // each CTA's iterations over gridDim.z so that there are >= ~16 waves.
+    // each (page, KV head)'s iterations over up to 4 CTAs so that there are
+    // >= ~16 waves.
     int dev = 0, sm_count = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
     sm_count = std::max(sm_count, 1);
     const int64_t n_cta = ((n_keys + 127) / 128) * a.Hkv;
     const int splits = (int)std::min<int64_t>(4, std::max<int64_t>(1, (16 * (int64_t)sm_count + n_cta - 1) / n_cta));
-    dim3 g_kv((unsigned)((n_keys + 127) / 128), a.Hkv, splits);
+    p.kv_splits = splits;
+    dim3 g_kv((unsigned)(((n_keys + 127) / 128) * splits), a.Hkv);
     {
         ProfScope ps("bwd_kv_tc_kernel", s);
         bwd_kv_tc_kernel<<<g_kv, kThreads, kv_SMEM, s>>>(tq64, tdo64, *a.tmap_v, p);
