@@ -288,11 +288,7 @@ pkv_status pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
         if (!make_tmap_2d(&p->tmap_k, kb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
                           128, &why) ||
             !make_tmap_2d(&p->tmap_v, vb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
-                          128, &why) ||
-            !make_tmap_2d(&p->tmap_k64, kb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
-                          64, &why) ||
-            !make_tmap_2d(&p->tmap_v64, vb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
-                          64, &why)) {
+                          128, &why)) {
             cleanup();
             return fail(PKV_ERR_CUDA, "pkv_pool_create: " + why);
         }
@@ -508,8 +504,6 @@ static pkv_status attn_common(pkv_seq* s, const void* q, int64_t q_start, int64_
     a->err = p->d_err;
     a->tmap_k = p->tmaps_ready ? &p->tmap_k : nullptr;
     a->tmap_v = p->tmaps_ready ? &p->tmap_v : nullptr;
-    a->tmap_k64 = p->tmaps_ready ? &p->tmap_k64 : nullptr;
-    a->tmap_v64 = p->tmaps_ready ? &p->tmap_v64 : nullptr;
     if (sel) {
         const int64_t n_qp = (n_q + P - 1) / P;
         if (!sel->pages || sel->kmax <= 0 || sel->n_qp != n_qp)

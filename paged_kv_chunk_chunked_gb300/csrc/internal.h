@@ -35,7 +35,7 @@ struct pkv_pool {
     // TMA descriptors over the K and V page pools (2-D: rows x d), with boxes
     // of 64 columns x 128 rows (whole pages) and 64 x 64 (half pages). For a
     // PINNED_HOST pool they describe the device slots.
-    CUtensorMap tmap_k{}, tmap_v{}, tmap_k64{}, tmap_v64{};
+    CUtensorMap tmap_k{}, tmap_v{};
     bool tmaps_ready = false;
     // PINNED_HOST pools: k/v/dk/dv above are mapped pinned host pages; the
     // attention kernels read these device slots instead.
@@ -124,8 +124,6 @@ struct AttnArgs {
     int* err;
     const CUtensorMap* tmap_k;       // tensor-core path only: whole-page boxes
     const CUtensorMap* tmap_v;
-    const CUtensorMap* tmap_k64;     // half-page boxes
-    const CUtensorMap* tmap_v64;
 };
 
 cudaError_t launch_attn_fwd_simt(const AttnArgs& a, cudaStream_t s);

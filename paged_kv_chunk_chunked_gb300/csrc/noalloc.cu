@@ -104,8 +104,6 @@ extern "C" pkv_status pkv_chunk_attn_bwd_noalloc(pkv_seq* s, const void* q, cons
     a.err = p->d_err;
     a.tmap_k = p->tmaps_ready ? &p->tmap_k : nullptr;
     a.tmap_v = p->tmaps_ready ? &p->tmap_v : nullptr;
-    a.tmap_k64 = p->tmaps_ready ? &p->tmap_k64 : nullptr;
-    a.tmap_v64 = p->tmaps_ready ? &p->tmap_v64 : nullptr;
     if (sel) {
         if (!sel->pages || sel->kmax <= 0 || sel->n_qp != (n_q + P - 1) / P)
             return fail(PKV_ERR_INVALID, std::string(who) + ": selection does not match chunk");
