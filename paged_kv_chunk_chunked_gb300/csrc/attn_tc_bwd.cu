@@ -71,13 +71,6 @@ struct BwdParams {
 
 constexpr int kMaxSelQp = 256;   // query pages per chunk the sparse dK/dV kernel can list
 
-// Number of listed pages of (query page qp, KV head kvh): ascending, -1 padded.
-__device__ __forceinline__ int sel_count(const BwdParams& p, int qp, int kvh) {
-    const int32_t* row = p.sel + ((size_t)qp * p.Hkv + kvh) * p.kmax;
-    int n = 0;
-    while (n < p.kmax && row[n] >= 0) ++n;
-    return n;
-}
 
 
 // ============================================================================ dK / dV
@@ -141,25 +134,32 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // Query tiles that see this page: dense, every tile from i0 on; sparse, the
     // two 64-query halves of every query page whose selection lists page j.
     if (p.sel) {
+        // Every thread checks a slice of all entries (coalesced, independent loads).
         const int n_qp = (int)((p.n_q + 127) / 128);
-        for (int qp = threadIdx.x; qp < n_qp; qp += kThreads) {
-            const int32_t* srow = p.sel + ((size_t)qp * p.Hkv + kvh) * p.kmax;
-            uint8_t f = 0;
-            for (int e = 0; e < p.kmax; ++e) {
-                const int32_t x = srow[e];
-                if (x == j) { f = 1; break; }
-                if (x < 0 || x > j) break;
-            }
-            B.sel_flag[qp] = f;
+        for (int qp = threadIdx.x; qp < n_qp; qp += kThreads) B.sel_flag[qp] = 0;
+        __syncthreads();
+        const int n_ent = n_qp * p.kmax;
+        for (int e = threadIdx.x; e < n_ent; e += kThreads) {
+            const int qp = e / p.kmax, k = e - qp * p.kmax;
+            if (p.sel[((size_t)qp * p.Hkv + kvh) * p.kmax + k] == j) B.sel_flag[qp] = 1;
         }
         __syncthreads();
-        if (threadIdx.x == 0) {
+        if (warp == 0) {
+            // Compaction, 32 query pages per ballot; only the last query page
+            // can hold a single 64-query tile (odd n_qt), and it lists last.
             int n = 0;
-            for (int qp = 0; qp < n_qp; ++qp)
-                if (B.sel_flag[qp])
-                    for (int hf = 0; hf < 2; ++hf)
-                        if (2 * qp + hf < n_qt) B.tiles[n++] = (int16_t)(2 * qp + hf);
-            B.n_i = n;
+            for (int q0 = 0; q0 < n_qp; q0 += 32) {
+                const int qp = q0 + lane;
+                const bool f = qp < n_qp && B.sel_flag[qp];
+                const unsigned m = __ballot_sync(0xffffffffu, f);
+                if (f) {
+                    const int pos = n + 2 * __popc(m & ((1u << lane) - 1u));
+                    B.tiles[pos] = (int16_t)(2 * qp);
+                    if (2 * qp + 1 < n_qt) B.tiles[pos + 1] = (int16_t)(2 * qp + 1);
+                }
+                n += 2 * __popc(m);
+            }
+            if (lane == 0) B.n_i = n - (((n_qt & 1) && B.sel_flag[n_qp - 1]) ? 1 : 0);
         }
     } else if (threadIdx.x == 0) {
         B.n_i = n_qt - i0;
@@ -501,8 +501,8 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant
     const int h = blockIdx.y;
     const int kvh = h / (p.Hq / p.Hkv);
     // Key tiles = visible pages (dense: pages 0..own; sparse: the listed pages).
-    const int T = p.sel ? sel_count(p, qt, kvh) : (int)(p.q_start / 128) + qt + 1;
     const int32_t* sel_row = p.sel ? p.sel + ((size_t)qt * p.Hkv + kvh) * p.kmax : nullptr;
+    const int T = sel_row ? sel_count_warp(sel_row, p.kmax, lane) : (int)(p.q_start / 128) + qt + 1;
 
     if (threadIdx.x == 0) {
         tc::mbar_init(&B.q_full, 1);

@@ -81,14 +81,6 @@ struct __align__(8) FwdBarriers {
     float red[2][2][kTile];          // [parity][warpgroup][row]
 };
 
-// Number of key tiles for this CTA.
-__device__ __forceinline__ int tile_count(const FwdParams& p, int qt, int kvh) {
-    if (!p.sel) return (int)(p.q_start / kTile) + qt + 1;
-    const int32_t* row = p.sel + ((size_t)qt * p.Hkv + kvh) * p.kmax;
-    int n = 0;
-    while (n < p.kmax && row[n] >= 0) ++n;
-    return n;
-}
 
 // Tensor-memory column (within an S buffer) of P for keys [16 kk, 16 kk + 16):
 // warpgroup wg packs its 64 keys into the first 32 of the 64 columns it read.
@@ -173,12 +165,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
         tc::mbar_init(&B.p_full, kSoftmaxThreads);
         tc::mbar_init(&B.o_done, 1);
         tc::mbar_init(&B.drain, 1);
-        B.n_tiles = tile_count(p, qt, kvh);
         tc::fence_barrier_init();
     }
     if (warp == 1) {
         tc::tmem_alloc(&B.tmem_base, 512);
         tc::tmem_relinquish();
+    } else if (warp == 0) {
+        // Key tiles of this CTA: dense, pages 0..own; sparse, the listed pages.
+        const int n = p.sel ? sel_count_warp(p.sel + ((size_t)qt * p.Hkv + kvh) * p.kmax, p.kmax, lane)
+                            : (int)(p.q_start / kTile) + qt + 1;
+        if (lane == 0) B.n_tiles = n;
     }
     tc::tc_fence_before();
     __syncthreads();

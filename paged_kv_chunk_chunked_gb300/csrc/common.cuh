@@ -66,6 +66,17 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Number of listed pages in a selection row (ascending, -1 padded), by one
+// warp: 32 entries per coalesced load; every lane gets the count.
+__device__ __forceinline__ int sel_count_warp(const int32_t* row, int kmax, int lane) {
+    int n = 0;
+    for (int b = 0; b < kmax; b += 32) {
+        const int e = b + lane;
+        n += __popc(__ballot_sync(0xffffffffu, e < kmax && row[e] >= 0));
+    }
+    return n;
+}
+
 // Vectorised fp32 reduction into global memory (sm_90+ red.global.add.v4.f32).
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
