@@ -340,10 +340,9 @@ def run_pkv(args, world, rank):
 def run_e2e(args, w, sw, step, world):
     """Same step with inputs in pinned host memory: H2D of every chunk's Q, K,
     V, dO and D2H of every chunk's dQ and the gathered dK, dV inside the
-    timed region."""
+    timed region, through ChunkSweep.run_from_host (side-stream copies
+    overlapped with the kernels)."""
     import torch
-    from paged_kv_chunk_chunked_gb300 import binding as B
-    stream = torch.cuda.current_stream()
     host_in = [[t.cpu().pin_memory() for t in lst] for lst in (sw.q, sw.k, sw.v, sw.do)]
     host_dq = [t.cpu().pin_memory() for t in sw.dq]
     dk = torch.empty((w.N, w.Hkv, w.d), dtype=torch.float32, device="cuda")
@@ -353,16 +352,13 @@ def run_e2e(args, w, sw, step, world):
     h2d = sum(t.numel() * t.element_size() for lst in host_in for t in lst)
     d2h = sum(t.numel() * t.element_size() for t in host_dq) + 2 * dk.numel() * 4
 
+    host = dict(zip(("q", "k", "v", "do"), host_in))
+    out = {"dq": host_dq, "dk": host_dk, "dv": host_dv}
+    h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
+
     def e2e_step():
-        for dst_l, src_l in zip((sw.q, sw.k, sw.v, sw.do), host_in):
-            for d_, s_ in zip(dst_l, src_l):
-                d_.copy_(s_, non_blocking=True)
-        step()
-        B.pkv_gather(sw.seq, None, None, dk, dv, None, stream)
-        for d_, s_ in zip(host_dq, sw.dq):
-            d_.copy_(s_, non_blocking=True)
-        host_dk.copy_(dk, non_blocking=True)
-        host_dv.copy_(dv, non_blocking=True)
+        # The package's host-buffer sweep: copies overlapped with the kernels.
+        sw.run_from_host(host, out, dk, dv, h2d_stream, d2h_stream)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()

@@ -230,6 +230,15 @@ pkv_status pkv_grad_zero(pkv_seq* seq, void* stream);
 pkv_status pkv_gather(const pkv_seq* seq, void* k, void* v, float* dk, float* dv, float* rep,
                       void* stream);
 
+/* The rows [row0, row0 + n_rows) of pkv_gather (row0 a multiple of the page
+ * size, row0 + n_rows <= length) into buffers [n_rows, Hkv, d] whose row 0
+ * is logical row row0; any output may be NULL. In a backward sweep over the
+ * chunks in reverse, a chunk's dK/dV rows are final once its own backward has
+ * run, so they can leave the GPU while earlier chunks are still computed.
+ * PKV_ERR_INVALID for a bad range. */
+pkv_status pkv_gather_rows(const pkv_seq* seq, int64_t row0, int64_t n_rows, void* k, void* v,
+                           float* dk, float* dv, void* stream);
+
 /* ---------------------------------------------------------------- page selection (a5)
  * For every query page qp of the chunk (P tokens, the last one possibly
  * partial) and KV head h:

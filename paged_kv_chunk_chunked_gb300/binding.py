@@ -69,6 +69,7 @@ _SIGS = {
                                          ctypes.POINTER(pkv_sel), _P]),
     "pkv_grad_zero": (_ST, [_P, _P]),
     "pkv_gather": (_ST, [_P, _P, _P, _P, _P, _P, _P]),
+    "pkv_gather_rows": (_ST, [_P, _I64, _I64, _P, _P, _P, _P, _P]),
     "pkv_page_topk": (_ST, [_P, _P, _I64, _I64, _I32, _I32, _I32, _P, _P, _P]),
     "pkv_prefetch": (_ST, [_P, _P, _I64, _I32, _P]),
     "pkv_writeback_grads": (_ST, [_P, _P]),
@@ -231,6 +232,11 @@ def pkv_grad_zero(seq, stream=None) -> None:
 
 def pkv_gather(seq, k=None, v=None, dk=None, dv=None, rep=None, stream=None) -> None:
     _check(lib().pkv_gather(seq, ptr(k), ptr(v), ptr(dk), ptr(dv), ptr(rep), stream_ptr(stream)))
+
+
+def pkv_gather_rows(seq, row0, n_rows, k=None, v=None, dk=None, dv=None, stream=None) -> None:
+    _check(lib().pkv_gather_rows(seq, row0, n_rows, ptr(k), ptr(v), ptr(dk), ptr(dv),
+                                 stream_ptr(stream)))
 
 
 def pkv_page_topk(seq, q, q_start, n_q, k, n_sink, n_local, pages_out, counts_out=None,

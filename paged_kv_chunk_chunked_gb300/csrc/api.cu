@@ -148,6 +148,11 @@ static pkv_status claim_pages(pkv_seq* s, int64_t new_len) {
 
 static void release_pages(pkv_seq* s) {
     pkv_pool* p = s->pool;
+    // Later claims rewrite h_bt from entry 0: uploads still queued must have read it.
+    if (s->bt_pending) {
+        cudaEventSynchronize(s->bt_sent);
+        s->bt_pending = false;
+    }
     // Push back in reverse so a fresh sequence gets the same pages in the same order.
     for (auto it = s->bt.rbegin(); it != s->bt.rend(); ++it) {
         p->in_use[*it] = 0;
@@ -165,7 +170,9 @@ static pkv_status upload_bt(pkv_seq* s, int64_t from, cudaStream_t st) {
     if (n <= 0) return PKV_OK;
     cudaError_t e = cudaMemcpyAsync(s->d_bt + from, s->h_bt + from, n * sizeof(int32_t),
                                     cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaEventRecord(s->bt_sent, st);
     if (e != cudaSuccess) return cuda_fail(e, "block-table upload");
+    s->bt_pending = true;
     return PKV_OK;
 }
 
@@ -347,6 +354,7 @@ pkv_status pkv_seq_create(pkv_pool* p, pkv_seq** out) {
         cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&s->h_bt), bytes,
                                       cudaHostAllocDefault);
         if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&s->d_bt), bytes);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->bt_sent, cudaEventDisableTiming);
         if (e == cudaSuccess && p->desc.residency == PKV_RES_PINNED_HOST) {
             e = cudaMalloc(reinterpret_cast<void**>(&s->d_slot_of), bytes);
             if (e == cudaSuccess) e = cudaMemset(s->d_slot_of, 0xff, bytes);   // all -1
@@ -364,6 +372,8 @@ pkv_status pkv_seq_create(pkv_pool* p, pkv_seq** out) {
             cudaFreeHost(s->h_bt);
             cudaFree(s->d_bt); cudaFree(s->d_slot_of); cudaFree(s->d_slot_page); cudaFree(s->d_flags);
             if (s->staged) cudaEventDestroy(s->staged);
+            if (s->used) cudaEventDestroy(s->used);
+            if (s->bt_sent) cudaEventDestroy(s->bt_sent);
             delete s;
             return cuda_fail(e, "pkv_seq_create: block table");
         }
@@ -384,6 +394,7 @@ void pkv_seq_free(pkv_seq* s) {
         cudaFree(s->d_slot_of); cudaFree(s->d_slot_page); cudaFree(s->d_flags);
         if (s->staged) cudaEventDestroy(s->staged);
         if (s->used) cudaEventDestroy(s->used);
+        if (s->bt_sent) cudaEventDestroy(s->bt_sent);
     }
     delete s;
 }
@@ -441,6 +452,10 @@ pkv_status pkv_set_block_table(pkv_seq* s, const int32_t* bt, int64_t n) {
     for (int64_t i = 0; i < n; ++i) p->in_use[bt[i]] = 1;
     s->n_reserved_pages = n;
     if (is_device(p) && n > 0) {
+        if (s->bt_pending) {                         // h_bt may still be a queued copy's source
+            cudaEventSynchronize(s->bt_sent);
+            s->bt_pending = false;
+        }
         std::memcpy(s->h_bt, bt, n * sizeof(int32_t));
         cudaError_t e = cudaMemcpy(s->d_bt, s->h_bt, n * sizeof(int32_t), cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return cuda_fail(e, "pkv_set_block_table: upload");
@@ -581,9 +596,23 @@ pkv_status pkv_gather(const pkv_seq* s, void* k, void* v, float* dk, float* dv, 
     if (!s) return fail(PKV_ERR_INVALID, "pkv_gather: seq is NULL");
     if (!is_device(s->pool)) return fail(PKV_ERR_INVALID, "pkv_gather: META pool");
     if (s->len == 0) return PKV_OK;
-    cudaError_t e = launch_gather(s->pool, s->d_bt, s->len, k, v, dk, dv, rep,
+    cudaError_t e = launch_gather(s->pool, s->d_bt, 0, s->len, k, v, dk, dv, rep,
                                   static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "pkv_gather: launch");
+    return PKV_OK;
+}
+
+pkv_status pkv_gather_rows(const pkv_seq* s, int64_t row0, int64_t n_rows, void* k, void* v,
+                           float* dk, float* dv, void* stream) {
+    if (!s) return fail(PKV_ERR_INVALID, "pkv_gather_rows: seq is NULL");
+    if (!is_device(s->pool)) return fail(PKV_ERR_INVALID, "pkv_gather_rows: META pool");
+    const int64_t P = s->pool->desc.page_size;
+    if (row0 < 0 || n_rows < 0 || row0 % P != 0 || row0 + n_rows > s->len)
+        return fail(PKV_ERR_INVALID, "pkv_gather_rows: need row0 % P == 0 and row0 + n_rows <= length");
+    if (n_rows == 0) return PKV_OK;
+    cudaError_t e = launch_gather(s->pool, s->d_bt, row0 / P, row0 + n_rows, k, v, dk, dv, nullptr,
+                                  static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_gather_rows: launch");
     return PKV_OK;
 }
 

@@ -120,9 +120,9 @@ __global__ void grad_zero_kernel(float* dk, float* dv, const int32_t* bt, int64_
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) gather_kernel(const T* kpool, const T* vpool,
         const float* dkpool, const float* dvpool, const float* reppool, const int32_t* bt,
-        int64_t num_phys, int P, int Hkv, int64_t len, T* k, T* v, float* dk, float* dv,
-        float* rep, int* err) {
-    const int64_t lp = blockIdx.x;
+        int64_t num_phys, int P, int Hkv, int64_t lp0, int64_t len, T* k, T* v, float* dk,
+        float* dv, float* rep, int* err) {
+    const int64_t lp = lp0 + blockIdx.x;            // logical page; outputs start at page lp0
     const int h = blockIdx.y;
     const int32_t pp = bt[lp];
     if (pp < 0 || pp >= num_phys) {
@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const T* kpool, const 
     const int rows = (int)min64(P, len - lp * P);
     for (int i = threadIdx.x; i < rows * D; i += kThreads) {
         const int r = i / D, c = i % D;
-        const size_t dst = ((size_t)(lp * P + r) * Hkv + h) * D + c;
+        const size_t dst = ((size_t)((lp - lp0) * P + r) * Hkv + h) * D + c;
         const size_t src = page_off + (size_t)r * D + c;
         if (k) k[dst] = kpool[src];
         if (v) v[dst] = vpool[src];
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const T* kpool, const 
         if (dv) dv[dst] = dvpool[src];
     }
     if (rep && threadIdx.x < D)
-        rep[((size_t)lp * Hkv + h) * D + threadIdx.x] =
+        rep[((size_t)(lp - lp0) * Hkv + h) * D + threadIdx.x] =
             reppool[((size_t)pp * Hkv + h) * D + threadIdx.x];
 }
 
@@ -154,14 +154,14 @@ cudaError_t append_dispatch_d(const AppendArgs& a, cudaStream_t s, dim3 grid) {
 }
 
 template <typename T>
-cudaError_t gather_dispatch(const pkv_pool* p, const int32_t* bt, int64_t len, void* k, void* v,
-                            float* dk, float* dv, float* rep, cudaStream_t s) {
+cudaError_t gather_dispatch(const pkv_pool* p, const int32_t* bt, int64_t lp0, int64_t len, void* k,
+                            void* v, float* dk, float* dv, float* rep, cudaStream_t s) {
     const int P = p->desc.page_size, Hkv = p->desc.n_kv_heads;
-    dim3 grid((unsigned)((len + P - 1) / P), Hkv);
+    dim3 grid((unsigned)((len + P - 1) / P - lp0), Hkv);
 #define PKV_GATHER_ARGS                                                                      \
     static_cast<const T*>(p->k), static_cast<const T*>(p->v), p->dk, p->dv, p->rep, bt,     \
-        p->desc.num_phys_pages, P, Hkv, len, static_cast<T*>(k), static_cast<T*>(v), dk, dv, \
-        rep, p->d_err
+        p->desc.num_phys_pages, P, Hkv, lp0, len, static_cast<T*>(k), static_cast<T*>(v), dk, \
+        dv, rep, p->d_err
     ProfScope ps("gather_kernel", s);
     if (p->desc.head_dim == 128) gather_kernel<T, 128><<<grid, kThreads, 0, s>>>(PKV_GATHER_ARGS);
     else gather_kernel<T, 64><<<grid, kThreads, 0, s>>>(PKV_GATHER_ARGS);
@@ -190,10 +190,11 @@ cudaError_t launch_grad_zero(const pkv_pool* p, const int32_t* d_bt, int64_t p0,
     return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const pkv_pool* p, const int32_t* d_bt, int64_t len, void* k, void* v,
-                          float* dk, float* dv, float* rep, cudaStream_t s) {
-    return p->desc.dtype == PKV_BF16 ? gather_dispatch<__nv_bfloat16>(p, d_bt, len, k, v, dk, dv, rep, s)
-                                     : gather_dispatch<float>(p, d_bt, len, k, v, dk, dv, rep, s);
+cudaError_t launch_gather(const pkv_pool* p, const int32_t* d_bt, int64_t lp0, int64_t len, void* k,
+                          void* v, float* dk, float* dv, float* rep, cudaStream_t s) {
+    return p->desc.dtype == PKV_BF16
+               ? gather_dispatch<__nv_bfloat16>(p, d_bt, lp0, len, k, v, dk, dv, rep, s)
+               : gather_dispatch<float>(p, d_bt, lp0, len, k, v, dk, dv, rep, s);
 }
 
 }  // namespace pkv

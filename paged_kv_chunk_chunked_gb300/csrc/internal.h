@@ -52,6 +52,10 @@ struct pkv_seq {
     int64_t n_reserved_pages = 0;    // pages pre-assigned by pkv_set_block_table not yet filled
     int32_t* h_bt = nullptr;         // pinned mirror used as the copy source
     int32_t* d_bt = nullptr;         // device block table, capacity num_phys_pages
+    // Recorded after every asynchronous upload from h_bt: entries already sent
+    // are rewritten (after a reset) only once the last upload has executed.
+    cudaEvent_t bt_sent = nullptr;
+    bool bt_pending = false;
     int64_t len = 0;
     // PINNED_HOST pools: staging state (device), capacity num_phys_pages.
     int32_t* d_slot_of = nullptr;    // logical page -> device slot, or -1
@@ -99,8 +103,9 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 // Zero the gradient rows of the given logical pages range [p0, p1).
 cudaError_t launch_grad_zero(const pkv_pool* pool, const int32_t* d_bt, int64_t p0, int64_t p1,
                              cudaStream_t s);
-cudaError_t launch_gather(const pkv_pool* pool, const int32_t* d_bt, int64_t len, void* k,
-                          void* v, float* dk, float* dv, float* rep, cudaStream_t s);
+// Logical pages [lp0, ceil(len / P)) -> outputs starting at row lp0 * P.
+cudaError_t launch_gather(const pkv_pool* pool, const int32_t* d_bt, int64_t lp0, int64_t len,
+                          void* k, void* v, float* dk, float* dv, float* rep, cudaStream_t s);
 
 struct AttnArgs {
     int P, Hq, Hkv, d, dtype;

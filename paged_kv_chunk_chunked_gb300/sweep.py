@@ -102,6 +102,52 @@ class ChunkSweep:
         for c in reversed(range(w.n_chunks)):
             self.backward(c, stream)
 
+    def run_from_host(self, host: dict, out: dict, dk: torch.Tensor, dv: torch.Tensor,
+                      h2d_stream, d2h_stream):
+        """One layer sweep whose inputs start and whose results end in pinned
+        host memory: host["q"|"k"|"v"|"do"][c] -> device, then out["dq"][c],
+        out["dk"], out["dv"] <- device (dk, dv: device [N, Hkv, d] fp32 staging).
+
+        The copies run on two side streams, overlapped with the kernels on the
+        current stream: chunk c's forward waits only for chunk c's Q, K, V; dO
+        arrives (last chunk first) while the forward runs; chunk c's dQ and
+        the dK/dV rows of chunk c's keys (final once chunk c's own backward has
+        run: no earlier chunk sees them) go back while the backward of chunk
+        c - 1 runs. Only the first chunk's inputs and chunk 0's results are
+        exposed."""
+        w = self.w
+        n = w.n_chunks
+        comp = torch.cuda.current_stream()
+        fwd_ready = [torch.cuda.Event() for _ in range(n)]
+        bwd_ready = [torch.cuda.Event() for _ in range(n)]
+        dq_done = [torch.cuda.Event() for _ in range(n)]
+        h2d_stream.wait_stream(comp)              # the previous user of the buffers is done
+        with torch.cuda.stream(h2d_stream):
+            for c in range(n):
+                for dst, src in ((self.q[c], host["q"][c]), (self.k[c], host["k"][c]),
+                                 (self.v[c], host["v"][c])):
+                    dst.copy_(src, non_blocking=True)
+                fwd_ready[c].record(h2d_stream)
+            for c in reversed(range(n)):
+                self.do[c].copy_(host["do"][c], non_blocking=True)
+                bwd_ready[c].record(h2d_stream)
+        self.reset()
+        for c in range(n):
+            comp.wait_event(fwd_ready[c])
+            self.forward(c, comp)
+        for c in reversed(range(n)):
+            s, e = w.chunk_range(c)
+            comp.wait_event(bwd_ready[c])
+            self.backward(c, comp)
+            B.pkv_gather_rows(self.seq, s, e - s, None, None, dk[s:e], dv[s:e], comp)
+            dq_done[c].record(comp)
+            d2h_stream.wait_event(dq_done[c])
+            with torch.cuda.stream(d2h_stream):
+                out["dq"][c].copy_(self.dq[c], non_blocking=True)
+                out["dk"][s:e].copy_(dk[s:e], non_blocking=True)
+                out["dv"][s:e].copy_(dv[s:e], non_blocking=True)
+        comp.wait_stream(d2h_stream)
+
     def gather(self):
         """Logical-order K, V, dK, dV [N, Hkv, d] and representatives [n_pages, Hkv, d]."""
         w = self.w
