@@ -8,24 +8,27 @@
 // §2.B: gradients accumulated in place; sciencestack.ai Fig. 3).
 // D_i = rowsum(dO_i * O_i) comes from the row-dot kernel run before these.
 //
-// Two kernels, so that no output needs atomics between CTAs:
-//   bwd_kv_tc_kernel  one CTA per (key page, KV head). K of the page stays in
-//                     tensor memory, V in shared memory; the CTA walks every 64-query tile of
-//                     the chunk that sees the page, for each of the g query
-//                     heads of the group, and accumulates dK and dV in tensor
-//                     memory. At the end it adds them into the page's gradient
-//                     rows with vectorised red.global.add.v4.f32 (the CTA owns
-//                     those rows within the call; the red keeps earlier chunks'
-//                     contributions).
+// Two kernels, so that dQ needs no atomics and dK/dV one addition per element
+// per CTA:
+//   bwd_kv_tc_kernel  one CTA per (key page, KV head) -- or per share of its
+//                     iterations when the grid is small. K of the page sits in
+//                     tensor memory, V in shared memory; the CTA walks every
+//                     64-query tile of the chunk that sees the page, for each
+//                     of the g query heads of the group, and accumulates dK
+//                     and dV in tensor memory. At the end it adds them into
+//                     the page's gradient rows with vectorised
+//                     red.global.add.v4.f32 (the red keeps earlier chunks'
+//                     contributions and those of the page's other CTAs).
 //   bwd_q_tc_kernel   one CTA per (128-query tile, query head); walks the
-//                     visible keys in half-page tiles of 64 and accumulates dQ
-//                     in tensor memory, written once as bf16.
-// Both have the forward's warp roles: warp 0 TMA producer, warp 1 MMA issuer
-// (elected lane), then two softmax warpgroups, one thread per accumulator row,
-// that split each tile's columns. The S/dP (or S^T/dP^T) buffer is released
+//                     visible keys a page (128 keys) at a time and accumulates
+//                     dQ in tensor memory, written once as bf16.
+// Warp roles in both: warp 0 TMA producer; warp 1 issues the S/dP (or
+// S^T/dP^T) MMAs; warps 2..9 two softmax warpgroups, one thread per
+// accumulator row, splitting each tile's columns; warp 10 issues the MMAs
+// that consume the softmax output (dV/dK, or dQ). The S/dP buffer is released
 // as soon as the softmax warps have read it, so the tensor core computes tile
-// t+1 while they work on tile t. Wherever tensor memory has room, the MMAs take
-// their A operand from it rather than from shared memory (an A operand in
+// t+1 while they work on tile t. Wherever tensor memory has room, the MMAs
+// take their A operand from it rather than from shared memory (an A operand in
 // shared memory costs the tensor core ~33 extra cycles per instruction on this
 // part): K, P^T and dS^T in the dK/dV kernel, Q and dS in the dQ kernel.
 #include <cuda_bf16.h>
