@@ -309,6 +309,9 @@ pkv_status pkv_profile_collect(int32_t max_kernels, char* names, double* total_m
  *   mode 2: a [64(K), 128(M)], b [64(K), 128(N)]  (both MN-major): d = a^T . b
  *   mode 3: a [128(M), 64(K)] placed in tensor memory, b [64(K), 128(N)]
  *           (B MN-major): d = a . b
+ *   mode 4: issues no MMA, so the kernel's bounded wait for it expires (after
+ *           about 4 s) and must return PKV_ERR_DEVICE_FAULT with the device
+ *           in a usable state: the failure path of every kernel wait.
  * lbo/sbo override the MN-major descriptor byte offsets (0 = library
  * default). PKV_ERR_DEVICE_FAULT if a bounded wait expired. */
 pkv_status pkv_selftest_umma(int32_t mode, const void* a, const void* b, float* d,

@@ -716,7 +716,7 @@ pkv_status pkv_wait(pkv_seq* s, void* main, int64_t timeout_us) {
 
 pkv_status pkv_selftest_umma(int32_t mode, const void* a, const void* b, float* d, int32_t lbo,
                              int32_t sbo) {
-    if (mode < 0 || mode > 3 || !a || !b || !d)
+    if (mode < 0 || mode > 4 || !a || !b || !d)
         return fail(PKV_ERR_INVALID, "pkv_selftest_umma: bad argument");
     int* d_err = nullptr;
     cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&d_err), sizeof(int));

@@ -4,6 +4,9 @@
 // memory, read back with tcgen05.ld. One CTA, one 128x128x64 product.
 // Mode 3 takes A from tensor memory instead (written by the threads with
 // tcgen05.st, row i in lane i, two bf16 per column) and B MN-major.
+// Mode 4 issues nothing: the wait for the MMA's completion can never succeed,
+// so it must give up after its bound, record kErrWaitTimeout, free the tensor
+// memory and return -- the failure path every kernel's waits take.
 //
 // Operands are staged into shared memory by the threads (the same byte
 // layout a 128-byte-swizzle TMA load produces), inside a 200 KB dynamic
@@ -41,13 +44,17 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(int mode, const __nv
     const int warp = threadIdx.x / 32;
 
     // Stage operands.
-    if (mode == 2) {                    // A stored [K=64][M=128]: two 64-wide M halves
+    if (mode == 4) {
+        // nothing to stage
+    } else if (mode == 2) {                    // A stored [K=64][M=128]: two 64-wide M halves
         stage_sw128(sA, a, 64, 128, 0);
         stage_sw128(sA + 8192, a, 64, 128, 64);
     } else if (mode != 3) {             // A stored [M=128][K=64]
         stage_sw128(sA, a, 128, 64, 0);
     }
-    if (mode >= 1) {                    // B stored [K=64][N=128]
+    if (mode == 4) {
+        // nothing to stage
+    } else if (mode >= 1) {             // B stored [K=64][N=128]
         stage_sw128(sB, b, 64, 128, 0);
         stage_sw128(sB + 8192, b, 64, 128, 64);
     } else {                            // B stored [N=128][K=64]
@@ -85,7 +92,7 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(int mode, const __nv
 
     const uint32_t mn_lbo = lbo ? (uint32_t)lbo : 8192u;
     const uint32_t mn_sbo = sbo ? (uint32_t)sbo : 1024u;
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && mode != 4) {
         const uint32_t idesc = tc::idesc_bf16(128, 128, mode == 2, mode >= 1);
         const uint32_t a0 = tc::smem_u32(sA), b0 = tc::smem_u32(sB);
         for (int kk = 0; kk < 4; ++kk) {

@@ -151,3 +151,48 @@ def test_host_buffer_sweep_matches_device_sweep():
         assert _rel(out["dv"].numpy(), to_numpy(ref["dv"])) < 1e-6
     finally:
         sw.close()
+
+
+def test_bounded_wait_gives_up_reports_and_leaves_the_device_usable():
+    """Every kernel wait is bounded. Self-test mode 4 issues no MMA, so its wait
+    for the MMA can never succeed: it must give up after its bound (~4 s),
+    record the timeout in the error word, free its tensor memory and return.
+    The next launch on the same context then works normally."""
+    import time
+    a = torch.zeros((128, 64), dtype=torch.bfloat16, device="cuda")
+    b = torch.zeros((64, 128), dtype=torch.bfloat16, device="cuda")
+    d = torch.empty((128, 128), dtype=torch.float32, device="cuda")
+    t0 = time.time()
+    with pytest.raises(B.PkvError) as e:
+        B.pkv_selftest_umma(4, a, b, d)
+    assert e.value.status == B.PKV_ERR_DEVICE_FAULT and "device error 1" in str(e.value)
+    assert time.time() - t0 < 60
+    g = torch.Generator().manual_seed(0)
+    a = torch.randn((128, 64), generator=g).to(torch.bfloat16)
+    b = torch.randn((128, 64), generator=g).to(torch.bfloat16)
+    B.pkv_selftest_umma(0, a.cuda(), b.cuda(), d)
+    np.testing.assert_allclose(d.cpu().double().numpy(), (a.double() @ b.double().T).numpy(),
+                               rtol=1e-5, atol=1e-4)
+
+
+def test_host_wait_with_a_deadline_times_out_then_completes():
+    """pkv_wait with a deadline polls the staging event and returns
+    PKV_ERR_TIMEOUT instead of blocking; without one it orders the streams."""
+    w = synth.workload("qwen7b_dense_32k", N=8192, C=8192, Hq=4, Hkv=2, name="wait_deadline")
+    pool = B.pkv_pool_create(w.P, w.Hkv, w.Hq, w.d, B.PKV_BF16, w.n_phys,
+                             residency=B.PKV_RES_PINNED_HOST, n_device_slots=w.n_pages)
+    try:
+        seq = B.pkv_seq_create(pool)
+        kv = to_device(synth.chunk_k(w, 0), "bf16")
+        B.pkv_append(seq, kv, kv, w.N)
+        torch.cuda.synchronize()
+        side = torch.cuda.Stream()
+        B.pkv_prefetch(seq, None, 0, B.PKV_STAGE_KV | B.PKV_STAGE_GRADS, side)
+        with pytest.raises(B.PkvError) as e:
+            B.pkv_wait(seq, None, 1)                 # 1 us: the copies take far longer
+        assert e.value.status == B.PKV_ERR_TIMEOUT
+        B.pkv_wait(seq, None, 0)
+        torch.cuda.synchronize()
+        B.pkv_check(pool)
+    finally:
+        B.pkv_pool_destroy(pool)
