@@ -485,6 +485,13 @@ def run_sparse(args, world, rank):
     qb_cnt, qb_ms = prof.get("qbar_kernel", (1, float("nan")))
     qbar_gbs = q_bytes * qb_cnt / (qb_ms * 1e-3) / 1e9
     sel_cnt, sel_ms = prof.get("select_kernel", (1, float("nan")))
+    # Dominant kernel (by device time) with the FLOPs it runs over the attended
+    # pairs: dK/dV kernel 8 (S^T, dP^T, dV, dK), dQ kernel 6, forward 4, times d.
+    units = {"bwd_kv_tc_kernel": 8, "bwd_q_tc_kernel": 6, "fwd_tc_kernel": 4}
+    dom = max(prof, key=lambda k: prof[k][1])
+    dom_cnt, dom_ms = prof[dom]
+    dom_flops = units.get(dom, 0) * w.d * pairs * args.steps
+    dom_ach = dom_flops / (dom_ms * 1e-3) / 1e12 if dom in units else None
     return {
         "metric": METRIC, "value": round(tflops, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
@@ -499,11 +506,16 @@ def run_sparse(args, world, rank):
         "pct_bf16_peak": round(100 * tflops / peak_tc, 2),
         "dense_ms_per_step": round(dense_ms, 3),
         "sparse_speedup_vs_dense": round(dense_ms / ms, 2),
-        "roofline": {"bound": "hbm", "kernel": "qbar_kernel", "unit": "GB/s",
-                     "achieved": round(qbar_gbs, 1), "peak": pk["hbm_gbs"],
-                     "frac": round(qbar_gbs / pk["hbm_gbs"], 4),
-                     "bytes_per_launch": q_bytes, "peak_kind": f"{pk_kind} hbm_gbs",
-                     "traffic": None},
+        "roofline": {"bound": "tensor", "kernel": dom, "unit": "TFLOP/s",
+                     "achieved": round(dom_ach, 2) if dom_ach else None, "peak": peak_tc,
+                     "frac": round(dom_ach / peak_tc, 4) if dom_ach else None,
+                     "flops_per_launch": dom_flops / max(dom_cnt, 1),
+                     "peak_kind": f"{pk_kind} bf16_tflops_sustained", "traffic": None},
+        # page scoring: the page-query kernel reads the chunk's Q once (HBM-bound)
+        "page_query_roofline": {"bound": "hbm", "kernel": "qbar_kernel", "unit": "GB/s",
+                                "achieved": round(qbar_gbs, 1), "peak": pk["hbm_gbs"],
+                                "frac": round(qbar_gbs / pk["hbm_gbs"], 4),
+                                "bytes_per_launch": q_bytes, "peak_kind": f"{pk_kind} hbm_gbs"},
         "select_kernel_us_per_launch": round(1e3 * sel_ms / sel_cnt, 2),
         "kernels": kernels, "gpu_launches": sum(v[0] for v in prof.values()),
         "clocks": clk,
