@@ -22,8 +22,10 @@
 //                buffered TMEM tile, then O += P_{j-1} V_{j-1} (O in TMEM).
 //   warps 2..9   softmax, two warpgroups: thread (wg, row) owns keys
 //                [64 wg, 64 wg + 64) of query row `row` in every tile. The two
-//                partial row maxima meet through shared memory (an mbarrier
-//                per tile parity). O (with l) is rescaled in TMEM only when m
+//                partial row maxima meet through shared memory under a named
+//                barrier shared by just the two warps that own those rows
+//                (every iteration passes it exactly once, error or not, so it
+//                cannot be left waiting). O (with l) is rescaled in TMEM only when m
 //                grows by more than 2^8 (P <= 256 then, exactly representable
 //                range for bf16), each warpgroup its own half of the columns.
 //                Epilogue: O / l, LSE.
@@ -74,7 +76,6 @@ struct __align__(8) FwdBarriers {
     uint64_t s_full[2];
     uint64_t p_full;
     uint64_t o_done;
-    uint64_t xchg[2];                // row-statistics exchange, by tile parity
     uint64_t drain;
     uint32_t tmem_base;
     int n_tiles;
@@ -158,10 +159,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
             tc::mbar_init(&B.v_full[s], 1);
             tc::mbar_init(&B.v_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            tc::mbar_init(&B.s_full[s], 1);
-            tc::mbar_init(&B.xchg[s], kSoftmaxThreads);
-        }
+        for (int s = 0; s < 2; ++s) tc::mbar_init(&B.s_full[s], 1);
         tc::mbar_init(&B.p_full, kSoftmaxThreads);
         tc::mbar_init(&B.o_done, 1);
         tc::mbar_init(&B.drain, 1);
@@ -276,12 +274,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
         }
         float m = -INFINITY;
         bool ok = true;
+        // Named barrier of the two warps (one per warpgroup) that own rows 32 quad ..
+        const uint32_t pair_bar = 1 + quad;
         for (int j = 0; j < nt; ++j) {
             const int st = j & 1;
-            ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.s_full[st], (j >> 1) & 1, p.err));
-            if (!ok) break;
-            tc::tc_fence_after();
+            if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.s_full[st], (j >> 1) & 1, p.err));
             // Raw logits q.k of my 64 keys; the scale is folded into the exp2 argument.
+            // (After a failed wait the loads just read stale columns: the loop goes
+            // on only to keep meeting the partner warp, and writes nothing.)
+            tc::tc_fence_after();
             float x[64];
             {
                 uint32_t r0[32], r1[32];
@@ -300,7 +301,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
                 for (int c = 0; c < 64; ++c)
                     if (wg * 64 + c > row) x[c] = -INFINITY;
             }
-            // Row max with 8 independent chains, then the other warpgroup's half.
+            // Row max with 8 independent chains.
             float mpart[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) mpart[k] = x[k];
@@ -310,11 +311,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
             for (int k = 4; k > 0; k >>= 1)
 #pragma unroll
                 for (int i = 0; i < k; ++i) mpart[i] = fmaxf(mpart[i], mpart[i + k]);
-            B.red[st][wg][row] = mpart[0];
-            tc::mbar_arrive(&B.xchg[st]);             // release: the partial max is visible
-            ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.xchg[st], (j >> 1) & 1, p.err));
-            if (!ok) break;
-            const float mx = fmaxf(mpart[0], B.red[st][wg ^ 1][row]) * sl2;   // scaled, log2 units
+            const float part = mpart[0];
+            // The other warpgroup's half of the row (double-buffered by tile parity:
+            // a slot is rewritten only after both warps have passed the next barrier).
+            B.red[st][wg][row] = part;
+            asm volatile("bar.sync %0, 64;" :: "r"(pair_bar) : "memory");
+            if (!ok) continue;                        // keep meeting the partner warp
+            const float mx = fmaxf(part, B.red[st][wg ^ 1][row]) * sl2;   // scaled, log2 units
             float alpha = 1.f;
             bool rescale = false;
             if (mx > m + kRescaleThreshold) {
@@ -333,7 +336,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
             if (j > 0 && __any_sync(0xffffffffu, rescale)) {
                 // PV_{j-1} must be done before O is touched (PV_j waits for this tile's P).
                 ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.o_done, (j - 1) & 1, p.err));
-                if (!ok) break;
+                if (!ok) continue;
                 tc::tc_fence_after();
                 const float f = rescale ? alpha : 1.f;
 #pragma unroll
