@@ -47,6 +47,9 @@ def parse_args():
                     help="offload workload: chunks measured at the end of the sequence")
     ap.add_argument("--slots", type=int, default=0,
                     help="offload workload: device page slots (0 = the context's page count)")
+    ap.add_argument("--offload-layers", type=int, default=0,
+                    help="dense workload: measure L layers in pinned host memory, the next "
+                         "layer's pages staged while the current one computes (0 = off)")
     return ap.parse_args()
 
 
@@ -640,6 +643,100 @@ def run_offload(args, world, rank):
     }
 
 
+def run_offload_dense(args, world, rank):
+    """Dense offload across layers: every layer's K/V pages and fp32 gradient
+    pages live in pinned host memory. The measured step is the last chunk's
+    forward + backward in each of L layers; layer l + 1's pages (K, V, dK, dV)
+    are staged into its HBM slots on a side stream while layer l computes, and
+    layer l's gradients go back after it. The same step with HBM-resident
+    layers gives the overhead."""
+    import torch
+    from paged_kv_chunk_chunked_gb300 import binding as B
+    from paged_kv_chunk_chunked_gb300 import build as pkv_build
+    from paged_kv_chunk_chunked_gb300 import synth
+    from paged_kv_chunk_chunked_gb300.sweep import to_device
+
+    pkv_build.build()
+    B.lib()
+    w = synth.workload(args.workload)
+    L = args.offload_layers
+    c = w.n_chunks - 1
+    s, e = w.chunk_range(c)
+    main_s = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    q = to_device(synth.chunk_q(w, c), w.dtype)
+    do = to_device(synth.chunk_do(w, c), w.dtype)
+    o, dq = torch.empty_like(q), torch.empty_like(q)
+    lse = torch.empty((w.Hq, e - s), dtype=torch.float32, device="cuda")
+    kv = [(to_device(synth.chunk_k(w, i), w.dtype), to_device(synth.chunk_v(w, i), w.dtype))
+          for i in range(w.n_chunks)]
+    res = {}
+    for mode in ("pinned_host", "device"):
+        host = mode == "pinned_host"
+        pools, seqs = [], []
+        for _ in range(L):
+            pool = B.pkv_pool_create(w.P, w.Hkv, w.Hq, w.d, B.PKV_BF16, w.n_phys,
+                                     residency=B.PKV_RES_PINNED_HOST if host else B.PKV_RES_DEVICE,
+                                     n_device_slots=w.n_pages if host else 0)
+            seq = B.pkv_seq_create(pool)
+            for i, (k_, v_) in enumerate(kv):
+                a, b_ = w.chunk_range(i)
+                B.pkv_append(seq, k_, v_, b_ - a, main_s)
+            pools.append(pool)
+            seqs.append(seq)
+        torch.cuda.synchronize()
+
+        def step():
+            if host:
+                B.pkv_prefetch(seqs[0], None, 0, B.PKV_STAGE_KV | B.PKV_STAGE_GRADS, side)
+            for l in range(L):
+                if host:
+                    if l + 1 < L:
+                        B.pkv_prefetch(seqs[l + 1], None, 0, B.PKV_STAGE_KV | B.PKV_STAGE_GRADS, side)
+                    B.pkv_wait(seqs[l], main_s, 0)
+                B.pkv_chunk_attn_fwd(seqs[l], q, s, e - s, o, lse, None, main_s)
+                B.pkv_chunk_attn_bwd(seqs[l], q, o, do, lse, s, e - s, dq, None, main_s)
+                if host:
+                    B.pkv_writeback_grads(seqs[l], side)
+            if host:
+                for l in range(L):
+                    B.pkv_wait(seqs[l], main_s, 0)
+
+        for _ in range(max(1, args.warmup)):
+            step()
+        torch.cuda.synchronize()
+        for pool in pools:
+            B.pkv_check(pool)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(main_s)
+        for _ in range(args.steps):
+            step()
+        ev1.record(main_s)
+        torch.cuda.synchronize()
+        for pool in pools:
+            B.pkv_check(pool)
+        res[mode] = ev0.elapsed_time(ev1) / args.steps
+        for pool in pools:
+            B.pkv_pool_destroy(pool)
+    page_kv = w.Hkv * w.P * w.d * 2 * 2
+    page_g = w.Hkv * w.P * w.d * 4 * 2
+    bytes_moved = L * w.n_pages * (page_kv + 2 * page_g)
+    overhead = res["pinned_host"] / res["device"] - 1.0
+    return {
+        "metric": "dense layer offload: next layer's pages staged over the host link while the "
+                  "current layer computes, overhead vs HBM-resident",
+        "value": round(overhead * 100, 2), "unit": "% step-time overhead", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": False,
+        "ms_per_step_pinned_host": round(res["pinned_host"], 3),
+        "ms_per_step_device": round(res["device"], 3),
+        "config": {"workload": w.name, "N": w.N, "C": w.C, "P": w.P, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "d": w.d, "layers": L, "measured_chunk": c},
+        "bytes_moved_per_step": bytes_moved,
+        "link_gbs_needed_to_hide": round(bytes_moved / (res["device"] * 1e-3) / 1e9, 1),
+        "data": "synthetic (seeded N(0,1) K/V/Q/dO, the same for every layer)",
+    }
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -651,7 +748,9 @@ def main():
     world, rank, _ = dist_setup(args)
     from paged_kv_chunk_chunked_gb300 import synth
     wl = synth.workload(args.workload)
-    if wl.offload:
+    if args.offload_layers > 0:
+        out = run_offload_dense(args, world, rank)
+    elif wl.offload:
         out = run_offload(args, world, rank)
     elif wl.topk:
         out = run_sparse(args, world, rank)

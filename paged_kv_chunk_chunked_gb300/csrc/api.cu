@@ -161,6 +161,7 @@ static void release_pages(pkv_seq* s) {
     s->bt.clear();
     s->len = 0;
     s->n_reserved_pages = 0;
+    s->staged_all = 0;          // slots no longer mirror this sequence's pages
 }
 
 // Uploads block-table entries [from, bt.size()) to the device copy on stream.
@@ -662,6 +663,38 @@ static pkv_status host_pool_check(pkv_seq* s, const char* who) {
     return check_stream_device(s->pool);
 }
 
+// Whole-sequence staging with the copy engines instead of copy kernels (no SM
+// time taken from the attention kernels running meanwhile): logical page i goes
+// to slot i, which is the plan kernel's assignment when every page is staged,
+// in one cudaMemcpyAsync per run of consecutive physical pages per array.
+static cudaError_t stage_all_dma(const pkv_seq* s, int64_t n, int what, bool to_host, cudaStream_t cs) {
+    const pkv_pool* p = s->pool;
+    const size_t kv_page = p->page_elems * p->elem, g_page = p->page_elems * sizeof(float);
+    for (int64_t i0 = 0; i0 < n;) {
+        int64_t i1 = i0 + 1;
+        while (i1 < n && s->bt[i1] == s->bt[i1 - 1] + 1) ++i1;
+        const size_t pp = (size_t)s->bt[i0], len = (size_t)(i1 - i0), slot = (size_t)i0;
+        auto cp = [&](void* slots, void* pages, size_t page_bytes) {
+            uint8_t* d = static_cast<uint8_t*>(slots) + slot * page_bytes;
+            uint8_t* h = static_cast<uint8_t*>(pages) + pp * page_bytes;
+            return to_host ? cudaMemcpyAsync(h, d, len * page_bytes, cudaMemcpyDeviceToHost, cs)
+                           : cudaMemcpyAsync(d, h, len * page_bytes, cudaMemcpyHostToDevice, cs);
+        };
+        cudaError_t e = cudaSuccess;
+        if (what & PKV_STAGE_KV) {
+            e = cp(p->kslot, p->k, kv_page);
+            if (e == cudaSuccess) e = cp(p->vslot, p->v, kv_page);
+        }
+        if (e == cudaSuccess && (what & PKV_STAGE_GRADS)) {
+            e = cp(p->dkslot, p->dk, g_page);
+            if (e == cudaSuccess) e = cp(p->dvslot, p->dv, g_page);
+        }
+        if (e != cudaSuccess) return e;
+        i0 = i1;
+    }
+    return cudaSuccess;
+}
+
 pkv_status pkv_prefetch(pkv_seq* s, const int32_t* pages, int64_t n, int32_t what, void* side) {
     pkv_status st = host_pool_check(s, "pkv_prefetch");
     if (st != PKV_OK) return st;
@@ -673,7 +706,11 @@ pkv_status pkv_prefetch(pkv_seq* s, const int32_t* pages, int64_t n, int32_t wha
     // Slots are rewritten: wait for the last append/attention call on this sequence.
     cudaError_t e = cudaStreamWaitEvent(cs, s->used, 0);
     if (e == cudaSuccess) e = launch_stage_plan(s, n > 0 ? pages : nullptr, n, cs);
-    if (e == cudaSuccess) e = launch_stage_copy(s, what, cs);
+    const int64_t n_pages = (int64_t)s->bt.size();
+    const bool all = n == 0 && n_pages <= s->pool->n_slots;
+    s->staged_all = all ? n_pages : 0;
+    if (e == cudaSuccess)
+        e = all ? stage_all_dma(s, n_pages, what, false, cs) : launch_stage_copy(s, what, cs);
     if (e == cudaSuccess) e = cudaEventRecord(s->staged, cs);
     if (e != cudaSuccess) return cuda_fail(e, "pkv_prefetch");
     return PKV_OK;
@@ -685,7 +722,10 @@ pkv_status pkv_writeback_grads(pkv_seq* s, void* side) {
     if (s->bt.empty()) return PKV_OK;
     cudaStream_t cs = static_cast<cudaStream_t>(side);
     cudaError_t e = cudaStreamWaitEvent(cs, s->used, 0);
-    if (e == cudaSuccess) e = launch_stage_writeback(s, cs);
+    if (e == cudaSuccess)
+        e = s->staged_all > 0 ? stage_all_dma(s, std::min<int64_t>(s->staged_all, (int64_t)s->bt.size()),
+                                              PKV_STAGE_GRADS, true, cs)
+                              : launch_stage_writeback(s, cs);
     if (e == cudaSuccess) e = cudaEventRecord(s->staged, cs);
     if (e != cudaSuccess) return cuda_fail(e, "pkv_writeback_grads");
     return PKV_OK;

@@ -33,8 +33,8 @@ struct pkv_pool {
     float* sel_scratch = nullptr;
     size_t sel_scratch_floats = 0;
     // TMA descriptors over the K and V page pools (2-D: rows x d), with boxes
-    // of 64 columns x 128 rows (whole pages) and 64 x 64 (half pages). For a
-    // PINNED_HOST pool they describe the device slots.
+    // of 64 columns x 128 rows (whole pages). For a PINNED_HOST pool they
+    // describe the device slots.
     CUtensorMap tmap_k{}, tmap_v{};
     bool tmaps_ready = false;
     // PINNED_HOST pools: k/v/dk/dv above are mapped pinned host pages; the
@@ -63,6 +63,7 @@ struct pkv_seq {
     int32_t* d_flags = nullptr;      // planning scratch [num_phys_pages + 1]
     cudaEvent_t staged = nullptr;    // last event recorded on the side stream
     cudaEvent_t used = nullptr;      // last append/attention call on the sequence's slots
+    int64_t staged_all = 0;          // > 0: the last prefetch staged pages [0, staged_all), slot i = page i
 };
 
 namespace pkv {
