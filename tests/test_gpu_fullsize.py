@@ -19,7 +19,7 @@ import oracle
 from paged_kv_chunk_chunked_gb300 import binding as B
 from paged_kv_chunk_chunked_gb300 import build as pkv_build
 from paged_kv_chunk_chunked_gb300 import synth
-from paged_kv_chunk_chunked_gb300.sweep import ChunkSweep, to_numpy
+from paged_kv_chunk_chunked_gb300.sweep import ChunkSweep, to_device, to_numpy
 
 pytestmark = pytest.mark.gpu
 
@@ -165,3 +165,116 @@ def test_sparse_256k_full_size_sampled():
         _check_identities(w, g, dos_sum)
     finally:
         sw.close()
+
+
+def test_sparse_1m_pinned_host_full_size_sampled():
+    """The 1M-token pinned-host workload as bench.py runs it: every K/V page and
+    fp32 gradient page in mapped pinned host memory, the last chunk's selected
+    pages staged into HBM slots on a side stream for its forward and backward,
+    the gradients written back. Checked against the oracle: the selection of
+    every query page (representatives from the seeded keys, ties within 1e-5);
+    O, LSE and dQ of sampled rows, each computed by the oracle over that row's
+    selected pages gathered into a compact key sequence (the row's own page
+    last, so the causal mask falls where it does in the full sequence); and,
+    over the whole written-back gradient pool, sum dK = 0 and sum dV = sum dO
+    per KV head (the pool holds only this chunk's contribution)."""
+    w = synth.workload("qwen7b_sparse_1m_offload")
+    K, ns, nl = w.topk
+    n = w.n_chunks
+    c = n - 1
+    s, e = w.chunk_range(c)
+    ppc = w.C // w.P                                    # pages per chunk
+    bt = synth.block_table(w)
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    pool = B.pkv_pool_create(w.P, w.Hkv, w.Hq, w.d, B.PKV_BF16, w.n_phys,
+                             residency=B.PKV_RES_PINNED_HOST, n_device_slots=w.n_pages)
+    try:
+        seq = B.pkv_seq_create(pool)
+        B.pkv_set_block_table(seq, bt)
+        rep = np.zeros((w.n_pages, w.Hkv, w.d))
+        for i in range(n):
+            a, b_ = w.chunk_range(i)
+            k_np = synth.chunk_k(w, i)
+            rep[i * ppc:(i + 1) * ppc] = oracle.page_representatives(k_np, w.P)
+            B.pkv_append(seq, to_device(k_np, "bf16"), to_device(synth.chunk_v(w, i), "bf16"),
+                         b_ - a, main)
+        q_np, do_np = synth.chunk_q(w, c), synth.chunk_do(w, c)
+        q, do = to_device(q_np, "bf16"), to_device(do_np, "bf16")
+        o, dq = torch.empty_like(q), torch.empty_like(q)
+        lse = torch.empty((w.Hq, e - s), dtype=torch.float32, device="cuda")
+        sel = torch.empty((w.C // w.P, w.Hkv, K + ns + nl), dtype=torch.int32, device="cuda")
+        B.pkv_page_topk(seq, q, s, e - s, K, ns, nl, sel, None, main)
+        B.pkv_prefetch(seq, sel, sel.numel(), B.PKV_STAGE_KV, side)
+        B.pkv_wait(seq, main, 0)
+        B.pkv_chunk_attn_fwd(seq, q, s, e - s, o, lse, sel, main)
+        B.pkv_prefetch(seq, sel, sel.numel(), B.PKV_STAGE_KV | B.PKV_STAGE_GRADS, side)
+        B.pkv_wait(seq, main, 0)
+        B.pkv_chunk_attn_bwd(seq, q, o, do, lse, s, e - s, dq, sel, main)
+        B.pkv_writeback_grads(seq, side)
+        B.pkv_wait(seq, main, 60_000_000)
+        torch.cuda.synchronize()
+        B.pkv_check(pool)
+
+        # selection of every query page and KV head
+        sel_gpu = sel.cpu().numpy()
+        qbar = oracle.query_page_means(q_np, w.P, w.Hkv)
+        qp0 = s // w.P
+        lists = {}
+        for i in range(sel_gpu.shape[0]):
+            for kv in range(w.Hkv):
+                got = [int(x) for x in sel_gpu[i, kv] if x >= 0]
+                want = oracle.select_pages(qbar[i, kv], rep[:, kv, :], qp0 + i, K, ns, nl)
+                if got != want:
+                    cand = np.arange(ns, qp0 + i - nl + 1)
+                    kth = np.sort(rep[cand, kv] @ qbar[i, kv])[::-1][K - 1]
+                    for pg in set(got) ^ set(want):
+                        assert abs(rep[pg, kv] @ qbar[i, kv] - kth) <= 1e-5, (i, kv, pg)
+                lists[(i, kv)] = got
+
+        # sampled rows over their selected pages (compact key sequences)
+        rng = np.random.default_rng(11)
+        rows = np.sort(rng.choice(e - s, size=6, replace=False))
+        heads = (0, 13, w.Hq - 1)
+        need = sorted({pg for r in rows for h in heads for pg in lists[(int(r) // w.P, h // w.g)]})
+        kv_rows = {}
+        for ch in sorted({pg // ppc for pg in need}):
+            kc, vc = synth.chunk_k(w, ch), synth.chunk_v(w, ch)
+            for pg in need:
+                if pg // ppc == ch:
+                    o0 = (pg - ch * ppc) * w.P
+                    kv_rows[pg] = (kc[o0:o0 + w.P], vc[o0:o0 + w.P])
+        o_gpu, lse_gpu, dq_gpu = to_numpy(o), to_numpy(lse), to_numpy(dq)
+        dq_ref, dq_got = [], []
+        for h in heads:
+            kv = h // w.g
+            for r in rows:
+                pages = lists[(int(r) // w.P, kv)]
+                assert pages[-1] == qp0 + int(r) // w.P           # own page listed last
+                kc = np.concatenate([kv_rows[pg][0][:, kv:kv + 1] for pg in pages])
+                vc = np.concatenate([kv_rows[pg][1][:, kv:kv + 1] for pg in pages])
+                pos = (len(pages) - 1) * w.P + int(r) % w.P       # compact position
+                qr, dor = q_np[r:r + 1, h:h + 1], do_np[r:r + 1, h:h + 1]
+                o_r, lse_r = oracle.attention_forward(qr, kc[:pos + 1], vc[:pos + 1], pos)
+                dq_r, _, _ = oracle.attention_backward(qr, kc[:pos + 1], vc[:pos + 1], o_r, dor,
+                                                       lse_r, pos)
+                assert abs(o_gpu[r, h] - o_r[0, 0]).max() <= 1e-2, (h, r)
+                assert abs(lse_gpu[h, r] - lse_r[0, 0]) <= 1e-2, (h, r)
+                dq_ref.append(dq_r[0, 0])
+                dq_got.append(dq_gpu[r, h])
+        assert _rel(np.array(dq_got), np.array(dq_ref)) <= 2e-2
+
+        # gradient-pool identities over the whole written-back pool
+        dk = torch.empty((w.N, w.Hkv, w.d), dtype=torch.float32, device="cuda")
+        dv = torch.empty_like(dk)
+        B.pkv_gather(seq, None, None, dk, dv, None, main)
+        torch.cuda.synchronize()
+        sk = dk.double().sum(0).cpu().numpy()
+        sv = dv.double().sum(0).cpu().numpy()
+        nk = torch.sqrt((dk.double() ** 2).sum(0).sum(-1)).cpu().numpy()
+        do64 = do_np.astype(np.float64)
+        for kv in range(w.Hkv):
+            assert np.linalg.norm(sk[kv]) <= 2e-2 * nk[kv], kv
+            assert _rel(sv[kv], do64[:, kv * w.g:(kv + 1) * w.g].sum((0, 1))) <= 2e-2, kv
+    finally:
+        B.pkv_pool_destroy(pool)
