@@ -663,7 +663,7 @@ def run_offload_dense(args, world, rank):
     c = w.n_chunks - 1
     s, e = w.chunk_range(c)
     main_s = torch.cuda.current_stream()
-    side = torch.cuda.Stream()
+    side, side_out = torch.cuda.Stream(), torch.cuda.Stream()   # host-to-device, device-to-host
     q = to_device(synth.chunk_q(w, c), w.dtype)
     do = to_device(synth.chunk_do(w, c), w.dtype)
     o, dq = torch.empty_like(q), torch.empty_like(q)
@@ -697,7 +697,7 @@ def run_offload_dense(args, world, rank):
                 B.pkv_chunk_attn_fwd(seqs[l], q, s, e - s, o, lse, None, main_s)
                 B.pkv_chunk_attn_bwd(seqs[l], q, o, do, lse, s, e - s, dq, None, main_s)
                 if host:
-                    B.pkv_writeback_grads(seqs[l], side)
+                    B.pkv_writeback_grads(seqs[l], side_out)
             if host:
                 for l in range(L):
                     B.pkv_wait(seqs[l], main_s, 0)

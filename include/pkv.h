@@ -276,6 +276,8 @@ pkv_status pkv_page_topk(pkv_seq* seq, const void* q, int64_t q_start, int64_t n
  * over the host link; nothing is allocated and the host does not wait.
  * pkv_writeback_grads: on `side`, after the sequence's last attention call,
  * copies the staged slots' dK/dV back into the host gradient pages.
+ * A prefetch also waits for the sequence's previous prefetch or writeback, so
+ * write-backs may go on their own stream (both copy directions at once).
  * pkv_wait: makes stream `main` wait (on the GPU) for the sequence's last
  * prefetch or writeback; with timeout_us > 0 the host first polls for its
  * completion and returns PKV_ERR_TIMEOUT, enqueuing nothing, after

@@ -703,8 +703,11 @@ pkv_status pkv_prefetch(pkv_seq* s, const int32_t* pages, int64_t n, int32_t wha
         return fail(PKV_ERR_INVALID, "pkv_prefetch: bad pages/n/what");
     if (s->bt.empty()) return PKV_OK;
     cudaStream_t cs = static_cast<cudaStream_t>(side);
-    // Slots are rewritten: wait for the last append/attention call on this sequence.
+    // Slots are rewritten: wait for the last append/attention call on this
+    // sequence and for its last prefetch or writeback (which may have been
+    // issued on another stream, e.g. write-backs on a device-to-host stream).
     cudaError_t e = cudaStreamWaitEvent(cs, s->used, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, s->staged, 0);
     if (e == cudaSuccess) e = launch_stage_plan(s, n > 0 ? pages : nullptr, n, cs);
     const int64_t n_pages = (int64_t)s->bt.size();
     const bool all = n == 0 && n_pages <= s->pool->n_slots;
