@@ -331,12 +331,71 @@ def run_pkv(args, world, rank):
 
     if not args.no_e2e:
         out["e2e"] = run_e2e(args, w, sw, step, world)
+    out["hbm_kernels"] = hbm_kernels(args, w, sw, prof, pk)
     if rank == 0 and world == 1 and not args.no_cpu:
         flops, dt, desc = oracle_sample(w, w.C)
         out["cpu_baseline"] = {"value": round(flops / dt / 1e12, 6), "unit": UNIT,
                                "cores": cpu_threads(), "kind": "oracle", "sample": desc,
                                "seconds": round(dt, 2)}
     sw.close()
+    return out
+
+
+def hbm_kernels(args, w, sw, prof, pk):
+    """HBM-bound kernels of the path against the measured copy bandwidth.
+
+    grad_accumulate_kernel: a standalone read-modify-write of the whole
+    sequence's fp32 dK/dV pages (pkv_grad_accumulate over rows [0, N)), 12
+    bytes per element (delta read, pool read and write). Each launch is timed
+    alone with CUDA events on the launching stream, after a 512 MB write that
+    flushes L2. append_kernel: from the timed step's per-kernel event times;
+    per launch it reads the chunk's K and V, writes them into the pages, writes
+    the representatives and zeroes the fresh pages' fp32 gradients."""
+    import torch
+    from paged_kv_chunk_chunked_gb300 import binding as B
+
+    hbm = pk.get("hbm_gbs")
+    stream = torch.cuda.current_stream()
+    sw.reset()
+    for c in range(w.n_chunks):
+        s, e = w.chunk_range(c)
+        B.pkv_append(sw.seq, sw.k[c], sw.v[c], e - s, stream)
+    gen = torch.Generator(device="cuda").manual_seed(w.seed)
+    dk = torch.randn((w.N, w.Hkv, w.d), device="cuda", generator=gen)
+    dv = torch.randn((w.N, w.Hkv, w.d), device="cuda", generator=gen)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        B.pkv_grad_accumulate(sw.seq, 0, w.N, dk, dv, stream)
+    n_it = max(args.steps, 5)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_it)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        B.pkv_grad_accumulate(sw.seq, 0, w.N, dk, dv, stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    B.pkv_check(sw.pool)
+    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+    acc_bytes = 12 * w.N * w.Hkv * w.d * 2
+    out = {"grad_accumulate_kernel": {
+        "bound": "hbm", "unit": "GB/s", "bytes_per_launch": acc_bytes,
+        "ms_per_launch": round(ms, 4), "achieved": round(acc_bytes / (ms * 1e-3) / 1e9, 1),
+        "peak": hbm, "peak_kind": "measured hbm_gbs (copy, timed alone)",
+        "rows": w.N, "l2": "flushed (512 MB write) before each launch"}}
+    if hbm:
+        out["grad_accumulate_kernel"]["frac"] = round(out["grad_accumulate_kernel"]["achieved"] / hbm, 4)
+    if "append_kernel" in prof:
+        cnt, tot = prof["append_kernel"]
+        el = 2 if w.dtype == "bf16" else 4
+        per = w.C * w.Hkv * w.d
+        a_bytes = 2 * per * el * 2 + (w.C // w.P) * w.Hkv * w.d * 4 + 2 * per * 4
+        ach = a_bytes / (tot / cnt * 1e-3) / 1e9
+        out["append_kernel"] = {"bound": "hbm", "unit": "GB/s", "bytes_per_launch": a_bytes,
+                                "ms_per_launch": round(tot / cnt, 4), "achieved": round(ach, 1),
+                                "peak": hbm, "frac": round(ach / hbm, 4) if hbm else None,
+                                "peak_kind": "measured hbm_gbs (copy)"}
+    del flush, dk, dv
     return out
 
 

@@ -223,6 +223,23 @@ pkv_status pkv_chunk_attn_bwd_noalloc(pkv_seq* seq, const void* q, const void* o
 /* Zeroes the gradient pages of the sequence's pages. */
 pkv_status pkv_grad_zero(pkv_seq* seq, void* stream);
 
+/* Adds contiguous float32 gradients into the sequence's gradient pages:
+ * for rows r in [row0, row0 + n_rows) (any row0 >= 0, row0 + n_rows <= length)
+ * and KV heads h, dK_pool[r, h, :] += dk[r - row0, h, :], and likewise dv;
+ * dk/dv are caller-owned buffers [n_rows, Hkv, d], 16-byte aligned, either
+ * may be NULL. One float32 addition per element, in stream order, no
+ * atomics: the result is exact and deterministic. The gradient pages are the
+ * paged, in-place accumulated dK/dV of "Out of the Memory Barrier"
+ * (gist.science/de §2.B "Paged Memory Management"); this call lets gradients
+ * of the cached keys computed elsewhere join them, and is the plain
+ * read-modify-write stream of that pool (12 bytes of HBM per element).
+ * For a PINNED_HOST pool it adds into the host gradient pages, so it must not
+ * run while those pages are staged in device slots (the write-back would
+ * overwrite the sum); a later gradient prefetch is ordered after it.
+ * PKV_ERR_INVALID for a bad range or misaligned buffer. */
+pkv_status pkv_grad_accumulate(pkv_seq* seq, int64_t row0, int64_t n_rows, const float* dk,
+                               const float* dv, void* stream);
+
 /* Copies the sequence's pages in logical order into contiguous device
  * buffers [len, Hkv, d]: any of the outputs may be NULL. k/v in pool dtype,
  * dk/dv float32, rep [n_pages, Hkv, d] float32. For tests and for handing

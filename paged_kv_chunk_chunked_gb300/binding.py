@@ -70,6 +70,7 @@ _SIGS = {
     "pkv_grad_zero": (_ST, [_P, _P]),
     "pkv_gather": (_ST, [_P, _P, _P, _P, _P, _P, _P]),
     "pkv_gather_rows": (_ST, [_P, _I64, _I64, _P, _P, _P, _P, _P]),
+    "pkv_grad_accumulate": (_ST, [_P, _I64, _I64, _P, _P, _P]),
     "pkv_page_topk": (_ST, [_P, _P, _I64, _I64, _I32, _I32, _I32, _P, _P, _P]),
     "pkv_prefetch": (_ST, [_P, _P, _I64, _I32, _P]),
     "pkv_writeback_grads": (_ST, [_P, _P]),
@@ -228,6 +229,10 @@ def pkv_chunk_attn_bwd_noalloc(seq, q, o, dout, lse, q_start, n_q, dq, sel=None,
 
 def pkv_grad_zero(seq, stream=None) -> None:
     _check(lib().pkv_grad_zero(seq, stream_ptr(stream)))
+
+
+def pkv_grad_accumulate(seq, row0, n_rows, dk=None, dv=None, stream=None) -> None:
+    _check(lib().pkv_grad_accumulate(seq, row0, n_rows, ptr(dk), ptr(dv), stream_ptr(stream)))
 
 
 def pkv_gather(seq, k=None, v=None, dk=None, dv=None, rep=None, stream=None) -> None:

@@ -592,6 +592,25 @@ pkv_status pkv_grad_zero(pkv_seq* s, void* stream) {
     return PKV_OK;
 }
 
+pkv_status pkv_grad_accumulate(pkv_seq* s, int64_t row0, int64_t n_rows, const float* dk,
+                               const float* dv, void* stream) {
+    if (!s) return fail(PKV_ERR_INVALID, "pkv_grad_accumulate: seq is NULL");
+    if (!is_device(s->pool)) return fail(PKV_ERR_INVALID, "pkv_grad_accumulate: META pool");
+    if (row0 < 0 || n_rows < 0 || row0 + n_rows > s->len)
+        return fail(PKV_ERR_INVALID, "pkv_grad_accumulate: need 0 <= row0 and row0 + n_rows <= length");
+    if ((reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) & 15)
+        return fail(PKV_ERR_INVALID, "pkv_grad_accumulate: dk and dv must be 16-byte aligned");
+    if (n_rows == 0 || (!dk && !dv)) return PKV_OK;
+    pkv_status st = check_stream_device(s->pool);
+    if (st != PKV_OK) return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_grad_accumulate(s->pool, s->d_bt, row0, n_rows, dk, dv, cs);
+    // A later gradient prefetch of a host pool copies these pages: order it after.
+    if (e == cudaSuccess && s->used) e = cudaEventRecord(s->used, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_grad_accumulate: launch");
+    return PKV_OK;
+}
+
 pkv_status pkv_gather(const pkv_seq* s, void* k, void* v, float* dk, float* dv, float* rep,
                       void* stream) {
     if (!s) return fail(PKV_ERR_INVALID, "pkv_gather: seq is NULL");

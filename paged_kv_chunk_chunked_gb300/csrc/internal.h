@@ -104,6 +104,10 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 // Zero the gradient rows of the given logical pages range [p0, p1).
 cudaError_t launch_grad_zero(const pkv_pool* pool, const int32_t* d_bt, int64_t p0, int64_t p1,
                              cudaStream_t s);
+// Contiguous fp32 rows [row0, row0 + n_rows) x Hkv x d added into the gradient pages.
+cudaError_t launch_grad_accumulate(const pkv_pool* pool, const int32_t* d_bt, int64_t row0,
+                                   int64_t n_rows, const float* dk, const float* dv,
+                                   cudaStream_t s);
 // Logical pages [lp0, ceil(len / P)) -> outputs starting at row lp0 * P.
 cudaError_t launch_gather(const pkv_pool* pool, const int32_t* d_bt, int64_t lp0, int64_t len,
                           void* k, void* v, float* dk, float* dv, float* rep, cudaStream_t s);

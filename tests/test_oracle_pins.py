@@ -250,3 +250,24 @@ def test_synth_bf16_rounding_is_nearest_even():
     np.testing.assert_array_equal(r, np.array([1.0, 1.0, 1.0078125, 1.0078125, -2.0], np.float32))
     t = torch.tensor(x).to(torch.bfloat16).float().numpy()
     np.testing.assert_array_equal(r, t)
+
+
+def test_paged_gradient_accumulation_equals_contiguous_sums():
+    """scatter_rows(accumulate=True) through a permuted block table, read back in
+    logical order, equals the same additions on a contiguous [N, Hkv, d] array;
+    rows outside every range and physical pages outside the table stay zero.
+    In float32 each element takes exactly one rounded addition per call."""
+    P, Hkv, d, n_pages, extra = 16, 2, 8, 10, 3
+    N = n_pages * P - 5                                   # partial last page
+    bt = np.random.default_rng(7).permutation(n_pages + extra)[:n_pages].astype(np.int32)
+    pool = np.zeros((n_pages + extra, Hkv, P, d), np.float32)
+    flat = np.zeros((N, Hkv, d), np.float32)
+    for i, (r0, n) in enumerate([(0, N), (37, 60), (3 * P - 1, 2), (N - 1, 1), (20, 90)]):
+        delta = np.random.default_rng(100 + i).standard_normal((n, Hkv, d)).astype(np.float32)
+        orc.scatter_rows(pool, bt, r0, delta, P, accumulate=True)
+        flat[r0:r0 + n] = flat[r0:r0 + n] + delta
+    np.testing.assert_array_equal(orc.logical_rows(pool, bt, N, P), flat)
+    unused = np.setdiff1d(np.arange(n_pages + extra), bt)
+    assert not pool[unused].any()
+    assert not pool[bt[-1], :, P - 5:].any()             # rows beyond the sequence
+    assert pool.dtype == np.float32
