@@ -656,7 +656,8 @@ pkv_status pkv_page_topk(pkv_seq* s, const void* q, int64_t q_start, int64_t n_q
                                              " candidate pages");
     pkv_status st = check_stream_device(p);
     if (st != PKV_OK) return st;
-    const size_t need = (size_t)n_qp * p->desc.n_kv_heads * p->desc.head_dim;
+    const size_t need = page_topk_scratch_floats(q_start, n_q, (int)P, p->desc.n_kv_heads,
+                                                 p->desc.head_dim, n_sink, n_local);
     if (p->sel_scratch_floats < need) {
         cudaError_t e = cudaDeviceSynchronize();
         if (e != cudaSuccess) return cuda_fail(e, "pkv_page_topk: sync");

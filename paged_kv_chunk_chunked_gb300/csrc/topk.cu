@@ -15,11 +15,16 @@
 // Kernel 1 (qbar): one CTA per (query page, KV head); reads the page's
 //   P x g query rows (g*d contiguous elements per token) with 16-byte loads and
 //   reduces in fp32. This is the HBM-bound part: it reads the whole chunk's Q.
-// Kernel 2 (select): one CTA per (query page, KV head); one warp per candidate
-//   scores it with a coalesced 512-byte read of the representative, packs
-//   (score, page) into one 64-bit key whose ascending order is the selection
-//   order, sorts the keys in shared memory (bitonic), and compacts the chosen
-//   pages in ascending order.
+// Kernel 2 (score): one CTA per (tile of 64 candidate pages, KV head) reads
+//   the tile's representatives once and scores them against every query page
+//   of the chunk (a [n_qp x d] x [d x 64] product in fp32 on the CUDA cores:
+//   64 query pages x 2048 pages x 128 is 17 MFLOP per head, too small for a
+//   tensor-core pipeline to pay), so each representative leaves L2 once per
+//   chunk instead of once per query page.
+// Kernel 3 (select): one CTA per (query page, KV head) reads its score row,
+//   packs (score, page) into one 64-bit key whose ascending order is the
+//   selection order, sorts the keys in shared memory (bitonic), and compacts
+//   the chosen pages in ascending order.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -90,22 +95,85 @@ __device__ __forceinline__ uint32_t orderable(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+constexpr int kScoreThreads = 256;
+constexpr int kScoreTile = 64;            // candidate pages per CTA
+constexpr int kScoreQpMax = 16;           // query pages held in shared memory at once
+
+// scores[h][qp][c] = qbar[qp, h, :] . rep[bt[n_sink + c], h, :] for the tile's
+// candidates c. The tile's representatives are stored transposed ([k][c]), so
+// thread t, which scores candidate t % 64 against query pages t / 64,
+// t / 64 + 4, ..., reads them without bank conflicts; a warp shares its query
+// pages, whose rows are read as broadcasts.
+template <int D>
+__global__ void __launch_bounds__(kScoreThreads) score_kernel(const float* qbar, const float* rep,
+        const int32_t* bt, int64_t num_phys, int Hkv, int n_qp, int64_t c_lo, int n_cand,
+        int stride, float* scores, int* err) {
+    __shared__ float rt[D][kScoreTile];
+    __shared__ __align__(16) float qs[kScoreQpMax][D];
+    const int h = blockIdx.y, c0 = blockIdx.x * kScoreTile;
+    const int tid = threadIdx.x;
+    for (int i = tid; i < kScoreTile * (D / 4); i += kScoreThreads) {
+        const int c = i % kScoreTile, k4 = i / kScoreTile;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c0 + c < n_cand) {
+            const int32_t pp = bt[c_lo + c0 + c];
+            if (pp >= 0 && pp < num_phys)
+                v = reinterpret_cast<const float4*>(rep + ((size_t)pp * Hkv + h) * D)[k4];
+            else if (k4 == 0)
+                report_error(err, kErrBadPage);
+        }
+        rt[4 * k4][c] = v.x; rt[4 * k4 + 1][c] = v.y; rt[4 * k4 + 2][c] = v.z; rt[4 * k4 + 3][c] = v.w;
+    }
+    constexpr int G = kScoreThreads / kScoreTile;            // query-page groups
+    constexpr int QPT = kScoreQpMax / G;                      // query pages per thread and pass
+    const int c = tid % kScoreTile, g0 = tid / kScoreTile;
+    for (int qb = 0; qb < n_qp; qb += kScoreQpMax) {
+        const int nq = min(kScoreQpMax, n_qp - qb);
+        __syncthreads();                                      // rt ready; qs free
+        for (int i = tid; i < kScoreQpMax * (D / 4); i += kScoreThreads) {
+            const int r = i / (D / 4), k4 = i % (D / 4);
+            reinterpret_cast<float4*>(qs[r])[k4] =
+                r < nq ? reinterpret_cast<const float4*>(qbar + ((size_t)(qb + r) * Hkv + h) * D)[k4]
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        __syncthreads();
+        float acc[QPT];
+#pragma unroll
+        for (int j = 0; j < QPT; ++j) acc[j] = 0.f;
+#pragma unroll 4
+        for (int k = 0; k < D; k += 4) {
+            const float r0 = rt[k][c], r1 = rt[k + 1][c], r2 = rt[k + 2][c], r3 = rt[k + 3][c];
+#pragma unroll
+            for (int j = 0; j < QPT; ++j) {
+                const float4 qv = reinterpret_cast<const float4*>(qs[g0 + j * G])[k / 4];
+                acc[j] = fmaf(qv.x, r0, acc[j]);
+                acc[j] = fmaf(qv.y, r1, acc[j]);
+                acc[j] = fmaf(qv.z, r2, acc[j]);
+                acc[j] = fmaf(qv.w, r3, acc[j]);
+            }
+        }
+        if (c0 + c < n_cand) {
+#pragma unroll
+            for (int j = 0; j < QPT; ++j) {
+                const int r = g0 + j * G;
+                if (r < nq) scores[((size_t)h * n_qp + qb + r) * stride + c0 + c] = acc[j];
+            }
+        }
+    }
+}
+
 struct SelArgs {
-    const float* qbar;        // [n_qp, Hkv, D]
-    const float* rep;         // [num_phys, Hkv, D]
-    const int32_t* bt;
-    int64_t num_phys;
-    int Hkv, D;
+    const float* scores;      // [Hkv, n_qp, stride]
+    int stride, n_qp;
+    int Hkv;
     int64_t qp0;              // q_start / P
     int K, n_sink, n_local, kmax;
     int32_t* out;             // [n_qp, Hkv, kmax]
     int32_t* counts;          // [n_qp, Hkv] or null
-    int* err;
 };
 
 __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
     extern __shared__ uint64_t keys[];             // [n_pow2] sort keys; reused as flags
-    __shared__ float qb[128];
     __shared__ int scan[kSelThreads];
     const int qp = blockIdx.x, h = blockIdx.y;
     const int64_t qpg = a.qp0 + qp;                // query page index in the sequence
@@ -113,31 +181,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
     const int n_cand = (int)max64(0, c_hi - c_lo + 1);
     int n_pow2 = 1;
     while (n_pow2 < n_cand) n_pow2 <<= 1;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid < a.D) qb[tid] = a.qbar[((size_t)qp * a.Hkv + h) * a.D + tid];
-    __syncthreads();
-
-    // Scores: one warp per candidate, lane l reads floats 4l..4l+3 of the rep row.
-    for (int c = warp; c < n_pow2; c += kSelThreads / 32) {
+    const int tid = threadIdx.x;
+    const float* srow = a.scores + ((size_t)h * a.n_qp + qp) * a.stride;
+    for (int c = tid; c < n_pow2; c += kSelThreads) {
         uint64_t key = ~0ull;                      // padding sorts last
-        if (c < n_cand) {
-            const int64_t page = c_lo + c;
-            const int32_t pp = a.bt[page];
-            float s = 0.f;
-            if (pp >= 0 && pp < a.num_phys) {
-                const float* row = a.rep + ((size_t)pp * a.Hkv + h) * a.D;
-                for (int k = lane * 4; k < a.D; k += 128) {
-                    const float4 r = *reinterpret_cast<const float4*>(row + k);
-                    s += r.x * qb[k] + r.y * qb[k + 1] + r.z * qb[k + 2] + r.w * qb[k + 3];
-                }
-            } else if (lane == 0) {
-                report_error(a.err, kErrBadPage);
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-            key = ((uint64_t)(~orderable(s)) << 32) | (uint32_t)page;
-        }
-        if (lane == 0) keys[c] = key;
+        if (c < n_cand) key = ((uint64_t)(~orderable(srow[c])) << 32) | (uint32_t)(c_lo + c);
+        keys[c] = key;
     }
     __syncthreads();
 
@@ -215,13 +264,28 @@ cudaError_t launch_page_topk(const pkv_pool* p, const int32_t* d_bt, const void*
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    SelArgs a{};
-    a.qbar = qbar; a.rep = p->rep; a.bt = d_bt; a.num_phys = p->desc.num_phys_pages;
-    a.Hkv = Hkv; a.D = D; a.qp0 = q_start / P; a.K = K; a.n_sink = n_sink; a.n_local = n_local;
-    a.kmax = K + n_sink + n_local; a.out = out; a.counts = counts; a.err = p->d_err;
-    // Largest candidate count of the chunk (its last query page) sizes the sort buffer.
+    // Largest candidate count of the chunk (its last query page) sizes the
+    // score rows and the sort buffer.
     const int64_t last_qpg = q_start / P + n_qp - 1;
     const int64_t n_cand = std::max<int64_t>(0, last_qpg - n_local - n_sink + 1);
+    const int stride = (int)((n_cand + 3) / 4 * 4);
+    float* scores = qbar + n_qp * Hkv * D;
+    if (n_cand > 0) {
+        dim3 sgrid((unsigned)((n_cand + kScoreTile - 1) / kScoreTile), Hkv);
+        ProfScope ps("score_kernel", s);
+        if (D == 128)
+            score_kernel<128><<<sgrid, kScoreThreads, 0, s>>>(qbar, p->rep, d_bt, p->desc.num_phys_pages,
+                    Hkv, (int)n_qp, n_sink, (int)n_cand, stride, scores, p->d_err);
+        else
+            score_kernel<64><<<sgrid, kScoreThreads, 0, s>>>(qbar, p->rep, d_bt, p->desc.num_phys_pages,
+                    Hkv, (int)n_qp, n_sink, (int)n_cand, stride, scores, p->d_err);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    SelArgs a{};
+    a.scores = scores; a.stride = stride; a.n_qp = (int)n_qp;
+    a.Hkv = Hkv; a.qp0 = q_start / P; a.K = K; a.n_sink = n_sink; a.n_local = n_local;
+    a.kmax = K + n_sink + n_local; a.out = out; a.counts = counts;
     int64_t n_pow2 = 1;
     while (n_pow2 < n_cand) n_pow2 <<= 1;
     const size_t smem = std::max<size_t>((size_t)n_pow2 * 8, (size_t)(last_qpg + 1));
@@ -238,5 +302,12 @@ cudaError_t launch_page_topk(const pkv_pool* p, const int32_t* d_bt, const void*
 }
 
 int64_t page_topk_max_candidates() { return kMaxCand; }
+
+size_t page_topk_scratch_floats(int64_t q_start, int64_t n_q, int P, int Hkv, int D, int n_sink,
+                                int n_local) {
+    const int64_t n_qp = (n_q + P - 1) / P;
+    const int64_t n_cand = std::max<int64_t>(0, q_start / P + n_qp - 1 - n_local - n_sink + 1);
+    return (size_t)n_qp * Hkv * D + (size_t)Hkv * n_qp * ((n_cand + 3) / 4 * 4);
+}
 
 }  // namespace pkv
