@@ -488,7 +488,7 @@ def run_sparse(args, world, rank):
     pkv_build.build()
     B.lib()
     w = synth.workload(args.workload)
-    K, ns, nl = w.topk
+    K, ns, nl = w.topk if w.topk else (0,) + tuple(w.local)
     sw = ChunkSweep(w, flags=args.flags).load_inputs()
     stream = torch.cuda.current_stream()
     n = w.n_chunks
@@ -500,7 +500,9 @@ def run_sparse(args, world, rank):
         for c in range(n):
             s, e = w.chunk_range(c)
             B.pkv_append(sw.seq, sw.k[c], sw.v[c], e - s, stream)
-            if sparse:
+            if sparse and w.local:
+                B.pkv_page_local(sw.seq, s, e - s, ns, nl, sels[c], None, stream)
+            elif sparse:
                 B.pkv_page_topk(sw.seq, sw.q[c], s, e - s, K, ns, nl, sels[c], None, stream)
             B.pkv_chunk_attn_fwd(sw.seq, sw.q[c], s, e - s, sw.o[c], sw.lse[c],
                                  sels[c] if sparse else None, stream)
@@ -554,13 +556,14 @@ def run_sparse(args, world, rank):
     dom_cnt, dom_ms = prof[dom]
     dom_flops = units.get(dom, 0) * w.d * pairs * args.steps
     dom_ach = dom_flops / (dom_ms * 1e-3) / 1e12 if dom in units else None
-    return {
+    out = {
         "metric": METRIC, "value": round(tflops, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded clustered keys, N(0,1) Q/V/dO, bf16-rounded)",
+        "data": f"synthetic (seeded {w.keys} keys, N(0,1) Q/V/dO, bf16-rounded)",
         "config": {"workload": w.name, "N": w.N, "C": w.C, "P": w.P, "Hq": w.Hq, "Hkv": w.Hkv,
-                   "d": w.d, "topk": list(w.topk), "block_table": w.table,
+                   "d": w.d, **({"topk": list(w.topk)} if w.topk else {"local": list(w.local)}),
+                   "block_table": w.table,
                    "flops": "14*d*attended pairs (from the selections)"},
         "attended_pairs_per_step": pairs,
         "dense_pairs": w.Hq * pairs_dense(w.N),
@@ -573,15 +576,18 @@ def run_sparse(args, world, rank):
                      "frac": round(dom_ach / peak_tc, 4) if dom_ach else None,
                      "flops_per_launch": dom_flops / max(dom_cnt, 1),
                      "peak_kind": f"{pk_kind} bf16_tflops_sustained", "traffic": None},
-        # page scoring: the page-query kernel reads the chunk's Q once (HBM-bound)
-        "page_query_roofline": {"bound": "hbm", "kernel": "qbar_kernel", "unit": "GB/s",
-                                "achieved": round(qbar_gbs, 1), "peak": pk["hbm_gbs"],
-                                "frac": round(qbar_gbs / pk["hbm_gbs"], 4),
-                                "bytes_per_launch": q_bytes, "peak_kind": f"{pk_kind} hbm_gbs"},
-        "select_kernel_us_per_launch": round(1e3 * sel_ms / sel_cnt, 2),
         "kernels": kernels, "gpu_launches": sum(v[0] for v in prof.values()),
         "clocks": clk,
     }
+    if "qbar_kernel" in prof:
+        # page scoring: the page-query kernel reads the chunk's Q once (HBM-bound)
+        out["page_query_roofline"] = {
+            "bound": "hbm", "kernel": "qbar_kernel", "unit": "GB/s",
+            "achieved": round(qbar_gbs, 1), "peak": pk["hbm_gbs"],
+            "frac": round(qbar_gbs / pk["hbm_gbs"], 4),
+            "bytes_per_launch": q_bytes, "peak_kind": f"{pk_kind} hbm_gbs"}
+        out["select_kernel_us_per_launch"] = round(1e3 * sel_ms / sel_cnt, 2)
+    return out
 
 
 def run_offload(args, world, rank):
@@ -811,7 +817,7 @@ def main():
         out = run_offload_dense(args, world, rank)
     elif wl.offload:
         out = run_offload(args, world, rank)
-    elif wl.topk:
+    elif wl.topk or wl.local:
         out = run_sparse(args, world, rank)
     else:
         out = run_pkv(args, world, rank)

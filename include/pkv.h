@@ -271,6 +271,20 @@ pkv_status pkv_page_topk(pkv_seq* seq, const void* q, int64_t q_start, int64_t n
                          int32_t n_sink, int32_t n_local, int32_t* pages_out,
                          int32_t* counts_out, void* stream);
 
+/* Page lists of a local attention layer: natively sparse models use local
+ * attention layers instead of a page scorer ("Out of the Memory Barrier",
+ * gist.science/nl "Pagina-niveau Sparse Attention"). Page granular: query page
+ * qp_glob of the chunk sees the sink pages [0, n_sink) and the local pages
+ * qp_glob-n_local+1 .. qp_glob (causal inside its own page), the same list
+ * for every KV head. Writes pages_out (device int32 [n_qp, Hkv,
+ * n_sink+n_local], ascending, -1 padded) and, if not NULL, counts_out (device
+ * int32 [n_qp, Hkv]) in the format pkv_page_topk writes, so the attention
+ * calls and pkv_prefetch take it as a selection. Reads neither queries nor
+ * representatives. q_start and n_q as for attention; n_sink >= 0,
+ * n_local >= 1, else PKV_ERR_INVALID. */
+pkv_status pkv_page_local(pkv_seq* seq, int64_t q_start, int64_t n_q, int32_t n_sink,
+                          int32_t n_local, int32_t* pages_out, int32_t* counts_out, void* stream);
+
 /* ---------------------------------------------------------------- host offload (a7)
  * For PINNED_HOST pools the K/V pages and their fp32 gradient pages live in
  * mapped pinned host memory (appends write them there; pkv_gather and

@@ -33,7 +33,9 @@ repository's design notes):
   page, page query = mean over the query page's tokens and the g heads of a
   KV group;  R7 one selection per (query page, KV head);  R8 sink = pages
   [0, n_sink), local = the n_local pages ending at the query page, candidates =
-  every page in between;  R13 score ties go to the lower page index.
+  every page in between;  R13 score ties go to the lower page index;
+  R16 local attention layers are page-granular: the query page, the n_local - 1
+  pages before it and the sink pages.
 
 Every function here is pinned by tests in ``tests/test_oracle_*.py`` against
 something other than itself (library attention, finite differences, closed
@@ -273,6 +275,36 @@ def chunk_selection(q_chunk: np.ndarray, q_start: int, k_logical: np.ndarray,
     return lists, padded
 
 
+def local_pages(qp: int, n_sink: int, n_local: int) -> list:
+    """Visible pages of global query page qp in a local attention layer.
+
+    The pages use local attention layers, not a scorer, for natively sparse
+    models (gist.science/nl "Pagina-niveau Sparse Attention"). Read at page
+    granularity (R16): the query page itself (causal inside), the n_local - 1
+    pages before it, and the sink pages [0, n_sink); sorted ascending."""
+    keep = set(range(0, min(n_sink, qp + 1)))
+    keep |= set(range(max(0, qp - n_local + 1), qp + 1))
+    return sorted(keep)
+
+
+def chunk_local_selection(q_start: int, n_q: int, n_kv_heads: int, page_size: int,
+                          n_sink: int, n_local: int):
+    """local_pages for every query page of a chunk, the same list for every KV
+    head. Returns (lists, padded) as chunk_selection does, padded being int32
+    [n_qp, Hkv, n_sink + n_local]."""
+    if q_start % page_size:
+        raise ValueError("chunks start on page boundaries")
+    n_qp = (n_q + page_size - 1) // page_size
+    qp0 = q_start // page_size
+    padded = np.full((n_qp, n_kv_heads, n_sink + n_local), -1, np.int32)
+    lists = []
+    for i in range(n_qp):
+        sel = local_pages(qp0 + i, n_sink, n_local)
+        padded[i, :, :len(sel)] = sel
+        lists.append([sel] * n_kv_heads)
+    return lists, padded
+
+
 def page_allowed_from_lists(lists: Sequence, n_pages: int) -> np.ndarray:
     """[n_qp, Hkv, n_pages] bool mask from per-(query page, KV head) page lists."""
     n_qp, Hkv = len(lists), len(lists[0])
@@ -286,7 +318,7 @@ def page_allowed_from_lists(lists: Sequence, n_pages: int) -> np.ndarray:
 # --------------------------------------------------------------------------- chunk recurrence
 
 def chunk_recurrent_step(qs, ks, vs, dos, block_table, page_size: int, n_phys: int,
-                         topk: Optional[tuple] = None):
+                         topk: Optional[tuple] = None, local: Optional[tuple] = None):
     """One training step of one attention layer, chunk by chunk (gist.science/de §2.A).
 
     qs/ks/vs/dos are lists of per-chunk arrays. Forward: for c = 0, 1, ...
@@ -294,7 +326,8 @@ def chunk_recurrent_step(qs, ks, vs, dos, block_table, page_size: int, n_phys: i
     key so far. Backward (R4: reverse chunk order): recompute from the saved
     O/LSE, write dQ and add dK/dV into the paged gradient pools in place.
     With ``topk`` = (K, n_sink, n_local) each chunk attends only to the pages
-    selected for its query pages. Returns a dict of per-chunk outputs and the
+    selected for its query pages; with ``local`` = (n_sink, n_local) only to
+    its local pages (local_pages). Returns a dict of per-chunk outputs and the
     final pools (physical layout [n_phys, Hkv, P, d])."""
     Hkv, d = ks[0].shape[1], ks[0].shape[2]
     P = page_size
@@ -314,6 +347,10 @@ def chunk_recurrent_step(qs, ks, vs, dos, block_table, page_size: int, n_phys: i
         allowed = None
         if topk is not None:
             lists, padded = chunk_selection(qs[c], st, k_log, P, *topk)
+            allowed = page_allowed_from_lists(lists, (L + P - 1) // P)
+            sels.append(padded)
+        elif local is not None:
+            lists, padded = chunk_local_selection(st, qs[c].shape[0], Hkv, P, *local)
             allowed = page_allowed_from_lists(lists, (L + P - 1) // P)
             sels.append(padded)
         o, lse = attention_forward(qs[c], k_log, v_log, st, P, allowed)

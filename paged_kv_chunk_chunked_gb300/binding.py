@@ -71,6 +71,7 @@ _SIGS = {
     "pkv_gather": (_ST, [_P, _P, _P, _P, _P, _P, _P]),
     "pkv_gather_rows": (_ST, [_P, _I64, _I64, _P, _P, _P, _P, _P]),
     "pkv_grad_accumulate": (_ST, [_P, _I64, _I64, _P, _P, _P]),
+    "pkv_page_local": (_ST, [_P, _I64, _I64, _I32, _I32, _P, _P, _P]),
     "pkv_page_topk": (_ST, [_P, _P, _I64, _I64, _I32, _I32, _I32, _P, _P, _P]),
     "pkv_prefetch": (_ST, [_P, _P, _I64, _I32, _P]),
     "pkv_writeback_grads": (_ST, [_P, _P]),
@@ -248,6 +249,12 @@ def pkv_page_topk(seq, q, q_start, n_q, k, n_sink, n_local, pages_out, counts_ou
                   stream=None) -> None:
     _check(lib().pkv_page_topk(seq, ptr(q), q_start, n_q, k, n_sink, n_local, ptr(pages_out),
                                ptr(counts_out), stream_ptr(stream)))
+
+
+def pkv_page_local(seq, q_start, n_q, n_sink, n_local, pages_out, counts_out=None,
+                   stream=None) -> None:
+    _check(lib().pkv_page_local(seq, q_start, n_q, n_sink, n_local, ptr(pages_out),
+                                ptr(counts_out), stream_ptr(stream)))
 
 
 def pkv_prefetch(seq, logical_pages=None, n=0, what=3, side=None) -> None:

@@ -676,6 +676,28 @@ pkv_status pkv_page_topk(pkv_seq* s, const void* q, int64_t q_start, int64_t n_q
     return PKV_OK;
 }
 
+pkv_status pkv_page_local(pkv_seq* s, int64_t q_start, int64_t n_q, int32_t n_sink,
+                          int32_t n_local, int32_t* pages_out, int32_t* counts_out, void* stream) {
+    if (!s || !pages_out) return fail(PKV_ERR_INVALID, "pkv_page_local: NULL argument");
+    pkv_pool* p = s->pool;
+    if (!is_device(p)) return fail(PKV_ERR_INVALID, "pkv_page_local: META pool");
+    const int64_t P = p->desc.page_size;
+    if (n_q <= 0 || q_start < 0 || q_start % P != 0 || q_start + n_q > s->len)
+        return fail(PKV_ERR_INVALID, "pkv_page_local: need q_start % P == 0 and q_start + n_q <= length");
+    if (n_sink < 0 || n_local < 1 || (int64_t)n_sink + n_local > (1 << 20))
+        return fail(PKV_ERR_INVALID, "pkv_page_local: need n_sink >= 0 and 1 <= n_local "
+                                     "(the query page itself is always visible)");
+    pkv_status st = check_stream_device(p);
+    if (st != PKV_OK) return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_page_local(q_start, n_q, (int)P, p->desc.n_kv_heads, n_sink, n_local,
+                                      pages_out, counts_out, cs);
+    // A later pkv_prefetch of this selection must wait for it.
+    if (e == cudaSuccess && s->used) e = cudaEventRecord(s->used, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_page_local: launch");
+    return PKV_OK;
+}
+
 static pkv_status host_pool_check(pkv_seq* s, const char* who) {
     if (!s) return fail(PKV_ERR_INVALID, std::string(who) + ": seq is NULL");
     if (s->pool->desc.residency != PKV_RES_PINNED_HOST)

@@ -144,6 +144,8 @@ cudaError_t launch_page_topk(const pkv_pool* p, const int32_t* d_bt, const void*
                              int64_t q_start, int64_t n_q, int K, int n_sink, int n_local,
                              int32_t* out, int32_t* counts, float* qbar, cudaStream_t s);
 int64_t page_topk_max_candidates();
+cudaError_t launch_page_local(int64_t q_start, int64_t n_q, int P, int Hkv, int n_sink,
+                              int n_local, int32_t* out, int32_t* counts, cudaStream_t s);
 // Floats of page-selection scratch: page queries [n_qp, Hkv, d], then scores
 // [Hkv, n_qp, candidates rounded up to 4].
 size_t page_topk_scratch_floats(int64_t q_start, int64_t n_q, int P, int Hkv, int D, int n_sink,

@@ -243,7 +243,40 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a) {
     if (a.counts && tid == 0) a.counts[(size_t)qp * a.Hkv + h] = min(total, a.kmax);
 }
 
+// Local attention layers (gist.science/nl "Pagina-niveau Sparse Attention":
+// natively sparse models use local attention instead of a scorer), page
+// granular: query page qpg sees the sink pages [0, n_sink) and the local pages
+// qpg-n_local+1 .. qpg, ascending, -1 padded; the same list for every KV head.
+// One thread per output entry.
+__global__ void local_kernel(int64_t qp0, int n_qp, int Hkv, int n_sink, int n_local,
+                             int32_t* out, int32_t* counts) {
+    const int kmax = n_sink + n_local;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)n_qp * Hkv * kmax) return;
+    const int j = (int)(i % kmax);
+    const int64_t row = i / kmax;                        // (query page, KV head)
+    const int64_t qpg = qp0 + row / Hkv;
+    const int64_t s_end = min64(n_sink, qpg + 1);        // sink pages [0, s_end)
+    const int64_t l_beg = max64(s_end, qpg - n_local + 1);   // local pages [l_beg, qpg]
+    const int64_t count = s_end + (qpg - l_beg + 1);
+    int64_t page = -1;
+    if (j < s_end) page = j;
+    else if (j < count) page = l_beg + (j - s_end);
+    out[i] = (int32_t)page;
+    if (counts && j == 0) counts[row] = (int32_t)count;
+}
+
 }  // namespace
+
+cudaError_t launch_page_local(int64_t q_start, int64_t n_q, int P, int Hkv, int n_sink,
+                              int n_local, int32_t* out, int32_t* counts, cudaStream_t s) {
+    const int64_t n_qp = (n_q + P - 1) / P;
+    const int64_t total = n_qp * Hkv * (n_sink + n_local);
+    ProfScope ps("local_kernel", s);
+    local_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(q_start / P, (int)n_qp, Hkv,
+                                                                 n_sink, n_local, out, counts);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_page_topk(const pkv_pool* p, const int32_t* d_bt, const void* q, int64_t q_start,
                              int64_t n_q, int K, int n_sink, int n_local, int32_t* out,

@@ -48,6 +48,7 @@ class Workload:
     table: str = "identity"    # "identity" or "perm" (seeded permutation of physical pages)
     keys: str = "normal"       # "normal": K ~ N(0,1); "clustered": page centre N(0,2^2) + N(0,1)
     topk: Optional[tuple] = None   # (K, n_sink, n_local) for the page-sparse variant
+    local: Optional[tuple] = None  # (n_sink, n_local) for a local attention layer
     offload: bool = False          # pools in pinned host memory, pages streamed to HBM
     extra_pages: int = 0           # physical pages beyond the sequence's need
 
@@ -96,6 +97,10 @@ WORKLOADS = {
                                          P=128, Hq=28, Hkv=4, d=128, dtype="bf16",
                                          seed=1239, table="perm", keys="clustered",
                                          topk=(64, 1, 2), offload=True),
+    # Local attention layer (natively sparse models): each query page sees its
+    # own page and the one before it, no sink; 256K context, Qwen2.5-7B shape.
+    "qwen7b_local_256k": Workload("qwen7b_local_256k", N=262144, C=8192, P=128, Hq=28, Hkv=4,
+                                  d=128, dtype="bf16", seed=1240, table="perm", local=(0, 2)),
 }
 
 

@@ -167,6 +167,72 @@ def test_sparse_256k_full_size_sampled():
         sw.close()
 
 
+def test_local_256k_full_size_sampled():
+    """The local-attention workload as bench.py runs it: every chunk's page lists
+    bit-exact, sampled rows of the first and last chunks over their local pages,
+    dK/dV of one page in the middle (seen by its own and the next query page
+    only) against the oracle, and the gradient identities."""
+    w = synth.workload("qwen7b_local_256k")
+    ns, nl = w.local
+    sw = ChunkSweep(w).load_inputs()
+    try:
+        sw.reset()
+        sels = []
+        for c in range(w.n_chunks):
+            s, e = w.chunk_range(c)
+            B.pkv_append(sw.seq, sw.k[c], sw.v[c], e - s)
+            sel = torch.empty(((e - s) // w.P, w.Hkv, ns + nl), dtype=torch.int32, device="cuda")
+            B.pkv_page_local(sw.seq, s, e - s, ns, nl, sel)
+            sels.append(sel)
+            B.pkv_chunk_attn_fwd(sw.seq, sw.q[c], s, e - s, sw.o[c], sw.lse[c], sel)
+        for c in reversed(range(w.n_chunks)):
+            sw.backward(c, sel=sels[c])
+        B.pkv_check(sw.pool)
+        g = sw.gather()
+        for c in range(w.n_chunks):
+            s, e = w.chunk_range(c)
+            _, want = oracle.chunk_local_selection(s, e - s, w.Hkv, w.P, ns, nl)
+            np.testing.assert_array_equal(sels[c].cpu().numpy(), want)
+        K_all, V_all = _logical_kv(w)
+        for c in (0, w.n_chunks - 1):
+            s, e = w.chunk_range(c)
+            allowed = {(i, kv): oracle.local_pages(s // w.P + i, ns, nl)
+                       for i in range((e - s) // w.P) for kv in range(w.Hkv)}
+            _check_rows(w, sw, K_all, V_all, c, heads=(0, 15, w.Hq - 1), n_rows=12,
+                        allowed_pages=allowed)
+        # page p's keys are seen by query pages p .. p + nl - 1 only
+        p = w.n_pages // 2 + 5
+        q0, q1 = p * w.P, (p + nl) * w.P
+        Q = np.concatenate([synth.chunk_q(w, c) for c in range(w.n_chunks)
+                            if w.chunk_range(c)[1] > q0 and w.chunk_range(c)[0] < q1])
+        DO = np.concatenate([synth.chunk_do(w, c) for c in range(w.n_chunks)
+                             if w.chunk_range(c)[1] > q0 and w.chunk_range(c)[0] < q1])
+        c_first = q0 // w.C
+        off = q0 - c_first * w.C
+        Q, DO = Q[off:off + (q1 - q0)], DO[off:off + (q1 - q0)]
+        # no sink pages: these queries see pages p - nl + 1 .. p + nl - 1 only, so
+        # the oracle runs on those keys, positions shifted to start at page b
+        assert ns == 0
+        b = p - nl + 1
+        lists = [[[x - b for x in oracle.local_pages(p + i, ns, nl)]] * w.Hkv for i in range(nl)]
+        allowed = oracle.page_allowed_from_lists(lists, p + nl - b)
+        Kw, Vw = K_all[b * w.P:q1], V_all[b * w.P:q1]
+        o, lse = oracle.attention_forward(Q, Kw, Vw, q0 - b * w.P, w.P, allowed)
+        _, dk, dv = oracle.attention_backward(Q, Kw, Vw, o, DO, lse, q0 - b * w.P, w.P, allowed)
+        rows = slice((p - b) * w.P, (p - b + 1) * w.P)
+        grow = slice(p * w.P, (p + 1) * w.P)
+        assert _rel(to_numpy(g["dk"])[grow], dk[rows]) <= 2e-2
+        assert _rel(to_numpy(g["dv"])[grow], dv[rows]) <= 2e-2
+        dos_sum = np.zeros((w.Hkv, w.d))
+        for c in range(w.n_chunks):
+            do = synth.chunk_do(w, c).astype(np.float64)
+            for kv in range(w.Hkv):
+                dos_sum[kv] += do[:, kv * w.g:(kv + 1) * w.g].sum((0, 1))
+        _check_identities(w, g, dos_sum)
+    finally:
+        sw.close()
+
+
 def test_sparse_1m_pinned_host_full_size_sampled():
     """The 1M-token pinned-host workload as bench.py runs it: every K/V page and
     fp32 gradient page in mapped pinned host memory, the last chunk's selected

@@ -97,10 +97,11 @@ def test_page_topk_matches_oracle(dtype, P, d, K):
 
 
 def _sparse_sweep(w, use_oracle_selection: bool, flags=0):
-    K, ns, nl = w.topk
+    K, ns, nl = w.topk if w.topk else (0,) + tuple(w.local)
     qs, ks, vs, dos = _inputs(w)
     bt = synth.block_table(w)
-    ref = oracle.chunk_recurrent_step(qs, ks, vs, dos, bt, w.P, w.n_phys, topk=w.topk)
+    ref = oracle.chunk_recurrent_step(qs, ks, vs, dos, bt, w.P, w.n_phys, topk=w.topk,
+                                      local=w.local)
     sw = ChunkSweep(w, flags=flags).load_inputs()
     try:
         sw.reset()
@@ -112,6 +113,11 @@ def _sparse_sweep(w, use_oracle_selection: bool, flags=0):
             n_qp = (e - s + w.P - 1) // w.P
             if use_oracle_selection:
                 sel = torch.from_numpy(ref["sel"][c]).cuda()
+            elif w.local:
+                sel = torch.full((n_qp, w.Hkv, ns + nl), 9, dtype=torch.int32, device="cuda")
+                B.pkv_page_local(sw.seq, s, e - s, ns, nl, sel)
+                torch.cuda.synchronize()
+                np.testing.assert_array_equal(sel.cpu().numpy(), ref["sel"][c])
             else:
                 sel = torch.empty((n_qp, w.Hkv, K + ns + nl), dtype=torch.int32, device="cuda")
                 B.pkv_page_topk(sw.seq, sw.q[c], s, e - s, K, ns, nl, sel)
@@ -184,3 +190,49 @@ def test_sparse_with_all_pages_equals_dense_on_gpu():
         assert _rel(to_numpy(sw.gather()["dk"]), dense[1]) < 1e-6
     finally:
         sw.close()
+
+
+# ---------------------------------------------------------------- local attention layers
+
+@pytest.mark.parametrize("N,C,ns,nl", [(2048, 1024, 0, 2), (1900, 1024, 1, 2), (3000, 1024, 2, 5),
+                                       (640, 256, 0, 1), (1024, 512, 0, 64)])
+def test_page_local_lists_bit_exact(N, C, ns, nl):
+    """pkv_page_local writes the oracle's local page lists and counts exactly
+    (partial last query page, windows reaching page 0, windows wider than the
+    sequence), and ignores the previous contents of the output."""
+    w = _w(N=N, C=C, topk=None, local=(ns, nl))
+    sw = ChunkSweep(w).load_inputs([])
+    try:
+        sw.reset()
+        for c in range(w.n_chunks):
+            s, e = w.chunk_range(c)
+            k = torch.zeros((e - s, w.Hkv, w.d), dtype=torch.bfloat16, device="cuda")
+            B.pkv_append(sw.seq, k, k, e - s)
+            n_qp = (e - s + w.P - 1) // w.P
+            sel = torch.full((n_qp, w.Hkv, ns + nl), 5, dtype=torch.int32, device="cuda")
+            cnt = torch.full((n_qp, w.Hkv), 77, dtype=torch.int32, device="cuda")
+            B.pkv_page_local(sw.seq, s, e - s, ns, nl, sel, cnt)
+            torch.cuda.synchronize()
+            _, want = oracle.chunk_local_selection(s, e - s, w.Hkv, w.P, ns, nl)
+            np.testing.assert_array_equal(sel.cpu().numpy(), want)
+            np.testing.assert_array_equal(cnt.cpu().numpy(), (want >= 0).sum(-1))
+        with pytest.raises(B.PkvError):
+            B.pkv_page_local(sw.seq, 0, 128, 0, 0, sel)
+        with pytest.raises(B.PkvError):
+            B.pkv_page_local(sw.seq, 64, 128, 0, 2, sel)
+        B.pkv_check(sw.pool)
+    finally:
+        sw.close()
+
+
+@pytest.mark.parametrize("kw", [dict(local=(0, 2)), dict(local=(1, 2), N=1900),
+                                dict(local=(0, 1), N=1536, C=512)])
+def test_local_attention_tensor_cores(kw):
+    base = dict(topk=None, keys="normal")
+    base.update(kw)
+    _sparse_sweep(_w(**base), use_oracle_selection=False)
+
+
+def test_local_attention_cuda_cores():
+    _sparse_sweep(_w(dtype="f32", P=16, d=64, N=512, C=256, topk=None, local=(1, 3)),
+                  use_oracle_selection=False)

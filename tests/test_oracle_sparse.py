@@ -183,3 +183,70 @@ def test_padded_selection_layout():
             assert list(padded[i, h, :n]) == lists[i][h]
             assert (padded[i, h, n:] == -1).all()
             assert lists[i][h][-1] == 4 + i    # own page is always last
+
+
+# ---------------------------------------------------------------- local attention layers
+
+@pytest.mark.parametrize("n_sink,n_local", [(0, 1), (0, 2), (1, 2), (3, 4), (2, 1)])
+def test_local_pages_counts_and_order(n_sink, n_local):
+    """Closed forms: |list| = min(qp + 1, n_sink + n_local); the query page is
+    last; a window reaching page 0 gives every page; K = 0 top-K gives the same
+    list (nothing to score)."""
+    rep, qb = np.zeros((40, 4)), np.ones(4)
+    for qp in range(40):
+        got = orc.local_pages(qp, n_sink, n_local)
+        assert len(got) == min(qp + 1, n_sink + n_local)
+        assert got == sorted(set(got)) and got[-1] == qp
+        if qp < n_sink + n_local:
+            assert got == list(range(qp + 1))
+        else:
+            assert got[:n_sink] == list(range(n_sink))
+            assert got[n_sink:] == list(range(qp - n_local + 1, qp + 1))
+        assert got == orc.select_pages(qb, rep, qp, 0, n_sink, n_local)
+
+
+def test_local_one_page_equals_blockwise_library_attention():
+    """n_local = 1, no sink: every query attends causally inside its own page only,
+    i.e. independent causal attention per P-token block (library attention, fp64),
+    forward and backward (autograd), through the paged chunk recurrence."""
+    w = _sparse_w(N=96, C=32, P=16, Hq=4, Hkv=2, d=8, keys="normal")
+    qs, ks, vs, dos = _inputs(w)
+    bt = synth.block_table(w)
+    res = orc.chunk_recurrent_step(qs, ks, vs, dos, bt, w.P, w.n_phys, local=(0, 1))
+    q, k, v, do = (np.concatenate(x) for x in (qs, ks, vs, dos))
+    o = np.concatenate(res["o"])
+    dq = np.concatenate(res["dq"])
+    dk = orc.logical_rows(res["dkpool"], bt, w.N, w.P)
+    for b in range(w.N // w.P):
+        sl = slice(b * w.P, (b + 1) * w.P)
+        tq = torch.tensor(q[sl], dtype=torch.float64).permute(1, 0, 2).requires_grad_()
+        tk = torch.tensor(k[sl], dtype=torch.float64).repeat_interleave(w.g, 1).permute(1, 0, 2).requires_grad_()
+        tv = torch.tensor(v[sl], dtype=torch.float64).repeat_interleave(w.g, 1).permute(1, 0, 2)
+        ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True)
+        (ref * torch.tensor(do[sl], dtype=torch.float64).permute(1, 0, 2)).sum().backward()
+        np.testing.assert_allclose(o[sl], ref.permute(1, 0, 2).detach().numpy(), atol=1e-12)
+        np.testing.assert_allclose(dq[sl], tq.grad.permute(1, 0, 2).numpy(), atol=1e-10)
+        dk_ref = tk.grad.permute(1, 0, 2).numpy().reshape(w.P, w.Hkv, w.g, w.d).sum(2)
+        np.testing.assert_allclose(dk[sl], dk_ref, atol=1e-10)
+
+
+def test_local_window_covering_everything_equals_dense():
+    w = _sparse_w()
+    qs, ks, vs, dos = _inputs(w)
+    bt = synth.block_table(w)
+    dense = orc.chunk_recurrent_step(qs, ks, vs, dos, bt, w.P, w.n_phys)
+    local = orc.chunk_recurrent_step(qs, ks, vs, dos, bt, w.P, w.n_phys, local=(0, w.n_pages))
+    for key in ("o", "lse", "dq"):
+        for a, b in zip(dense[key], local[key]):
+            np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(dense["dkpool"], local["dkpool"])
+
+
+def test_local_padded_layout():
+    lists, padded = orc.chunk_local_selection(64, 40, 3, 16, 1, 2)
+    assert padded.shape == (3, 3, 3)
+    assert lists[0][2] == [0, 3, 4] and lists[2][0] == [0, 5, 6]
+    assert (padded[:, 0] == padded[:, 2]).all()
+    assert (padded[0, 0] == [0, 3, 4]).all()
+    with pytest.raises(ValueError):
+        orc.chunk_local_selection(8, 16, 1, 16, 0, 1)
