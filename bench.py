@@ -47,6 +47,10 @@ def parse_args():
                     help="offload workload: chunks measured at the end of the sequence")
     ap.add_argument("--slots", type=int, default=0,
                     help="offload workload: device page slots (0 = the context's page count)")
+    ap.add_argument("--study", default="", choices=["", "topk-error"],
+                    help="topk-error: sparse-vs-dense output and gradient error against "
+                         "the top-K budget on a page-sparse workload, and the paged pool's "
+                         "device footprint against the bytes its pages need")
     ap.add_argument("--offload-layers", type=int, default=0,
                     help="dense workload: measure L layers in pinned host memory, the next "
                          "layer's pages staged while the current one computes (0 = off)")
@@ -590,6 +594,88 @@ def run_sparse(args, world, rank):
     return out
 
 
+def run_topk_error_study(args, world, rank):
+    """Gradient approximation error of page-level top-K against its budget.
+
+    One dense sweep and one sparse sweep per K of the same seeded workload,
+    all on the GPU through the library; errors are relative Frobenius norms of
+    the sparse result against the dense one over the whole sequence (O, dQ of
+    every chunk; dK, dV of the whole gradient pool). The pages report that the
+    gradient error stays small at adequate retrieval budgets (gist.science/de
+    §4 "Genauigkeit"; gist.science/ja §4). Also the device bytes the paged
+    pool took against what its pages need (the pages' Fig. 4: a non-paged
+    cache can take ~3x the theoretical requirement)."""
+    import numpy as np
+    import torch
+    from paged_kv_chunk_chunked_gb300 import binding as B
+    from paged_kv_chunk_chunked_gb300 import build as pkv_build
+    from paged_kv_chunk_chunked_gb300 import synth
+    from paged_kv_chunk_chunked_gb300.sweep import ChunkSweep, to_device
+
+    pkv_build.build()
+    B.lib()
+    name = args.workload if synth.workload(args.workload).topk else "qwen7b_sparse_256k"
+    w = synth.workload(name)
+    _, ns, nl = w.topk
+    ChunkSweep(synth.workload("tiny_dense_f32")).load_inputs([0]).close()   # device code loaded
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    sw = ChunkSweep(w).load_inputs([])
+    torch.cuda.synchronize()
+    pool_bytes = free0 - torch.cuda.mem_get_info()[0]
+    el = 2 if w.dtype == "bf16" else 4
+    need = w.n_phys * w.Hkv * w.P * w.d * (2 * el + 2 * 4) + w.n_phys * w.Hkv * w.d * 4
+    sw.load_inputs()
+    stream = torch.cuda.current_stream()
+
+    def sweep(K):
+        sw.reset()
+        sels = []
+        for c in range(w.n_chunks):
+            s, e = w.chunk_range(c)
+            B.pkv_append(sw.seq, sw.k[c], sw.v[c], e - s, stream)
+            sel = None
+            if K is not None:
+                sel = torch.empty(((e - s + w.P - 1) // w.P, w.Hkv, K + ns + nl),
+                                  dtype=torch.int32, device="cuda")
+                B.pkv_page_topk(sw.seq, sw.q[c], s, e - s, K, ns, nl, sel, None, stream)
+            sels.append(sel)
+            B.pkv_chunk_attn_fwd(sw.seq, sw.q[c], s, e - s, sw.o[c], sw.lse[c], sel, stream)
+        for c in reversed(range(w.n_chunks)):
+            sw.backward(c, stream, sel=sels[c])
+        g = sw.gather()
+        pairs = sum(sparse_pairs(x.cpu().numpy(), w.P, w.g) for x in sels) if K is not None \
+            else w.Hq * pairs_dense(w.N)
+        return (torch.cat([x.float() for x in sw.o]), torch.cat([x.float() for x in sw.dq]),
+                g["dk"], g["dv"], pairs)
+
+    rel = lambda a, b: float(torch.linalg.vector_norm(a - b) / torch.linalg.vector_norm(b))
+    rows = []
+    for queries in ("normal", "coherent"):
+        sw.w = w = w.with_(queries=queries)
+        sw.q = [to_device(synth.chunk_q(w, c), w.dtype) for c in range(w.n_chunks)]
+        dense = sweep(None)
+        for K in (4, 8, 16, 32, 64, 128, 256):
+            sp = sweep(K)
+            rows.append({"queries": queries, "K": K,
+                         "attended_frac": round(sp[4] / dense[4], 5),
+                         **{f"{n}_rel": round(rel(a, b), 5)
+                            for n, a, b in zip(("o", "dq", "dk", "dv"), sp[:4], dense[:4])}})
+            del sp
+        del dense
+    B.pkv_check(sw.pool)
+    sw.close()
+    return {"study": "topk_gradient_error", "workload": w.name, "n_sink": ns, "n_local": nl,
+            "data": "synthetic (seeded clustered keys; queries N(0,1) ('normal') or a "
+                    "(query page, KV group) centre N(0,1) + N(0,1) ('coherent'); V, dO "
+                    "N(0,1); bf16-rounded)",
+            "error": "relative Frobenius norm, sparse vs dense, both on the GPU",
+            "rows": rows,
+            "memory": {"pool_device_bytes": int(pool_bytes), "page_bytes_needed": int(need),
+                       "ratio": round(pool_bytes / need, 4),
+                       "what": "K, V, dK, dV pages and representatives of the context"}}
+
+
 def run_offload(args, world, rank):
     """Pinned-host offload of the 1M-token page-sparse workload. All 128 chunks'
     K/V are appended into pinned host pages; the measured step is the sparse
@@ -813,7 +899,9 @@ def main():
     world, rank, _ = dist_setup(args)
     from paged_kv_chunk_chunked_gb300 import synth
     wl = synth.workload(args.workload)
-    if args.offload_layers > 0:
+    if args.study == "topk-error":
+        out = run_topk_error_study(args, world, rank)
+    elif args.offload_layers > 0:
         out = run_offload_dense(args, world, rank)
     elif wl.offload:
         out = run_offload(args, world, rank)

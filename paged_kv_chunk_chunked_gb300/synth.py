@@ -30,7 +30,7 @@ __all__ = [
 ]
 
 # Tensor ids for the Philox key; changing one changes every draw of that tensor.
-_TENSOR_ID = {"q": 1, "k": 2, "v": 3, "do": 4, "mu": 5, "perm": 6, "misc": 7}
+_TENSOR_ID = {"q": 1, "k": 2, "v": 3, "do": 4, "mu": 5, "perm": 6, "misc": 7, "qmu": 8}
 
 
 @dataclass(frozen=True)
@@ -47,6 +47,7 @@ class Workload:
     seed: int
     table: str = "identity"    # "identity" or "perm" (seeded permutation of physical pages)
     keys: str = "normal"       # "normal": K ~ N(0,1); "clustered": page centre N(0,2^2) + N(0,1)
+    queries: str = "normal"    # "normal": Q ~ N(0,1); "coherent": (query page, KV group) centre N(0,1) + N(0,1)
     topk: Optional[tuple] = None   # (K, n_sink, n_local) for the page-sparse variant
     local: Optional[tuple] = None  # (n_sink, n_local) for a local attention layer
     offload: bool = False          # pools in pinned host memory, pages streamed to HBM
@@ -147,7 +148,18 @@ def _finish(w: Workload, x: np.ndarray) -> np.ndarray:
 def chunk_q(w: Workload, c: int) -> np.ndarray:
     """Queries of chunk c, [n, Hq, d] float32 (bf16-exact for bf16 workloads)."""
     s, e = w.chunk_range(c)
-    return _finish(w, draw_normal(w.seed, "q", c, (e - s, w.Hq, w.d)))
+    eps = draw_normal(w.seed, "q", c, (e - s, w.Hq, w.d))
+    if w.queries == "normal":
+        return _finish(w, eps)
+    if w.queries != "coherent":
+        raise ValueError(w.queries)
+    # "coherent": the tokens of a query page and the g heads of a KV group share
+    # a centre ~ N(0, I) (queries of neighbouring tokens point the same way).
+    n_pg = (e - s + w.P - 1) // w.P
+    mu = draw_normal(w.seed, "qmu", c, (n_pg, w.Hkv, w.d))
+    page_of_token = np.arange(e - s) // w.P
+    head_group = np.arange(w.Hq) // w.g
+    return _finish(w, mu[page_of_token][:, head_group] + eps)
 
 
 def chunk_k(w: Workload, c: int) -> np.ndarray:

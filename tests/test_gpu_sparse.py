@@ -236,3 +236,50 @@ def test_local_attention_tensor_cores(kw):
 def test_local_attention_cuda_cores():
     _sparse_sweep(_w(dtype="f32", P=16, d=64, N=512, C=256, topk=None, local=(1, 3)),
                   use_oracle_selection=False)
+
+
+@pytest.mark.parametrize("K", [1, 3])
+def test_topk_error_against_dense_matches_oracle(K):
+    """The sparse-vs-dense error the top-K budget study reports (relative
+    Frobenius norm of O, dQ, dK, dV), measured on the GPU, equals the oracle's
+    at a small size up to bf16 noise."""
+    w = _w(N=2048, C=1024, topk=(K, 1, 2))
+    qs, ks, vs, dos = _inputs(w)
+    bt = synth.block_table(w)
+    dense = oracle.chunk_recurrent_step(qs, ks, vs, dos, bt, w.P, w.n_phys)
+    sparse = oracle.chunk_recurrent_step(qs, ks, vs, dos, bt, w.P, w.n_phys, topk=w.topk)
+
+    def flat(r):
+        return (np.concatenate(r["o"]), np.concatenate(r["dq"]),
+                oracle.logical_rows(r["dkpool"], bt, w.N, w.P),
+                oracle.logical_rows(r["dvpool"], bt, w.N, w.P))
+
+    e_ref = [_rel(a, b) for a, b in zip(flat(sparse), flat(dense))]
+    sw = ChunkSweep(w).load_inputs()
+    try:
+        outs = []
+        for sparse_run in (False, True):
+            sw.reset()
+            sels = []
+            for c in range(w.n_chunks):
+                s, e = w.chunk_range(c)
+                B.pkv_append(sw.seq, sw.k[c], sw.v[c], e - s)
+                sel = None
+                if sparse_run:
+                    sel = torch.empty(((e - s) // w.P, w.Hkv, K + 3), dtype=torch.int32, device="cuda")
+                    B.pkv_page_topk(sw.seq, sw.q[c], s, e - s, K, 1, 2, sel)
+                sels.append(sel)
+                B.pkv_chunk_attn_fwd(sw.seq, sw.q[c], s, e - s, sw.o[c], sw.lse[c], sel)
+            for c in reversed(range(w.n_chunks)):
+                sw.backward(c, sel=sels[c])
+            g = sw.gather()
+            outs.append((np.concatenate([to_numpy(x) for x in sw.o]),
+                         np.concatenate([to_numpy(x) for x in sw.dq]),
+                         to_numpy(g["dk"]), to_numpy(g["dv"])))
+        B.pkv_check(sw.pool)
+        e_gpu = [_rel(a, b) for a, b in zip(outs[1], outs[0])]
+        assert min(e_ref) > 0.05, e_ref                 # the budget does cut attention
+        for got, want in zip(e_gpu, e_ref):
+            assert abs(got - want) <= 1e-2, (e_gpu, e_ref)
+    finally:
+        sw.close()
