@@ -51,6 +51,10 @@ def parse_args():
                     help="topk-error: sparse-vs-dense output and gradient error against "
                          "the top-K budget on a page-sparse workload, and the paged pool's "
                          "device footprint against the bytes its pages need")
+    ap.add_argument("--overlap-proj", action="store_true",
+                    help="offload workload: also run a synthetic bf16 K/V projection GEMM per "
+                         "chunk on the main stream while the selected pages stream in, and "
+                         "report how much of it the transfer hides")
     ap.add_argument("--offload-layers", type=int, default=0,
                     help="dense workload: measure L layers in pinned host memory, the next "
                          "layer's pages staged while the current one computes (0 = off)")
@@ -715,6 +719,12 @@ def run_offload(args, world, rank):
         lse = {c: torch.empty((w.Hq, w.C), dtype=torch.float32, device="cuda") for c in meas}
         sel = {c: torch.empty((w.C // w.P, w.Hkv, K + ns + nl), dtype=torch.int32, device="cuda")
                for c in meas}
+        # synthetic K/V projection of a chunk (Qwen2.5-7B: hidden 3584 -> 2 x Hkv x d),
+        # random weights; a plain cuBLAS GEMM on the main stream
+        gen = torch.Generator(device="cuda").manual_seed(w.seed)
+        x_proj = torch.randn((w.C, 3584), device="cuda", generator=gen).to(torch.bfloat16)
+        w_proj = (torch.randn((3584, 2 * w.Hkv * w.d), device="cuda", generator=gen)
+                  / 60.0).to(torch.bfloat16)
 
         def fill():
             B.pkv_seq_reset(seq)
@@ -726,13 +736,15 @@ def run_offload(args, world, rank):
                 B.pkv_append(seq, k, v, e - s, main_s)
             torch.cuda.synchronize()
 
-        def step():
-            staged = 0
+        def step(proj=False):
             for c in meas:
                 s, e = w.chunk_range(c)
                 B.pkv_page_topk(seq, q[c], s, e - s, K, ns, nl, sel[c], None, main_s)
                 if host:
                     B.pkv_prefetch(seq, sel[c], sel[c].numel(), B.PKV_STAGE_KV, side)
+                if proj:      # runs while the selected pages stream in (gist.science/nl)
+                    torch.matmul(x_proj, w_proj)
+                if host:
                     B.pkv_wait(seq, main_s, 0)
                 B.pkv_chunk_attn_fwd(seq, q[c], s, e - s, o[c], lse[c], sel[c], main_s)
             for c in reversed(meas):
@@ -767,6 +779,22 @@ def run_offload(args, world, rank):
         B.pkv_profile_enable(False)
         B.pkv_check(pool)
         res[mode] = dict(ms=ev0.elapsed_time(ev1) / args.steps, prof=prof, staged_pages=staged_pages)
+        if args.overlap_proj:
+            step(proj=True)
+            ev0.record(main_s)
+            for _ in range(args.steps):
+                step(proj=True)
+            ev1.record(main_s)
+            torch.cuda.synchronize()
+            B.pkv_check(pool)
+            res[mode]["ms_proj"] = ev0.elapsed_time(ev1) / args.steps
+            if not host:      # the step's GEMMs alone, back to back
+                ev0.record(main_s)
+                for _ in range(args.steps * len(meas)):
+                    torch.matmul(x_proj, w_proj)
+                ev1.record(main_s)
+                torch.cuda.synchronize()
+                res[mode]["gemm_ms"] = ev0.elapsed_time(ev1) / args.steps
         B.pkv_pool_destroy(pool)
         del q, do, o, dq, lse, sel
         torch.cuda.empty_cache()
@@ -779,6 +807,18 @@ def run_offload(args, world, rank):
     wb_cnt, wb_ms = hp["prof"].get("stage_writeback_kernel", (0, 0.0))
     link_gbs = bytes_moved * args.steps / ((copy_ms + wb_ms) * 1e-3) / 1e9 if copy_ms else None
     overhead = hp["ms"] / res["device"]["ms"] - 1.0
+    extra = {}
+    if args.overlap_proj:
+        proj_ms = res["device"]["gemm_ms"]                             # the GEMMs alone
+        hidden = hp["ms"] + proj_ms - hp["ms_proj"]
+        extra["projection_overlap"] = {
+            "gemm": f"bf16 [{w.C}, 3584] x [3584, {2 * w.Hkv * w.d}] per measured chunk (cuBLAS)",
+            "projection_ms_per_step": round(proj_ms, 3),
+            "ms_per_step_pinned_host_with_projection": round(hp["ms_proj"], 3),
+            "ms_per_step_device_with_projection": round(res["device"]["ms_proj"], 3),
+            "hidden_ms_per_step": round(hidden, 3),
+            "hidden_frac_of_projection": round(hidden / proj_ms, 3) if proj_ms > 0 else None,
+            "overhead_pct_with_projection": round(100 * (hp["ms_proj"] / res["device"]["ms_proj"] - 1), 2)}
     return {
         "metric": "page-sparse offload step: staged pages over the host link, overhead vs HBM-resident",
         "value": round(overhead * 100, 2), "unit": "% step-time overhead", "n_gpus": world,
@@ -791,6 +831,7 @@ def run_offload(args, world, rank):
         "kernels_pinned_host": {k: {"launches": c, "ms_per_step": round(t / args.steps, 3)}
                                 for k, (c, t) in hp["prof"].items()},
         "data": "synthetic (seeded clustered keys)",
+        **extra,
     }
 
 

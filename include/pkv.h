@@ -241,7 +241,8 @@ pkv_status pkv_grad_accumulate(pkv_seq* seq, int64_t row0, int64_t n_rows, const
                                const float* dv, void* stream);
 
 /* Copies the sequence's pages in logical order into contiguous device
- * buffers [len, Hkv, d]: any of the outputs may be NULL. k/v in pool dtype,
+ * buffers [len, Hkv, d] (k, v, dk, dv 16-byte aligned, else PKV_ERR_INVALID):
+ * any of the outputs may be NULL. k/v in pool dtype,
  * dk/dv float32, rep [n_pages, Hkv, d] float32. For tests and for handing
  * dK/dV to the K/V projections. */
 pkv_status pkv_gather(const pkv_seq* seq, void* k, void* v, float* dk, float* dv, float* rep,

@@ -165,12 +165,14 @@ static void release_pages(pkv_seq* s) {
 }
 
 // Uploads block-table entries [from, bt.size()) to the device copy on stream.
+// A kernel reads them from the mapped pinned mirror: a copy-engine transfer on
+// the compute stream would queue behind bulk host-to-device copies issued on
+// other streams (the inputs of later chunks) and hold the next kernel back.
 static pkv_status upload_bt(pkv_seq* s, int64_t from, cudaStream_t st) {
     if (!is_device(s->pool)) return PKV_OK;
     const int64_t n = (int64_t)s->bt.size() - from;
     if (n <= 0) return PKV_OK;
-    cudaError_t e = cudaMemcpyAsync(s->d_bt + from, s->h_bt + from, n * sizeof(int32_t),
-                                    cudaMemcpyHostToDevice, st);
+    cudaError_t e = launch_bt_upload(s->h_bt_dev + from, s->d_bt + from, n, st);
     if (e == cudaSuccess) e = cudaEventRecord(s->bt_sent, st);
     if (e != cudaSuccess) return cuda_fail(e, "block-table upload");
     s->bt_pending = true;
@@ -353,7 +355,9 @@ pkv_status pkv_seq_create(pkv_pool* p, pkv_seq** out) {
     if (is_device(p)) {
         const size_t bytes = (size_t)p->desc.num_phys_pages * sizeof(int32_t);
         cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&s->h_bt), bytes,
-                                      cudaHostAllocDefault);
+                                      cudaHostAllocMapped | cudaHostAllocPortable);
+        if (e == cudaSuccess)
+            e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&s->h_bt_dev), s->h_bt, 0);
         if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&s->d_bt), bytes);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->bt_sent, cudaEventDisableTiming);
         if (e == cudaSuccess && p->desc.residency == PKV_RES_PINNED_HOST) {
@@ -615,6 +619,9 @@ pkv_status pkv_gather(const pkv_seq* s, void* k, void* v, float* dk, float* dv, 
                       void* stream) {
     if (!s) return fail(PKV_ERR_INVALID, "pkv_gather: seq is NULL");
     if (!is_device(s->pool)) return fail(PKV_ERR_INVALID, "pkv_gather: META pool");
+    if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+         reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) & 15)
+        return fail(PKV_ERR_INVALID, "pkv_gather: outputs must be 16-byte aligned");
     if (s->len == 0) return PKV_OK;
     cudaError_t e = launch_gather(s->pool, s->d_bt, 0, s->len, k, v, dk, dv, rep,
                                   static_cast<cudaStream_t>(stream));
@@ -629,6 +636,9 @@ pkv_status pkv_gather_rows(const pkv_seq* s, int64_t row0, int64_t n_rows, void*
     const int64_t P = s->pool->desc.page_size;
     if (row0 < 0 || n_rows < 0 || row0 % P != 0 || row0 + n_rows > s->len)
         return fail(PKV_ERR_INVALID, "pkv_gather_rows: need row0 % P == 0 and row0 + n_rows <= length");
+    if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+         reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) & 15)
+        return fail(PKV_ERR_INVALID, "pkv_gather_rows: outputs must be 16-byte aligned");
     if (n_rows == 0) return PKV_OK;
     cudaError_t e = launch_gather(s->pool, s->d_bt, row0 / P, row0 + n_rows, k, v, dk, dv, nullptr,
                                   static_cast<cudaStream_t>(stream));

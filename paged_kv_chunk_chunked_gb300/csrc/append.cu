@@ -12,6 +12,8 @@
 // threads so that every warp touches whole 32-byte sectors.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -184,12 +186,15 @@ __global__ void __launch_bounds__(kThreads) grad_accumulate_kernel(float* dkpool
     }
 }
 
-// Copies rows of one (logical page, KV head) into logical-order outputs.
+// Copies rows of one (logical page, KV head) into logical-order outputs, 16
+// bytes per access (the page rows are contiguous; output rows are Hkv*D apart).
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) gather_kernel(const T* kpool, const T* vpool,
         const float* dkpool, const float* dvpool, const float* reppool, const int32_t* bt,
         int64_t num_phys, int P, int Hkv, int64_t lp0, int64_t len, T* k, T* v, float* dk,
         float* dv, float* rep, int* err) {
+    constexpr int VT = D * (int)sizeof(T) / 16;     // 16-byte vectors per K/V row
+    constexpr int VF = D / 4;                       // 16-byte vectors per gradient row
     const int64_t lp = lp0 + blockIdx.x;            // logical page; outputs start at page lp0
     const int h = blockIdx.y;
     const int32_t pp = bt[lp];
@@ -199,14 +204,26 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const T* kpool, const 
     }
     const size_t page_off = ((size_t)pp * Hkv + h) * (size_t)P * D;
     const int rows = (int)min64(P, len - lp * P);
-    for (int i = threadIdx.x; i < rows * D; i += kThreads) {
-        const int r = i / D, c = i % D;
-        const size_t dst = ((size_t)((lp - lp0) * P + r) * Hkv + h) * D + c;
-        const size_t src = page_off + (size_t)r * D + c;
-        if (k) k[dst] = kpool[src];
-        if (v) v[dst] = vpool[src];
-        if (dk) dk[dst] = dkpool[src];
-        if (dv) dv[dst] = dvpool[src];
+    const size_t out_row0 = (size_t)(lp - lp0) * P;
+    if (k || v) {
+        const uint4* ks = reinterpret_cast<const uint4*>(kpool + page_off);
+        const uint4* vs = reinterpret_cast<const uint4*>(vpool + page_off);
+        for (int i = threadIdx.x; i < rows * VT; i += kThreads) {
+            const int r = i / VT, c = i % VT;
+            const size_t dst = ((out_row0 + r) * Hkv + h) * VT + c;
+            if (k) reinterpret_cast<uint4*>(k)[dst] = ks[i];
+            if (v) reinterpret_cast<uint4*>(v)[dst] = vs[i];
+        }
+    }
+    if (dk || dv) {
+        const float4* gk = reinterpret_cast<const float4*>(dkpool + page_off);
+        const float4* gv = reinterpret_cast<const float4*>(dvpool + page_off);
+        for (int i = threadIdx.x; i < rows * VF; i += kThreads) {
+            const int r = i / VF, c = i % VF;
+            const size_t dst = ((out_row0 + r) * Hkv + h) * VF + c;
+            if (dk) reinterpret_cast<float4*>(dk)[dst] = gk[i];
+            if (dv) reinterpret_cast<float4*>(dv)[dst] = gv[i];
+        }
     }
     if (rep && threadIdx.x < D)
         rep[((size_t)(lp - lp0) * Hkv + h) * D + threadIdx.x] =
@@ -237,7 +254,20 @@ cudaError_t gather_dispatch(const pkv_pool* p, const int32_t* bt, int64_t lp0, i
     return cudaGetLastError();
 }
 
+__global__ void bt_upload_kernel(const int32_t* src, int32_t* dst, int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+
 }  // namespace
+
+cudaError_t launch_bt_upload(const int32_t* src, int32_t* dst, int64_t n, cudaStream_t s) {
+    const int blocks = (int)std::min<int64_t>(64, (n + kThreads - 1) / kThreads);
+    ProfScope ps("bt_upload_kernel", s);
+    bt_upload_kernel<<<blocks, kThreads, 0, s>>>(src, dst, n);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
     const int64_t first = a.old_len / a.P;

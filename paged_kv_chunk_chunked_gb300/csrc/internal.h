@@ -51,6 +51,7 @@ struct pkv_seq {
     std::vector<int32_t> bt;         // host block table
     int64_t n_reserved_pages = 0;    // pages pre-assigned by pkv_set_block_table not yet filled
     int32_t* h_bt = nullptr;         // pinned mirror used as the copy source
+    int32_t* h_bt_dev = nullptr;     // the mirror's device-side address (mapped)
     int32_t* d_bt = nullptr;         // device block table, capacity num_phys_pages
     // Recorded after every asynchronous upload from h_bt: entries already sent
     // are rewritten (after a reset) only once the last upload has executed.
@@ -101,6 +102,8 @@ struct AppendArgs {
 };
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 
+// dst[i] = src[i], i < n, src in mapped pinned host memory (no copy engine).
+cudaError_t launch_bt_upload(const int32_t* src, int32_t* dst, int64_t n, cudaStream_t s);
 // Zero the gradient rows of the given logical pages range [p0, p1).
 cudaError_t launch_grad_zero(const pkv_pool* pool, const int32_t* d_bt, int64_t p0, int64_t p1,
                              cudaStream_t s);
