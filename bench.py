@@ -40,6 +40,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--workload", default="qwen7b_dense_32k")
+    ap.add_argument("--context", type=int, default=0,
+                    help="override the workload's context length N (a multiple of its chunk "
+                         "length; 0 = the workload's own), e.g. for small profiling runs")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--flags", type=int, default=0, help="pool flags (1 = CUDA cores only)")
@@ -59,6 +62,17 @@ def parse_args():
                     help="dense workload: measure L layers in pinned host memory, the next "
                          "layer's pages staged while the current one computes (0 = off)")
     return ap.parse_args()
+
+
+def bench_workload(args):
+    """The named workload, with --context replacing its context length."""
+    from paged_kv_chunk_chunked_gb300 import synth
+    w = synth.workload(args.workload)
+    if args.context:
+        if args.context <= 0 or args.context % w.C:
+            raise SystemExit(f"--context must be a positive multiple of the chunk length {w.C}")
+        w = w.with_(N=args.context, name=f"{w.name} at context {args.context}")
+    return w
 
 
 def pairs_dense(N: int) -> int:
@@ -232,7 +246,7 @@ def run_pkv(args, world, rank):
         pkv_build.build()
     barrier(world)
     B.lib()
-    w = synth.workload(args.workload)
+    w = bench_workload(args)
     sw = ChunkSweep(w, flags=args.flags).load_inputs()
     stream = torch.cuda.current_stream()
     n = w.n_chunks
@@ -390,7 +404,8 @@ def hbm_kernels(args, w, sw, prof, pk):
         "bound": "hbm", "unit": "GB/s", "bytes_per_launch": acc_bytes,
         "ms_per_launch": round(ms, 4), "achieved": round(acc_bytes / (ms * 1e-3) / 1e9, 1),
         "peak": hbm, "peak_kind": "measured hbm_gbs (copy, timed alone)",
-        "rows": w.N, "l2": "flushed (512 MB write) before each launch"}}
+        "rows": w.N, "l2": "flushed (512 MB write) before each launch",
+        "traffic": traffic_for("grad_accumulate_kernel", "paged_kv_chunk_chunked_gb300/csrc/append.cu")}}
     if hbm:
         out["grad_accumulate_kernel"]["frac"] = round(out["grad_accumulate_kernel"]["achieved"] / hbm, 4)
     if "append_kernel" in prof:
@@ -448,7 +463,7 @@ def run_e2e(args, w, sw, step, world):
 
 def run_reference(args, world, rank):
     from paged_kv_chunk_chunked_gb300 import synth
-    w = synth.workload(args.workload)
+    w = bench_workload(args)
     n_q = 512
     for _ in range(args.warmup):
         oracle_sample(w, n_q)
@@ -495,7 +510,7 @@ def run_sparse(args, world, rank):
 
     pkv_build.build()
     B.lib()
-    w = synth.workload(args.workload)
+    w = bench_workload(args)
     K, ns, nl = w.topk if w.topk else (0,) + tuple(w.local)
     sw = ChunkSweep(w, flags=args.flags).load_inputs()
     stream = torch.cuda.current_stream()
@@ -696,7 +711,7 @@ def run_offload(args, world, rank):
 
     pkv_build.build()
     B.lib()
-    w = synth.workload(args.workload)
+    w = bench_workload(args)
     K, ns, nl = w.topk
     n = w.n_chunks
     meas = list(range(n - args.offload_chunks, n))
@@ -850,7 +865,7 @@ def run_offload_dense(args, world, rank):
 
     pkv_build.build()
     B.lib()
-    w = synth.workload(args.workload)
+    w = bench_workload(args)
     L = args.offload_layers
     c = w.n_chunks - 1
     s, e = w.chunk_range(c)
@@ -939,7 +954,7 @@ def main():
         return 0
     world, rank, _ = dist_setup(args)
     from paged_kv_chunk_chunked_gb300 import synth
-    wl = synth.workload(args.workload)
+    wl = bench_workload(args)
     if args.study == "topk-error":
         out = run_topk_error_study(args, world, rank)
     elif args.offload_layers > 0:
