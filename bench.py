@@ -50,6 +50,10 @@ def parse_args():
                     help="offload workload: chunks measured at the end of the sequence")
     ap.add_argument("--slots", type=int, default=0,
                     help="offload workload: device page slots (0 = the context's page count)")
+    ap.add_argument("--layer-loop", action="store_true",
+                    help="train one attention block (hidden 3584, random weights) chunk by "
+                         "chunk with recomputation at 32K, 64K and 128K (or --context) and "
+                         "report time and device memory per context length")
     ap.add_argument("--study", default="", choices=["", "topk-error"],
                     help="topk-error: sparse-vs-dense output and gradient error against "
                          "the top-K budget on a page-sparse workload, and the paged pool's "
@@ -695,6 +699,79 @@ def run_topk_error_study(args, world, rank):
                        "what": "K, V, dK, dV pages and representatives of the context"}}
 
 
+def run_layer_loop(args, world, rank):
+    """Chunk-recurrent training of one attention block (``layer.ChunkRecurrentBlock``):
+    forward chunk by chunk, backward in reverse with the chunk's Q and attention
+    recomputed; projections are cuBLAS GEMMs, attention runs in the library.
+    Per context length: step time, tokens/s, the bytes of the paged pool, and
+    the transient device memory of a step beyond its inputs and outputs, which
+    the pages say chunk-recurrent recomputation keeps constant in the context
+    (gist.science/de §2.A; sciencestack.ai Fig. 1 caption)."""
+    import torch
+    from paged_kv_chunk_chunked_gb300 import binding as B
+    from paged_kv_chunk_chunked_gb300 import build as pkv_build
+    from paged_kv_chunk_chunked_gb300 import synth
+    from paged_kv_chunk_chunked_gb300.layer import ChunkRecurrentBlock
+    from paged_kv_chunk_chunked_gb300.sweep import to_device
+
+    pkv_build.build()
+    B.lib()
+    w0 = synth.workload(args.workload)
+    hidden = 3584
+    contexts = [args.context] if args.context else [32768, 65536, 131072]
+    rows = []
+    for N in contexts:
+        w = w0.with_(N=N)
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
+        blk = ChunkRecurrentBlock(w, hidden)
+        torch.cuda.synchronize()
+        pool_bytes = free0 - torch.cuda.mem_get_info()[0]
+        xs = [to_device(synth.block_x(w, c, hidden), w.dtype) for c in range(w.n_chunks)]
+        dys = [to_device(synth.block_dy(w, c, hidden), w.dtype) for c in range(w.n_chunks)]
+        for _ in range(args.warmup):
+            ys = blk.forward(xs)
+            dxs, g = blk.backward(xs, dys)
+            del ys, dxs, g
+        torch.cuda.synchronize()
+        B.pkv_check(blk.pool)
+        torch.cuda.reset_peak_memory_stats()
+        base = torch.cuda.memory_allocated()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        out_bytes = 0
+        for _ in range(args.steps):
+            ys = blk.forward(xs)
+            dxs, g = blk.backward(xs, dys)
+            out_bytes = sum(t.numel() * t.element_size() for t in ys + dxs) + \
+                sum(t.numel() * 4 for t in g.values())
+            del ys, dxs, g
+        b.record()
+        torch.cuda.synchronize()
+        B.pkv_check(blk.pool)
+        ms = a.elapsed_time(b) / args.steps
+        peak = torch.cuda.max_memory_allocated() - base
+        rows.append({"N": N, "ms_per_step": round(ms, 3),
+                     "tokens_per_s": round(N / (ms * 1e-3), 1),
+                     "kv_pool_bytes": int(pool_bytes),
+                     "kv_pool_bytes_per_token": round(pool_bytes / N, 1),
+                     "step_transient_bytes": int(peak - out_bytes),
+                     "step_output_bytes": int(out_bytes)})
+        blk.close()
+        del xs, dys
+        torch.cuda.empty_cache()
+    return {"metric": "chunk-recurrent training step of one attention block: time and device memory vs context",
+            "unit": "ms/step", "value": rows[-1]["ms_per_step"], "higher_is_better": False,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "dtype": w0.dtype,
+            "data": "synthetic (seeded N(0,1) inputs and upstream gradients, random weights)",
+            "config": {"workload": w0.name, "C": w0.C, "P": w0.P, "Hq": w0.Hq, "Hkv": w0.Hkv,
+                       "d": w0.d, "hidden": hidden, "block": "x + attention(x wq, x wk, x wv) wo"},
+            "rows": rows,
+            "memory_note": "step_transient_bytes = peak torch allocation during a step minus the "
+                           "step's outputs (y, dx, weight gradients); the paged pool is outside "
+                           "torch's allocator and reported separately"}
+
+
 def run_offload(args, world, rank):
     """Pinned-host offload of the 1M-token page-sparse workload. All 128 chunks'
     K/V are appended into pinned host pages; the measured step is the sparse
@@ -957,6 +1034,8 @@ def main():
     wl = bench_workload(args)
     if args.study == "topk-error":
         out = run_topk_error_study(args, world, rank)
+    elif args.layer_loop:
+        out = run_layer_loop(args, world, rank)
     elif args.offload_layers > 0:
         out = run_offload_dense(args, world, rank)
     elif wl.offload:

@@ -196,6 +196,37 @@ def full_causal_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray):
     return o, lse
 
 
+# --------------------------------------------------------------------------- attention block
+
+def attention_block(x: np.ndarray, wq: np.ndarray, wk: np.ndarray, wv: np.ndarray,
+                    wo: np.ndarray, dy: np.ndarray, n_q_heads: int, n_kv_heads: int):
+    """One attention block over the whole sequence, forward and backward.
+
+    y = x + A wo with A = causal GQA attention(x wq, x wk, x wv) (heads laid
+    out [.., H, d] in the projection outputs); the loss is sum(y * dy). This is
+    the layer that chunk-recurrent training processes chunk by chunk while
+    recomputing activations (gist.science/de §2.A; sciencestack.ai Fig. 1
+    caption); chunking and recomputation do not change it, so the whole-sequence
+    definition is the reference. Returns y and the gradients of x, wq, wk, wv,
+    wo (fp64)."""
+    x = np.asarray(x, F64); dy = np.asarray(dy, F64)
+    wq, wk, wv, wo = (np.asarray(t, F64) for t in (wq, wk, wv, wo))
+    N = x.shape[0]
+    d = wq.shape[1] // n_q_heads
+    q = (x @ wq).reshape(N, n_q_heads, d)
+    k = (x @ wk).reshape(N, n_kv_heads, d)
+    v = (x @ wv).reshape(N, n_kv_heads, d)
+    o, lse = attention_forward(q, k, v, 0)
+    a = o.reshape(N, n_q_heads * d)
+    y = x + a @ wo
+    da = dy @ wo.T
+    dwo = a.T @ dy
+    dq, dk, dv = attention_backward(q, k, v, o, da.reshape(N, n_q_heads, d), lse, 0)
+    dq, dk, dv = (t.reshape(N, -1) for t in (dq, dk, dv))
+    dx = dy + dq @ wq.T + dk @ wk.T + dv @ wv.T
+    return y, dict(x=dx, wq=x.T @ dq, wk=x.T @ dk, wv=x.T @ dv, wo=dwo)
+
+
 # --------------------------------------------------------------------------- page selection
 
 def page_representatives(k_logical: np.ndarray, page_size: int) -> np.ndarray:

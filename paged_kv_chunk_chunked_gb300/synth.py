@@ -30,7 +30,8 @@ __all__ = [
 ]
 
 # Tensor ids for the Philox key; changing one changes every draw of that tensor.
-_TENSOR_ID = {"q": 1, "k": 2, "v": 3, "do": 4, "mu": 5, "perm": 6, "misc": 7, "qmu": 8}
+_TENSOR_ID = {"q": 1, "k": 2, "v": 3, "do": 4, "mu": 5, "perm": 6, "misc": 7, "qmu": 8,
+              "wq": 9, "wk": 10, "wv": 11, "wo": 12, "x": 13, "dy": 14}
 
 
 @dataclass(frozen=True)
@@ -190,6 +191,27 @@ def chunk_do(w: Workload, c: int) -> np.ndarray:
     """Upstream gradient dL/dO of chunk c, [n, Hq, d]."""
     s, e = w.chunk_range(c)
     return _finish(w, draw_normal(w.seed, "do", c, (e - s, w.Hq, w.d)))
+
+
+def block_weights(w: Workload, hidden: int) -> dict:
+    """Random projection weights of one attention block, N(0, 1/hidden) (wo:
+    N(0, 1/(Hq d))): wq [hidden, Hq d], wk and wv [hidden, Hkv d], wo [Hq d, hidden]."""
+    shapes = {"wq": (hidden, w.Hq * w.d), "wk": (hidden, w.Hkv * w.d),
+              "wv": (hidden, w.Hkv * w.d), "wo": (w.Hq * w.d, hidden)}
+    return {n: _finish(w, draw_normal(w.seed, n, 0, sh, std=float(sh[0]) ** -0.5))
+            for n, sh in shapes.items()}
+
+
+def block_x(w: Workload, c: int, hidden: int) -> np.ndarray:
+    """Input of the attention block for chunk c, [n, hidden], N(0, 1)."""
+    s, e = w.chunk_range(c)
+    return _finish(w, draw_normal(w.seed, "x", c, (e - s, hidden)))
+
+
+def block_dy(w: Workload, c: int, hidden: int) -> np.ndarray:
+    """Upstream gradient of the block's output for chunk c, [n, hidden], N(0, 1)."""
+    s, e = w.chunk_range(c)
+    return _finish(w, draw_normal(w.seed, "dy", c, (e - s, hidden)))
 
 
 def block_table(w: Workload) -> np.ndarray:

@@ -115,6 +115,12 @@ def test_compute_calls_reject_meta_pools_and_bad_chunks(lib):
     with pytest.raises(B.PkvError) as e:
         B.pkv_gather_rows(seq, 0, 16, dk=16)
     assert e.value.status == B.PKV_ERR_INVALID
+    with pytest.raises(B.PkvError) as e:
+        B.pkv_grad_accumulate(seq, 0, 16, dk=16)
+    assert e.value.status == B.PKV_ERR_INVALID
+    with pytest.raises(B.PkvError) as e:
+        B.pkv_page_local(seq, 0, 16, 0, 2, 16)
+    assert e.value.status == B.PKV_ERR_INVALID
     assert B.pkv_seq_length(seq) == 0
     B.pkv_pool_destroy(pool)
 

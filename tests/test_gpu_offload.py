@@ -145,3 +145,48 @@ def test_offload_calls_reject_device_pools():
             assert e.value.status == B.PKV_ERR_INVALID
     finally:
         B.pkv_pool_destroy(pool)
+
+
+def test_grad_accumulate_into_pinned_host_pages_then_prefetch():
+    """pkv_grad_accumulate on a PINNED_HOST pool adds into the host gradient
+    pages (bit-exact against the oracle's scatter-add), and a gradient prefetch
+    issued on a side stream afterwards stages the sums (ordered by the
+    sequence's event)."""
+    w = synth.workload("qwen7b_sparse_256k", N=1024, C=512, Hq=4, Hkv=2, extra_pages=2,
+                       topk=(2, 1, 2))
+    bt = synth.block_table(w)
+    pool = B.pkv_pool_create(w.P, w.Hkv, w.Hq, w.d, B.PKV_BF16, w.n_phys,
+                             residency=B.PKV_RES_PINNED_HOST, n_device_slots=w.n_pages)
+    side = torch.cuda.Stream()
+    try:
+        seq = B.pkv_seq_create(pool)
+        B.pkv_set_block_table(seq, bt)
+        for c in range(w.n_chunks):
+            s, e = w.chunk_range(c)
+            k = to_device(synth.chunk_k(w, c), "bf16")
+            B.pkv_append(seq, k, k, e - s)
+        ref = {t: np.zeros((w.n_phys, w.Hkv, w.P, w.d), np.float32) for t in ("dk", "dv")}
+        for i, (r0, n) in enumerate([(0, w.N), (100, 300), (w.N - 1, 1)]):
+            x = synth.draw_normal(w.seed, "misc", 200 + i, (n, w.Hkv, w.d))
+            y = synth.draw_normal(w.seed, "misc", 300 + i, (n, w.Hkv, w.d))
+            oracle.scatter_rows(ref["dk"], bt, r0, x, w.P, accumulate=True)
+            oracle.scatter_rows(ref["dv"], bt, r0, y, w.P, accumulate=True)
+            B.pkv_grad_accumulate(seq, r0, n, torch.from_numpy(x).cuda(), torch.from_numpy(y).cuda())
+        B.pkv_prefetch(seq, None, 0, B.PKV_STAGE_GRADS, side)
+        B.pkv_wait(seq, torch.cuda.current_stream(), 0)
+        torch.cuda.synchronize()
+        B.pkv_check(pool)
+        dk = torch.empty((w.N, w.Hkv, w.d), dtype=torch.float32, device="cuda")
+        dv = torch.empty_like(dk)
+        B.pkv_gather(seq, None, None, dk, dv, None)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(to_numpy(dk), oracle.logical_rows(ref["dk"], bt, w.N, w.P))
+        np.testing.assert_array_equal(to_numpy(dv), oracle.logical_rows(ref["dv"], bt, w.N, w.P))
+        # the staged slots hold the same sums: write them back unchanged
+        B.pkv_writeback_grads(seq, side)
+        B.pkv_wait(seq, torch.cuda.current_stream(), 0)
+        B.pkv_gather(seq, None, None, dk, dv, None)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(to_numpy(dk), oracle.logical_rows(ref["dk"], bt, w.N, w.P))
+    finally:
+        B.pkv_pool_destroy(pool)

@@ -271,3 +271,27 @@ def test_paged_gradient_accumulation_equals_contiguous_sums():
     assert not pool[unused].any()
     assert not pool[bt[-1], :, P - 5:].any()             # rows beyond the sequence
     assert pool.dtype == np.float32
+
+
+def test_attention_block_matches_library_autograd():
+    """The whole-sequence attention block (projections, causal GQA attention,
+    output projection, residual) and all five gradients against torch autograd
+    in fp64 through scaled_dot_product_attention."""
+    N, hidden, Hq, Hkv, d = 48, 24, 4, 2, 8
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((N, hidden))
+    ws = [rng.standard_normal(s) / 4 for s in ((hidden, Hq * d), (hidden, Hkv * d),
+                                               (hidden, Hkv * d), (Hq * d, hidden))]
+    dy = rng.standard_normal((N, hidden))
+    y, grads = orc.attention_block(x, *ws, dy, Hq, Hkv)
+    tx = torch.tensor(x, requires_grad=True)
+    tw = [torch.tensor(w, requires_grad=True) for w in ws]
+    q = (tx @ tw[0]).view(N, Hq, d).permute(1, 0, 2)
+    k = (tx @ tw[1]).view(N, Hkv, d).repeat_interleave(Hq // Hkv, dim=1).permute(1, 0, 2)
+    v = (tx @ tw[2]).view(N, Hkv, d).repeat_interleave(Hq // Hkv, dim=1).permute(1, 0, 2)
+    a = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True)
+    ty = tx + a.permute(1, 0, 2).reshape(N, Hq * d) @ tw[3]
+    (ty * torch.tensor(dy)).sum().backward()
+    np.testing.assert_allclose(y, ty.detach().numpy(), atol=1e-12)
+    for name, t in zip(("x", "wq", "wk", "wv", "wo"), [tx] + tw):
+        np.testing.assert_allclose(grads[name], t.grad.numpy(), atol=1e-10, err_msg=name)
