@@ -41,7 +41,11 @@ class ChunkRecurrentBlock:
         self.dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
         self.weights = {n: to_device(a, w.dtype) for n, a in synth.block_weights(w, hidden).items()}
         pdt = B.PKV_BF16 if w.dtype == "bf16" else B.PKV_F32
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
         self.pool = B.pkv_pool_create(w.P, w.Hkv, w.Hq, w.d, pdt, w.n_phys, flags=flags)
+        torch.cuda.synchronize()
+        self.pool_device_bytes = free0 - torch.cuda.mem_get_info()[0]   # K, V, dK, dV pages, reps
         self.seq = B.pkv_seq_create(self.pool)
         C = w.C
         self.o = torch.empty((C, w.Hq, w.d), dtype=self.dt, device="cuda")
