@@ -50,7 +50,7 @@ struct pkv_seq {
     pkv_pool* pool = nullptr;
     std::vector<int32_t> bt;         // host block table
     int64_t n_reserved_pages = 0;    // pages pre-assigned by pkv_set_block_table not yet filled
-    int32_t* h_bt = nullptr;         // pinned mirror used as the copy source
+    int32_t* h_bt = nullptr;         // pinned mirror the upload kernel reads (mapped)
     int32_t* h_bt_dev = nullptr;     // the mirror's device-side address (mapped)
     int32_t* d_bt = nullptr;         // device block table, capacity num_phys_pages
     // Recorded after every asynchronous upload from h_bt: entries already sent
