@@ -102,11 +102,16 @@ def lib() -> ctypes.CDLL:
 
 
 def ptr(x) -> Optional[int]:
-    """Address of a tensor-like (``data_ptr()``), an int, or None."""
+    """Address of a tensor-like (``data_ptr()``), an int, or None. Every array
+    the library reads or writes is dense in the layout its header states, so a
+    strided view is refused here instead of being read as if it were dense."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
+    if hasattr(x, "is_contiguous") and not x.is_contiguous():
+        raise ValueError(f"tensor of shape {tuple(x.shape)} with strides {x.stride()} is not "
+                         "contiguous; pass .contiguous()")
     return x.data_ptr()
 
 

@@ -125,6 +125,17 @@ def test_compute_calls_reject_meta_pools_and_bad_chunks(lib):
     B.pkv_pool_destroy(pool)
 
 
+def test_strided_tensors_are_refused_before_the_call(lib):
+    import torch
+    pool = _meta_pool()
+    seq = B.pkv_seq_create(pool)
+    with pytest.raises(ValueError):
+        B.pkv_gather_rows(seq, 0, 16, dk=torch.zeros(8, 4).t())
+    with pytest.raises(ValueError):
+        B.pkv_grad_accumulate(seq, 0, 4, dk=torch.zeros(4, 8)[:, ::2])
+    B.pkv_pool_destroy(pool)
+
+
 def test_null_arguments(lib):
     assert lib.pkv_pool_create(None, None) == B.PKV_ERR_INVALID
     assert lib.pkv_seq_create(None, None) == B.PKV_ERR_INVALID
