@@ -79,6 +79,18 @@ def bench_workload(args):
     return w
 
 
+def ensure_library(world: int, rank: int):
+    """Rank 0 builds libpkv (a no-op when it is up to date) while the others
+    wait, so replicas never write the same objects at once; then every rank
+    loads it."""
+    from paged_kv_chunk_chunked_gb300 import binding as B
+    from paged_kv_chunk_chunked_gb300 import build as pkv_build
+    if rank == 0 or world == 1:
+        pkv_build.build()
+    barrier(world)
+    B.lib()
+
+
 def pairs_dense(N: int) -> int:
     return N * (N + 1) // 2
 
@@ -242,14 +254,10 @@ def traffic_for(kernel: str, source: str):
 def run_pkv(args, world, rank):
     import torch
     from paged_kv_chunk_chunked_gb300 import binding as B
-    from paged_kv_chunk_chunked_gb300 import build as pkv_build
     from paged_kv_chunk_chunked_gb300 import synth
     from paged_kv_chunk_chunked_gb300.sweep import ChunkSweep
 
-    if rank == 0 or world == 1:
-        pkv_build.build()
-    barrier(world)
-    B.lib()
+    ensure_library(world, rank)
     w = bench_workload(args)
     sw = ChunkSweep(w, flags=args.flags).load_inputs()
     stream = torch.cuda.current_stream()
@@ -508,12 +516,10 @@ def run_sparse(args, world, rank):
     sweep of the same context once for the sparse/dense speedup."""
     import torch
     from paged_kv_chunk_chunked_gb300 import binding as B
-    from paged_kv_chunk_chunked_gb300 import build as pkv_build
     from paged_kv_chunk_chunked_gb300 import synth
     from paged_kv_chunk_chunked_gb300.sweep import ChunkSweep
 
-    pkv_build.build()
-    B.lib()
+    ensure_library(world, rank)
     w = bench_workload(args)
     K, ns, nl = w.topk if w.topk else (0,) + tuple(w.local)
     sw = ChunkSweep(w, flags=args.flags).load_inputs()
@@ -631,12 +637,10 @@ def run_topk_error_study(args, world, rank):
     import numpy as np
     import torch
     from paged_kv_chunk_chunked_gb300 import binding as B
-    from paged_kv_chunk_chunked_gb300 import build as pkv_build
     from paged_kv_chunk_chunked_gb300 import synth
     from paged_kv_chunk_chunked_gb300.sweep import ChunkSweep, to_device
 
-    pkv_build.build()
-    B.lib()
+    ensure_library(world, rank)
     name = args.workload if synth.workload(args.workload).topk else "qwen7b_sparse_256k"
     w = synth.workload(name)
     _, ns, nl = w.topk
@@ -709,13 +713,11 @@ def run_layer_loop(args, world, rank):
     (gist.science/de §2.A; sciencestack.ai Fig. 1 caption)."""
     import torch
     from paged_kv_chunk_chunked_gb300 import binding as B
-    from paged_kv_chunk_chunked_gb300 import build as pkv_build
     from paged_kv_chunk_chunked_gb300 import synth
     from paged_kv_chunk_chunked_gb300.layer import ChunkRecurrentBlock
     from paged_kv_chunk_chunked_gb300.sweep import to_device
 
-    pkv_build.build()
-    B.lib()
+    ensure_library(world, rank)
     w0 = synth.workload(args.workload)
     hidden = 3584
     ChunkRecurrentBlock(w0.with_(N=w0.C), 64).close()     # device code loaded before measuring
@@ -780,12 +782,10 @@ def run_offload(args, world, rank):
     import numpy as np
     import torch
     from paged_kv_chunk_chunked_gb300 import binding as B
-    from paged_kv_chunk_chunked_gb300 import build as pkv_build
     from paged_kv_chunk_chunked_gb300 import synth
     from paged_kv_chunk_chunked_gb300.sweep import to_device
 
-    pkv_build.build()
-    B.lib()
+    ensure_library(world, rank)
     w = bench_workload(args)
     K, ns, nl = w.topk
     n = w.n_chunks
@@ -934,12 +934,10 @@ def run_offload_dense(args, world, rank):
     layers gives the overhead."""
     import torch
     from paged_kv_chunk_chunked_gb300 import binding as B
-    from paged_kv_chunk_chunked_gb300 import build as pkv_build
     from paged_kv_chunk_chunked_gb300 import synth
     from paged_kv_chunk_chunked_gb300.sweep import to_device
 
-    pkv_build.build()
-    B.lib()
+    ensure_library(world, rank)
     w = bench_workload(args)
     L = args.offload_layers
     c = w.n_chunks - 1
