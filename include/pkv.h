@@ -15,7 +15,9 @@
  *     technique" §2.B; sciencestack.ai Fig. 3 and Fig. 4 captions);
  *   - page-level sparse attention: top-K pages per query page picked by
  *     per-page representative vectors (gist.science/de §2.D; gist.science/nl
- *     "Pagina-niveau Sparse Attention"; sciencestack.ai Fig. 5 caption);
+ *     "Pagina-niveau Sparse Attention"; sciencestack.ai Fig. 5 caption), and
+ *     local attention layers for natively sparse models (gist.science/nl,
+ *     same section);
  *   - asynchronous offload of the cache and its gradients to pinned host
  *     memory, overlapped with compute on CUDA streams (gist.science/de §2.C;
  *     gist.science/nl "Asynchrone CPU Offloading"; gist.science/ja §2.3).
@@ -92,7 +94,8 @@ typedef struct pkv_pool_desc {
 typedef struct pkv_pool pkv_pool;
 typedef struct pkv_seq pkv_seq;
 
-/* A page selection for the sparse variant (see pkv_page_topk).
+/* A page selection for the sparse variant (written by pkv_page_topk or
+ * pkv_page_local, or by the caller in the same format).
  * pages: device int32 [n_qp, Hkv, kmax]; entry (qp, h, :) lists the logical
  * pages visible to the chunk's query page qp through KV head h, ascending,
  * padded with -1. The last listed page of every row is the query page itself. */
