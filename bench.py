@@ -19,6 +19,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -1017,13 +1018,25 @@ def run_offload_dense(args, world, rank):
     }
 
 
+def json_safe(x):
+    """The result with every non-finite float replaced by None: the line must
+    be strict JSON (NaN and Infinity are not)."""
+    if isinstance(x, float):
+        return x if math.isfinite(x) else None
+    if isinstance(x, dict):
+        return {k: json_safe(v) for k, v in x.items()}
+    if isinstance(x, (list, tuple)):
+        return [json_safe(v) for v in x]
+    return x
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         if rank != 0:
             return 0
-        print(json.dumps(run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), rank)))
+        print(json.dumps(json_safe(run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), rank)), allow_nan=False))
         return 0
     world, rank, _ = dist_setup(args)
     from paged_kv_chunk_chunked_gb300 import synth
@@ -1041,7 +1054,7 @@ def main():
     else:
         out = run_pkv(args, world, rank)
     if rank == 0:
-        print(json.dumps(out), flush=True)
+        print(json.dumps(json_safe(out), allow_nan=False), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

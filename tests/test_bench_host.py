@@ -63,3 +63,10 @@ def test_context_override():
     assert bench.bench_workload(_args()).N == 262144
     with pytest.raises(SystemExit):
         bench.bench_workload(_args(context=65536 + 128))
+
+
+def test_result_line_is_strict_json():
+    import json
+    out = bench.json_safe({"a": float("nan"), "b": [1.0, float("inf")], "c": {"d": 2.5}, "e": "x"})
+    assert out == {"a": None, "b": [1.0, None], "c": {"d": 2.5}, "e": "x"}
+    json.dumps(out, allow_nan=False)
