@@ -39,7 +39,18 @@ repository's design notes):
 
 Every function here is pinned by tests in ``tests/test_oracle_*.py`` against
 something other than itself (library attention, finite differences, closed
-forms, invariants, brute force).
+forms, invariants, brute force):
+  attention_forward / attention_backward / full_causal_attention -- torch SDPA
+      and autograd in fp64, finite differences, closed forms, shift invariance,
+      sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i, a hand-worked example;
+  chunk_recurrent_step, logical_rows, scatter_rows -- equal one-shot attention
+      over random shapes and permuted tables; scatter-add equals contiguous sums;
+  page_representatives, query_page_means, select_pages, chunk_selection --
+      constructed means, brute-force ranking, ties, a planted page, K >= every
+      candidate equals dense;
+  local_pages, chunk_local_selection -- closed-form counts, the set definition,
+      K = 0 selection, blockwise library attention for one local page;
+  attention_block -- torch autograd of the same block in fp64.
 """
 from __future__ import annotations
 
