@@ -218,7 +218,9 @@ pkv_status pkv_chunk_attn_bwd(pkv_seq* seq, const void* q, const void* o, const 
  * array's device address (no allocation) and should come before any stream
  * capture. All calls share the array: calls that overlap on the GPU race and
  * must be serialised by the caller. Each call rewrites what it reads, so
- * nothing needs clearing between calls. */
+ * nothing needs clearing between calls. Like pkv_chunk_attn_bwd it marks the
+ * sequence as used on `stream`, so pkv_prefetch and pkv_writeback_grads on a
+ * side stream wait for it before touching the staged slots. */
 pkv_status pkv_chunk_attn_bwd_noalloc(pkv_seq* seq, const void* q, const void* o,
                                       const void* dout, const float* lse, int64_t q_start,
                                       int64_t n_q, void* dq, const pkv_sel* sel, void* stream);

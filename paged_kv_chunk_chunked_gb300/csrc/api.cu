@@ -496,8 +496,10 @@ pkv_status pkv_append(pkv_seq* s, const void* k, const void* v, int64_t n_tok, v
     return PKV_OK;
 }
 
-static pkv_status attn_common(pkv_seq* s, const void* q, int64_t q_start, int64_t n_q,
-                              const pkv_sel* sel, AttnArgs* a, const char* who) {
+}  // extern "C"
+
+pkv_status pkv::attn_common(pkv_seq* s, const void* q, int64_t q_start, int64_t n_q,
+                            const pkv_sel* sel, AttnArgs* a, const char* who) {
     if (!s || !q) return fail(PKV_ERR_INVALID, std::string(who) + ": NULL argument");
     pkv_pool* p = s->pool;
     if (!is_device(p)) return fail(PKV_ERR_INVALID, std::string(who) + ": META pool");
@@ -534,9 +536,11 @@ static pkv_status attn_common(pkv_seq* s, const void* q, int64_t q_start, int64_
     return PKV_OK;
 }
 
-static bool use_tc(const pkv_pool* p, const AttnArgs& a) {
+bool pkv::use_tc(const pkv_pool* p, const AttnArgs& a) {
     return !(p->desc.flags & PKV_FLAG_SIMT_ONLY) && p->tmaps_ready && tc_supported(a);
 }
+
+extern "C" {
 
 pkv_status pkv_chunk_attn_fwd(pkv_seq* s, const void* q, int64_t q_start, int64_t n_q, void* o,
                               float* lse, const pkv_sel* sel, void* stream) {

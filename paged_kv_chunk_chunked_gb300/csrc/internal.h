@@ -139,6 +139,15 @@ struct AttnArgs {
     const CUtensorMap* tmap_v;
 };
 
+// Validates the arguments shared by the attention entry points and fills a
+// with the sequence's pools, block table (or slot table for PINNED_HOST pools),
+// tensor maps and selection. Host-only; returns PKV_OK or an error with the
+// last-error message set, naming `who`.
+pkv_status attn_common(pkv_seq* s, const void* q, int64_t q_start, int64_t n_q,
+                       const pkv_sel* sel, AttnArgs* a, const char* who);
+// True when the tensor-core kernels take this call.
+bool use_tc(const pkv_pool* p, const AttnArgs& a);
+
 cudaError_t launch_attn_fwd_simt(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_attn_bwd_simt(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_rowdot(const AttnArgs& a, cudaStream_t s);

@@ -66,55 +66,31 @@ extern "C" pkv_status pkv_chunk_attn_bwd_noalloc(pkv_seq* s, const void* q, cons
                                                  int64_t q_start, int64_t n_q, void* dq,
                                                  const pkv_sel* sel, void* stream) {
     static const char* who = "pkv_chunk_attn_bwd_noalloc";
-    if (!s || !q || !o || !dout || !lse || !dq)
-        return fail(PKV_ERR_INVALID, std::string(who) + ": NULL argument");
-    pkv_pool* p = s->pool;
-    if (p->desc.residency == PKV_RES_META)
-        return fail(PKV_ERR_INVALID, std::string(who) + ": META pool holds no data");
-    const int64_t P = p->desc.page_size;
-    if (n_q <= 0 || q_start < 0 || q_start % P != 0 || q_start + n_q > s->len)
-        return fail(PKV_ERR_INVALID, std::string(who) +
-                                         ": need q_start % P == 0 and q_start + n_q <= length");
-    const size_t need = (size_t)p->desc.n_q_heads * (size_t)n_q;
+    // The same argument checks, pools, tables and dispatch as pkv_chunk_attn_bwd;
+    // only the scratch differs.
+    AttnArgs a;
+    pkv_status st = attn_common(s, q, q_start, n_q, sel, &a, who);
+    if (st != PKV_OK) return st;
+    if (!o || !dout || !lse || !dq)
+        return fail(PKV_ERR_INVALID, std::string(who) + ": o, dout, lse or dq is NULL");
+    const size_t need = (size_t)a.Hq * (size_t)n_q;
     if (need > kNoAllocMaxFloats)
         return fail(PKV_ERR_INVALID,
                     std::string(who) + ": n_q_heads * n_q = " + std::to_string(need) +
                         " exceeds the fixed scratch of " + std::to_string(kNoAllocMaxFloats) +
                         " floats; use pkv_chunk_attn_bwd or a smaller chunk");
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev != p->device)
-        return fail(PKV_ERR_INVALID, std::string(who) + ": current device is not the pool's");
     float* scratch = nullptr;
-    pkv_status st = scratch_for_current_device(&scratch);
+    st = scratch_for_current_device(&scratch);
     if (st != PKV_OK) return st;
-
-    AttnArgs a{};
-    a.P = (int)P; a.Hq = p->desc.n_q_heads; a.Hkv = p->desc.n_kv_heads;
-    a.d = p->desc.head_dim; a.dtype = p->desc.dtype;
-    a.q_start = q_start; a.n_q = n_q; a.q = q;
-    if (p->desc.residency == PKV_RES_PINNED_HOST) {      // staged pages: read the slots
-        a.kpool = p->kslot; a.vpool = p->vslot; a.dkpool = p->dkslot; a.dvpool = p->dvslot;
-        a.bt = s->d_slot_of; a.num_phys = p->n_slots;
-    } else {
-        a.kpool = p->k; a.vpool = p->v; a.dkpool = p->dk; a.dvpool = p->dv;
-        a.bt = s->d_bt; a.num_phys = p->desc.num_phys_pages;
-    }
-    a.err = p->d_err;
-    a.tmap_k = p->tmaps_ready ? &p->tmap_k : nullptr;
-    a.tmap_v = p->tmaps_ready ? &p->tmap_v : nullptr;
-    if (sel) {
-        if (!sel->pages || sel->kmax <= 0 || sel->n_qp != (n_q + P - 1) / P)
-            return fail(PKV_ERR_INVALID, std::string(who) + ": selection does not match chunk");
-        a.sel = sel->pages;
-        a.kmax = sel->kmax;
-    }
     a.o_in = o; a.dout = dout; a.lse_in = lse; a.dq = dq; a.Dbuf = scratch;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const bool tc = !(p->desc.flags & PKV_FLAG_SIMT_ONLY) && p->tmaps_ready && tc_supported(a);
-    e = launch_bwd_rowdot(a, cs);
-    if (e == cudaSuccess) e = tc ? launch_attn_bwd_tc(a, cs) : launch_attn_bwd_simt(a, cs);
+    cudaError_t e = launch_bwd_rowdot(a, cs);
+    if (e == cudaSuccess)
+        e = use_tc(s->pool, a) ? launch_attn_bwd_tc(a, cs) : launch_attn_bwd_simt(a, cs);
+    // Staging on a side stream (pkv_prefetch, pkv_writeback_grads) orders itself
+    // after this event: the slots this call reads and adds into stay untouched
+    // until it has finished.
+    if (e == cudaSuccess && s->used) e = cudaEventRecord(s->used, cs);
     if (e != cudaSuccess) return cuda_fail(e, "pkv_chunk_attn_bwd_noalloc: launch");
     return PKV_OK;
 }

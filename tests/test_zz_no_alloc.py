@@ -1,12 +1,20 @@
-"""pkv_chunk_attn_bwd_noalloc against pkv_chunk_attn_bwd, through the C ABI.
+"""pkv_chunk_attn_bwd_noalloc against the oracle, through the C ABI.
 
-The no-allocation variant exists for callers that cannot let the library
-allocate device memory when the backward runs: a fixed memory budget, an
-allocator that owns all device memory, code that must not synchronize the
-device, or a loop that forbids allocation after start-up. It keeps its
-per-row scratch in one fixed array of the library's device image instead of a
-cudaMalloc'd buffer. Its results must equal the allocating entry point's, call
-after call (the array keeps the previous call's contents).
+Who needs it: a caller that cannot let the library allocate device memory
+while the backward runs. Examples are a trainer under a fixed memory budget,
+a framework whose caching allocator owns all device memory (a cudaMalloc
+behind its back can fail or fragment it), code that must not synchronize the
+device (cudaMalloc and cudaFree can), and loops that forbid allocation after
+start-up. The variant keeps its per-row scratch in one fixed array of the
+library's device image instead of a cudaMalloc'd buffer.
+
+Checked here: dQ and the accumulated dK/dV pages equal the oracle's
+chunk-recurrent backward (relative Frobenius 2e-2 for bf16, 1e-4 for fp32),
+on two backward sweeps in a row (the array keeps the previous call's
+contents); with a page selection made by pkv_page_topk; and on a pinned-host
+pool, where the gradient write-back runs on a side stream right after the
+call and must wait for it (the call marks the sequence as used, as
+pkv_chunk_attn_bwd does).
 
 The file is named to be collected last, so a run that stops at the first
 failure has already run every other test; it also passes on its own.
@@ -15,10 +23,11 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from paged_kv_chunk_chunked_gb300 import binding as B
 from paged_kv_chunk_chunked_gb300 import build as pkv_build
 from paged_kv_chunk_chunked_gb300 import synth
-from paged_kv_chunk_chunked_gb300.sweep import ChunkSweep, to_numpy
+from paged_kv_chunk_chunked_gb300.sweep import ChunkSweep, to_device, to_numpy
 
 pytestmark = pytest.mark.gpu
 
@@ -37,44 +46,125 @@ def _rel(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
 
 
+def _oracle(w):
+    n = w.n_chunks
+    qs = [synth.chunk_q(w, c) for c in range(n)]
+    ks = [synth.chunk_k(w, c) for c in range(n)]
+    vs = [synth.chunk_v(w, c) for c in range(n)]
+    dos = [synth.chunk_do(w, c) for c in range(n)]
+    bt = synth.block_table(w)
+    ref = oracle.chunk_recurrent_step(qs, ks, vs, dos, bt, w.P, w.n_phys, topk=w.topk)
+    return ref, bt
+
+
 CASES = {
-    # tensor-core kernels: bf16, page 128, d 128, permuted block table
-    "bf16_tensor_cores": synth.workload("qwen7b_dense_32k", N=768, C=256, Hq=4, Hkv=2,
+    # tensor-core kernels: bf16, page 128, d 128, 7:1 grouping, permuted block table
+    "bf16_tensor_cores": synth.workload("qwen7b_dense_32k", N=768, C=256, Hq=14, Hkv=2,
                                         table="perm", extra_pages=2),
     # CUDA-core kernels: fp32, page 16, d 64
     "f32_cuda_cores": synth.workload("tiny_dense_f32"),
+    # page-sparse: the selection comes from pkv_page_topk
+    "bf16_sparse_topk": synth.workload("qwen7b_sparse_256k", N=2048, C=1024, Hq=4, Hkv=2,
+                                       extra_pages=3, topk=(3, 1, 2)),
 }
 
 
 @pytest.mark.parametrize("case", sorted(CASES))
-def test_noalloc_backward_matches_allocating_backward(case):
+def test_noalloc_backward_matches_oracle(case):
     w = CASES[case]
+    ref, bt = _oracle(w)
+    tol = REL_TOL[w.dtype]
+    dk_ref = oracle.logical_rows(ref["dkpool"], bt, w.N, w.P)
+    dv_ref = oracle.logical_rows(ref["dvpool"], bt, w.N, w.P)
     sw = ChunkSweep(w).load_inputs()
     try:
         sw.reset()
+        sels = []
         for c in range(w.n_chunks):
-            sw.forward(c)
-        for c in reversed(range(w.n_chunks)):
-            sw.backward(c)
-        ref = sw.gather()
-        dq_ref = [to_numpy(x) for x in sw.dq]
-        dk_ref, dv_ref = to_numpy(ref["dk"]), to_numpy(ref["dv"])
-        for call in range(2):                       # two calls in a row share the array
+            s, e = w.chunk_range(c)
+            sel = None
+            if w.topk is not None:
+                B.pkv_append(sw.seq, sw.k[c], sw.v[c], e - s)
+                K, ns, nl = w.topk
+                sel = torch.empty(((e - s + w.P - 1) // w.P, w.Hkv, K + ns + nl),
+                                  dtype=torch.int32, device="cuda")
+                B.pkv_page_topk(sw.seq, sw.q[c], s, e - s, K, ns, nl, sel)
+                # clustered keys leave no score ties: the selection is the oracle's
+                np.testing.assert_array_equal(sel.cpu().numpy(), ref["sel"][c])
+                B.pkv_chunk_attn_fwd(sw.seq, sw.q[c], s, e - s, sw.o[c], sw.lse[c], sel)
+            else:
+                sw.forward(c)
+            sels.append(sel)
+        for call in range(2):                       # two sweeps in a row share the array
             B.pkv_grad_zero(sw.seq)
             dq = [torch.full_like(x, float("nan")) for x in sw.dq]
             for c in reversed(range(w.n_chunks)):
                 s, e = w.chunk_range(c)
                 B.pkv_chunk_attn_bwd_noalloc(sw.seq, sw.q[c], sw.o[c], sw.do[c], sw.lse[c], s,
-                                             e - s, dq[c])
+                                             e - s, dq[c], sels[c])
             got = sw.gather()
             B.pkv_check(sw.pool)
-            tol = REL_TOL[w.dtype]
             for c in range(w.n_chunks):
-                assert _rel(to_numpy(dq[c]), dq_ref[c]) <= tol, (call, c)
+                assert _rel(to_numpy(dq[c]), ref["dq"][c]) <= tol, (call, c)
             assert _rel(to_numpy(got["dk"]), dk_ref) <= tol, call
             assert _rel(to_numpy(got["dv"]), dv_ref) <= tol, call
     finally:
         sw.close()
+
+
+def test_noalloc_backward_on_pinned_host_pool_orders_the_writeback():
+    """Pinned-host pool: per chunk in reverse, stage K/V and gradient pages on a
+    side stream, run the no-allocation backward on the main stream, and queue
+    the gradient write-back on the side stream at once (no host wait between).
+    The written-back host gradient pages must equal the oracle's."""
+    w = synth.workload("qwen7b_sparse_1m_offload", N=3072, C=1024, Hq=4, Hkv=2,
+                       extra_pages=5, topk=(3, 1, 2))
+    ref, bt = _oracle(w)
+    K, ns, nl = w.topk
+    pool = B.pkv_pool_create(w.P, w.Hkv, w.Hq, w.d, B.PKV_BF16, w.n_phys,
+                             residency=B.PKV_RES_PINNED_HOST, n_device_slots=w.n_pages)
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    try:
+        seq = B.pkv_seq_create(pool)
+        B.pkv_set_block_table(seq, bt)
+        dev = lambda x: to_device(x, "bf16")
+        q = [dev(synth.chunk_q(w, c)) for c in range(w.n_chunks)]
+        do = [dev(synth.chunk_do(w, c)) for c in range(w.n_chunks)]
+        o, lse, dq, sels = [], [], [], []
+        for c in range(w.n_chunks):
+            s, e = w.chunk_range(c)
+            B.pkv_append(seq, dev(synth.chunk_k(w, c)), dev(synth.chunk_v(w, c)), e - s, main)
+            sel = torch.empty(((e - s) // w.P, w.Hkv, K + ns + nl), dtype=torch.int32,
+                              device="cuda")
+            B.pkv_page_topk(seq, q[c], s, e - s, K, ns, nl, sel, None, main)
+            sels.append(sel)
+            o.append(torch.empty_like(q[c]))
+            lse.append(torch.empty((w.Hq, e - s), dtype=torch.float32, device="cuda"))
+            dq.append(torch.empty_like(q[c]))
+            B.pkv_prefetch(seq, sel, sel.numel(), B.PKV_STAGE_KV, side)
+            B.pkv_wait(seq, main, 0)
+            B.pkv_chunk_attn_fwd(seq, q[c], s, e - s, o[c], lse[c], sel, main)
+        for c in reversed(range(w.n_chunks)):
+            s, e = w.chunk_range(c)
+            B.pkv_prefetch(seq, sels[c], sels[c].numel(), B.PKV_STAGE_KV | B.PKV_STAGE_GRADS, side)
+            B.pkv_wait(seq, main, 0)
+            B.pkv_chunk_attn_bwd_noalloc(seq, q[c], o[c], do[c], lse[c], s, e - s, dq[c],
+                                         sels[c], main)
+            B.pkv_writeback_grads(seq, side)
+        B.pkv_wait(seq, main, 10_000_000)
+        dk = torch.empty((w.N, w.Hkv, w.d), dtype=torch.float32, device="cuda")
+        dv = torch.empty_like(dk)
+        B.pkv_gather(seq, None, None, dk, dv, None, main)
+        torch.cuda.synchronize()
+        B.pkv_check(pool)
+        for c in range(w.n_chunks):
+            np.testing.assert_array_equal(sels[c].cpu().numpy(), ref["sel"][c])
+            assert _rel(to_numpy(dq[c]), ref["dq"][c]) <= 2e-2, c
+        assert _rel(to_numpy(dk), oracle.logical_rows(ref["dkpool"], bt, w.N, w.P)) <= 2e-2
+        assert _rel(to_numpy(dv), oracle.logical_rows(ref["dvpool"], bt, w.N, w.P)) <= 2e-2
+    finally:
+        B.pkv_pool_destroy(pool)
 
 
 def test_noalloc_rejects_chunks_beyond_the_fixed_scratch():
