@@ -1,16 +1,30 @@
 """Full-size parity: the bench workloads, run exactly as bench.py runs them,
 checked against the oracle on sampled outputs and on identities that hold at
-any size.
+any size; plus the bench's head layout (28 query heads, 4 KV heads, d 128,
+page 128) in full at a size the oracle finishes.
 
 Sampled: O, LSE and dQ of seeded query rows (the oracle computes each row
-alone, over every key it sees); dK and dV of the last page (seen only by the
-last page's queries). Sparse: the selection of every query page of the last
-chunk (ties within 1e-5 allowed), and rows over the selected pages. Identities:
-sum_j dK_j = 0 and sum_j dV_j = sum of dO over the group's heads and queries,
-per KV head (rows of P sum to one; rows of dS sum to zero), for dense and
-sparse alike. Tolerances as in the other parity tests: O/LSE max-abs 1e-2,
-dQ/dK/dV relative Frobenius 2e-2; identities relative 2e-2.
+alone, over every key it sees). dK and dV of sampled pages for every KV head,
+each against the oracle's sum over every query that sees the page (computed
+in parallel by tests/oracle_pool.py):
+  dense 32K: the final pool rows of a page of chunk 0, the pages on both
+      sides of a chunk boundary, a page inside a later chunk and the last page;
+  dense 128K, permuted table: the contribution of two whole chunks (the
+      difference of the pool before and after each chunk's backward) to pages
+      of chunk 0, on a chunk boundary and further on; these launches split
+      each page's dK/dV over several CTAs that all add into the same rows;
+  sparse 256K: every chunk's selection against the oracle (ties within 1e-5),
+      then the final rows of pages that many query pages of many chunks
+      selected, per KV head, over those selections;
+  sparse 1M, pinned host: the sink page (selected by every query page), the
+      most-selected candidate page and the chunk's first page, per KV head.
+Identities: sum_j dK_j = 0 and sum_j dV_j = sum of dO over the group's heads
+and queries, per KV head (rows of P sum to one; rows of dS sum to zero).
+Tolerances as in the other parity tests: O/LSE max-abs 1e-2, dQ/dK/dV
+relative Frobenius 2e-2 (per sampled page and KV head); identities 2e-2.
 """
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -21,7 +35,10 @@ from paged_kv_chunk_chunked_gb300 import build as pkv_build
 from paged_kv_chunk_chunked_gb300 import synth
 from paged_kv_chunk_chunked_gb300.sweep import ChunkSweep, to_device, to_numpy
 
+from oracle_pool import OraclePool
+
 pytestmark = pytest.mark.gpu
+TIE = 1e-5
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -29,6 +46,12 @@ def _lib():
     pkv_build.build()
     B.lib()
     torch.cuda.set_device(0)
+
+
+@pytest.fixture(scope="module")
+def opool():
+    with OraclePool() as p:
+        yield p
 
 
 def _rel(a, b):
@@ -83,9 +106,39 @@ def _check_identities(w, g, dos_sum):
         assert _rel(sv, dos_sum[kv]) <= 2e-2, kv
 
 
-@pytest.mark.parametrize("name", ["qwen7b_dense_32k", "qwen7b_dense_128k_perm"])
-def test_dense_full_size_sampled(name):
-    w = synth.workload(name)
+def _dos_sum(w):
+    dos_sum = np.zeros((w.Hkv, w.d))
+    for c in range(w.n_chunks):
+        do = synth.chunk_do(w, c).astype(np.float64)
+        for kv in range(w.Hkv):
+            dos_sum[kv] += do[:, kv * w.g:(kv + 1) * w.g].sum((0, 1))
+    return dos_sum
+
+
+def _page_rows(seq, w, pages, stream=None):
+    """The gradient pool's dK/dV rows of the given logical pages, [P, Hkv, d] each."""
+    out = {}
+    for p in pages:
+        dk = torch.empty((w.P, w.Hkv, w.d), dtype=torch.float32, device="cuda")
+        dv = torch.empty_like(dk)
+        B.pkv_gather_rows(seq, p * w.P, w.P, None, None, dk, dv, stream)
+        out[p] = (dk, dv)
+    torch.cuda.synchronize()
+    return {p: (to_numpy(a).astype(np.float64), to_numpy(b).astype(np.float64))
+            for p, (a, b) in out.items()}
+
+
+def _check_pages(got, want, what):
+    """Per page and KV head: relative Frobenius <= 2e-2 for dK and dV."""
+    for p in want:
+        for kv in range(want[p][0].shape[1]):
+            for t, name in ((0, "dk"), (1, "dv")):
+                e = _rel(got[p][t][:, kv], want[p][t][:, kv])
+                assert e <= 2e-2, (what, name, p, kv, e)
+
+
+def test_dense_32k_full_size_sampled(opool):
+    w = synth.workload("qwen7b_dense_32k")
     sw = ChunkSweep(w).load_inputs()
     try:
         sw.run()
@@ -95,28 +148,82 @@ def test_dense_full_size_sampled(name):
         last = w.n_chunks - 1
         _check_rows(w, sw, K_all, V_all, last, heads=(0, 13, w.Hq - 1), n_rows=16)
         _check_rows(w, sw, K_all, V_all, 0, heads=(6, 20), n_rows=16)
-        dos_sum = np.zeros((w.Hkv, w.d))
-        for c in range(w.n_chunks):
-            do = synth.chunk_do(w, c).astype(np.float64)
-            for kv in range(w.Hkv):
-                dos_sum[kv] += do[:, kv * w.g:(kv + 1) * w.g].sum((0, 1))
-        _check_identities(w, g, dos_sum)
-        # the last page: only the last page's own queries see it
-        page = w.n_pages - 1
-        p0 = page * w.P
-        dk_gpu, dv_gpu = to_numpy(g["dk"]), to_numpy(g["dv"])
-        s, e = w.chunk_range(last)
-        q = synth.chunk_q(w, last)[p0 - s:]
-        do = synth.chunk_do(w, last)[p0 - s:]
-        o, lse = oracle.attention_forward(q, K_all, V_all, p0)
-        _, dk, dv = oracle.attention_backward(q, K_all, V_all, o, do, lse, p0)
-        assert _rel(dk_gpu[p0:], dk[p0:]) <= 2e-2
-        assert _rel(dv_gpu[p0:], dv[p0:]) <= 2e-2
+        _check_identities(w, g, _dos_sum(w))
+        # final rows: chunk 0's page 3 (every chunk adds into it), both sides of
+        # the chunk 3 / chunk 4 boundary, a page inside chunk 6, the last page
+        ppc = w.C // w.P
+        pages = [3, 4 * ppc - 1, 4 * ppc, 6 * ppc + 8, w.n_pages - 1]
+        want = opool.dense_page_grads(w, pages)
+        dk, dv = to_numpy(g["dk"]), to_numpy(g["dv"])
+        got = {p: (dk[p * w.P:(p + 1) * w.P], dv[p * w.P:(p + 1) * w.P]) for p in pages}
+        _check_pages(got, want, "final")
     finally:
         sw.close()
 
 
-def test_sparse_256k_full_size_sampled():
+def test_dense_128k_perm_full_size_sampled(opool):
+    w = synth.workload("qwen7b_dense_128k_perm")
+    ppc = w.C // w.P
+    # chunk -> the pages whose contribution from that chunk is checked
+    probe = {8: [3, ppc - 1, ppc, 8 * ppc - 1, 8 * ppc, 8 * ppc + 58],
+             1: [3, ppc - 1, ppc, 2 * ppc - 1]}
+    sw = ChunkSweep(w).load_inputs()
+    try:
+        sw.reset()
+        for c in range(w.n_chunks):
+            sw.forward(c)
+        snaps = {}
+        for c in reversed(range(w.n_chunks)):
+            if c in probe:
+                snaps[(c, "before")] = _page_rows(sw.seq, w, probe[c])
+            sw.backward(c)
+            if c in probe:
+                snaps[(c, "after")] = _page_rows(sw.seq, w, probe[c])
+        B.pkv_check(sw.pool)
+        g = sw.gather()
+        for c, pages in probe.items():
+            got = {p: (snaps[(c, "after")][p][0] - snaps[(c, "before")][p][0],
+                       snaps[(c, "after")][p][1] - snaps[(c, "before")][p][1]) for p in pages}
+            want = opool.dense_page_grads(w, pages, chunks=[c])
+            _check_pages(got, want, f"chunk {c}")
+        K_all, V_all = _logical_kv(w)
+        last = w.n_chunks - 1
+        _check_rows(w, sw, K_all, V_all, last, heads=(0, 13, w.Hq - 1), n_rows=16)
+        _check_rows(w, sw, K_all, V_all, 0, heads=(6, 20), n_rows=16)
+        _check_identities(w, g, _dos_sum(w))
+        # the last page's final rows: only the last page's own queries see it
+        page = w.n_pages - 1
+        want = opool.dense_page_grads(w, [page], chunks=[last], block=128)
+        dk, dv = to_numpy(g["dk"]), to_numpy(g["dv"])
+        _check_pages({page: (dk[page * w.P:], dv[page * w.P:])}, want, "final")
+    finally:
+        sw.close()
+
+
+def _check_selection(sel_gpu, q, s, K_all, w, K, ns, nl):
+    """The GPU's selection of every query page and KV head of a chunk against
+    the oracle (a differing page must score within 1e-5 of the K-th score).
+    Returns {(i, kv): the GPU's list}."""
+    e = s + q.shape[0]
+    lists, _ = oracle.chunk_selection(q, s, K_all[:e], w.P, K, ns, nl)
+    qbar = oracle.query_page_means(q, w.P, w.Hkv)
+    rep = oracle.page_representatives(K_all[:e], w.P)
+    got_lists = {}
+    for i in range(len(lists)):
+        for kv in range(w.Hkv):
+            got = [int(x) for x in sel_gpu[i, kv] if x >= 0]
+            want = lists[i][kv]
+            if got != want:
+                qpg = s // w.P + i
+                cand = np.arange(ns, qpg - nl + 1)
+                kth = np.sort(rep[cand, kv] @ qbar[i, kv])[::-1][K - 1]
+                for pg in set(got) ^ set(want):
+                    assert abs(rep[pg, kv] @ qbar[i, kv] - kth) <= TIE, (s, i, kv, pg)
+            got_lists[(i, kv)] = got
+    return got_lists
+
+
+def test_sparse_256k_full_size_sampled(opool):
     w = synth.workload("qwen7b_sparse_256k")
     K, ns, nl = w.topk
     sw = ChunkSweep(w).load_inputs()
@@ -135,34 +242,40 @@ def test_sparse_256k_full_size_sampled():
         B.pkv_check(sw.pool)
         g = sw.gather()
         K_all, V_all = _logical_kv(w)
-        last = w.n_chunks - 1
-        s, e = w.chunk_range(last)
-        q = synth.chunk_q(w, last)
-        sel_gpu = sels[last].cpu().numpy()
-        # selection of every query page of the last chunk vs the oracle (tie rule 1e-5)
-        lists, _ = oracle.chunk_selection(q, s, K_all[:e], w.P, K, ns, nl)
-        qbar = oracle.query_page_means(q, w.P, w.Hkv)
-        rep = oracle.page_representatives(K_all[:e], w.P)
-        allowed = {}
-        for i in range(len(lists)):
-            for kv in range(w.Hkv):
-                got = [int(x) for x in sel_gpu[i, kv] if x >= 0]
-                want = lists[i][kv]
-                if got != want:
-                    qpg = s // w.P + i
-                    cand = np.arange(ns, qpg - nl + 1)
-                    kth = np.sort(rep[cand, kv] @ qbar[i, kv])[::-1][K - 1]
-                    for pg in set(got) ^ set(want):
-                        assert abs(rep[pg, kv] @ qbar[i, kv] - kth) <= 1e-5, (i, kv, pg)
-                allowed[(i, kv)] = got          # the pages the GPU attended to
-        _check_rows(w, sw, K_all, V_all, last, heads=(0, 15, w.Hq - 1), n_rows=12,
-                    allowed_pages=allowed)
-        dos_sum = np.zeros((w.Hkv, w.d))
+        # every chunk's selection against the oracle
+        lists = {}
         for c in range(w.n_chunks):
-            do = synth.chunk_do(w, c).astype(np.float64)
-            for kv in range(w.Hkv):
-                dos_sum[kv] += do[:, kv * w.g:(kv + 1) * w.g].sum((0, 1))
-        _check_identities(w, g, dos_sum)
+            s, e = w.chunk_range(c)
+            lists[c] = _check_selection(sels[c].cpu().numpy(), synth.chunk_q(w, c), s, K_all, w,
+                                        K, ns, nl)
+        last = w.n_chunks - 1
+        _check_rows(w, sw, K_all, V_all, last, heads=(0, 15, w.Hq - 1), n_rows=12,
+                    allowed_pages=lists[last])
+        _check_identities(w, g, _dos_sum(w))
+        # sampled pages per KV head: the page of chunk 0 (not the sink) picked
+        # by query pages of the most chunks, among those picked by at most 160
+        # query pages; the last page of chunk 15 (a chunk boundary); page 1500
+        ppc = w.C // w.P
+        count, chunks_of = {}, {}
+        for c, lc in lists.items():
+            for (i, kv), pl in lc.items():
+                for p in pl:
+                    count[(p, kv)] = count.get((p, kv), 0) + 1
+                    chunks_of.setdefault((p, kv), set()).add(c)
+        pages_by_kv = {}
+        for kv in range(w.Hkv):
+            early = [p for p in range(ns, ppc) if 16 <= count.get((p, kv), 0) <= 160]
+            assert early, kv
+            p0 = max(early, key=lambda p: (len(chunks_of[(p, kv)]), -p))
+            assert len(chunks_of[(p0, kv)]) >= 3, (kv, p0, chunks_of[(p0, kv)])
+            pages_by_kv[kv] = [p0, 16 * ppc - 1, 1500]
+        want, n_tasks = opool.sparse_page_grads(
+            w, lists, pages_by_kv, lambda p: (K_all[p * w.P:(p + 1) * w.P], V_all[p * w.P:(p + 1) * w.P]))
+        dk, dv = to_numpy(g["dk"]), to_numpy(g["dv"])
+        for (p, kv), (wk, wv) in want.items():
+            rows = slice(p * w.P, (p + 1) * w.P)
+            assert _rel(dk[rows, kv], wk) <= 2e-2, ("dk", p, kv)
+            assert _rel(dv[rows, kv], wv) <= 2e-2, ("dv", p, kv)
     finally:
         sw.close()
 
@@ -223,17 +336,12 @@ def test_local_256k_full_size_sampled():
         grow = slice(p * w.P, (p + 1) * w.P)
         assert _rel(to_numpy(g["dk"])[grow], dk[rows]) <= 2e-2
         assert _rel(to_numpy(g["dv"])[grow], dv[rows]) <= 2e-2
-        dos_sum = np.zeros((w.Hkv, w.d))
-        for c in range(w.n_chunks):
-            do = synth.chunk_do(w, c).astype(np.float64)
-            for kv in range(w.Hkv):
-                dos_sum[kv] += do[:, kv * w.g:(kv + 1) * w.g].sum((0, 1))
-        _check_identities(w, g, dos_sum)
+        _check_identities(w, g, _dos_sum(w))
     finally:
         sw.close()
 
 
-def test_sparse_1m_pinned_host_full_size_sampled():
+def test_sparse_1m_pinned_host_full_size_sampled(opool):
     """The 1M-token pinned-host workload as bench.py runs it: every K/V page and
     fp32 gradient page in mapped pinned host memory, the last chunk's selected
     pages staged into HBM slots on a side stream for its forward and backward,
@@ -335,6 +443,32 @@ def test_sparse_1m_pinned_host_full_size_sampled():
         dv = torch.empty_like(dk)
         B.pkv_gather(seq, None, None, dk, dv, None, main)
         torch.cuda.synchronize()
+        # sampled pages per KV head against the oracle over this chunk's
+        # selections: the sink page (every query page lists it), the candidate
+        # page the most query pages picked, and the chunk's first page
+        pages_by_kv = {}
+        for kv in range(w.Hkv):
+            cnt = {}
+            for i in range(sel_gpu.shape[0]):
+                for pg in lists[(i, kv)]:
+                    if ns <= pg < qp0:
+                        cnt[pg] = cnt.get(pg, 0) + 1
+            top = max(cnt, key=lambda pg: (cnt[pg], -pg))
+            pages_by_kv[kv] = [0, top, qp0]
+        @functools.lru_cache(maxsize=1)
+        def kv_chunk(ch):
+            return synth.chunk_k(w, ch), synth.chunk_v(w, ch)
+
+        def page_kv(pg):                          # pages are asked for in ascending order
+            kc, vc = kv_chunk(pg // ppc)
+            o0 = (pg % ppc) * w.P
+            return kc[o0:o0 + w.P], vc[o0:o0 + w.P]
+
+        want, _ = opool.sparse_page_grads(w, {c: lists}, pages_by_kv, page_kv)
+        for (pg, kv), (wk, wv) in want.items():
+            rows = slice(pg * w.P, (pg + 1) * w.P)
+            assert _rel(dk[rows, kv].double().cpu().numpy(), wk) <= 2e-2, ("dk", pg, kv)
+            assert _rel(dv[rows, kv].double().cpu().numpy(), wv) <= 2e-2, ("dv", pg, kv)
         sk = dk.double().sum(0).cpu().numpy()
         sv = dv.double().sum(0).cpu().numpy()
         nk = torch.sqrt((dk.double() ** 2).sum(0).sum(-1)).cpu().numpy()
@@ -344,3 +478,66 @@ def test_sparse_1m_pinned_host_full_size_sampled():
             assert _rel(sv[kv], do64[:, kv * w.g:(kv + 1) * w.g].sum((0, 1))) <= 2e-2, kv
     finally:
         B.pkv_pool_destroy(pool)
+
+
+def _gpu_sweep_outputs(sw):
+    g = sw.gather()
+    return dict(o=[to_numpy(x) for x in sw.o], lse=[to_numpy(x) for x in sw.lse],
+                dq=[to_numpy(x) for x in sw.dq], dk=to_numpy(g["dk"]), dv=to_numpy(g["dv"]))
+
+
+def _compare_all(w, got, ref):
+    for c in range(w.n_chunks):
+        assert np.abs(got["o"][c] - ref["o"][c]).max() <= 1e-2, ("o", c)
+        assert np.abs(got["lse"][c] - ref["lse"][c]).max() <= 1e-2, ("lse", c)
+        assert _rel(got["dq"][c], ref["dq"][c]) <= 2e-2, ("dq", c)
+    for kv in range(w.Hkv):
+        assert _rel(got["dk"][:, kv], ref["dk"][:, kv]) <= 2e-2, ("dk", kv)
+        assert _rel(got["dv"][:, kv], ref["dv"][:, kv]) <= 2e-2, ("dv", kv)
+
+
+def test_bench_head_layout_dense_8k_every_output(opool):
+    """28 query heads / 4 KV heads, d 128, page 128, chunks of 4096 as in the
+    dense bench workload, at 8192 tokens (two chunks, permuted pages): O, LSE,
+    dQ, dK, dV of every position against the oracle, element by element."""
+    w = synth.workload("qwen7b_dense_32k", N=8192, table="perm", extra_pages=5)
+    sw = ChunkSweep(w).load_inputs()
+    try:
+        sw.run()
+        B.pkv_check(sw.pool)
+        got = _gpu_sweep_outputs(sw)
+    finally:
+        sw.close()
+    _compare_all(w, got, opool.dense_full(w))
+
+
+def test_bench_head_layout_sparse_16k_every_output(opool):
+    """The page-sparse bench workload's layout and selection (top-64 + 1 sink +
+    2 local, clustered keys, chunks of 8192, permuted pages) at 16384 tokens:
+    the selections against the oracle, then O, LSE, dQ, dK, dV of every
+    position against the oracle over those selections."""
+    w = synth.workload("qwen7b_sparse_256k", N=16384)
+    K, ns, nl = w.topk
+    sw = ChunkSweep(w).load_inputs()
+    try:
+        sw.reset()
+        sels = []
+        for c in range(w.n_chunks):
+            s, e = w.chunk_range(c)
+            B.pkv_append(sw.seq, sw.k[c], sw.v[c], e - s)
+            sel = torch.empty(((e - s) // w.P, w.Hkv, K + ns + nl), dtype=torch.int32, device="cuda")
+            B.pkv_page_topk(sw.seq, sw.q[c], s, e - s, K, ns, nl, sel)
+            sels.append(sel)
+            B.pkv_chunk_attn_fwd(sw.seq, sw.q[c], s, e - s, sw.o[c], sw.lse[c], sel)
+        for c in reversed(range(w.n_chunks)):
+            sw.backward(c, sel=sels[c])
+        B.pkv_check(sw.pool)
+        got = _gpu_sweep_outputs(sw)
+        K_all, V_all = _logical_kv(w)
+        lists = {c: _check_selection(sels[c].cpu().numpy(), synth.chunk_q(w, c),
+                                     w.chunk_range(c)[0], K_all, w, K, ns, nl)
+                 for c in range(w.n_chunks)}
+    finally:
+        sw.close()
+    _compare_all(w, got, opool.sparse_full(
+        w, lists, lambda p: (K_all[p * w.P:(p + 1) * w.P], V_all[p * w.P:(p + 1) * w.P])))
