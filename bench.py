@@ -46,6 +46,10 @@ def parse_args():
                          "length; 0 = the workload's own), e.g. for small profiling runs")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-sparse", action="store_true",
+                    help="dense line only: skip its sub-record of the page-sparse 256K workload")
+    ap.add_argument("--sparse-steps", type=int, default=5,
+                    help="timed steps of the page-sparse sub-record (2 warm-up steps)")
     ap.add_argument("--flags", type=int, default=0, help="pool flags (1 = CUDA cores only)")
     ap.add_argument("--offload-chunks", type=int, default=8,
                     help="offload workload: chunks measured at the end of the sequence")
@@ -250,6 +254,22 @@ def traffic_for(kernel: str, source: str):
         return None
 
 
+def dense_config(w, world: int) -> dict:
+    """The `config` of the dense line; the reference arm reports the same."""
+    return {"workload": w.name, "N": w.N, "C": w.C, "P": w.P, "Hq": w.Hq, "Hkv": w.Hkv,
+            "d": w.d, "block_table": w.table, "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (Q, dO, O, dQ: 4 x 235 MB per step)"}
+
+
+def tensor_peak(pk: dict, kind: str):
+    """The bf16 tensor peak for kernels timed in a timed region of about a
+    second or less at full clocks: MEASURED_PEAKS' burst figure (a cuBLAS GEMM
+    timed alone); the sustained figure was taken under the power cap at lower
+    clocks."""
+    return pk.get("bf16_tflops", pk.get("bf16_tflops_sustained")), \
+        f"{kind} bf16_tflops (burst: the kernels run at full clocks in a short timed region)"
+
+
 # ------------------------------------------------------------------ pkv arm
 
 def run_pkv(args, world, rank):
@@ -312,7 +332,7 @@ def run_pkv(args, world, rank):
     flops_s, ms_step = replica_rate(flops_fwd + flops_bwd, t0.elapsed_time(t1) / args.steps, world)
     tflops = flops_s / 1e12
     pk, pk_kind = peaks()
-    peak_tc = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
+    peak_tc, peak_kind = tensor_peak(pk, pk_kind)
     fwd_call = statistics.mean(fwd_ms) / n
     bwd_call = statistics.mean(bwd_ms) / n
     fwd_ach = flops_fwd / n / (fwd_call * 1e-3) / 1e12
@@ -332,8 +352,7 @@ def run_pkv(args, world, rank):
     dom = max(prof, key=lambda k: prof[k][1])
     dom_cnt, dom_ms = prof[dom]
     roof = {
-        "bound": "tensor", "unit": "TFLOP/s", "peak": peak_tc,
-        "peak_kind": f"{pk_kind} bf16_tflops_sustained (kernels timed inside a long step)",
+        "bound": "tensor", "unit": "TFLOP/s", "peak": peak_tc, "peak_kind": peak_kind,
         "kernel": dom,
     }
     if dom in per_step:
@@ -350,13 +369,15 @@ def run_pkv(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) Q/K/V/dO, bf16-rounded)",
-        "config": {"workload": w.name, "N": w.N, "C": w.C, "P": w.P, "Hq": w.Hq, "Hkv": w.Hkv,
-                   "d": w.d, "block_table": w.table, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (Q, dO, O, dQ: 4 x 235 MB per step)"},
+        "config": dense_config(w, world),
         "tokens_per_s_per_layer": round(world * w.N / (ms_step * 1e-3), 1),
         "pct_bf16_peak": round(100 * tflops / world / peak_tc, 2),
         "fwd_ms_per_step": round(statistics.mean(fwd_ms), 3),
         "bwd_ms_per_step": round(statistics.mean(bwd_ms), 3),
+        "fwd_ms_per_chunk": [round(statistics.mean(fwd_ev[k][c][0].elapsed_time(fwd_ev[k][c][1])
+                                                   for k in range(args.steps)), 4) for c in range(n)],
+        "bwd_ms_per_chunk": [round(statistics.mean(bwd_ev[k][c][0].elapsed_time(bwd_ev[k][c][1])
+                                                   for k in range(args.steps)), 4) for c in range(n)],
         "fwd_tflops": round(fwd_ach, 2), "bwd_tflops": round(bwd_ach, 2),
         "roofline": roof,
         "kernels": kernels,
@@ -367,12 +388,14 @@ def run_pkv(args, world, rank):
     if not args.no_e2e:
         out["e2e"] = run_e2e(args, w, sw, step, world)
     out["hbm_kernels"] = hbm_kernels(args, w, sw, prof, pk)
+    sw.close()
+    if world == 1 and not args.no_sparse:
+        out["sparse"] = sparse_subrecord(args, world, rank)
     if rank == 0 and world == 1 and not args.no_cpu:
-        flops, dt, desc = oracle_sample(w, w.C)
+        flops, dt, desc = oracle_sample(w, REF_SAMPLE_QUERIES(w))
         out["cpu_baseline"] = {"value": round(flops / dt / 1e12, 6), "unit": UNIT,
                                "cores": cpu_threads(), "kind": "oracle", "sample": desc,
                                "seconds": round(dt, 2)}
-    sw.close()
     return out
 
 
@@ -474,10 +497,15 @@ def run_e2e(args, w, sw, step, world):
 
 # ------------------------------------------------------------------ reference arm (the oracle)
 
+def REF_SAMPLE_QUERIES(w) -> int:
+    """Queries of the oracle's sample (cpu_baseline and the reference arm): the
+    last chunk's, one query head, against every earlier key."""
+    return w.C
+
+
 def run_reference(args, world, rank):
-    from paged_kv_chunk_chunked_gb300 import synth
     w = bench_workload(args)
-    n_q = 512
+    n_q = REF_SAMPLE_QUERIES(w)
     for _ in range(args.warmup):
         oracle_sample(w, n_q)
     times, flops, desc = [], 0, ""
@@ -490,9 +518,8 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "N": w.N, "C": w.C, "P": w.P, "Hq": w.Hq, "Hkv": w.Hkv,
-                   "d": w.d, "block_table": w.table},
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) Q/K/V/dO, bf16-rounded)",
+        "config": dense_config(w, world),
         "cpu_baseline": {"value": round(val, 6), "unit": UNIT, "cores": cpu_threads(),
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(val, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -576,7 +603,7 @@ def run_sparse(args, world, rank):
     flops_s, ms = replica_rate(flops, ms, world)
     tflops = flops_s / 1e12
     pk, pk_kind = peaks()
-    peak_tc = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
+    peak_tc, peak_kind = tensor_peak(pk, pk_kind)
     kernels = {k: {"launches": c, "ms_per_step": round(t / args.steps, 3)} for k, (c, t) in prof.items()}
     # page selection: the page-query kernel reads the chunk's Q once (HBM-bound)
     q_bytes = w.C * w.Hq * w.d * 2
@@ -609,10 +636,13 @@ def run_sparse(args, world, rank):
                      "achieved": round(dom_ach, 2) if dom_ach else None, "peak": peak_tc,
                      "frac": round(dom_ach / peak_tc, 4) if dom_ach else None,
                      "flops_per_launch": dom_flops / max(dom_cnt, 1),
-                     "peak_kind": f"{pk_kind} bf16_tflops_sustained", "traffic": None},
+                     "peak_kind": peak_kind, "traffic": None},
         "kernels": kernels, "gpu_launches": sum(v[0] for v in prof.values()),
         "clocks": clk,
     }
+    sel = selection_record(w, prof, args.steps, pk, pk_kind, K + ns + nl)
+    if sel:
+        out["selection"] = sel
     if "qbar_kernel" in prof:
         # page scoring: the page-query kernel reads the chunk's Q once (HBM-bound)
         out["page_query_roofline"] = {
@@ -622,6 +652,62 @@ def run_sparse(args, world, rank):
             "bytes_per_launch": q_bytes, "peak_kind": f"{pk_kind} hbm_gbs"}
         out["select_kernel_us_per_launch"] = round(1e3 * sel_ms / sel_cnt, 2)
     return out
+
+
+# Kernels of the page-selection chain (page queries, scores, top-K).
+SELECTION_KERNELS = ("qbar_kernel", "score_kernel", "select_kernel", "topk_fused_kernel",
+                     "topk_select_kernel")
+
+
+def selection_bytes(w, kmax: int) -> int:
+    """Algorithmic bytes of one sweep's page selection: per chunk, its queries
+    read once (n_q * Hq * d bf16), the representative of every candidate page
+    read once (fp32 [Hkv, d]) with its block-table entry, and the selection
+    written ([n_qp, Hkv, kmax] int32)."""
+    K, ns, nl = w.topk
+    el = 2 if w.dtype == "bf16" else 4
+    total = 0
+    for c in range(w.n_chunks):
+        s, e = w.chunk_range(c)
+        n_qp = (e - s + w.P - 1) // w.P
+        n_cand = max(0, s // w.P + n_qp - 1 - nl - ns + 1)
+        total += (e - s) * w.Hq * w.d * el + n_cand * (w.Hkv * w.d * 4 + 4) \
+            + n_qp * w.Hkv * kmax * 4
+    return total
+
+
+def selection_record(w, prof, steps, pk, pk_kind, kmax):
+    """HBM roofline of the page-selection chain over the timed steps: its
+    algorithmic bytes against the summed event time of its kernels."""
+    names = [k for k in SELECTION_KERNELS if k in prof]
+    if not w.topk or not names:
+        return None
+    ms = sum(prof[k][1] for k in names) / steps
+    byts = selection_bytes(w, kmax)
+    gbs = byts / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "unit": "GB/s", "kernels": names,
+            "bytes_per_step": byts, "ms_per_step": round(ms, 4),
+            "us_per_chunk": round(1e3 * ms / w.n_chunks, 2),
+            "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
+            "frac": round(gbs / pk["hbm_gbs"], 4), "peak_kind": f"{pk_kind} hbm_gbs",
+            "per_kernel_us_per_chunk": {k: round(1e3 * prof[k][1] / steps / w.n_chunks, 2)
+                                        for k in names}}
+
+
+def sparse_subrecord(args, world, rank):
+    """The page-sparse 256K workload, shortened (args.sparse_steps timed steps,
+    2 warm-up), for the dense line: its step time, TFLOP/s over attended
+    pairs, the dense sweep of the same context, the dominant kernel's tensor
+    roofline and the page-selection chain's HBM roofline."""
+    sub = argparse.Namespace(**vars(args))
+    sub.workload, sub.context = "qwen7b_sparse_256k", 0
+    sub.steps, sub.warmup = max(1, args.sparse_steps), 2
+    r = run_sparse(sub, world, rank)
+    keep = ("value", "unit", "steps", "warmup", "ms_per_step", "config", "tokens_per_s_per_layer",
+            "attended_pairs_per_step", "dense_ms_per_step", "sparse_speedup_vs_dense", "roofline",
+            "selection", "page_query_roofline", "select_kernel_us_per_launch", "kernels", "clocks",
+            "gpu_launches")
+    return {k: r[k] for k in keep if k in r}
 
 
 def run_topk_error_study(args, world, rank):

@@ -252,9 +252,10 @@ def test_sparse_256k_full_size_sampled(opool):
         _check_rows(w, sw, K_all, V_all, last, heads=(0, 15, w.Hq - 1), n_rows=12,
                     allowed_pages=lists[last])
         _check_identities(w, g, _dos_sum(w))
-        # sampled pages per KV head: the page of chunk 0 (not the sink) picked
-        # by query pages of the most chunks, among those picked by at most 160
-        # query pages; the last page of chunk 15 (a chunk boundary); page 1500
+        # sampled pages per KV head: among the pages of chunks 0 and 1 (not the
+        # sink) that query pages of at least 3 chunks picked, the one picked
+        # least often (bounding the oracle's work); the last page of chunk 15
+        # (a chunk boundary); page 1500
         ppc = w.C // w.P
         count, chunks_of = {}, {}
         for c, lc in lists.items():
@@ -264,10 +265,9 @@ def test_sparse_256k_full_size_sampled(opool):
                     chunks_of.setdefault((p, kv), set()).add(c)
         pages_by_kv = {}
         for kv in range(w.Hkv):
-            early = [p for p in range(ns, ppc) if 16 <= count.get((p, kv), 0) <= 160]
+            early = [p for p in range(ns, 2 * ppc) if len(chunks_of.get((p, kv), ())) >= 3]
             assert early, kv
-            p0 = max(early, key=lambda p: (len(chunks_of[(p, kv)]), -p))
-            assert len(chunks_of[(p0, kv)]) >= 3, (kv, p0, chunks_of[(p0, kv)])
+            p0 = min(early, key=lambda p: (count[(p, kv)], p))
             pages_by_kv[kv] = [p0, 16 * ppc - 1, 1500]
         want, n_tasks = opool.sparse_page_grads(
             w, lists, pages_by_kv, lambda p: (K_all[p * w.P:(p + 1) * w.P], V_all[p * w.P:(p + 1) * w.P]))
