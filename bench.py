@@ -862,10 +862,22 @@ def run_layer_loop(args, world, rank):
 def run_offload(args, world, rank):
     """Pinned-host offload of the 1M-token page-sparse workload. All 128 chunks'
     K/V are appended into pinned host pages; the measured step is the sparse
-    forward + backward of the last `--offload-chunks` chunks, each staging its
-    selected pages (K/V, then K/V + gradients) into HBM slots on a side stream
-    and writing the gradients back. The same step on a device-resident pool
-    gives the staging overhead."""
+    forward + backward of the last `--offload-chunks` chunks. Each chunk stages
+    its selected pages (K/V, then K/V + gradients) into the sequence's slot
+    cache on a side stream: pages already staged by an earlier chunk stay, so
+    only the difference crosses the host link; the gradients go back once, at
+    the end of the backward sweep, when the step releases the slots (every
+    step starts with an empty cache). The same step on a device-resident pool
+    gives the staging overhead.
+
+    --overlap-proj adds the computations the pages overlap with the transfer
+    (gist.science/de §2.C: with sparse attention, the key/value projections
+    that follow): the next chunk's Q and K/V projections while a chunk's pages
+    stream in for its forward, and the chunk's recomputed projections while
+    its pages and gradients stream in for its backward (bf16 cuBLAS GEMMs,
+    hidden 3584). It reports the copy time (the staging kernels' own event time), the
+    part of it the step exposes (pinned-host step minus device-resident step,
+    both with the GEMMs) and overlap = 1 - exposed / copy time."""
     import numpy as np
     import torch
     from paged_kv_chunk_chunked_gb300 import binding as B
@@ -882,6 +894,7 @@ def run_offload(args, world, rank):
     bt = synth.block_table(w)
     if args.slots <= 0:
         args.slots = w.n_pages
+    hidden = 3584
     res = {}
     for mode in ("pinned_host", "device"):
         host = mode == "pinned_host"
@@ -896,12 +909,12 @@ def run_offload(args, world, rank):
         lse = {c: torch.empty((w.Hq, w.C), dtype=torch.float32, device="cuda") for c in meas}
         sel = {c: torch.empty((w.C // w.P, w.Hkv, K + ns + nl), dtype=torch.int32, device="cuda")
                for c in meas}
-        # synthetic K/V projection of a chunk (Qwen2.5-7B: hidden 3584 -> 2 x Hkv x d),
-        # random weights; a plain cuBLAS GEMM on the main stream
+        # synthetic projections of a chunk (Qwen2.5-7B: hidden 3584; K/V 2 x Hkv x d
+        # columns, Q Hq x d), random weights; plain cuBLAS GEMMs on the main stream
         gen = torch.Generator(device="cuda").manual_seed(w.seed)
-        x_proj = torch.randn((w.C, 3584), device="cuda", generator=gen).to(torch.bfloat16)
-        w_proj = (torch.randn((3584, 2 * w.Hkv * w.d), device="cuda", generator=gen)
-                  / 60.0).to(torch.bfloat16)
+        x_proj = torch.randn((w.C, hidden), device="cuda", generator=gen).to(torch.bfloat16)
+        w_kv = (torch.randn((hidden, 2 * w.Hkv * w.d), device="cuda", generator=gen) / 60.0).to(torch.bfloat16)
+        w_q = (torch.randn((hidden, w.Hq * w.d), device="cuda", generator=gen) / 60.0).to(torch.bfloat16)
 
         def fill():
             B.pkv_seq_reset(seq)
@@ -913,26 +926,42 @@ def run_offload(args, world, rank):
                 B.pkv_append(seq, k, v, e - s, main_s)
             torch.cuda.synchronize()
 
-        def step(proj=False):
-            for c in meas:
-                s, e = w.chunk_range(c)
-                B.pkv_page_topk(seq, q[c], s, e - s, K, ns, nl, sel[c], None, main_s)
-                if host:
-                    B.pkv_prefetch(seq, sel[c], sel[c].numel(), B.PKV_STAGE_KV, side)
-                if proj:      # runs while the selected pages stream in (gist.science/nl)
-                    torch.matmul(x_proj, w_proj)
-                if host:
-                    B.pkv_wait(seq, main_s, 0)
-                B.pkv_chunk_attn_fwd(seq, q[c], s, e - s, o[c], lse[c], sel[c], main_s)
-            for c in reversed(meas):
-                s, e = w.chunk_range(c)
-                if host:
-                    B.pkv_prefetch(seq, sel[c], sel[c].numel(), B.PKV_STAGE_KV | B.PKV_STAGE_GRADS, side)
-                    B.pkv_wait(seq, main_s, 0)
-                B.pkv_chunk_attn_bwd(seq, q[c], o[c], do[c], lse[c], s, e - s, dq[c], sel[c], main_s)
-                if host:
-                    B.pkv_writeback_grads(seq, side)
+        mk = lambda: torch.cuda.Event(enable_timing=True)
+
+        def step(proj=False, rec=None):
+            """rec: dict collecting per-chunk event pairs (main-stream span of
+            the chunk from its prefetch to its attention call; side-stream span
+            of its staging)."""
+            for phase, chunks in (("fwd", meas), ("bwd", list(reversed(meas)))):
+                for c in chunks:
+                    s, e = w.chunk_range(c)
+                    if phase == "fwd":
+                        B.pkv_page_topk(seq, q[c], s, e - s, K, ns, nl, sel[c], None, main_s)
+                    m0, m1, c0, c1 = mk(), mk(), mk(), mk()
+                    if rec is not None:
+                        m0.record(main_s)
+                    if host:
+                        if rec is not None:
+                            side.wait_stream(main_s)
+                            c0.record(side)
+                        what = B.PKV_STAGE_KV if phase == "fwd" else B.PKV_STAGE_KV | B.PKV_STAGE_GRADS
+                        B.pkv_prefetch(seq, sel[c], sel[c].numel(), what, side)
+                        if rec is not None:
+                            c1.record(side)
+                    if proj:      # fwd: the next chunk's Q, K, V projections; bwd: the recomputed ones
+                        torch.matmul(x_proj, w_q)
+                        torch.matmul(x_proj, w_kv)
+                    if host:
+                        B.pkv_wait(seq, main_s, 0)
+                    if phase == "fwd":
+                        B.pkv_chunk_attn_fwd(seq, q[c], s, e - s, o[c], lse[c], sel[c], main_s)
+                    else:
+                        B.pkv_chunk_attn_bwd(seq, q[c], o[c], do[c], lse[c], s, e - s, dq[c], sel[c], main_s)
+                    if rec is not None:
+                        m1.record(main_s)
+                        rec.setdefault(phase, []).append((m0, m1, c0, c1) if host else (m0, m1))
             if host:
+                B.pkv_release_slots(seq, side)        # gradients back once; cold cache next step
                 B.pkv_wait(seq, main_s, 0)
 
         fill()
@@ -940,11 +969,7 @@ def run_offload(args, world, rank):
             step()
         torch.cuda.synchronize()
         B.pkv_check(pool)
-        # pages staged per chunk (union of the selection), for the byte count
-        staged_pages = 0
-        for c in meas:
-            u = np.unique(sel[c].cpu().numpy())
-            staged_pages += int((u >= 0).sum())
+        st0 = B.pkv_stage_stats(seq) if host else None
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         B.pkv_profile_enable(True)
         ev0.record(main_s)
@@ -955,20 +980,36 @@ def run_offload(args, world, rank):
         prof = B.pkv_profile_collect()
         B.pkv_profile_enable(False)
         B.pkv_check(pool)
-        res[mode] = dict(ms=ev0.elapsed_time(ev1) / args.steps, prof=prof, staged_pages=staged_pages)
+        res[mode] = dict(ms=ev0.elapsed_time(ev1) / args.steps, prof=prof)
+        if host:
+            st1 = B.pkv_stage_stats(seq)
+            res[mode]["moved"] = {k: (st1[k] - st0[k]) / args.steps for k in st1}
+            res[mode]["union_pages"] = sum(int((np.unique(sel[c].cpu().numpy()) >= 0).sum())
+                                           for c in meas)
         if args.overlap_proj:
             step(proj=True)
+            B.pkv_profile_enable(True)
             ev0.record(main_s)
             for _ in range(args.steps):
                 step(proj=True)
             ev1.record(main_s)
             torch.cuda.synchronize()
+            res[mode]["prof_proj"] = B.pkv_profile_collect()
+            B.pkv_profile_enable(False)
             B.pkv_check(pool)
             res[mode]["ms_proj"] = ev0.elapsed_time(ev1) / args.steps
+            rec = {}
+            step(proj=True, rec=rec)
+            torch.cuda.synchronize()
+            res[mode]["chunks"] = {ph: [[round(ev[0].elapsed_time(ev[1]), 4)] +
+                                        ([round(ev[2].elapsed_time(ev[3]), 4)] if host else [])
+                                        for ev in evs] for ph, evs in rec.items()}
             if not host:      # the step's GEMMs alone, back to back
                 ev0.record(main_s)
-                for _ in range(args.steps * len(meas)):
-                    torch.matmul(x_proj, w_proj)
+                for _ in range(args.steps):
+                    for _c in range(2 * len(meas)):
+                        torch.matmul(x_proj, w_q)
+                        torch.matmul(x_proj, w_kv)
                 ev1.record(main_s)
                 torch.cuda.synchronize()
                 res[mode]["gemm_ms"] = ev0.elapsed_time(ev1) / args.steps
@@ -976,26 +1017,46 @@ def run_offload(args, world, rank):
         del q, do, o, dq, lse, sel
         torch.cuda.empty_cache()
     hp = res["pinned_host"]
-    page_head_kv = w.Hkv * w.P * w.d * 2 * 2          # K + V of one page, all KV heads
-    page_head_g = w.Hkv * w.P * w.d * 4 * 2           # dK + dV
-    # per step: fwd stages K/V; bwd stages K/V + grads and writes grads back
-    bytes_moved = hp["staged_pages"] * (page_head_kv + (page_head_kv + page_head_g) + page_head_g)
-    copy_cnt, copy_ms = hp["prof"].get("stage_copy_kernel", (0, 0.0))
-    wb_cnt, wb_ms = hp["prof"].get("stage_writeback_kernel", (0, 0.0))
-    link_gbs = bytes_moved * args.steps / ((copy_ms + wb_ms) * 1e-3) / 1e9 if copy_ms else None
+    kv_ph = w.P * w.d * 2 * 2          # K + V of one page of one KV head
+    g_ph = w.P * w.d * 4 * 2           # dK + dV
+    mv = hp["moved"]
+    bytes_moved = mv["kv_in"] * kv_ph + (mv["grads_in"] + mv["grads_out"]) * g_ph
+    # without the slot cache: every chunk's selection staged afresh, K/V for the
+    # forward, K/V and gradients in and gradients out for the backward
+    bytes_afresh = hp["union_pages"] * w.Hkv * (2 * kv_ph + 2 * g_ph)
+    stage_names = ("stage_plan_kernel", "stage_copy_kernel", "stage_writeback_kernel")
+
+    def copy_ms(prof):
+        return sum(prof.get(k, (0, 0.0))[1] for k in stage_names) / args.steps
+
     overhead = hp["ms"] / res["device"]["ms"] - 1.0
     extra = {}
     if args.overlap_proj:
-        proj_ms = res["device"]["gemm_ms"]                             # the GEMMs alone
-        hidden = hp["ms"] + proj_ms - hp["ms_proj"]
+        cp = copy_ms(hp["prof_proj"])
+        exposed = hp["ms_proj"] - res["device"]["ms_proj"]
+        # Per chunk with a warm slot cache (every chunk but the first of each
+        # sweep): main-stream time pinned-host minus device-resident (the
+        # exposed part of the staging) against the staging's own time.
+        per = {}
+        for ph in ("fwd", "bwd"):
+            hc, dc = hp["chunks"][ph], res["device"]["chunks"][ph]
+            cp_w = sum(x[1] for x in hc[1:])
+            ex_w = sum(max(0.0, hx[0] - dx[0]) for hx, dx in zip(hc[1:], dc[1:]))
+            per[ph] = {"copy_ms_per_chunk": [x[1] for x in hc],
+                       "exposed_ms_per_chunk": [round(hx[0] - dx[0], 4) for hx, dx in zip(hc, dc)],
+                       "warm_copy_ms": round(cp_w, 4), "warm_exposed_ms": round(ex_w, 4),
+                       "warm_overlap": round(1.0 - ex_w / cp_w, 3) if cp_w > 0 else None}
+        extra["projection_overlap_per_chunk"] = per
         extra["projection_overlap"] = {
-            "gemm": f"bf16 [{w.C}, 3584] x [3584, {2 * w.Hkv * w.d}] per measured chunk (cuBLAS)",
-            "projection_ms_per_step": round(proj_ms, 3),
+            "gemms": f"per measured chunk and sweep: a chunk's Q and K/V projections [{w.C}, {hidden}] x "
+                     f"[{hidden}, {w.Hq * w.d}] and x [{hidden}, {2 * w.Hkv * w.d}] (the next chunk's in "
+                     f"the forward, the recomputed ones in the backward), cuBLAS bf16",
+            "gemm_ms_per_step": round(res["device"]["gemm_ms"], 3),
+            "copy_ms_per_step": round(cp, 3),
             "ms_per_step_pinned_host_with_projection": round(hp["ms_proj"], 3),
             "ms_per_step_device_with_projection": round(res["device"]["ms_proj"], 3),
-            "hidden_ms_per_step": round(hidden, 3),
-            "hidden_frac_of_projection": round(hidden / proj_ms, 3) if proj_ms > 0 else None,
-            "overhead_pct_with_projection": round(100 * (hp["ms_proj"] / res["device"]["ms_proj"] - 1), 2)}
+            "exposed_copy_ms_per_step": round(exposed, 3),
+            "overlap": round(1.0 - exposed / cp, 3) if cp > 0 else None}
     return {
         "metric": "page-sparse offload step: staged pages over the host link, overhead vs HBM-resident",
         "value": round(overhead * 100, 2), "unit": "% step-time overhead", "n_gpus": world,
@@ -1003,8 +1064,11 @@ def run_offload(args, world, rank):
         "ms_per_step_pinned_host": round(hp["ms"], 3), "ms_per_step_device": round(res["device"]["ms"], 3),
         "config": {"workload": w.name, "N": w.N, "C": w.C, "P": w.P, "Hq": w.Hq, "Hkv": w.Hkv,
                    "d": w.d, "topk": list(w.topk), "measured_chunks": meas, "device_slots": args.slots},
-        "staged_pages_per_step": hp["staged_pages"], "bytes_moved_per_step": bytes_moved,
-        "link_gbs_in_copy_kernels": round(link_gbs, 1) if link_gbs else None,
+        "page_heads_moved_per_step": mv, "bytes_moved_per_step": bytes_moved,
+        "bytes_per_step_without_slot_cache": bytes_afresh,
+        "copy_ms_per_step": round(copy_ms(hp["prof"]), 3),
+        "link_gbs_in_copy_kernels": round(bytes_moved / (copy_ms(hp["prof"]) * 1e-3) / 1e9, 1)
+        if copy_ms(hp["prof"]) > 0 else None,
         "kernels_pinned_host": {k: {"launches": c, "ms_per_step": round(t / args.steps, 3)}
                                 for k, (c, t) in hp["prof"].items()},
         "data": "synthetic (seeded clustered keys)",

@@ -272,7 +272,11 @@ pkv_status pkv_gather_rows(const pkv_seq* seq, int64_t row0, int64_t n_rows, voi
  *   [0, n_sink) and the local pages qp_glob-n_local+1 .. qp_glob.
  * Writes pages_out (device int32 [n_qp, Hkv, K+n_sink+n_local], ascending,
  * -1 padded) and, if counts_out is not NULL, counts_out (device int32
- * [n_qp, Hkv]). q_start and n_q as for attention. */
+ * [n_qp, Hkv]). q_start and n_q as for attention. One kernel launch; it
+ * works in a pool-owned scratch buffer (grown on demand, which synchronizes
+ * the device) and the pool's selection counters, so selection calls on one
+ * pool must not overlap on the GPU. At most 2^24 candidate pages per query
+ * page, else PKV_ERR_UNSUPPORTED. */
 pkv_status pkv_page_topk(pkv_seq* seq, const void* q, int64_t q_start, int64_t n_q, int32_t k,
                          int32_t n_sink, int32_t n_local, int32_t* pages_out,
                          int32_t* counts_out, void* stream);
@@ -308,11 +312,25 @@ pkv_status pkv_page_local(pkv_seq* seq, int64_t q_start, int64_t n_q, int32_t n_
  * so a selection array from pkv_page_topk can be passed flattened -- or every
  * page of the sequence if logical_pages is NULL (n = 0). Pages get slots in
  * ascending page order; what = PKV_STAGE_KV copies K and V, PKV_STAGE_GRADS
- * copies dK and dV (or both). Staged pages beyond the slot count are not
- * staged and record PKV_ERR_DEVICE_FAULT for pkv_check. Kernels copy the pages
- * over the host link; nothing is allocated and the host does not wait.
+ * copies dK and dV (or both). Kernels copy the pages over the host link;
+ * nothing is allocated and the host does not wait.
+ * The slots of a sequence are a cache: a listed page that is already staged
+ * keeps its slot and gets only the contents it lacks, so consecutive chunks
+ * whose selections overlap move only the difference. A page not staged takes
+ * an empty slot, else the slot of a page this call does not list (evicted:
+ * if its gradients were staged, they go back to the host first). More listed
+ * pages than slots: the excess is not staged and records
+ * PKV_ERR_DEVICE_FAULT for pkv_check. Staged gradients are the authoritative
+ * copy until written back: host-side gradient calls (pkv_gather,
+ * pkv_grad_accumulate, pkv_grad_zero) see them only after pkv_writeback_grads
+ * or pkv_release_slots. Whole-sequence staging (logical_pages NULL, when the
+ * sequence fits the slots) puts page i in slot i and copies with the copy
+ * engines; it first writes back gradients still staged.
  * pkv_writeback_grads: on `side`, after the sequence's last attention call,
- * copies the staged slots' dK/dV back into the host gradient pages.
+ * copies the dK/dV of every slot whose gradients were staged since the last
+ * write-back into the host gradient pages; the pages stay staged.
+ * pkv_release_slots: the same write-back, then empties the sequence's slot
+ * cache (the next prefetch stages every page it lists).
  * A prefetch also waits for the sequence's previous prefetch or writeback, so
  * write-backs may go on their own stream (both copy directions at once).
  * pkv_wait: makes stream `main` wait (on the GPU) for the sequence's last
@@ -324,7 +342,14 @@ pkv_status pkv_page_local(pkv_seq* seq, int64_t q_start, int64_t n_q, int32_t n_
 pkv_status pkv_prefetch(pkv_seq* seq, const int32_t* logical_pages, int64_t n, int32_t what,
                         void* side);
 pkv_status pkv_writeback_grads(pkv_seq* seq, void* side);
+pkv_status pkv_release_slots(pkv_seq* seq, void* side);
 pkv_status pkv_wait(pkv_seq* seq, void* main, int64_t timeout_us);
+
+/* Page-heads (one logical page of one KV head) the sequence's staging has
+ * moved so far: K/V host-to-device, dK/dV host-to-device, dK/dV
+ * device-to-host (write-backs and evictions). Any output may be NULL.
+ * Synchronizes the device. PINNED_HOST pools only (else PKV_ERR_INVALID). */
+pkv_status pkv_stage_stats(pkv_seq* seq, int64_t* kv_in, int64_t* grads_in, int64_t* grads_out);
 
 /* ---------------------------------------------------------------- profiling
  * Per-kernel device time, for benchmarks. pkv_profile_enable(1) clears old

@@ -75,6 +75,8 @@ _SIGS = {
     "pkv_page_topk": (_ST, [_P, _P, _I64, _I64, _I32, _I32, _I32, _P, _P, _P]),
     "pkv_prefetch": (_ST, [_P, _P, _I64, _I32, _P]),
     "pkv_writeback_grads": (_ST, [_P, _P]),
+    "pkv_release_slots": (_ST, [_P, _P]),
+    "pkv_stage_stats": (_ST, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "pkv_wait": (_ST, [_P, _P, _I64]),
     "pkv_selftest_umma": (_ST, [_I32, _P, _P, _P, _I32, _I32]),
     "pkv_profile_enable": (_ST, [_I32]),
@@ -269,6 +271,17 @@ def pkv_prefetch(seq, logical_pages=None, n=0, what=3, side=None) -> None:
 
 def pkv_writeback_grads(seq, side=None) -> None:
     _check(lib().pkv_writeback_grads(seq, stream_ptr(side)))
+
+
+def pkv_release_slots(seq, side=None) -> None:
+    _check(lib().pkv_release_slots(seq, stream_ptr(side)))
+
+
+def pkv_stage_stats(seq) -> dict:
+    """Page-heads moved by the sequence's staging so far."""
+    kv, gi, go = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().pkv_stage_stats(seq, ctypes.byref(kv), ctypes.byref(gi), ctypes.byref(go)))
+    return {"kv_in": kv.value, "grads_in": gi.value, "grads_out": go.value}
 
 
 def pkv_wait(seq, main=None, timeout_us=10_000_000) -> None:

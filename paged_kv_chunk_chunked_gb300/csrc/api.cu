@@ -162,6 +162,16 @@ static void release_pages(pkv_seq* s) {
     s->len = 0;
     s->n_reserved_pages = 0;
     s->staged_all = 0;          // slots no longer mirror this sequence's pages
+    if (s->d_slot_of) {
+        // The slot cache holds the old pages: empty it (after every queued use).
+        const size_t nb = (size_t)p->desc.num_phys_pages * sizeof(int32_t);
+        cudaDeviceSynchronize();
+        cudaMemset(s->d_slot_of, 0xff, nb);
+        cudaMemset(s->d_slot_page, 0xff, p->n_slots * sizeof(int32_t));
+        cudaMemset(s->d_slot_state, 0, p->n_slots * sizeof(int32_t));
+        cudaDeviceSynchronize();
+        s->dirty_possible = false;
+    }
 }
 
 // Uploads block-table entries [from, bt.size()) to the device copy on stream.
@@ -248,7 +258,7 @@ pkv_status pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
         } else {
             cudaFree(p->k); cudaFree(p->v); cudaFree(p->dk); cudaFree(p->dv);
         }
-        cudaFree(p->rep); cudaFree(p->d_err);
+        cudaFree(p->rep); cudaFree(p->d_err); cudaFree(p->sel_state);
         delete p;
     };
     if (host) {
@@ -282,6 +292,12 @@ pkv_status pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
         cleanup();
         return cuda_fail(e, "pkv_pool_create: page memory");
     }
+    const size_t state_bytes = (size_t)page_topk_state_ints(desc->n_kv_heads) * sizeof(int);
+    if ((e = cudaMalloc(reinterpret_cast<void**>(&p->sel_state), state_bytes)) != cudaSuccess ||
+        (e = cudaMemset(p->sel_state, 0, state_bytes)) != cudaSuccess) {
+        cleanup();
+        return cuda_fail(e, "pkv_pool_create: selection state");
+    }
     if ((e = cudaMemset(p->d_err, 0, sizeof(int))) != cudaSuccess ||
         (!host && (e = cudaMemset(p->k, 0, kv_bytes)) != cudaSuccess) ||
         (!host && (e = cudaMemset(p->v, 0, kv_bytes)) != cudaSuccess) ||
@@ -289,15 +305,18 @@ pkv_status pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
         cleanup();
         return cuda_fail(e, "pkv_pool_create: memset");
     }
-    if (desc->dtype == PKV_BF16 && desc->head_dim == 128 && desc->page_size == 128) {
-        // The tensor-core kernels read K/V by TMA: the pool in HBM, or the slots.
+    if (desc->dtype == PKV_BF16 && (desc->head_dim == 128 || desc->head_dim == 64) &&
+        desc->page_size == 128) {
+        // The tensor-core kernels read K/V by TMA (boxes of 64 columns x 128
+        // rows): the pool in HBM, or the slots.
         std::string why;
         void* kb = host ? p->kslot : p->k;
         void* vb = host ? p->vslot : p->v;
         const uint64_t rows = (uint64_t)(host ? p->n_slots : np) * desc->n_kv_heads * desc->page_size;
-        if (!make_tmap_2d(&p->tmap_k, kb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
+        const uint64_t dd = (uint64_t)desc->head_dim;
+        if (!make_tmap_2d(&p->tmap_k, kb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dd, rows, dd * 2, 64,
                           128, &why) ||
-            !make_tmap_2d(&p->tmap_v, vb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, rows, 256, 64,
+            !make_tmap_2d(&p->tmap_v, vb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dd, rows, dd * 2, 64,
                           128, &why)) {
             cleanup();
             return fail(PKV_ERR_CUDA, "pkv_pool_create: " + why);
@@ -326,6 +345,7 @@ void pkv_pool_destroy(pkv_pool* p) {
     }
     if (is_device(p)) {
         cudaFree(p->rep); cudaFree(p->d_err); cudaFree(p->scratch); cudaFree(p->sel_scratch);
+        cudaFree(p->sel_state);
     }
     delete p;
 }
@@ -361,10 +381,18 @@ pkv_status pkv_seq_create(pkv_pool* p, pkv_seq** out) {
         if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&s->d_bt), bytes);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->bt_sent, cudaEventDisableTiming);
         if (e == cudaSuccess && p->desc.residency == PKV_RES_PINNED_HOST) {
+            const size_t sb = p->n_slots * sizeof(int32_t);
             e = cudaMalloc(reinterpret_cast<void**>(&s->d_slot_of), bytes);
             if (e == cudaSuccess) e = cudaMemset(s->d_slot_of, 0xff, bytes);   // all -1
+            if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&s->d_slot_page), sb);
+            if (e == cudaSuccess) e = cudaMemset(s->d_slot_page, 0xff, sb);   // every slot empty
+            if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&s->d_slot_state), sb);
+            if (e == cudaSuccess) e = cudaMemset(s->d_slot_state, 0, sb);
+            if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&s->d_avail), sb);
             if (e == cudaSuccess)
-                e = cudaMalloc(reinterpret_cast<void**>(&s->d_slot_page), p->n_slots * sizeof(int32_t));
+                e = cudaMalloc(reinterpret_cast<void**>(&s->d_jobs), p->n_slots * sizeof(int4));
+            if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&s->d_stats), 4 * sizeof(unsigned long long));
+            if (e == cudaSuccess) e = cudaMemset(s->d_stats, 0, 4 * sizeof(unsigned long long));
             if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&s->d_flags), bytes + sizeof(int32_t));
             if (e == cudaSuccess) e = cudaMemset(s->d_flags, 0, bytes + sizeof(int32_t));
             if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->staged, cudaEventDisableTiming);
@@ -376,6 +404,7 @@ pkv_status pkv_seq_create(pkv_pool* p, pkv_seq** out) {
         if (e != cudaSuccess) {
             cudaFreeHost(s->h_bt);
             cudaFree(s->d_bt); cudaFree(s->d_slot_of); cudaFree(s->d_slot_page); cudaFree(s->d_flags);
+            cudaFree(s->d_slot_state); cudaFree(s->d_avail); cudaFree(s->d_jobs); cudaFree(s->d_stats);
             if (s->staged) cudaEventDestroy(s->staged);
             if (s->used) cudaEventDestroy(s->used);
             if (s->bt_sent) cudaEventDestroy(s->bt_sent);
@@ -397,6 +426,7 @@ void pkv_seq_free(pkv_seq* s) {
         cudaFreeHost(s->h_bt);
         cudaFree(s->d_bt);
         cudaFree(s->d_slot_of); cudaFree(s->d_slot_page); cudaFree(s->d_flags);
+        cudaFree(s->d_slot_state); cudaFree(s->d_avail); cudaFree(s->d_jobs); cudaFree(s->d_stats);
         if (s->staged) cudaEventDestroy(s->staged);
         if (s->used) cudaEventDestroy(s->used);
         if (s->bt_sent) cudaEventDestroy(s->bt_sent);
@@ -482,6 +512,12 @@ pkv_status pkv_append(pkv_seq* s, const void* k, const void* v, int64_t n_tok, v
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     st = upload_bt(s, old_pages, cs);
     if (st != PKV_OK) return st;
+    if (s->d_slot_of && s->len % p->desc.page_size != 0) {
+        // Extending a partial page that may be staged: its slot's K/V goes stale.
+        cudaError_t e = cudaStreamWaitEvent(cs, s->staged, 0);
+        if (e == cudaSuccess) e = launch_stage_invalidate_kv(s, s->len / p->desc.page_size, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "pkv_append: slot invalidation");
+    }
     AppendArgs a{};
     a.P = p->desc.page_size; a.Hkv = p->desc.n_kv_heads; a.d = p->desc.head_dim;
     a.dtype = p->desc.dtype;
@@ -683,7 +719,8 @@ pkv_status pkv_page_topk(pkv_seq* s, const void* q, int64_t q_start, int64_t n_q
         p->sel_scratch_floats = need;
     }
     cudaError_t e = launch_page_topk(p, s->d_bt, q, q_start, n_q, k, n_sink, n_local, pages_out,
-                                     counts_out, p->sel_scratch, static_cast<cudaStream_t>(stream));
+                                     counts_out, p->sel_scratch, p->sel_state,
+                                     static_cast<cudaStream_t>(stream));
     // A later pkv_prefetch of this selection must wait for it.
     if (e == cudaSuccess && s->used) e = cudaEventRecord(s->used, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "pkv_page_topk: launch");
@@ -764,29 +801,87 @@ pkv_status pkv_prefetch(pkv_seq* s, const int32_t* pages, int64_t n, int32_t wha
     // issued on another stream, e.g. write-backs on a device-to-host stream).
     cudaError_t e = cudaStreamWaitEvent(cs, s->used, 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, s->staged, 0);
-    if (e == cudaSuccess) e = launch_stage_plan(s, n > 0 ? pages : nullptr, n, cs);
     const int64_t n_pages = (int64_t)s->bt.size();
     const bool all = n == 0 && n_pages <= s->pool->n_slots;
-    s->staged_all = all ? n_pages : 0;
-    if (e == cudaSuccess)
-        e = all ? stage_all_dma(s, n_pages, what, false, cs) : launch_stage_copy(s, what, cs);
+    if (all) {
+        // Whole sequence: slot i <- page i, runs of consecutive physical pages
+        // by the copy engines. Dirty gradient slots go back first.
+        if (e == cudaSuccess && s->dirty_possible) {
+            if (s->staged_all > 0) {
+                const int64_t m = std::min<int64_t>(s->staged_all, n_pages);
+                e = stage_all_dma(s, m, PKV_STAGE_GRADS, true, cs);
+                s->h_stats[2] += m * s->pool->desc.n_kv_heads;
+            } else {
+                e = launch_stage_writeback(s, true, cs);
+            }
+        }
+        if (e == cudaSuccess) e = launch_stage_identity(s, n_pages, what, cs);
+        if (e == cudaSuccess) e = stage_all_dma(s, n_pages, what, false, cs);
+        const int64_t ph = n_pages * s->pool->desc.n_kv_heads;
+        if (what & PKV_STAGE_KV) s->h_stats[0] += ph;
+        if (what & PKV_STAGE_GRADS) s->h_stats[1] += ph;
+        s->staged_all = n_pages;
+    } else {
+        if (e == cudaSuccess && s->staged_all > 0) {
+            // Leaving whole-sequence staging: its dirty gradients go back and
+            // the cache starts empty.
+            if (s->dirty_possible)
+                e = stage_all_dma(s, std::min<int64_t>(s->staged_all, n_pages), PKV_STAGE_GRADS, true, cs);
+            if (e == cudaSuccess) e = launch_stage_after_writeback(s, true, cs);
+            if (s->dirty_possible) s->h_stats[2] += s->staged_all * s->pool->desc.n_kv_heads;
+            s->dirty_possible = false;
+        }
+        s->staged_all = 0;
+        if (e == cudaSuccess) e = launch_stage_plan(s, n > 0 ? pages : nullptr, n, what, cs);
+        if (e == cudaSuccess) e = launch_stage_copy(s, cs);
+    }
+    if (what & PKV_STAGE_GRADS) s->dirty_possible = true;
     if (e == cudaSuccess) e = cudaEventRecord(s->staged, cs);
     if (e != cudaSuccess) return cuda_fail(e, "pkv_prefetch");
     return PKV_OK;
 }
 
-pkv_status pkv_writeback_grads(pkv_seq* s, void* side) {
-    pkv_status st = host_pool_check(s, "pkv_writeback_grads");
+static pkv_status writeback(pkv_seq* s, void* side, bool release, const char* who) {
+    pkv_status st = host_pool_check(s, who);
     if (st != PKV_OK) return st;
-    if (s->bt.empty()) return PKV_OK;
     cudaStream_t cs = static_cast<cudaStream_t>(side);
     cudaError_t e = cudaStreamWaitEvent(cs, s->used, 0);
-    if (e == cudaSuccess)
-        e = s->staged_all > 0 ? stage_all_dma(s, std::min<int64_t>(s->staged_all, (int64_t)s->bt.size()),
-                                              PKV_STAGE_GRADS, true, cs)
-                              : launch_stage_writeback(s, cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, s->staged, 0);
+    if (s->staged_all > 0) {
+        const int64_t n = std::min<int64_t>(s->staged_all, (int64_t)s->bt.size());
+        if (e == cudaSuccess && s->dirty_possible) {
+            e = stage_all_dma(s, n, PKV_STAGE_GRADS, true, cs);
+            s->h_stats[2] += n * s->pool->desc.n_kv_heads;
+        }
+        if (e == cudaSuccess) e = launch_stage_after_writeback(s, release, cs);
+        if (release) s->staged_all = 0;
+    } else if (e == cudaSuccess) {
+        e = launch_stage_writeback(s, release, cs);
+    }
+    s->dirty_possible = false;
     if (e == cudaSuccess) e = cudaEventRecord(s->staged, cs);
-    if (e != cudaSuccess) return cuda_fail(e, "pkv_writeback_grads");
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    return PKV_OK;
+}
+
+pkv_status pkv_writeback_grads(pkv_seq* s, void* side) {
+    return writeback(s, side, false, "pkv_writeback_grads");
+}
+
+pkv_status pkv_release_slots(pkv_seq* s, void* side) {
+    return writeback(s, side, true, "pkv_release_slots");
+}
+
+pkv_status pkv_stage_stats(pkv_seq* s, int64_t* kv_in, int64_t* grads_in, int64_t* grads_out) {
+    pkv_status st = host_pool_check(s, "pkv_stage_stats");
+    if (st != PKV_OK) return st;
+    unsigned long long d[3] = {0, 0, 0};
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(d, s->d_stats, sizeof(d), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_stage_stats");
+    if (kv_in) *kv_in = (int64_t)d[0] + s->h_stats[0];
+    if (grads_in) *grads_in = (int64_t)d[1] + s->h_stats[1];
+    if (grads_out) *grads_out = (int64_t)d[2] + s->h_stats[2];
     return PKV_OK;
 }
 

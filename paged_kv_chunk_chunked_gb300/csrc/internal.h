@@ -29,9 +29,11 @@ struct pkv_pool {
     // Scratch (bwd row statistics D = rowsum(dO * O)), grown on demand.
     float* scratch = nullptr;
     size_t scratch_floats = 0;
-    // Scratch of the page selection (page queries qbar [n_qp, Hkv, d]).
+    // Scratch of the page selection (partial page queries and scores), and
+    // its work-queue counters (zeroed at creation; each call leaves them zero).
     float* sel_scratch = nullptr;
     size_t sel_scratch_floats = 0;
+    int* sel_state = nullptr;
     // TMA descriptors over the K and V page pools (2-D: rows x d), with boxes
     // of 64 columns x 128 rows (whole pages). For a PINNED_HOST pool they
     // describe the device slots.
@@ -58,14 +60,24 @@ struct pkv_seq {
     cudaEvent_t bt_sent = nullptr;
     bool bt_pending = false;
     int64_t len = 0;
-    // PINNED_HOST pools: staging state (device), capacity num_phys_pages.
+    // PINNED_HOST pools: the slot cache (device), capacity num_phys_pages.
     int32_t* d_slot_of = nullptr;    // logical page -> device slot, or -1
-    int32_t* d_slot_page = nullptr;  // device slot -> logical page [n_slots]
-    int32_t* d_flags = nullptr;      // planning scratch [num_phys_pages + 1]
+    int32_t* d_slot_page = nullptr;  // device slot -> logical page or -1 [n_slots]
+    int32_t* d_slot_state = nullptr; // kSlot* bits per slot [n_slots]
+    int32_t* d_avail = nullptr;      // planning scratch [n_slots]
+    int4* d_jobs = nullptr;          // copy jobs of the last plan [n_slots]
+    int32_t* d_flags = nullptr;      // planning scratch [num_phys_pages + 1]; [num_phys_pages] = job count
+    unsigned long long* d_stats = nullptr;   // page-heads moved by kernels: K/V in, grads in, grads out
+    int64_t h_stats[3] = {0, 0, 0};  // the same, moved by the copy engines (whole-sequence staging)
+    bool dirty_possible = false;     // a prefetch staged gradients since the last write-back
     cudaEvent_t staged = nullptr;    // last event recorded on the side stream
     cudaEvent_t used = nullptr;      // last append/attention call on the sequence's slots
     int64_t staged_all = 0;          // > 0: the last prefetch staged pages [0, staged_all), slot i = page i
 };
+
+// Slot state bits (PINNED_HOST pools). KV and G match PKV_STAGE_KV and
+// PKV_STAGE_GRADS.
+enum : int { kSlotKV = 1, kSlotG = 2, kSlotDirty = 4, kSlotKeep = 8 };
 
 namespace pkv {
 
@@ -152,10 +164,15 @@ cudaError_t launch_attn_fwd_simt(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_attn_bwd_simt(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_rowdot(const AttnArgs& a, cudaStream_t s);
 
+// Page selection of one chunk in one launch (topk_fused_kernel). scratch:
+// page_topk_scratch_floats() floats; state: page_topk_state_ints(Hkv) ints,
+// zero before the first call (each call leaves it zero again).
 cudaError_t launch_page_topk(const pkv_pool* p, const int32_t* d_bt, const void* q,
                              int64_t q_start, int64_t n_q, int K, int n_sink, int n_local,
-                             int32_t* out, int32_t* counts, float* qbar, cudaStream_t s);
+                             int32_t* out, int32_t* counts, float* scratch, int* state,
+                             cudaStream_t s);
 int64_t page_topk_max_candidates();
+int page_topk_state_ints(int Hkv);
 cudaError_t launch_page_local(int64_t q_start, int64_t n_q, int P, int Hkv, int n_sink,
                               int n_local, int32_t* out, int32_t* counts, cudaStream_t s);
 // Floats of page-selection scratch: page queries [n_qp, Hkv, d], then scores
@@ -163,10 +180,20 @@ cudaError_t launch_page_local(int64_t q_start, int64_t n_q, int P, int Hkv, int 
 size_t page_topk_scratch_floats(int64_t q_start, int64_t n_q, int P, int Hkv, int D, int n_sink,
                                 int n_local);
 
-// Host offload (stream.cu).
-cudaError_t launch_stage_plan(const pkv_seq* s, const int32_t* pages, int64_t n, cudaStream_t st);
-cudaError_t launch_stage_copy(const pkv_seq* s, int what, cudaStream_t st);
-cudaError_t launch_stage_writeback(const pkv_seq* s, cudaStream_t st);
+// Host offload (stream.cu): the slot cache of a PINNED_HOST sequence.
+// Plan the staging of `pages` (null: every page) with contents `want`.
+cudaError_t launch_stage_plan(const pkv_seq* s, const int32_t* pages, int64_t n, int want,
+                              cudaStream_t st);
+// Run the copy jobs of the last plan.
+cudaError_t launch_stage_copy(const pkv_seq* s, cudaStream_t st);
+// Dirty gradient slots back to the host pages (release: then empty the cache).
+cudaError_t launch_stage_writeback(const pkv_seq* s, bool release, cudaStream_t st);
+// The slot-state update that follows a write-back done by the copy engines.
+cudaError_t launch_stage_after_writeback(const pkv_seq* s, bool release, cudaStream_t st);
+// Whole-sequence staging: slot i <- logical page i for i < n_pages.
+cudaError_t launch_stage_identity(const pkv_seq* s, int64_t n_pages, int want, cudaStream_t st);
+// The partial page lp was extended by an append: its staged K/V is stale.
+cudaError_t launch_stage_invalidate_kv(const pkv_seq* s, int64_t lp, cudaStream_t st);
 
 bool tc_supported(const AttnArgs& a);
 cudaError_t launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t s);

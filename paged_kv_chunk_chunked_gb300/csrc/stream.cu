@@ -4,17 +4,29 @@
 // gradients*; gist.science/ja §2.3).
 //
 // A PINNED_HOST pool keeps every K/V page and gradient page in mapped pinned
-// host memory and owns n_slots page slots in HBM. Staging runs on a side
-// stream, entirely in kernels (no per-page memcpy calls, no host sync):
-//   plan      one CTA: dedupe the requested logical pages (flags), assign
-//             slots in ascending page order (ordered compaction), fill the
-//             logical-page -> slot table the attention kernels read;
-//   copy      one CTA per (slot, KV head): copy the page's K and V (and, on
-//             request, dK and dV) from host memory over NVLink-C2C / PCIe
-//             into the slot with 16-byte loads;
-//   writeback one CTA per (slot, KV head): copy the slot's dK and dV back
-//             into the host gradient pages.
+// host memory and owns n_slots page slots in HBM. A sequence's slots form a
+// cache: a staged page keeps its slot across prefetches until another page
+// needs the slot, so consecutive chunks, whose selections overlap heavily,
+// move only the pages (and the contents) not already resident. Per slot the
+// state word records what it holds:
+//   KV     the page's keys and values;
+//   G      the page's dK/dV (the slot is the authoritative copy while staged);
+//   DIRTY  the gradients may differ from the host pages (set when gradients
+//          are staged, since a backward call follows and adds into them);
+//          written back on eviction, by pkv_writeback_grads and on release.
+// Staging runs on a side stream, entirely in kernels (no per-page memcpy
+// calls, no host sync):
+//   plan      one CTA: dedupe the requested logical pages; resident pages keep
+//             their slots and get only the missing contents; new pages take
+//             empty slots first, then slots of pages not requested this time
+//             (evicted); one copy job per slot that needs data;
+//   copy      one CTA per (job, KV head): write an evicted dirty page's
+//             gradients back, then copy the new page's K/V and/or dK/dV from
+//             host memory over NVLink-C2C into the slot, 16-byte accesses;
+//   writeback one CTA per (slot, KV head): copy a dirty slot's dK/dV back.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "internal.h"
@@ -25,49 +37,144 @@ namespace {
 constexpr int kPlanThreads = 1024;
 constexpr int kCopyThreads = 256;
 
-// flags has n_pages entries; *count_out receives the number of staged slots.
-__global__ void __launch_bounds__(kPlanThreads) stage_plan_kernel(const int32_t* pages, int64_t n,
-        int64_t n_pages, int64_t n_slots, int32_t* flags, int32_t* slot_of, int32_t* slot_page,
-        int32_t* count_out, int* err) {
-    __shared__ int scan[kPlanThreads];
+// Block-wide exclusive scan of per-thread counts (kPlanThreads threads, warp
+// shuffles then one pass over the warp totals); *total gets the sum.
+__device__ int plan_scan(int v, int* sh, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int kWarps = kPlanThreads / 32;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int t = lane < kWarps ? sh[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < kWarps) sh[lane] = t;                      // inclusive over warps
+    }
+    __syncthreads();
+    const int base = warp > 0 ? sh[warp - 1] : 0;
+    *total = sh[kWarps - 1];
+    __syncthreads();                                          // sh reusable
+    return base + x - v;
+}
+
+struct PlanArgs {
+    const int32_t* pages;        // requested logical pages (entries < 0 ignored), or null = all
+    int64_t n;
+    int64_t n_pages;             // the sequence's logical pages
+    int64_t n_slots;
+    int want;                    // PKV_STAGE_KV | PKV_STAGE_GRADS
+    int32_t* flags;              // [n_pages]: request flags
+    int32_t* count_out;          // number of copy jobs
+    int32_t* slot_of;            // [n_pages] logical -> slot or -1
+    int32_t* slot_page;          // [n_slots] slot -> logical or -1
+    int32_t* slot_state;         // [n_slots] kSlot* bits
+    int32_t* avail;              // [n_slots] scratch
+    int4* jobs;                  // [n_slots] (slot, page to write back or -1, new page, contents)
+    unsigned long long* stats;   // [3] page-head counts: K/V in, grads in, grads out
+    int Hkv;
+    int* err;
+};
+
+__global__ void __launch_bounds__(kPlanThreads) stage_plan_kernel(PlanArgs a) {
+    __shared__ int sh[kPlanThreads];
+    __shared__ int n_jobs, n_kv, n_g, n_wb;
     const int tid = threadIdx.x;
-    for (int64_t p = tid; p < n_pages; p += kPlanThreads) {
-        flags[p] = pages ? 0 : 1;
-        slot_of[p] = -1;
-    }
+    if (tid == 0) { n_jobs = 0; n_kv = 0; n_g = 0; n_wb = 0; }
+    for (int64_t p = tid; p < a.n_pages; p += kPlanThreads) a.flags[p] = a.pages ? 0 : 1;
     __syncthreads();
-    if (pages) {
-        for (int64_t i = tid; i < n; i += kPlanThreads) {
-            const int32_t lp = pages[i];
-            if (lp >= 0 && lp < n_pages) flags[lp] = 1;
+    if (a.pages) {
+        for (int64_t i = tid; i < a.n; i += kPlanThreads) {
+            const int32_t lp = a.pages[i];
+            if (lp >= 0 && lp < a.n_pages) a.flags[lp] = 1;
         }
     }
     __syncthreads();
-    const int64_t per = (n_pages + kPlanThreads - 1) / kPlanThreads;
-    const int64_t p0 = (int64_t)tid * per, p1 = min64(n_pages, p0 + per);
-    int cnt = 0;
-    for (int64_t p = p0; p < p1; ++p) cnt += flags[p];
-    scan[tid] = cnt;
-    __syncthreads();
-    for (int off = 1; off < kPlanThreads; off <<= 1) {
-        const int v = tid >= off ? scan[tid - off] : 0;
-        __syncthreads();
-        scan[tid] += v;
-        __syncthreads();
-    }
-    int rank = scan[tid] - cnt;
+    // Resident requested pages keep their slots (mark them); count the new ones.
+    const int64_t per = (a.n_pages + kPlanThreads - 1) / kPlanThreads;
+    const int64_t p0 = (int64_t)tid * per, p1 = min64(a.n_pages, p0 + per);
+    int n_new = 0;
     for (int64_t p = p0; p < p1; ++p) {
-        if (!flags[p]) continue;
-        if (rank < n_slots) {
-            slot_of[p] = rank;
-            slot_page[rank] = (int32_t)p;
-        } else {
-            report_error(err, kErrSlots);
-        }
-        ++rank;
+        if (!a.flags[p]) continue;
+        const int32_t s = a.slot_of[p];
+        if (s >= 0) a.slot_state[s] |= kSlotKeep;
+        else ++n_new;
     }
     __syncthreads();
-    if (tid == 0) *count_out = (int32_t)min64(scan[kPlanThreads - 1], n_slots);
+    int total_new;
+    const int new_rank0 = plan_scan(n_new, sh, &total_new);
+    // Slots a new page may take: empty ones first, then those of pages not
+    // requested this time, each in ascending slot order.
+    const int64_t sper = (a.n_slots + kPlanThreads - 1) / kPlanThreads;
+    const int64_t s0 = (int64_t)tid * sper, s1 = min64(a.n_slots, s0 + sper);
+    int n_empty = 0, n_evict = 0;
+    for (int64_t s = s0; s < s1; ++s) {
+        if (a.slot_page[s] < 0) ++n_empty;
+        else if (!(a.slot_state[s] & kSlotKeep)) ++n_evict;
+    }
+    int tot_empty, tot_evict;
+    const int e_rank0 = plan_scan(n_empty, sh, &tot_empty);
+    const int v_rank0 = plan_scan(n_evict, sh, &tot_evict);
+    {
+        int er = e_rank0, vr = tot_empty + v_rank0;
+        for (int64_t s = s0; s < s1; ++s) {
+            if (a.slot_page[s] < 0) a.avail[er++] = (int32_t)s;
+            else if (!(a.slot_state[s] & kSlotKeep)) a.avail[vr++] = (int32_t)s;
+        }
+    }
+    __syncthreads();
+    // Assign slots and emit copy jobs.
+    const int64_t n_avail = (int64_t)tot_empty + tot_evict;
+    int rank = new_rank0;
+    for (int64_t p = p0; p < p1; ++p) {
+        if (!a.flags[p]) continue;
+        int32_t s = a.slot_of[p];
+        int need, wb = -1;
+        if (s >= 0) {
+            need = a.want & ~a.slot_state[s] & (kSlotKV | kSlotG);
+        } else {
+            if (rank >= n_avail) {
+                report_error(a.err, kErrSlots);
+                ++rank;
+                continue;
+            }
+            s = a.avail[rank++];
+            const int32_t old = a.slot_page[s];
+            if (old >= 0) {
+                a.slot_of[old] = -1;
+                if (a.slot_state[s] & kSlotDirty) wb = old;
+            }
+            a.slot_of[p] = s;
+            a.slot_page[s] = (int32_t)p;
+            a.slot_state[s] = 0;
+            need = a.want & (kSlotKV | kSlotG);
+        }
+        if (need || wb >= 0) {
+            const int j = atomicAdd(&n_jobs, 1);
+            a.jobs[j] = make_int4(s, wb, (int)p, need);
+            if (need & kSlotKV) atomicAdd(&n_kv, 1);
+            if (need & kSlotG) atomicAdd(&n_g, 1);
+            if (wb >= 0) atomicAdd(&n_wb, 1);
+        }
+        // Staged gradients are about to be added into by a backward call.
+        a.slot_state[s] = (a.slot_state[s] | need | ((a.want & kSlotG) ? kSlotDirty : 0)) & ~kSlotKeep;
+    }
+    __syncthreads();
+    for (int64_t s = s0; s < s1; ++s) a.slot_state[s] &= ~kSlotKeep;
+    if (tid == 0) {
+        *a.count_out = n_jobs;
+        atomicAdd(&a.stats[0], (unsigned long long)n_kv * a.Hkv);
+        atomicAdd(&a.stats[1], (unsigned long long)n_g * a.Hkv);
+        atomicAdd(&a.stats[2], (unsigned long long)n_wb * a.Hkv);
+    }
 }
 
 __device__ __forceinline__ void copy16(void* dst, const void* src, size_t bytes) {
@@ -79,97 +186,191 @@ __device__ __forceinline__ void copy16(void* dst, const void* src, size_t bytes)
 
 struct StageArgs {
     const int32_t* bt;           // logical -> physical (host pages)
+    const int4* jobs;
+    const int32_t* count;        // number of jobs
     const int32_t* slot_page;    // slot -> logical
-    const int32_t* count;        // number of staged slots (flags[n_pages])
+    int32_t* slot_state;
     int64_t num_phys;
+    int64_t n_slots;
     int Hkv;
     size_t kv_bytes;             // one (page, head) tile of K or V
     size_t g_bytes;              // one (page, head) tile of dK or dV
-    const uint8_t* k; const uint8_t* v; const uint8_t* dk; const uint8_t* dv;   // host pages
-    uint8_t* ks; uint8_t* vs; uint8_t* dks; uint8_t* dvs;                       // slots
-    int what;
+    uint8_t* k; uint8_t* v; uint8_t* dk; uint8_t* dv;        // host pages
+    uint8_t* ks; uint8_t* vs; uint8_t* dks; uint8_t* dvs;    // slots
+    unsigned long long* stats;
     int* err;
 };
 
-__global__ void __launch_bounds__(kCopyThreads) stage_copy_kernel(StageArgs a) {
-    const int s = blockIdx.x, h = blockIdx.y;
-    if (s >= *a.count) return;
-    const int32_t lp = a.slot_page[s];
-    const int32_t pp = a.bt[lp];
-    if (pp < 0 || pp >= a.num_phys) {
+__device__ __forceinline__ bool page_ok(const StageArgs& a, int32_t lp, int64_t* pp) {
+    *pp = lp >= 0 ? a.bt[lp] : -1;
+    if (*pp < 0 || *pp >= a.num_phys) {
         if (threadIdx.x == 0) report_error(a.err, kErrBadPage);
-        return;
+        return false;
     }
-    const size_t src = (size_t)pp * a.Hkv + h, dst = (size_t)s * a.Hkv + h;
-    if (a.what & PKV_STAGE_KV) {
-        copy16(a.ks + dst * a.kv_bytes, a.k + src * a.kv_bytes, a.kv_bytes);
-        copy16(a.vs + dst * a.kv_bytes, a.v + src * a.kv_bytes, a.kv_bytes);
+    return true;
+}
+
+__device__ void stage_copy_job(const StageArgs& a, const int4 job, int h) {
+    const size_t slot = (size_t)job.x * a.Hkv + h;
+    int64_t pp;
+    if (job.y >= 0 && page_ok(a, job.y, &pp)) {                 // evicted dirty gradients
+        const size_t dst = (size_t)pp * a.Hkv + h;
+        copy16(a.dk + dst * a.g_bytes, a.dks + slot * a.g_bytes, a.g_bytes);
+        copy16(a.dv + dst * a.g_bytes, a.dvs + slot * a.g_bytes, a.g_bytes);
+        __syncthreads();                                          // slot read before it is reused
     }
-    if (a.what & PKV_STAGE_GRADS) {
-        copy16(a.dks + dst * a.g_bytes, a.dk + src * a.g_bytes, a.g_bytes);
-        copy16(a.dvs + dst * a.g_bytes, a.dv + src * a.g_bytes, a.g_bytes);
+    if (!job.w || !page_ok(a, job.z, &pp)) return;
+    const size_t src = (size_t)pp * a.Hkv + h;
+    if (job.w & kSlotKV) {
+        copy16(a.ks + slot * a.kv_bytes, a.k + src * a.kv_bytes, a.kv_bytes);
+        copy16(a.vs + slot * a.kv_bytes, a.v + src * a.kv_bytes, a.kv_bytes);
+    }
+    if (job.w & kSlotG) {
+        copy16(a.dks + slot * a.g_bytes, a.dk + src * a.g_bytes, a.g_bytes);
+        copy16(a.dvs + slot * a.g_bytes, a.dv + src * a.g_bytes, a.g_bytes);
     }
 }
 
+// One CTA per (job, KV head), the grid striding over the jobs of the plan
+// (their number is known only on the device).
+__global__ void __launch_bounds__(kCopyThreads) stage_copy_kernel(StageArgs a) {
+    const int h = blockIdx.y;
+    const int n_jobs = *a.count;
+    for (int j = blockIdx.x; j < n_jobs; j += gridDim.x) stage_copy_job(a, a.jobs[j], h);
+}
+
+// Dirty gradient slots back to the host pages; with `release`, every slot's
+// state is cleared afterwards by stage_release_kernel.
 __global__ void __launch_bounds__(kCopyThreads) stage_writeback_kernel(StageArgs a) {
     const int s = blockIdx.x, h = blockIdx.y;
-    if (s >= *a.count) return;
-    const int32_t lp = a.slot_page[s];
-    const int32_t pp = a.bt[lp];
-    if (pp < 0 || pp >= a.num_phys) {
-        if (threadIdx.x == 0) report_error(a.err, kErrBadPage);
-        return;
-    }
+    if (!(a.slot_state[s] & kSlotDirty)) return;
+    int64_t pp;
+    if (!page_ok(a, a.slot_page[s], &pp)) return;
     const size_t src = (size_t)s * a.Hkv + h, dst = (size_t)pp * a.Hkv + h;
-    copy16(const_cast<uint8_t*>(a.dk) + dst * a.g_bytes, a.dks + src * a.g_bytes, a.g_bytes);
-    copy16(const_cast<uint8_t*>(a.dv) + dst * a.g_bytes, a.dvs + src * a.g_bytes, a.g_bytes);
+    copy16(a.dk + dst * a.g_bytes, a.dks + src * a.g_bytes, a.g_bytes);
+    copy16(a.dv + dst * a.g_bytes, a.dvs + src * a.g_bytes, a.g_bytes);
+    if (threadIdx.x == 0) atomicAdd(&a.stats[2], 1ull);
 }
 
-StageArgs stage_args(const pkv_seq* s, int what) {
+// After a write-back: clear DIRTY (release: empty every slot).
+__global__ void stage_after_writeback_kernel(int32_t* slot_page, int32_t* slot_state,
+                                             int32_t* slot_of, int64_t n_slots, int release) {
+    for (int64_t s = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; s < n_slots;
+         s += (int64_t)gridDim.x * blockDim.x) {
+        if (release) {
+            const int32_t p = slot_page[s];
+            if (p >= 0) slot_of[p] = -1;
+            slot_page[s] = -1;
+            slot_state[s] = 0;
+        } else {
+            slot_state[s] &= ~kSlotDirty;
+        }
+    }
+}
+
+// Whole-sequence staging: slot i holds logical page i (the copy engines move
+// runs of consecutive physical pages); every other slot is empty.
+__global__ void stage_identity_kernel(int32_t* slot_page, int32_t* slot_state, int32_t* slot_of,
+                                      int64_t n_pages, int64_t n_logical_cap, int64_t n_slots,
+                                      int state) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_logical_cap; i += stride) {
+        if (i < n_slots) {
+            slot_page[i] = i < n_pages ? (int32_t)i : -1;
+            slot_state[i] = i < n_pages ? state : 0;
+        }
+        slot_of[i] = i < n_pages ? (int32_t)i : -1;
+    }
+}
+
+StageArgs stage_args(const pkv_seq* s) {
     const pkv_pool* p = s->pool;
     StageArgs a{};
     a.bt = s->d_bt;
-    a.slot_page = s->d_slot_page;
+    a.jobs = s->d_jobs;
     a.count = s->d_flags + p->desc.num_phys_pages;
+    a.slot_page = s->d_slot_page;
+    a.slot_state = s->d_slot_state;
     a.num_phys = p->desc.num_phys_pages;
+    a.n_slots = p->n_slots;
     a.Hkv = p->desc.n_kv_heads;
     a.kv_bytes = (size_t)p->desc.page_size * p->desc.head_dim * p->elem;
     a.g_bytes = (size_t)p->desc.page_size * p->desc.head_dim * sizeof(float);
-    a.k = static_cast<const uint8_t*>(p->k); a.v = static_cast<const uint8_t*>(p->v);
-    a.dk = reinterpret_cast<const uint8_t*>(p->dk); a.dv = reinterpret_cast<const uint8_t*>(p->dv);
+    a.k = static_cast<uint8_t*>(p->k); a.v = static_cast<uint8_t*>(p->v);
+    a.dk = reinterpret_cast<uint8_t*>(p->dk); a.dv = reinterpret_cast<uint8_t*>(p->dv);
     a.ks = static_cast<uint8_t*>(p->kslot); a.vs = static_cast<uint8_t*>(p->vslot);
     a.dks = reinterpret_cast<uint8_t*>(p->dkslot); a.dvs = reinterpret_cast<uint8_t*>(p->dvslot);
-    a.what = what;
+    a.stats = s->d_stats;
     a.err = p->d_err;
     return a;
 }
 
 }  // namespace
 
-cudaError_t launch_stage_plan(const pkv_seq* s, const int32_t* pages, int64_t n, cudaStream_t st) {
+cudaError_t launch_stage_plan(const pkv_seq* s, const int32_t* pages, int64_t n, int want,
+                              cudaStream_t st) {
     const pkv_pool* p = s->pool;
-    // Planning covers the sequence's pages; the count goes to flags[num_phys_pages].
-    const int64_t n_pages = (int64_t)s->bt.size();
+    PlanArgs a{};
+    a.pages = pages; a.n = n;
+    a.n_pages = (int64_t)s->bt.size();
+    a.n_slots = p->n_slots;
+    a.want = want;
+    a.flags = s->d_flags; a.count_out = s->d_flags + p->desc.num_phys_pages;
+    a.slot_of = s->d_slot_of; a.slot_page = s->d_slot_page;
+    a.slot_state = s->d_slot_state; a.avail = s->d_avail; a.jobs = s->d_jobs;
+    a.stats = s->d_stats; a.Hkv = p->desc.n_kv_heads; a.err = p->d_err;
     ProfScope ps("stage_plan_kernel", st);
-    stage_plan_kernel<<<1, kPlanThreads, 0, st>>>(pages, n, n_pages, p->n_slots, s->d_flags,
-                                                 s->d_slot_of, s->d_slot_page,
-                                                 s->d_flags + p->desc.num_phys_pages, p->d_err);
+    stage_plan_kernel<<<1, kPlanThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_stage_copy(const pkv_seq* s, int what, cudaStream_t st) {
+cudaError_t launch_stage_copy(const pkv_seq* s, cudaStream_t st) {
     const pkv_pool* p = s->pool;
     ProfScope ps("stage_copy_kernel", st);
-    dim3 grid((unsigned)p->n_slots, p->desc.n_kv_heads);
-    stage_copy_kernel<<<grid, kCopyThreads, 0, st>>>(stage_args(s, what));
+    dim3 grid((unsigned)std::min<int64_t>(p->n_slots, 512), p->desc.n_kv_heads);
+    stage_copy_kernel<<<grid, kCopyThreads, 0, st>>>(stage_args(s));
     return cudaGetLastError();
 }
 
-cudaError_t launch_stage_writeback(const pkv_seq* s, cudaStream_t st) {
+cudaError_t launch_stage_writeback(const pkv_seq* s, bool release, cudaStream_t st) {
     const pkv_pool* p = s->pool;
-    ProfScope ps("stage_writeback_kernel", st);
-    dim3 grid((unsigned)p->n_slots, p->desc.n_kv_heads);
-    stage_writeback_kernel<<<grid, kCopyThreads, 0, st>>>(stage_args(s, PKV_STAGE_GRADS));
+    {
+        ProfScope ps("stage_writeback_kernel", st);
+        dim3 grid((unsigned)p->n_slots, p->desc.n_kv_heads);
+        stage_writeback_kernel<<<grid, kCopyThreads, 0, st>>>(stage_args(s));
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return launch_stage_after_writeback(s, release, st);
+}
+
+cudaError_t launch_stage_after_writeback(const pkv_seq* s, bool release, cudaStream_t st) {
+    const pkv_pool* p = s->pool;
+    const unsigned blocks = (unsigned)std::min<int64_t>(1024, (p->n_slots + 255) / 256);
+    stage_after_writeback_kernel<<<blocks, 256, 0, st>>>(s->d_slot_page, s->d_slot_state,
+                                                         s->d_slot_of, p->n_slots, release ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stage_identity(const pkv_seq* s, int64_t n_pages, int want, cudaStream_t st) {
+    const pkv_pool* p = s->pool;
+    const int state = (want & (kSlotKV | kSlotG)) | ((want & kSlotG) ? kSlotDirty : 0);
+    const int64_t cap = p->desc.num_phys_pages;
+    const unsigned blocks = (unsigned)std::min<int64_t>(1024, (cap + 255) / 256);
+    stage_identity_kernel<<<blocks, 256, 0, st>>>(s->d_slot_page, s->d_slot_state, s->d_slot_of,
+                                                  n_pages, cap, p->n_slots, state);
+    return cudaGetLastError();
+}
+
+namespace {
+__global__ void stage_invalidate_kv_kernel(const int32_t* slot_of, int32_t* slot_state, int64_t lp) {
+    const int32_t s = slot_of[lp];
+    if (s >= 0) slot_state[s] &= ~kSlotKV;
+}
+}  // namespace
+
+cudaError_t launch_stage_invalidate_kv(const pkv_seq* s, int64_t lp, cudaStream_t st) {
+    stage_invalidate_kv_kernel<<<1, 1, 0, st>>>(s->d_slot_of, s->d_slot_state, lp);
     return cudaGetLastError();
 }
 

@@ -190,3 +190,192 @@ def test_grad_accumulate_into_pinned_host_pages_then_prefetch():
         np.testing.assert_array_equal(to_numpy(dk), oracle.logical_rows(ref["dk"], bt, w.N, w.P))
     finally:
         B.pkv_pool_destroy(pool)
+
+
+def test_projections_overlapping_the_page_transfer_match_oracle():
+    """The sparse-offload overlap ("Out of the Memory Barrier", gist.science/de
+    §2.C: with sparse attention the transfer overlaps the key/value projections
+    that follow): chunk c's selected pages stream in on a side stream while the
+    main stream runs the next chunk's K/V projection, a bf16 cuBLAS GEMM
+    x_{c+1} [wk | wv], whose output becomes chunk c+1's keys and values; in the
+    backward, the chunk's query projection is recomputed (chunk-recurrent
+    recomputation, gist.science/de §2.A) while its K/V and gradient pages
+    stream in, and the recomputed queries feed the backward. Against the
+    oracle on the same projections computed in fp64 and rounded to bf16 (the
+    GEMM's own rounding may differ in the last bf16 place on a few elements).
+    Selections equal the oracle's; O and LSE within 1e-2, dQ, dK, dV within
+    2e-2 relative."""
+    w = _w(N=3072, C=1024, keys="normal")
+    K, ns, nl = w.topk
+    hidden = 512
+    n = w.n_chunks
+    wts = synth.block_weights(w, hidden)
+    xs = [synth.block_x(w, c, hidden) for c in range(n)]
+    proj = lambda x, m: synth.round_bf16((x.astype(np.float64) @ m.astype(np.float64)).astype(np.float32))
+    qs = [proj(x, wts["wq"]).reshape(-1, w.Hq, w.d) for x in xs]
+    ks = [proj(x, wts["wk"]).reshape(-1, w.Hkv, w.d) for x in xs]
+    vs = [proj(x, wts["wv"]).reshape(-1, w.Hkv, w.d) for x in xs]
+    dos = [synth.chunk_do(w, c) for c in range(n)]
+    bt = synth.block_table(w)
+    ref = oracle.chunk_recurrent_step(qs, ks, vs, dos, bt, w.P, w.n_phys, topk=w.topk)
+
+    dev = lambda x: to_device(x, "bf16")
+    X = [dev(x) for x in xs]
+    Wq, Wkv = dev(wts["wq"]), dev(np.concatenate([wts["wk"], wts["wv"]], axis=1))
+    do = [dev(x) for x in dos]
+    kvd = w.Hkv * w.d
+    pool = B.pkv_pool_create(w.P, w.Hkv, w.Hq, w.d, B.PKV_BF16, w.n_phys,
+                             residency=B.PKV_RES_PINNED_HOST, n_device_slots=w.n_pages)
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    try:
+        seq = B.pkv_seq_create(pool)
+        B.pkv_set_block_table(seq, bt)
+        o, lse, dq, sels = [], [], [], []
+        kv_next = torch.matmul(X[0], Wkv)                      # chunk 0's K/V
+        for c in range(n):
+            s, e = w.chunk_range(c)
+            kv = kv_next
+            k_c = kv[:, :kvd].contiguous().view(e - s, w.Hkv, w.d)
+            v_c = kv[:, kvd:].contiguous().view(e - s, w.Hkv, w.d)
+            B.pkv_append(seq, k_c, v_c, e - s, main)
+            q_c = torch.matmul(X[c], Wq).view(e - s, w.Hq, w.d)
+            sel = torch.empty(((e - s) // w.P, w.Hkv, K + ns + nl), dtype=torch.int32, device="cuda")
+            B.pkv_page_topk(seq, q_c, s, e - s, K, ns, nl, sel, None, main)
+            sels.append(sel)
+            B.pkv_prefetch(seq, sel, sel.numel(), B.PKV_STAGE_KV, side)
+            if c + 1 < n:
+                kv_next = torch.matmul(X[c + 1], Wkv)          # overlaps the transfer
+            B.pkv_wait(seq, main, 0)
+            o.append(torch.empty_like(q_c))
+            lse.append(torch.empty((w.Hq, e - s), dtype=torch.float32, device="cuda"))
+            dq.append(torch.empty_like(q_c))
+            B.pkv_chunk_attn_fwd(seq, q_c, s, e - s, o[c], lse[c], sel, main)
+        for c in reversed(range(n)):
+            s, e = w.chunk_range(c)
+            B.pkv_prefetch(seq, sels[c], sels[c].numel(), B.PKV_STAGE_KV | B.PKV_STAGE_GRADS, side)
+            q_c = torch.matmul(X[c], Wq).view(e - s, w.Hq, w.d)    # recomputed, overlapping
+            B.pkv_wait(seq, main, 0)
+            B.pkv_chunk_attn_bwd(seq, q_c, o[c], do[c], lse[c], s, e - s, dq[c], sels[c], main)
+            B.pkv_writeback_grads(seq, side)
+        B.pkv_wait(seq, main, 10_000_000)
+        dk = torch.empty((w.N, w.Hkv, w.d), dtype=torch.float32, device="cuda")
+        dv = torch.empty_like(dk)
+        B.pkv_gather(seq, None, None, dk, dv, None, main)
+        torch.cuda.synchronize()
+        B.pkv_check(pool)
+        for c in range(n):
+            np.testing.assert_array_equal(sels[c].cpu().numpy(), ref["sel"][c])
+            assert np.abs(to_numpy(o[c]) - ref["o"][c]).max() <= 1e-2, c
+            assert np.abs(to_numpy(lse[c]) - ref["lse"][c]).max() <= 1e-2, c
+            assert _rel(to_numpy(dq[c]), ref["dq"][c]) <= 2e-2, c
+        assert _rel(to_numpy(dk), oracle.logical_rows(ref["dkpool"], bt, w.N, w.P)) <= 2e-2
+        assert _rel(to_numpy(dv), oracle.logical_rows(ref["dvpool"], bt, w.N, w.P)) <= 2e-2
+    finally:
+        B.pkv_pool_destroy(pool)
+
+
+def _unions(sels):
+    return [np.unique(s[s >= 0]) for s in sels]
+
+
+def test_slot_cache_with_evictions_matches_oracle_and_moves_fewer_pages():
+    """The slot cache: fewer slots than pages, so pages (with dirty gradients
+    in the backward) are evicted between chunks; no per-chunk write-back, one
+    release at the end. Gradients, outputs and selections equal the oracle's;
+    the K/V page-heads moved are fewer than staging every chunk's selection
+    afresh, and every page staged with gradients was written back."""
+    w = _w(N=4096, C=1024)
+    K, ns, nl = w.topk
+    n = w.n_chunks
+    qs = [synth.chunk_q(w, c) for c in range(n)]
+    ks = [synth.chunk_k(w, c) for c in range(n)]
+    vs = [synth.chunk_v(w, c) for c in range(n)]
+    dos = [synth.chunk_do(w, c) for c in range(n)]
+    bt = synth.block_table(w)
+    ref = oracle.chunk_recurrent_step(qs, ks, vs, dos, bt, w.P, w.n_phys, topk=w.topk)
+    unions = _unions(ref["sel"])
+    n_slots = max(len(u) for u in unions)
+    assert n_slots < w.n_pages                       # evictions must happen
+    pool = B.pkv_pool_create(w.P, w.Hkv, w.Hq, w.d, B.PKV_BF16, w.n_phys,
+                             residency=B.PKV_RES_PINNED_HOST, n_device_slots=n_slots)
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    try:
+        seq = B.pkv_seq_create(pool)
+        B.pkv_set_block_table(seq, bt)
+        dev = lambda x: to_device(x, "bf16")
+        q = [dev(x) for x in qs]
+        do = [dev(x) for x in dos]
+        o, lse, dq, sels = [], [], [], []
+        for c in range(n):
+            s, e = w.chunk_range(c)
+            B.pkv_append(seq, dev(ks[c]), dev(vs[c]), e - s, main)
+            sel = torch.empty(((e - s) // w.P, w.Hkv, K + ns + nl), dtype=torch.int32, device="cuda")
+            B.pkv_page_topk(seq, q[c], s, e - s, K, ns, nl, sel, None, main)
+            sels.append(sel)
+            o.append(torch.empty_like(q[c]))
+            lse.append(torch.empty((w.Hq, e - s), dtype=torch.float32, device="cuda"))
+            dq.append(torch.empty_like(q[c]))
+            B.pkv_prefetch(seq, sel, sel.numel(), B.PKV_STAGE_KV, side)
+            B.pkv_wait(seq, main, 0)
+            B.pkv_chunk_attn_fwd(seq, q[c], s, e - s, o[c], lse[c], sel, main)
+        for c in reversed(range(n)):
+            s, e = w.chunk_range(c)
+            B.pkv_prefetch(seq, sels[c], sels[c].numel(), B.PKV_STAGE_KV | B.PKV_STAGE_GRADS, side)
+            B.pkv_wait(seq, main, 0)
+            B.pkv_chunk_attn_bwd(seq, q[c], o[c], do[c], lse[c], s, e - s, dq[c], sels[c], main)
+        B.pkv_release_slots(seq, side)
+        B.pkv_wait(seq, main, 10_000_000)
+        dk = torch.empty((w.N, w.Hkv, w.d), dtype=torch.float32, device="cuda")
+        dv = torch.empty_like(dk)
+        B.pkv_gather(seq, None, None, dk, dv, None, main)
+        torch.cuda.synchronize()
+        B.pkv_check(pool)
+        for c in range(n):
+            np.testing.assert_array_equal(sels[c].cpu().numpy(), ref["sel"][c])
+            assert np.abs(to_numpy(o[c]) - ref["o"][c]).max() <= 1e-2, c
+            assert _rel(to_numpy(dq[c]), ref["dq"][c]) <= 2e-2, c
+        assert _rel(to_numpy(dk), oracle.logical_rows(ref["dkpool"], bt, w.N, w.P)) <= 2e-2
+        assert _rel(to_numpy(dv), oracle.logical_rows(ref["dvpool"], bt, w.N, w.P)) <= 2e-2
+        st = B.pkv_stage_stats(seq)
+        afresh = 2 * sum(len(u) for u in unions) * w.Hkv        # forward + backward
+        graded = len(np.unique(np.concatenate(unions))) * w.Hkv
+        assert st["kv_in"] < afresh, (st, afresh)
+        assert st["grads_in"] >= graded and st["grads_out"] >= graded, (st, graded)
+    finally:
+        B.pkv_pool_destroy(pool)
+
+
+def test_append_into_a_staged_partial_page_restages_it():
+    """A page staged while partial is refreshed once an append completes it:
+    the forward of the completed page matches the oracle."""
+    w = _w(N=256, C=256, keys="normal", extra_pages=2)
+    bt = synth.block_table(w)
+    k, v, q = synth.chunk_k(w, 0), synth.chunk_v(w, 0), synth.chunk_q(w, 0)
+    pool = B.pkv_pool_create(w.P, w.Hkv, w.Hq, w.d, B.PKV_BF16, w.n_phys,
+                             residency=B.PKV_RES_PINNED_HOST, n_device_slots=w.n_pages)
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    try:
+        seq = B.pkv_seq_create(pool)
+        B.pkv_set_block_table(seq, bt)
+        dev = lambda x: to_device(np.ascontiguousarray(x), "bf16")
+        pages = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
+        B.pkv_append(seq, dev(k[:200]), dev(v[:200]), 200, main)      # page 1 partial
+        B.pkv_prefetch(seq, pages, 2, B.PKV_STAGE_KV, side)
+        B.pkv_wait(seq, main, 0)
+        B.pkv_append(seq, dev(k[200:]), dev(v[200:]), 56, main)       # completes page 1
+        B.pkv_prefetch(seq, pages, 2, B.PKV_STAGE_KV, side)
+        B.pkv_wait(seq, main, 0)
+        qd = dev(q[128:])
+        o = torch.empty_like(qd)
+        lse = torch.empty((w.Hq, 128), dtype=torch.float32, device="cuda")
+        B.pkv_chunk_attn_fwd(seq, qd, 128, 128, o, lse, None, main)
+        torch.cuda.synchronize()
+        B.pkv_check(pool)
+        o_ref, lse_ref = oracle.attention_forward(q[128:], k, v, 128)
+        assert np.abs(to_numpy(o) - o_ref).max() <= 1e-2
+        assert np.abs(to_numpy(lse) - lse_ref).max() <= 1e-2
+    finally:
+        B.pkv_pool_destroy(pool)
