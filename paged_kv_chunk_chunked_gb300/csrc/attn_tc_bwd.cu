@@ -72,7 +72,10 @@ struct BwdParams {
     int* err;
 };
 
-constexpr int kMaxSelQp = 256;   // query pages per chunk the sparse dK/dV kernel can list
+// Query pages per chunk the sparse dK/dV kernel lists in shared memory (3
+// bytes each): chunks of up to 262144 tokens at page 128. Longer chunks run
+// on the CUDA-core kernel.
+constexpr int kMaxSelQp = 2048;
 
 
 
@@ -88,13 +91,19 @@ constexpr int kMaxSelQp = 256;   // query pages per chunk the sparse dK/dV kerne
 // overlaps their work on tile t; P^T/dS^T are rewritten once the gradient
 // MMAs of the previous tile have read them (p_free).
 constexpr int kv_STAGES = 4;
-constexpr uint32_t kv_V = 0;                 // [128 keys][128 d]: two 16 KB halves
-constexpr uint32_t kv_Q = 32 * KB;           // stages x [64 q][128 d]: two 8 KB halves
-constexpr uint32_t kv_dO = kv_Q + kv_STAGES * 16 * KB;
-constexpr uint32_t kv_STAT = kv_dO + kv_STAGES * 16 * KB;   // stages x (64 lse*log2e + 64 D) floats
-constexpr uint32_t kv_SMEM = kv_STAT + kv_STAGES * 512 + 1024;
+// Head dimension D = 128 or 64: a page (or a Q/dO tile) of one head is D / 64
+// blocks of 64 columns.
+template <int D> struct KVLayout {
+    static_assert(D == 64 || D == 128, "head dim 64 or 128");
+    static constexpr uint32_t kV = 0;                          // [128 keys][D]: D/64 16 KB blocks
+    static constexpr uint32_t kQ = (D / 64) * 16 * KB;         // stages x [64 q][D]: D/64 8 KB blocks
+    static constexpr uint32_t kQStage = (D / 64) * 8 * KB;
+    static constexpr uint32_t kdO = kQ + kv_STAGES * kQStage;
+    static constexpr uint32_t kSTAT = kdO + kv_STAGES * kQStage;   // stages x (64 lse*log2e + 64 D) floats
+    static constexpr uint32_t kSMEM = kSTAT + kv_STAGES * 512 + 1024;
+};
 // Tensor-memory columns: S^T, dP^T (64 fp32 each), P^T, dS^T (64 bf16 = 32
-// each), K (128 bf16 = 64), dK, dV accumulators (128 fp32 each).
+// each), K (D bf16 = D/2), dK, dV accumulators (D fp32 each).
 constexpr uint32_t kv_TS = 0, kv_TDP = 64, kv_TP = 128, kv_TDS = 160, kv_TK = 192, kv_TDK = 256,
                    kv_TDV = 384;
 
@@ -112,9 +121,13 @@ struct __align__(8) KVBar {
     uint8_t sel_flag[kMaxSelQp];
 };
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                  const __grid_constant__ CUtensorMap tm_v, BwdParams p) {
+    using L = KVLayout<D>;
+    constexpr uint32_t kv_V = L::kV, kv_Q = L::kQ, kv_dO = L::kdO, kv_STAT = L::kSTAT;
+    constexpr uint32_t kQS = L::kQStage;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -215,9 +228,10 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (lane == 0) {
             tc::prefetch_tmap(&tm_q);
             tc::prefetch_tmap(&tm_do);
-            tc::mbar_arrive_expect_tx(&B.kv_full, 32 * KB);
-            tc::tma_load_2d(smem + kv_V, &tm_v, &B.kv_full, 0, row);
-            tc::tma_load_2d(smem + kv_V + 16 * KB, &tm_v, &B.kv_full, 64, row);
+            tc::mbar_arrive_expect_tx(&B.kv_full, (D / 64) * 16 * KB);
+#pragma unroll
+            for (int b = 0; b < D / 64; ++b)
+                tc::tma_load_2d(smem + kv_V + b * 16 * KB, &tm_v, &B.kv_full, 64 * b, row);
         }
         // Per-query statistics of tile t (log2e * LSE, +inf past the chunk, and D),
         // two columns per lane; loaded one tile ahead so their latency overlaps
@@ -243,13 +257,14 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (lane == 0) {
                 const int h = head_of(t);
                 const int i = tile_of(t);
-                uint8_t* q_dst = smem + kv_Q + st * 16 * KB;
-                uint8_t* do_dst = smem + kv_dO + st * 16 * KB;
-                tc::mbar_expect_tx(&B.qdo_full[st], 32 * KB);
-                tc::tma_load_3d(q_dst, &tm_q, &B.qdo_full[st], 0, h, i * 64);
-                tc::tma_load_3d(q_dst + 8 * KB, &tm_q, &B.qdo_full[st], 64, h, i * 64);
-                tc::tma_load_3d(do_dst, &tm_do, &B.qdo_full[st], 0, h, i * 64);
-                tc::tma_load_3d(do_dst + 8 * KB, &tm_do, &B.qdo_full[st], 64, h, i * 64);
+                uint8_t* q_dst = smem + kv_Q + st * kQS;
+                uint8_t* do_dst = smem + kv_dO + st * kQS;
+                tc::mbar_expect_tx(&B.qdo_full[st], 2 * kQS);
+#pragma unroll
+                for (int b = 0; b < D / 64; ++b) {
+                    tc::tma_load_3d(q_dst + b * 8 * KB, &tm_q, &B.qdo_full[st], 64 * b, h, i * 64);
+                    tc::tma_load_3d(do_dst + b * 8 * KB, &tm_do, &B.qdo_full[st], 64 * b, h, i * 64);
+                }
             }
             load_stats(t + 1, fill);
             float* sst = stat + st * 128;
@@ -278,7 +293,7 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // loop (warp-uniform descriptors); the elected lane issues.
         const bool leader = tc::elect_one_sync();
         const uint32_t id_s = tc::idesc_bf16(128, 64, false, false);    // S^T = K Q^T
-        const uint32_t id_g = tc::idesc_bf16(128, 128, false, true);    // dV += P^T dO
+        const uint32_t id_g = tc::idesc_bf16(128, D, false, true);      // dV += P^T dO
         const uint32_t t_dK = tmem + kv_TDK, t_dV = tmem + kv_TDV;
         const uint32_t t_S = tmem + kv_TS, t_dP = tmem + kv_TDP, t_K = tmem + kv_TK;
         bool ok = true;
@@ -293,15 +308,15 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (!tc::warp_wait(&B.qdo_full[st], (t / kv_STAGES) & 1, p.err)) return false;
             if (t > 0 && !tc::warp_wait(&B.s_free, (t - 1) & 1, p.err)) return false;
             tc::tc_fence_after();
-            const uint32_t so = st * 16 * KB;
+            const uint32_t so = st * kQS;
             if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {    // K = d: 16 per MMA (8 columns of K)
+                for (int kk = 0; kk < D / 16; ++kk) {   // K = d: 16 per MMA (8 columns of K)
                     const uint32_t ob = (kk >> 2) * 8 * KB + (kk & 3) * 32;
                     tc::mma_bf16_ts(t_S, t_K + kk * 8, tc::sdesc_at(dQk0, so + ob), id_s, kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
+                for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t oa = (kk >> 2) * 16 * KB + (kk & 3) * 32;
                     const uint32_t ob = (kk >> 2) * 8 * KB + (kk & 3) * 32;
                     tc::mma_bf16(t_dP, tc::sdesc_at(dV0, oa), tc::sdesc_at(ddOk0, so + ob), id_s,
@@ -316,7 +331,7 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int st = t % kv_STAGES;
             if (!tc::warp_wait(&B.p_full, t & 1, p.err)) return false;
             tc::tc_fence_after();
-            const uint32_t so = st * 16 * KB;
+            const uint32_t so = st * kQS;
             if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)      // K = 64 queries, 16 per MMA (8 columns)
@@ -356,18 +371,20 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int r = quad * 32 + lane;                      // key row of the page
         const int64_t kpos = kfirst + r;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        const float sl2 = rsqrtf(128.f) * kLog2e;
+        const float sl2 = rsqrtf((float)D) * kLog2e;
         {
-            // K row r, head dims [64 wg, 64 wg + 64) -> TMEM columns kv_TK + 32 wg ..
+            // K row r, head dims [D/2 wg, D/2 wg + D/2) -> TMEM columns kv_TK + D/4 wg ..
+            constexpr int NW = D / 4;
             const uint4* src = reinterpret_cast<const uint4*>(
-                static_cast<const __nv_bfloat16*>(p.kpool) + (((size_t)pp * p.Hkv + kvh) * 128 + r) * 128 + wg * 64);
-            uint32_t w[32];
+                static_cast<const __nv_bfloat16*>(p.kpool) + (((size_t)pp * p.Hkv + kvh) * 128 + r) * D + wg * (D / 2));
+            uint32_t w[NW];
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
+            for (int v = 0; v < NW / 4; ++v) {
                 const uint4 u = __ldg(src + v);
                 w[4 * v] = u.x; w[4 * v + 1] = u.y; w[4 * v + 2] = u.z; w[4 * v + 3] = u.w;
             }
-            tc::tmem_st32(lane_base + kv_TK + wg * 32, w);
+            if constexpr (D == 128) tc::tmem_st32(lane_base + kv_TK + wg * 32, w);
+            else tc::tmem_st16(lane_base + kv_TK + wg * 16, w);
             tc::tmem_wait_st();
             tc::tc_fence_before();
             tc::mbar_arrive(&B.k_tmem);
@@ -432,12 +449,12 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // Warpgroup 0 adds dK (scaled), warpgroup 1 adds dV.
             tc::tc_fence_after();
             const bool live = kpos < p.q_start + p.n_q;
-            const size_t off = (((size_t)pp * p.Hkv + kvh) * 128 + r) * 128;
-            const float scale = wg == 0 ? rsqrtf(128.f) : 1.f;
+            const size_t off = (((size_t)pp * p.Hkv + kvh) * 128 + r) * D;
+            const float scale = wg == 0 ? rsqrtf((float)D) : 1.f;
             float* dst = (wg == 0 ? p.dkpool : p.dvpool) + off;
             const uint32_t col = wg == 0 ? kv_TDK : kv_TDV;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < D / 32; ++c) {
                 uint32_t a[32];
                 tc::tmem_ld32(lane_base + col + c * 32, a);
                 tc::tmem_wait_ld(a);
@@ -472,11 +489,15 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 // K and V travel in separate rings: V is free once dP is computed, K only after dQ.
 constexpr int q_KST = 4;
 constexpr int q_VST = 2;
-constexpr uint32_t q_dO = 0;                 // [128 q][128 d]: two 16 KB halves
-constexpr uint32_t q_K = 32 * KB;            // stages x [128 keys][128 d]: two 16 KB halves
-constexpr uint32_t q_V = q_K + q_KST * 32 * KB;
-constexpr uint32_t q_SMEM = q_V + q_VST * 32 * KB + 1024;
-// Tensor-memory columns.
+template <int D> struct QLayout {
+    static constexpr uint32_t kTile = (D / 64) * 16 * KB;    // [128 rows][D]: D/64 16 KB blocks
+    static constexpr uint32_t kdO = 0;
+    static constexpr uint32_t kK = kTile;                     // stages x [128 keys][D]
+    static constexpr uint32_t kV = kK + q_KST * kTile;
+    static constexpr uint32_t kSMEM = kV + q_VST * kTile + 1024;
+};
+// Tensor-memory columns: S, dP (128 fp32 each), dQ (D fp32), dS (128 bf16 =
+// 64), Q (D bf16 = D/2).
 constexpr uint32_t q_TS = 0, q_TDP = 128, q_TDQ = 256, q_TDS = 384, q_TQ = 448;
 
 struct __align__(8) QBar {
@@ -491,9 +512,12 @@ struct __align__(8) QBar {
     uint32_t tmem_base;
 };
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, BwdParams p) {
+    using L = QLayout<D>;
+    constexpr uint32_t q_dO = L::kdO, q_K = L::kK, q_V = L::kV, kT = L::kTile;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -542,9 +566,10 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant
             tc::prefetch_tmap(&tm_k);
             tc::prefetch_tmap(&tm_v);
             const int q_row0 = qt * 128;
-            tc::mbar_arrive_expect_tx(&B.q_full, 32 * KB);
-            tc::tma_load_3d(smem + q_dO, &tm_do, &B.q_full, 0, h, q_row0);
-            tc::tma_load_3d(smem + q_dO + 16 * KB, &tm_do, &B.q_full, 64, h, q_row0);
+            tc::mbar_arrive_expect_tx(&B.q_full, kT);
+#pragma unroll
+            for (int b = 0; b < D / 64; ++b)
+                tc::tma_load_3d(smem + q_dO + b * 16 * KB, &tm_do, &B.q_full, 64 * b, h, q_row0);
         }
         tc::PageBatch pages;
         pages.init(p.bt, sel_row, T, lane);
@@ -561,20 +586,22 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant
             }
             const int row = (int)(((int64_t)pp * p.Hkv + kvh) * 128);
             if (lane == 0) {
-                uint8_t* kd = smem + q_K + ks * 32 * KB;
-                tc::mbar_arrive_expect_tx(&B.k_full[ks], 32 * KB);
-                tc::tma_load_2d(kd, &tm_k, &B.k_full[ks], 0, row);
-                tc::tma_load_2d(kd + 16 * KB, &tm_k, &B.k_full[ks], 64, row);
+                uint8_t* kd = smem + q_K + ks * kT;
+                tc::mbar_arrive_expect_tx(&B.k_full[ks], kT);
+#pragma unroll
+                for (int b = 0; b < D / 64; ++b)
+                    tc::tma_load_2d(kd + b * 16 * KB, &tm_k, &B.k_full[ks], 64 * b, row);
             }
             k_issued = t + 1;
             if (t >= q_VST &&
                 !__all_sync(0xffffffffu, tc::mbar_wait(&B.v_empty[vs], ((t / q_VST) - 1) & 1, p.err)))
                 break;
             if (lane == 0) {
-                uint8_t* vd = smem + q_V + vs * 32 * KB;
-                tc::mbar_arrive_expect_tx(&B.v_full[vs], 32 * KB);
-                tc::tma_load_2d(vd, &tm_v, &B.v_full[vs], 0, row);
-                tc::tma_load_2d(vd + 16 * KB, &tm_v, &B.v_full[vs], 64, row);
+                uint8_t* vd = smem + q_V + vs * kT;
+                tc::mbar_arrive_expect_tx(&B.v_full[vs], kT);
+#pragma unroll
+                for (int b = 0; b < D / 64; ++b)
+                    tc::tma_load_2d(vd + b * 16 * KB, &tm_v, &B.v_full[vs], 64 * b, row);
             }
             v_issued = t + 1;
         }
@@ -590,7 +617,7 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant
         // (warp-uniform descriptors); the elected lane issues.
         const bool leader = tc::elect_one_sync();
         const uint32_t id_s = tc::idesc_bf16(128, 128, false, false);   // S = Q K^T
-        const uint32_t id_q = tc::idesc_bf16(128, 128, false, true);    // dQ += dS K
+        const uint32_t id_q = tc::idesc_bf16(128, D, false, true);      // dQ += dS K
         const uint32_t t_S = tmem + q_TS, t_dP = tmem + q_TDP, t_dQ = tmem + q_TDQ, t_Q = tmem + q_TQ;
         bool ok = true;
         // Base descriptors; each MMA advances them by a compile-time offset.
@@ -604,15 +631,15 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant
             if (!tc::warp_wait(&B.v_full[vs], (t / q_VST) & 1, p.err)) return false;
             if (t > 0 && !tc::warp_wait(&B.s_free, (t - 1) & 1, p.err)) return false;
             tc::tc_fence_after();
-            const uint32_t k_off = ks * 32 * KB, v_off = vs * 32 * KB;
+            const uint32_t k_off = ks * kT, v_off = vs * kT;
             if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {    // K = d = 128, 16 per MMA (8 columns of Q)
+                for (int kk = 0; kk < D / 16; ++kk) {   // K = d, 16 per MMA (8 columns of Q)
                     const uint32_t o = (kk >> 2) * 16 * KB + (kk & 3) * 32;
                     tc::mma_bf16_ts(t_S, t_Q + kk * 8, tc::sdesc_at(dKk0, k_off + o), id_s, kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
+                for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t o = (kk >> 2) * 16 * KB + (kk & 3) * 32;
                     tc::mma_bf16(t_dP, tc::sdesc_at(ddO0, o), tc::sdesc_at(dVk0, v_off + o), id_s,
                                  kk > 0 ? 1u : 0u);
@@ -627,7 +654,7 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant
             const int ks = t % q_KST;
             if (!tc::warp_wait(&B.ds_full, t & 1, p.err)) return false;
             tc::tc_fence_after();
-            const uint32_t t_dS = tmem + q_TDS, k_off = ks * 32 * KB;
+            const uint32_t t_dS = tmem + q_TDS, k_off = ks * kT;
             if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)      // K = 128 keys, 16 per MMA (8 columns)
@@ -666,23 +693,25 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant
         const float lse2 = valid ? p.lse[(size_t)h * p.n_q + q_local] * kLog2e : INFINITY;
         const float Dr = valid ? p.Dbuf[(size_t)h * p.n_q + q_local] : 0.f;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        const float sl2 = rsqrtf(128.f) * kLog2e;
+        const float sl2 = rsqrtf((float)D) * kLog2e;
         const int64_t first_diag = p.q_start + (int64_t)qt * 128;   // first key of the own page
         {
-            // Q row, head dims [64 wg, 64 wg + 64) -> TMEM columns q_TQ + 32 wg ..
-            uint32_t w[32];
+            // Q row, head dims [D/2 wg, D/2 wg + D/2) -> TMEM columns q_TQ + D/4 wg ..
+            constexpr int NW = D / 4;
+            uint32_t w[NW];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) w[e] = 0u;          // rows past the chunk: Q = 0
+            for (int e = 0; e < NW; ++e) w[e] = 0u;          // rows past the chunk: Q = 0
             if (valid) {
                 const uint4* src = reinterpret_cast<const uint4*>(
-                    static_cast<const __nv_bfloat16*>(p.q) + ((size_t)q_local * p.Hq + h) * 128 + wg * 64);
+                    static_cast<const __nv_bfloat16*>(p.q) + ((size_t)q_local * p.Hq + h) * D + wg * (D / 2));
 #pragma unroll
-                for (int v = 0; v < 8; ++v) {
+                for (int v = 0; v < NW / 4; ++v) {
                     const uint4 u = __ldg(src + v);
                     w[4 * v] = u.x; w[4 * v + 1] = u.y; w[4 * v + 2] = u.z; w[4 * v + 3] = u.w;
                 }
             }
-            tc::tmem_st32(lane_base + q_TQ + wg * 32, w);
+            if constexpr (D == 128) tc::tmem_st32(lane_base + q_TQ + wg * 32, w);
+            else tc::tmem_st16(lane_base + q_TQ + wg * 16, w);
             tc::tmem_wait_st();
             tc::tc_fence_before();
             tc::mbar_arrive(&B.q_tmem);
@@ -737,10 +766,10 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant
         if (ok && T > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.acc_done, 0, p.err));
         if (ok && T > 0) {
             tc::tc_fence_after();
-            const float scale = rsqrtf(128.f);
-            __nv_bfloat16* row = static_cast<__nv_bfloat16*>(p.dq) + ((size_t)q_local * p.Hq + h) * 128;
+            const float scale = rsqrtf((float)D);
+            __nv_bfloat16* row = static_cast<__nv_bfloat16*>(p.dq) + ((size_t)q_local * p.Hq + h) * D;
 #pragma unroll
-            for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
+            for (int c = (D / 64) * wg; c < (D / 64) * (wg + 1); ++c) {
                 uint32_t a[32];
                 tc::tmem_ld32(lane_base + q_TDQ + c * 32, a);
                 tc::tmem_wait_ld(a);
@@ -767,25 +796,22 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant
     }
 }
 
-}  // namespace
-
-cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
-    // The sparse dK/dV kernel lists the selecting query pages in shared memory.
-    if (a.sel && (a.n_q + 127) / 128 > kMaxSelQp) return launch_attn_bwd_simt(a, s);
-    if ((reinterpret_cast<uintptr_t>(a.dout) & 15) || !a.tmap_k) return cudaErrorInvalidValue;
+template <int D>
+static cudaError_t launch_bwd(const AttnArgs& a, cudaStream_t s) {
     CUtensorMap tq64, tdo64, tdo128;
     std::string why;
-    const uint64_t s2 = (uint64_t)a.Hq * 256;
-    if (!make_tmap_3d(&tq64, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, a.Hq, a.n_q, 256, s2, 64, 1, 64, &why) ||
-        !make_tmap_3d(&tdo64, a.dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, a.Hq, a.n_q, 256, s2, 64, 1, 64, &why) ||
-        !make_tmap_3d(&tdo128, a.dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, a.Hq, a.n_q, 256, s2, 64, 1, 128, &why))
+    const uint64_t s1 = (uint64_t)D * 2, s2 = (uint64_t)a.Hq * D * 2;
+    if (!make_tmap_3d(&tq64, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, a.Hq, a.n_q, s1, s2, 64, 1, 64, &why) ||
+        !make_tmap_3d(&tdo64, a.dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, a.Hq, a.n_q, s1, s2, 64, 1, 64, &why) ||
+        !make_tmap_3d(&tdo128, a.dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, a.Hq, a.n_q, s1, s2, 64, 1, 128, &why))
         return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(bwd_kv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kv_SMEM);
+        cudaError_t e = cudaFuncSetAttribute(bwd_kv_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)KVLayout<D>::kSMEM);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(bwd_q_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)q_SMEM);
+            e = cudaFuncSetAttribute(bwd_q_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)QLayout<D>::kSMEM);
         if (e != cudaSuccess) return e;
         attr = true;
     }
@@ -797,25 +823,36 @@ cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
     const int64_t n_keys = a.q_start + a.n_q;
     // Small grids (early chunks) leave SMs idle behind a few long CTAs: split
     // each (page, KV head)'s iterations over up to 4 CTAs so that there are
-    // >= ~16 waves.
+    // >= ~8 waves. Every split adds the page's dK/dV rows into the pool once
+    // more; measured on the dense 32K sweep, 8 waves was as fast as 16 (which
+    // split the last chunk's pages 3 ways instead of 2) and faster than 4.
     int dev = 0, sm_count = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
     sm_count = std::max(sm_count, 1);
     const int64_t n_cta = ((n_keys + 127) / 128) * a.Hkv;
-    const int splits = (int)std::min<int64_t>(4, std::max<int64_t>(1, (16 * (int64_t)sm_count + n_cta - 1) / n_cta));
+    const int splits = (int)std::min<int64_t>(4, std::max<int64_t>(1, (8 * (int64_t)sm_count + n_cta - 1) / n_cta));
     p.kv_splits = splits;
     dim3 g_kv((unsigned)(((n_keys + 127) / 128) * splits), a.Hkv);
     {
         ProfScope ps("bwd_kv_tc_kernel", s);
-        bwd_kv_tc_kernel<<<g_kv, kThreads, kv_SMEM, s>>>(tq64, tdo64, *a.tmap_v, p);
+        bwd_kv_tc_kernel<D><<<g_kv, kThreads, KVLayout<D>::kSMEM, s>>>(tq64, tdo64, *a.tmap_v, p);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dim3 g_q((unsigned)((a.n_q + 127) / 128), a.Hq);
     ProfScope ps("bwd_q_tc_kernel", s);
-    bwd_q_tc_kernel<<<g_q, kThreads, q_SMEM, s>>>(tdo128, *a.tmap_k, *a.tmap_v, p);
+    bwd_q_tc_kernel<D><<<g_q, kThreads, QLayout<D>::kSMEM, s>>>(tdo128, *a.tmap_k, *a.tmap_v, p);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
+    // The sparse dK/dV kernel lists the selecting query pages in shared memory.
+    if (a.sel && (a.n_q + 127) / 128 > kMaxSelQp) return launch_attn_bwd_simt(a, s);
+    if ((reinterpret_cast<uintptr_t>(a.dout) & 15) || !a.tmap_k) return cudaErrorInvalidValue;
+    return a.d == 64 ? launch_bwd<64>(a, s) : launch_bwd<128>(a, s);
 }
 
 }  // namespace pkv

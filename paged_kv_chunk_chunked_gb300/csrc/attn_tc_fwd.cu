@@ -9,14 +9,15 @@
 //
 // One CTA per (query tile of 128 rows = one query page, query head); key
 // tiles are whole pages (P = 128), fetched by TMA with the physical page
-// taken from the block table. Both MMAs take their A operand from tensor
+// taken from the block table. Head dimension D = 128 or 64 (a template
+// parameter; a page of one head is D / 64 blocks of 64 columns). Both MMAs take their A operand from tensor
 // memory (an A operand in shared memory costs the tensor core a fixed ~33
 // cycles per instruction on top of the math): Q is placed there once, and
 // P overwrites the S columns it came from. Warp roles (352 threads):
 //   warp 0       TMA producer: K pages into a 3-stage ring.
 //   warp 10      TMA producer: V pages into a 2-stage ring. Each V stage
-//                carries a constant third 64-column block whose first column
-//                is 1, so the PV MMA (N = 144) also accumulates the row sum
+//                carries a constant extra 64-column block whose first column
+//                is 1, so the PV MMA (N = D + 16) also accumulates the row sum
 //                l = sum_j P_ij of exactly the bf16 weights it multiplies.
 //   warp 1       MMA issuer (elected lane): S_j = Q K_j^T into a double-
 //                buffered TMEM tile, then O += P_{j-1} V_{j-1} (O in TMEM).
@@ -29,7 +30,8 @@
 //                grows by more than 2^8 (P <= 256 then, exactly representable
 //                range for bf16), each warpgroup its own half of the columns.
 //                Epilogue: O / l, LSE.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256,384), l 384, Q [400,464).
+// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D), l 256+D,
+// Q [400, 400+D/2).
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -40,22 +42,28 @@
 namespace pkv {
 namespace {
 
-constexpr int kTile = 128;                   // query rows = keys per tile = head dim
+constexpr int kTile = 128;                   // query rows = keys per tile
 constexpr int kThreads = 352;
 constexpr int kSoftmaxThreads = 256;
 constexpr uint32_t kHalfBytes = 128 * 128;   // [128 rows][64 bf16] = 16 KB
-constexpr uint32_t kTileBytes = 2 * kHalfBytes;
-// Shared-memory tile offsets (bytes from a 1024-aligned base).
+constexpr int kKStages = 3, kVStages = 2;
+constexpr float kRescaleThreshold = 8.0f;                         // log2 units
+
+// Shared-memory tile offsets (bytes from a 1024-aligned base) and tensor-
+// memory columns for head dimension D.
 // K and V have separate rings: a K stage is free as soon as S_j completes, so
 // K loads run kKStages - 1 tiles ahead; a V stage is free after PV_j.
-constexpr int kKStages = 3, kVStages = 2;
-constexpr uint32_t kVStageBytes = kTileBytes + kHalfBytes;        // V + the ones block
-constexpr uint32_t kOffK = 0;
-constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
-constexpr uint32_t kTilesBytes = kOffV + kVStages * kVStageBytes; // 192 KB
-constexpr uint32_t kSmemBytes = kTilesBytes + 1024;               // + alignment slack
-constexpr float kRescaleThreshold = 8.0f;                         // log2 units
-constexpr uint32_t kColO = 256, kColL = kColO + 128, kColQ = 400;
+template <int D> struct FwdLayout {
+    static_assert(D == 64 || D == 128, "head dim 64 or 128");
+    static constexpr int kBlocks = D / 64;                                 // 64-column blocks
+    static constexpr uint32_t kTileBytes = kBlocks * kHalfBytes;
+    static constexpr uint32_t kVStageBytes = kTileBytes + kHalfBytes;      // V + the ones block
+    static constexpr uint32_t kOffK = 0;
+    static constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
+    static constexpr uint32_t kTilesBytes = kOffV + kVStages * kVStageBytes;
+    static constexpr uint32_t kSmemBytes = kTilesBytes + 1024;             // + alignment slack
+    static constexpr uint32_t kColO = 256, kColL = kColO + D, kColQ = 400;
+};
 
 struct FwdParams {
     int Hq, Hkv;
@@ -92,13 +100,15 @@ using tc::drain_wait;
 // One producer warp: streams the K ring or the V ring. The whole warp walks
 // the tiles (page indices come 32 at a time from a PageBatch); lane 0 issues
 // the copies. A K load never waits behind a V stage in use.
+template <int D>
 __device__ __forceinline__ void produce_ring(const FwdParams& p, uint8_t* smem, FwdBarriers& B,
                                              const CUtensorMap& tmap, bool is_k, int qt, int kvh,
                                              int nt, int lane) {
+    using L = FwdLayout<D>;
     const int nst = is_k ? kKStages : kVStages;
     uint64_t* full = is_k ? B.k_full : B.v_full;
     uint64_t* empty = is_k ? B.k_empty : B.v_empty;
-    uint8_t* base = smem + (is_k ? kOffK : kOffV);
+    uint8_t* base = smem + (is_k ? L::kOffK : L::kOffV);
     if (lane == 0) tc::prefetch_tmap(&tmap);
     tc::PageBatch pages;
     pages.init(p.bt, p.sel ? p.sel + ((size_t)qt * p.Hkv + kvh) * p.kmax : nullptr, nt, lane);
@@ -115,10 +125,11 @@ __device__ __forceinline__ void produce_ring(const FwdParams& p, uint8_t* smem, 
         }
         if (lane == 0) {
             const int row = (int)(((int64_t)pp * p.Hkv + kvh) * kTile);
-            uint8_t* dst = base + st * (is_k ? kTileBytes : kVStageBytes);
-            tc::mbar_arrive_expect_tx(&full[st], kTileBytes);
-            tc::tma_load_2d(dst, &tmap, &full[st], 0, row);
-            tc::tma_load_2d(dst + kHalfBytes, &tmap, &full[st], 64, row);
+            uint8_t* dst = base + st * (is_k ? L::kTileBytes : L::kVStageBytes);
+            tc::mbar_arrive_expect_tx(&full[st], L::kTileBytes);
+#pragma unroll
+            for (int b = 0; b < L::kBlocks; ++b)
+                tc::tma_load_2d(dst + b * kHalfBytes, &tmap, &full[st], 64 * b, row);
         }
         issued = j + 1;
     }
@@ -127,9 +138,14 @@ __device__ __forceinline__ void produce_ring(const FwdParams& p, uint8_t* smem, 
         for (int j = max(0, issued - nst); j < issued; ++j) drain_wait(&full[j % nst], (j / nst) & 1);
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
               FwdParams p) {
+    using L = FwdLayout<D>;
+    constexpr uint32_t kTileBytes = L::kTileBytes, kVStageBytes = L::kVStageBytes;
+    constexpr uint32_t kOffK = L::kOffK, kOffV = L::kOffV;
+    constexpr uint32_t kColO = L::kColO, kColL = L::kColL, kColQ = L::kColQ;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -182,17 +198,17 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
 
     if (warp == 0) {
         // ------------------------------------------------------------ K producer
-        produce_ring(p, smem, B, tmap_k, true, qt, kvh, nt, lane);
+        produce_ring<D>(p, smem, B, tmap_k, true, qt, kvh, nt, lane);
     } else if (warp == kThreads / 32 - 1) {
         // ------------------------------------------------------------ V producer
-        produce_ring(p, smem, B, tmap_v, false, qt, kvh, nt, lane);
+        produce_ring<D>(p, smem, B, tmap_v, false, qt, kvh, nt, lane);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // The whole warp runs the loop (warp-uniform descriptors); one elected
         // lane issues the tcgen05 instructions and commits.
         const bool leader = tc::elect_one_sync();
         const uint32_t idesc = tc::idesc_bf16(128, 128, false, false);       // S = Q K^T
-        const uint32_t idesc_pv = tc::idesc_bf16(128, 144, false, true);     // [O l] += P [V 1]
+        const uint32_t idesc_pv = tc::idesc_bf16(128, D + 16, false, true);  // [O l] += P [V 1]
         const uint32_t tmem_o = tmem + kColO, tmem_q = tmem + kColQ;
         const uint64_t dk0 = tc::sdesc(tc::smem_u32(smem + kOffK), 16, 1024);            // K-major
         const uint64_t dv0 = tc::sdesc(tc::smem_u32(smem + kOffV), kHalfBytes, 1024);    // MN-major
@@ -204,9 +220,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
             if (!tc::warp_wait(&B.p_full, i & 1, p.err)) return false;
             if (!tc::warp_wait(&B.v_full[vs], (i / kVStages) & 1, p.err)) return false;
             tc::tc_fence_after();
-            // B = [V 1] [128 keys][144] MN-major: 16 keys = 2 K-groups of 8 rows
-            // (1024 B apart); columns span three 64-column blocks 16 KB apart
-            // (V's two halves, then the ones block).
+            // B = [V 1] [128 keys][D + 16] MN-major: 16 keys = 2 K-groups of 8
+            // rows (1024 B apart); columns span 64-column blocks 16 KB apart
+            // (V's D / 64 blocks, then the ones block).
             const uint32_t tmem_p = tmem + (i & 1) * 128;
             if (leader) {
 #pragma unroll
@@ -226,7 +242,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
             const uint32_t tmem_s = tmem + (j & 1) * 128;
             if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {    // K = d: 16 per MMA, 8 TMEM columns of Q
+                for (int kk = 0; kk < D / 16; ++kk) {   // K = d: 16 per MMA, 8 TMEM columns of Q
                     const uint32_t koff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
                     tc::mma_bf16_ts(tmem_s, tmem_q + kk * 8, tc::sdesc_at(dk0, ks * kTileBytes + koff),
                                     idesc, kk > 0 ? 1u : 0u);
@@ -250,24 +266,26 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
         const int quad = warp & 3;                    // TMEM lane quadrant of this warp
         const int row = quad * 32 + lane;             // query row within the tile
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        const float sl2 = rsqrtf(128.f) * kLog2e;
+        const float sl2 = rsqrtf((float)D) * kLog2e;
         const int64_t q_local = (int64_t)qt * kTile + row;
         const bool valid = q_local < p.n_q;
         {
-            // Q row, head dims [64 wg, 64 wg + 64) -> TMEM columns kColQ + 32 wg ..
-            uint32_t w[32];
+            // Q row, head dims [D/2 wg, D/2 wg + D/2) -> TMEM columns kColQ + D/4 wg ..
+            constexpr int NW = D / 4;                     // 32-bit words per warpgroup
+            uint32_t w[NW];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) w[e] = 0u;          // rows past the chunk: Q = 0
+            for (int e = 0; e < NW; ++e) w[e] = 0u;          // rows past the chunk: Q = 0
             if (valid) {
                 const uint4* src = reinterpret_cast<const uint4*>(
-                    static_cast<const __nv_bfloat16*>(p.q) + ((size_t)q_local * p.Hq + h) * kTile + wg * 64);
+                    static_cast<const __nv_bfloat16*>(p.q) + ((size_t)q_local * p.Hq + h) * D + wg * (D / 2));
 #pragma unroll
-                for (int v = 0; v < 8; ++v) {
+                for (int v = 0; v < NW / 4; ++v) {
                     const uint4 u = __ldg(src + v);
                     w[4 * v] = u.x; w[4 * v + 1] = u.y; w[4 * v + 2] = u.z; w[4 * v + 3] = u.w;
                 }
             }
-            tc::tmem_st32(lane_base + kColQ + wg * 32, w);
+            if constexpr (D == 128) tc::tmem_st32(lane_base + kColQ + wg * 32, w);
+            else tc::tmem_st16(lane_base + kColQ + wg * 16, w);
             tc::tmem_wait_st();
             tc::tc_fence_before();
             tc::mbar_arrive(&B.q_full);
@@ -340,13 +358,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
                 tc::tc_fence_after();
                 const float f = rescale ? alpha : 1.f;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < D / 64; ++c) {        // this warpgroup's D / 2 columns of O
                     uint32_t r[32];
-                    tc::tmem_ld32(lane_base + kColO + wg * 64 + c * 32, r);
+                    tc::tmem_ld32(lane_base + kColO + wg * (D / 2) + c * 32, r);
                     tc::tmem_wait_ld(r);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
-                    tc::tmem_st32(lane_base + kColO + wg * 64 + c * 32, r);
+                    tc::tmem_st32(lane_base + kColO + wg * (D / 2) + c * 32, r);
                 }
                 if (wg == 1)                          // and the row sum l
                     tc::tmem_st1(lane_base + kColL,
@@ -365,9 +383,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
             // O is a convex combination of values whatever the rounding of P.
             const float l = __uint_as_float(tc::tmem_ld1(lane_base + kColL));
             const float inv = 1.f / l;
-            __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + ((size_t)q_local * p.Hq + h) * kTile;
+            __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + ((size_t)q_local * p.Hq + h) * D;
 #pragma unroll
-            for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
+            for (int c = (D / 64) * wg; c < (D / 64) * (wg + 1); ++c) {
                 uint32_t r[32];
                 tc::tmem_ld32(lane_base + kColO + c * 32, r);
                 tc::tmem_wait_ld(r);
@@ -398,15 +416,17 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
 }  // namespace
 
 bool tc_supported(const AttnArgs& a) {
-    return a.dtype == PKV_BF16 && a.d == 128 && a.P == 128 && a.tmap_k && a.tmap_v &&
-           (reinterpret_cast<uintptr_t>(a.q) & 15) == 0;
+    return a.dtype == PKV_BF16 && (a.d == 128 || a.d == 64) && a.P == 128 && a.tmap_k &&
+           a.tmap_v && (reinterpret_cast<uintptr_t>(a.q) & 15) == 0;
 }
 
-cudaError_t launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t s) {
+template <int D>
+static cudaError_t launch_fwd(const AttnArgs& a, cudaStream_t s) {
+    constexpr uint32_t smem = FwdLayout<D>::kSmemBytes;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -416,8 +436,12 @@ cudaError_t launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t s) {
     p.sel = a.sel; p.kmax = a.kmax; p.err = a.err;
     dim3 grid((unsigned)((a.n_q + kTile - 1) / kTile), a.Hq);
     ProfScope ps("fwd_tc_kernel", s);
-    fwd_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(*a.tmap_k, *a.tmap_v, p);
+    fwd_tc_kernel<D><<<grid, kThreads, smem, s>>>(*a.tmap_k, *a.tmap_v, p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t s) {
+    return a.d == 64 ? launch_fwd<64>(a, s) : launch_fwd<128>(a, s);
 }
 
 }  // namespace pkv

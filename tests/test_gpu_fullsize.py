@@ -541,3 +541,28 @@ def test_bench_head_layout_sparse_16k_every_output(opool):
         sw.close()
     _compare_all(w, got, opool.sparse_full(
         w, lists, lambda p: (K_all[p * w.P:(p + 1) * w.P], V_all[p * w.P:(p + 1) * w.P])))
+
+
+def test_sparse_chunk_of_320_query_pages_every_output(opool):
+    """One chunk of 40960 tokens (320 query pages, more than 256) through the
+    page-sparse tensor-core kernels: selections against the oracle, then O,
+    LSE, dQ, dK, dV of every position against the oracle over them."""
+    w = synth.workload("qwen7b_sparse_256k", N=40960, C=40960, Hq=2, Hkv=1, topk=(4, 1, 2))
+    K, ns, nl = w.topk
+    sw = ChunkSweep(w).load_inputs()
+    try:
+        sw.reset()
+        s, e = w.chunk_range(0)
+        B.pkv_append(sw.seq, sw.k[0], sw.v[0], e - s)
+        sel = torch.empty(((e - s) // w.P, w.Hkv, K + ns + nl), dtype=torch.int32, device="cuda")
+        B.pkv_page_topk(sw.seq, sw.q[0], s, e - s, K, ns, nl, sel)
+        B.pkv_chunk_attn_fwd(sw.seq, sw.q[0], s, e - s, sw.o[0], sw.lse[0], sel)
+        sw.backward(0, sel=sel)
+        B.pkv_check(sw.pool)
+        got = _gpu_sweep_outputs(sw)
+        K_all, V_all = _logical_kv(w)
+        lists = {0: _check_selection(sel.cpu().numpy(), synth.chunk_q(w, 0), 0, K_all, w, K, ns, nl)}
+    finally:
+        sw.close()
+    _compare_all(w, got, opool.sparse_full(
+        w, lists, lambda p: (K_all[p * w.P:(p + 1) * w.P], V_all[p * w.P:(p + 1) * w.P])))

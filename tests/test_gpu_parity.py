@@ -89,6 +89,15 @@ def test_dense_bf16_page128_tensor_cores(N, C, Hq, Hkv):
     _sweep_vs_oracle(w)
 
 
+@pytest.mark.parametrize("N,C,Hq,Hkv", [(768, 256, 8, 1), (700, 256, 4, 2), (1024, 512, 16, 2)])
+def test_dense_bf16_page128_head_dim_64_tensor_cores(N, C, Hq, Hkv):
+    """Head dimension 64 (the natively sparse models' geometry) on the
+    tensor-core kernels: several tiles, a ragged last chunk, 8:1 and 2:1 groups."""
+    w = synth.workload("qwen7b_dense_32k", N=N, C=C, Hq=Hq, Hkv=Hkv, d=64, table="perm",
+                       extra_pages=3, name=f"bf16_p128_d64_{N}_{C}")
+    _sweep_vs_oracle(w)
+
+
 def test_dense_bf16_page128_cuda_cores_flag():
     w = synth.workload("qwen7b_dense_32k", N=512, C=256, Hq=4, Hkv=2, name="bf16_p128_simt")
     _sweep_vs_oracle(w, flags=B.PKV_FLAG_SIMT_ONLY)

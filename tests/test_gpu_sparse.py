@@ -96,6 +96,39 @@ def test_page_topk_matches_oracle(dtype, P, d, K):
         sw.close()
 
 
+def test_page_topk_beyond_sixteen_thousand_candidates():
+    """More candidate pages than a 16,384-entry sort buffer holds: page size 8
+    and 16,456 pages, so the last chunk's query pages have ~16,450 candidates
+    each (a 4M-token context at page 128 has 32,768 pages). Selection against
+    the oracle with the tie rule; counts equal the listed entries."""
+    P, C, n_pages = 8, 64, 16456
+    w = _w(dtype="f32", P=P, d=64, N=n_pages * P, C=C, Hq=2, Hkv=1, table="identity",
+           extra_pages=0, topk=(64, 1, 2))
+    K, ns, nl = w.topk
+    ks = [synth.chunk_k(w, c) for c in range(w.n_chunks)]
+    k_all = np.concatenate(ks)
+    c = w.n_chunks - 1
+    s, e = w.chunk_range(c)
+    q = synth.chunk_q(w, c)
+    pool = B.pkv_pool_create(P, w.Hkv, w.Hq, w.d, B.PKV_F32, w.n_phys)
+    try:
+        seq = B.pkv_seq_create(pool)
+        kt = torch.from_numpy(k_all).cuda()
+        B.pkv_append(seq, kt, kt, w.N)
+        n_qp = (e - s) // P
+        sel = torch.full((n_qp, w.Hkv, K + ns + nl), 7, dtype=torch.int32, device="cuda")
+        cnt = torch.zeros((n_qp, w.Hkv), dtype=torch.int32, device="cuda")
+        B.pkv_page_topk(seq, torch.from_numpy(q).cuda(), s, e - s, K, ns, nl, sel, cnt)
+        torch.cuda.synchronize()
+        B.pkv_check(pool)
+        got = sel.cpu().numpy()
+        assert s // P - nl - ns + 1 > 16384
+        _check_selection(got, q, s, k_all, P, K, ns, nl)
+        np.testing.assert_array_equal(cnt.cpu().numpy(), (got >= 0).sum(-1))
+    finally:
+        B.pkv_pool_destroy(pool)
+
+
 def _sparse_sweep(w, use_oracle_selection: bool, flags=0):
     K, ns, nl = w.topk if w.topk else (0,) + tuple(w.local)
     qs, ks, vs, dos = _inputs(w)
@@ -231,6 +264,18 @@ def test_local_attention_tensor_cores(kw):
     base = dict(topk=None, keys="normal")
     base.update(kw)
     _sparse_sweep(_w(**base), use_oracle_selection=False)
+
+
+@pytest.mark.parametrize("local", [None, (0, 2), (1, 3)])
+def test_head_dim_64_sparse_and_local_tensor_cores(local):
+    """Head dimension 64 through the tensor-core kernels with a selection: top-K
+    from the GPU's own page selection, and local attention layers (the
+    natively sparse models' page lists)."""
+    if local is None:
+        w = _w(d=64, N=2048, C=1024, Hq=8, Hkv=2)
+    else:
+        w = _w(d=64, N=2048, C=1024, Hq=8, Hkv=2, topk=None, keys="normal", local=local)
+    _sparse_sweep(w, use_oracle_selection=False)
 
 
 def test_local_attention_cuda_cores():
