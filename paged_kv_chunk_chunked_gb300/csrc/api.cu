@@ -614,9 +614,12 @@ pkv_status pkv_chunk_attn_bwd(pkv_seq* s, const void* q, const void* o, const vo
     if (st != PKV_OK) return st;
     if (!o || !dout || !lse || !dq)
         return fail(PKV_ERR_INVALID, "pkv_chunk_attn_bwd: o, dout, lse or dq is NULL");
-    st = ensure_scratch(s->pool, (size_t)a.Hq * n_q);
+    const size_t n_d = (size_t)a.Hq * n_q;
+    const size_t n_list = sel ? 1 + (size_t)bwd_pagelist_cap(a) : 0;
+    st = ensure_scratch(s->pool, n_d + n_list);
     if (st != PKV_OK) return st;
     a.o_in = o; a.dout = dout; a.lse_in = lse; a.dq = dq; a.Dbuf = s->pool->scratch;
+    a.pagelist = sel ? reinterpret_cast<int32_t*>(s->pool->scratch + n_d) : nullptr;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_bwd_rowdot(a, cs);
     if (e == cudaSuccess)

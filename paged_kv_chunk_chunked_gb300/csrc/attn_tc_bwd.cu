@@ -69,6 +69,7 @@ struct BwdParams {
     const int32_t* sel;        // sparse: [n_qp, Hkv, kmax] selected pages, or null
     int kmax;
     int kv_splits;             // dK/dV kernel: CTAs per (page, KV head)
+    const int32_t* pagelist;   // sparse: [count, pages...] the pages some query page lists
     int* err;
 };
 
@@ -138,7 +139,13 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // blockIdx.x = page * splits + split: the CTAs that share a page run side
     // by side, so their gradient additions meet in L2 rather than in DRAM.
     const int n_split = (int)p.kv_splits;
-    const int j = (int)blockIdx.x / n_split;         // logical key page
+    // Dense: one CTA (group) per key page. Sparse: per page of the chunk's
+    // selection union, so no CTA is spent on pages no query page lists.
+    int j = (int)blockIdx.x / n_split;               // logical key page
+    if (p.pagelist) {
+        if (j >= p.pagelist[0]) return;              // the whole CTA, before any barrier
+        j = p.pagelist[1 + j];
+    }
     const int split = (int)blockIdx.x % n_split;
     const int kvh = blockIdx.y;
     const int g = p.Hq / p.Hkv;
@@ -796,6 +803,50 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant
     }
 }
 
+// The ascending union of the pages listed in a selection [n_ent entries],
+// out = [count, pages...]. One CTA: flags in shared memory, then an ordered
+// compaction (thread t owns a contiguous run of pages).
+constexpr int kUnionThreads = 1024;
+__global__ void __launch_bounds__(kUnionThreads) sel_union_kernel(const int32_t* sel, int64_t n_ent,
+                                                                  int n_pages, int32_t* out) {
+    extern __shared__ uint8_t flag[];
+    __shared__ int wsum[kUnionThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < n_pages; i += kUnionThreads) flag[i] = 0;
+    __syncthreads();
+    for (int64_t e = tid; e < n_ent; e += kUnionThreads) {
+        const int32_t pg = sel[e];
+        if (pg >= 0 && pg < n_pages) flag[pg] = 1;
+    }
+    __syncthreads();
+    const int per = (n_pages + kUnionThreads - 1) / kUnionThreads;
+    const int p0 = min(n_pages, tid * per), p1 = min(n_pages, p0 + per);
+    int cnt = 0;
+    for (int i = p0; i < p1; ++i) cnt += flag[i];
+    int x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int t = wsum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        wsum[lane] = t;
+    }
+    __syncthreads();
+    int pos = (warp > 0 ? wsum[warp - 1] : 0) + x - cnt;
+    for (int i = p0; i < p1; ++i)
+        if (flag[i]) out[1 + pos++] = i;
+    if (tid == 0) out[0] = wsum[kUnionThreads / 32 - 1];
+}
+
 template <int D>
 static cudaError_t launch_bwd(const AttnArgs& a, cudaStream_t s) {
     CUtensorMap tq64, tdo64, tdo128;
@@ -821,6 +872,27 @@ static cudaError_t launch_bwd(const AttnArgs& a, cudaStream_t s) {
     p.bt = a.bt; p.num_phys = a.num_phys; p.err = a.err;
     p.sel = a.sel; p.kmax = a.kmax;
     const int64_t n_keys = a.q_start + a.n_q;
+    const int64_t n_key_pages = (n_keys + 127) / 128;
+    // Key pages the dK/dV grid covers: every page (dense), or at most the
+    // selection union's upper bound (its CTAs beyond the union's size exit).
+    int64_t grid_pages = n_key_pages;
+    if (a.sel) {
+        grid_pages = bwd_pagelist_cap(a);
+        const size_t fl = (size_t)n_key_pages;
+        static size_t attr_u = 0;
+        if (fl > 48 * 1024 && fl > attr_u) {
+            cudaError_t e = cudaFuncSetAttribute(sel_union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)fl);
+            if (e != cudaSuccess) return e;
+            attr_u = fl;
+        }
+        ProfScope ps("sel_union_kernel", s);
+        sel_union_kernel<<<1, kUnionThreads, fl, s>>>(a.sel, (int64_t)((a.n_q + 127) / 128) * a.Hkv * a.kmax,
+                                                      (int)n_key_pages, a.pagelist);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        p.pagelist = a.pagelist;
+    }
     // Small grids (early chunks) leave SMs idle behind a few long CTAs: split
     // each (page, KV head)'s iterations over up to 4 CTAs so that there are
     // >= ~8 waves. Every split adds the page's dK/dV rows into the pool once
@@ -830,10 +902,10 @@ static cudaError_t launch_bwd(const AttnArgs& a, cudaStream_t s) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
     sm_count = std::max(sm_count, 1);
-    const int64_t n_cta = ((n_keys + 127) / 128) * a.Hkv;
+    const int64_t n_cta = grid_pages * a.Hkv;
     const int splits = (int)std::min<int64_t>(4, std::max<int64_t>(1, (8 * (int64_t)sm_count + n_cta - 1) / n_cta));
     p.kv_splits = splits;
-    dim3 g_kv((unsigned)(((n_keys + 127) / 128) * splits), a.Hkv);
+    dim3 g_kv((unsigned)(grid_pages * splits), a.Hkv);
     {
         ProfScope ps("bwd_kv_tc_kernel", s);
         bwd_kv_tc_kernel<D><<<g_kv, kThreads, KVLayout<D>::kSMEM, s>>>(tq64, tdo64, *a.tmap_v, p);
@@ -848,10 +920,18 @@ static cudaError_t launch_bwd(const AttnArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+int64_t bwd_pagelist_cap(const AttnArgs& a) {
+    if (!a.sel) return 0;
+    const int64_t n_key_pages = (a.q_start + a.n_q + a.P - 1) / a.P;
+    const int64_t n_qp = (a.n_q + a.P - 1) / a.P;
+    return std::min<int64_t>(n_key_pages, n_qp * a.Hkv * (int64_t)a.kmax);
+}
+
 cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
     // The sparse dK/dV kernel lists the selecting query pages in shared memory.
     if (a.sel && (a.n_q + 127) / 128 > kMaxSelQp) return launch_attn_bwd_simt(a, s);
-    if ((reinterpret_cast<uintptr_t>(a.dout) & 15) || !a.tmap_k) return cudaErrorInvalidValue;
+    if ((reinterpret_cast<uintptr_t>(a.dout) & 15) || !a.tmap_k || (a.sel && !a.pagelist))
+        return cudaErrorInvalidValue;
     return a.d == 64 ? launch_bwd<64>(a, s) : launch_bwd<128>(a, s);
 }
 

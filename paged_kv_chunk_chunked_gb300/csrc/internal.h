@@ -138,6 +138,7 @@ struct AttnArgs {
     float* lse;                      // fwd out
     void* dq;                        // bwd out
     float* Dbuf;                     // bwd scratch [Hq, n_q]
+    int32_t* pagelist;               // bwd scratch with a selection: [1 + bwd_pagelist_cap(a)]
     const void* kpool;
     const void* vpool;
     float* dkpool;
@@ -197,6 +198,9 @@ cudaError_t launch_stage_invalidate_kv(const pkv_seq* s, int64_t lp, cudaStream_
 
 bool tc_supported(const AttnArgs& a);
 cudaError_t launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t s);
+// Entries of the backward's page-list scratch for a call with a selection:
+// at most every key page, at most every listed entry (0 without a selection).
+int64_t bwd_pagelist_cap(const AttnArgs& a);
 cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s);
 
 // TMA descriptor helpers (driver entry point fetched through the runtime).

@@ -11,7 +11,9 @@
 //
 // Limits and sharing:
 //   - the array holds kNoAllocMaxFloats floats (1 MiB); a call needs
-//     n_q_heads * n_q of them and is rejected (PKV_ERR_INVALID) above that;
+//     n_q_heads * n_q of them, plus, with a page selection, a page list of at
+//     most 1 + min(key pages, n_qp * n_kv_heads * kmax) entries, and is
+//     rejected (PKV_ERR_INVALID) above that;
 //   - every device that loads the library holds the array until exit;
 //   - all calls share the one array: calls that overlap on the GPU (other
 //     streams, other threads) race on it and must be serialised by the caller;
@@ -73,16 +75,19 @@ extern "C" pkv_status pkv_chunk_attn_bwd_noalloc(pkv_seq* s, const void* q, cons
     if (st != PKV_OK) return st;
     if (!o || !dout || !lse || !dq)
         return fail(PKV_ERR_INVALID, std::string(who) + ": o, dout, lse or dq is NULL");
-    const size_t need = (size_t)a.Hq * (size_t)n_q;
+    const size_t n_d = (size_t)a.Hq * (size_t)n_q;
+    const size_t need = n_d + (sel ? 1 + (size_t)bwd_pagelist_cap(a) : 0);
     if (need > kNoAllocMaxFloats)
         return fail(PKV_ERR_INVALID,
-                    std::string(who) + ": n_q_heads * n_q = " + std::to_string(need) +
-                        " exceeds the fixed scratch of " + std::to_string(kNoAllocMaxFloats) +
+                    std::string(who) + ": n_q_heads * n_q" + (sel ? " + the page list" : "") +
+                        " = " + std::to_string(need) + " exceeds the fixed scratch of " +
+                        std::to_string(kNoAllocMaxFloats) +
                         " floats; use pkv_chunk_attn_bwd or a smaller chunk");
     float* scratch = nullptr;
     st = scratch_for_current_device(&scratch);
     if (st != PKV_OK) return st;
     a.o_in = o; a.dout = dout; a.lse_in = lse; a.dq = dq; a.Dbuf = scratch;
+    a.pagelist = sel ? reinterpret_cast<int32_t*>(scratch + n_d) : nullptr;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_bwd_rowdot(a, cs);
     if (e == cudaSuccess)

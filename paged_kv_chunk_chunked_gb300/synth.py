@@ -103,6 +103,11 @@ WORKLOADS = {
     # own page and the one before it, no sink; 256K context, Qwen2.5-7B shape.
     "qwen7b_local_256k": Workload("qwen7b_local_256k", N=262144, C=8192, P=128, Hq=28, Hkv=4,
                                   d=128, dtype="bf16", seed=1240, table="perm", local=(0, 2)),
+    # The same local layer with head dimension 64 and 64 query / 8 KV heads:
+    # the attention geometry of the published GPT-OSS models, the natively
+    # sparse family the pages name (the pages give no shapes for it).
+    "gptoss_local_256k": Workload("gptoss_local_256k", N=262144, C=8192, P=128, Hq=64, Hkv=8,
+                                  d=64, dtype="bf16", seed=1241, table="perm", local=(0, 2)),
 }
 
 
