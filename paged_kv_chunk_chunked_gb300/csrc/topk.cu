@@ -18,12 +18,12 @@
 //      rows over the group's g heads, 16-byte loads, all of a thread's loads
 //      in flight at once. Together the A units read the chunk's queries
 //      once: this is the HBM stream of the chain.
-//   B  scores of a tile of 64 candidate pages against every query page of the
+//   B  scores of a tile of 32 candidate pages against every query page of the
 //      chunk (the representatives transposed in shared memory), fp32 FMAs;
 //      each representative leaves L2 once per chunk.
 //   C  the selection of one (query page, KV head): a radix select of the K-th
-//      best score over order-preserving 32-bit keys (four 8-bit digit passes
-//      over the score row, staged in shared memory when it fits), then an
+//      best score over order-preserving 32-bit keys (digits of 11, 11 and 10
+//      bits over the score row, staged in shared memory when it fits), then an
 //      ordered compaction (ties at the threshold go to the lower pages).
 // A B unit of head h waits until every A unit of h is done, a C unit until
 // every B unit of h is; the queue holds every A unit, then every B unit, then
@@ -44,9 +44,9 @@ namespace pkv {
 namespace {
 
 constexpr int kTkThreads = 256;
-constexpr int kTile = 64;                 // candidate pages per scoring unit
+constexpr int kTile = 32;                 // candidate pages per scoring unit
 constexpr int kQpBlk = 64;                // query pages per scoring pass
-constexpr int kMaxSeg = 48;
+constexpr int kMaxSeg = 3;
 constexpr int64_t kMaxCand = int64_t(1) << 24;
 constexpr uint64_t kTkWaitNs = 4000000000ull;
 
@@ -148,7 +148,7 @@ __device__ int block_excl_scan(int v, int* warp_sums, int* total) {
     return base + x - v;
 }
 
-static_assert(kTkThreads == 256, "one histogram bin per thread");
+static_assert(kTkThreads == 256, "8 of the 2048 histogram bins per thread");
 
 struct __align__(16) TopkSmem {
     int unit;
@@ -156,7 +156,6 @@ struct __align__(16) TopkSmem {
     uint32_t prefix;
     int krem;
     int warp_sums[kTkThreads / 32];
-    int hist[256];
 };
 
 // ------------------------------------------------------------------ unit A
@@ -207,37 +206,43 @@ __device__ void unit_page_query(const TopkArgs& a, int kv, int qp, float* red) {
 // ------------------------------------------------------------------ unit B
 // scores[kv][qp][c] = qbar[qp, kv, :] . rep[bt[n_sink + c], kv, :] for the
 // tile's candidates c. The representatives sit transposed ([k][c]) so thread
-// t, which scores candidate t % 64 against query pages t / 64, t / 64 + 4, ...,
+// t, which scores candidate t % 32 against query pages t / 32, t / 32 + 8, ...,
 // reads them without bank conflicts; a warp shares its query pages, whose rows
 // are read as broadcasts.
+// The tile's representatives, transposed into shared memory ([k][c]).
+template <int D>
+__device__ void load_rep_tile(const TopkArgs& a, int kv, int tile, float* smem) {
+    float* rt = smem;                                   // [D][kTile]
+    const int tid = threadIdx.x, c0 = tile * kTile;
+    constexpr int NL = kTile * (D / 4) / kTkThreads;    // all of a thread's loads issued first
+    float4 v[NL];
+#pragma unroll
+    for (int l = 0; l < NL; ++l) {
+        const int i = tid + l * kTkThreads, c = i % kTile, k4 = i / kTile;
+        v[l] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c0 + c < a.n_cand_max) {
+            const int32_t pp = a.bt[a.n_sink + c0 + c];
+            if (pp >= 0 && pp < a.num_phys)
+                v[l] = __ldg(reinterpret_cast<const float4*>(a.rep + ((size_t)pp * a.Hkv + kv) * D) + k4);
+            else if (k4 == 0)
+                report_error(a.err, kErrBadPage);
+        }
+    }
+#pragma unroll
+    for (int l = 0; l < NL; ++l) {
+        const int i = tid + l * kTkThreads, c = i % kTile, k4 = i / kTile;
+        rt[(4 * k4) * kTile + c] = v[l].x; rt[(4 * k4 + 1) * kTile + c] = v[l].y;
+        rt[(4 * k4 + 2) * kTile + c] = v[l].z; rt[(4 * k4 + 3) * kTile + c] = v[l].w;
+    }
+}
+
+// scores against every query page; the representatives are already in
+// shared memory (load_rep_tile; the first barrier below publishes them).
 template <int D>
 __device__ void unit_scores(const TopkArgs& a, int kv, int tile, float* smem) {
     float* rt = smem;                                   // [D][kTile]
     float* qs = smem + D * kTile;                       // [kQpBlk][D]
     const int tid = threadIdx.x, c0 = tile * kTile;
-    {
-        // the tile's representatives: all of a thread's loads issued first
-        constexpr int NL = kTile * (D / 4) / kTkThreads;
-        float4 v[NL];
-#pragma unroll
-        for (int l = 0; l < NL; ++l) {
-            const int i = tid + l * kTkThreads, c = i % kTile, k4 = i / kTile;
-            v[l] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (c0 + c < a.n_cand_max) {
-                const int32_t pp = a.bt[a.n_sink + c0 + c];
-                if (pp >= 0 && pp < a.num_phys)
-                    v[l] = __ldg(reinterpret_cast<const float4*>(a.rep + ((size_t)pp * a.Hkv + kv) * D) + k4);
-                else if (k4 == 0)
-                    report_error(a.err, kErrBadPage);
-            }
-        }
-#pragma unroll
-        for (int l = 0; l < NL; ++l) {
-            const int i = tid + l * kTkThreads, c = i % kTile, k4 = i / kTile;
-            rt[(4 * k4) * kTile + c] = v[l].x; rt[(4 * k4 + 1) * kTile + c] = v[l].y;
-            rt[(4 * k4 + 2) * kTile + c] = v[l].z; rt[(4 * k4 + 3) * kTile + c] = v[l].w;
-        }
-    }
     constexpr int G = kTkThreads / kTile;               // query-page groups
     constexpr int QPT = kQpBlk / G;                      // query pages per thread and pass
     const int c = tid % kTile, g0 = tid / kTile;
@@ -288,19 +293,23 @@ __device__ void unit_scores(const TopkArgs& a, int kv, int tile, float* smem) {
 }
 
 // ------------------------------------------------------------------ unit C
+// Padded position of score i in the staged row: one float of padding per 32,
+// so the compaction's per-thread runs (stride = run length) hit distinct banks.
+__device__ __forceinline__ int padded(int i) { return i + (i >> 5); }
+
 // Keys of the score row: from shared memory when the row was staged there
-// (rowbuf != null), else from L2.
+// (sm != null, padded layout), else from L2.
 struct RowKeys {
     const float* g;
     const float* sm;
     __device__ __forceinline__ uint32_t operator[](int i) const {
-        return orderable(sm ? sm[i] : __ldcg(g + i));
+        return orderable(sm ? sm[padded(i)] : __ldcg(g + i));
     }
 };
 
-__device__ void unit_select(const TopkArgs& a, int kv, int qp, TopkSmem& S, float* rowbuf,
-                            int rowbuf_cap) {
-    const int tid = threadIdx.x, lane = tid & 31;
+__device__ void unit_select(const TopkArgs& a, int kv, int qp, TopkSmem& S, int* hist2048,
+                            float* rowbuf, int rowbuf_cap) {
+    const int tid = threadIdx.x;
     const int64_t qpg = a.qp0 + qp;
     const int64_t c_lo = a.n_sink;
     const int n = (int)max64(0, qpg - a.n_local - c_lo + 1);      // candidates of this row
@@ -308,8 +317,8 @@ __device__ void unit_select(const TopkArgs& a, int kv, int qp, TopkSmem& S, floa
     const float* row = a.scores + ((size_t)kv * a.n_qp + qp) * a.stride;
     const bool all = n_top == n;
     RowKeys keys{row, nullptr};
-    if (!all && n_top > 0 && n <= rowbuf_cap) {
-        // Stage the row (16-byte aligned: the stride is a multiple of 4 floats).
+    if (!all && n_top > 0 && padded(n) <= rowbuf_cap) {
+        // Stage the row (16-byte aligned loads: the stride is a multiple of 4 floats).
         const int n4 = (n + 3) / 4;
         for (int i = tid; i < n4; i += 4 * kTkThreads) {
             float4 v[4];
@@ -317,8 +326,13 @@ __device__ void unit_select(const TopkArgs& a, int kv, int qp, TopkSmem& S, floa
             for (int l = 0; l < 4; ++l)
                 if (i + l * kTkThreads < n4) v[l] = __ldcg(reinterpret_cast<const float4*>(row) + i + l * kTkThreads);
 #pragma unroll
-            for (int l = 0; l < 4; ++l)
-                if (i + l * kTkThreads < n4) reinterpret_cast<float4*>(rowbuf)[i + l * kTkThreads] = v[l];
+            for (int l = 0; l < 4; ++l) {
+                const int b = 4 * (i + l * kTkThreads);
+                if (b < 4 * n4) {
+                    rowbuf[padded(b)] = v[l].x; rowbuf[padded(b + 1)] = v[l].y;
+                    rowbuf[padded(b + 2)] = v[l].z; rowbuf[padded(b + 3)] = v[l].w;
+                }
+            }
         }
         __syncthreads();
         keys.sm = rowbuf;
@@ -326,50 +340,44 @@ __device__ void unit_select(const TopkArgs& a, int kv, int qp, TopkSmem& S, floa
     uint32_t thr = 0;                                             // the n_top-th best key
     int take_eq = 0;                                              // keys == thr to keep
     if (!all && n_top > 0) {
+        // Radix select over digits of 11, 11 and 10 bits from the top: the first
+        // digit reaches into the mantissa, so even scores of one sign and
+        // magnitude spread over many of its 2048 bins.
         uint32_t prefix = 0, mask = 0;
         int krem = n_top;
-        for (int shift = 24; shift >= 0; shift -= 8) {
-            S.hist[tid] = 0;                                      // kTkThreads == 256 bins
+        int* hist = hist2048;
+        for (int pass = 0; pass < 3; ++pass) {
+            const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+            const int width = pass == 2 ? 10 : 11;
+            const uint32_t dmask = (1u << width) - 1u;
+            for (int b = tid; b < 2048; b += kTkThreads) hist[b] = 0;
             __syncthreads();
-            for (int i0 = 0; i0 < n; i0 += kTkThreads) {
-                const int i = i0 + tid;
-                const uint32_t key = i < n ? keys[i] : 0u;
-                const bool in = i < n && (key & mask) == prefix;
-                const uint32_t bin = in ? (key >> shift) & 255u : 256u + lane;   // unique if out
-                // one shared-memory atomic per distinct bin of the warp
-                const unsigned same = __match_any_sync(0xffffffffu, bin);
-                if (in && (__ffs(same) - 1) == lane) atomicAdd(&S.hist[bin], __popc(same));
+            for (int i = tid; i < n; i += kTkThreads) {
+                const uint32_t key = keys[i];
+                if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1);
             }
             __syncthreads();
-            if (tid < 32) {
-                // Lane l holds bins 255-8l .. 248-8l (best first); find the bin
-                // that holds the krem-th best key.
-                int c[8], sum = 0;
+            // Thread t holds bins 2047-8t .. 2040-8t (best first); the block scan
+            // finds the thread whose bins hold the krem-th best key.
+            int c[8], sum = 0;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) { c[j] = S.hist[255 - 8 * tid - j]; sum += c[j]; }
-                int incl = sum;
+            for (int j = 0; j < 8; ++j) { c[j] = hist[2047 - 8 * tid - j]; sum += c[j]; }
+            int total;
+            const int excl = block_excl_scan(sum, S.warp_sums, &total);
+            if (excl < krem && excl + sum >= krem) {
+                int above = excl, b = 0;
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (tid >= o) incl += y;
+                for (int j = 0; j < 8; ++j) {
+                    if (above + c[j] >= krem) { b = 2047 - 8 * tid - j; break; }
+                    above += c[j];
                 }
-                const int excl = incl - sum;
-                const unsigned hit = __ballot_sync(0xffffffffu, excl < krem && incl >= krem);
-                if (tid == __ffs(hit) - 1) {
-                    int above = excl, b = 0;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (above + c[j] >= krem) { b = 255 - 8 * tid - j; break; }
-                        above += c[j];
-                    }
-                    S.krem = krem - above;
-                    S.prefix = prefix | ((uint32_t)b << shift);
-                }
+                S.krem = krem - above;
+                S.prefix = prefix | ((uint32_t)b << shift);
             }
             __syncthreads();
             krem = S.krem;
             prefix = S.prefix;
-            mask |= 255u << shift;
+            mask |= dmask << shift;
         }
         thr = prefix;
         take_eq = krem;
@@ -419,6 +427,7 @@ __global__ void __launch_bounds__(kTkThreads) topk_fused_kernel(const __grid_con
                                                                 int rowbuf_cap) {
     extern __shared__ __align__(16) float dyn[];
     __shared__ TopkSmem S;
+    __shared__ int s_hist[2048];
     int* const q_ctr = a.state;
     int* const cta_done = a.state + 1;
     int* const doneA = a.state + 2;
@@ -444,11 +453,12 @@ __global__ void __launch_bounds__(kTkThreads) topk_fused_kernel(const __grid_con
         if (kind == kUnitA) {
             unit_page_query<T, D>(a, kv, loc, dyn);
         } else if (kind == kUnitB) {
+            load_rep_tile<D>(a, kv, loc, dyn);              // needs no A unit
             if (!block_wait_count(doneA + kv, a.n_qp, a.err, &S.ok)) break;
             unit_scores<D>(a, kv, loc, dyn);
         } else {
             if (!block_wait_count(doneB + kv, a.n_tiles, a.err, &S.ok)) break;
-            unit_select(a, kv, loc, S, dyn, rowbuf_cap);
+            unit_select(a, kv, loc, S, s_hist, dyn, rowbuf_cap);
         }
         __syncthreads();                                   // the unit's writes are issued
         if (threadIdx.x == 0 && kind != kUnitC) {
@@ -553,9 +563,10 @@ cudaError_t launch_page_topk(const pkv_pool* p, const int32_t* d_bt, const void*
     a.qbar = scratch;
     a.scores = scratch + (size_t)n_qp * Hkv * D;
     a.out = out; a.counts = counts; a.state = state; a.err = p->d_err;
-    // Queue order: every A unit, then every B unit, then every C unit. (The A
-    // units of all heads share the HBM stream and finish together, so
-    // interleaving the kinds would only park CTAs on waits early.)
+    // Queue order: every A unit, then every B unit, then every C unit. The A
+    // units of all heads share the HBM stream and finish together; an order
+    // interleaving the kinds over the heads was measured slower (the A units
+    // spread out over twice the time).
     int ns = 0;
     auto add = [&](int kind, int kv0, int nkv) {
         if (kind == kUnitB && a.n_tiles == 0) return;

@@ -220,7 +220,10 @@ def test_sparse_with_all_pages_equals_dense_on_gpu():
             sw.backward(c, sel=sels[c])
         for a, b in zip(dense[0], [to_numpy(x) for x in sw.o]):
             np.testing.assert_array_equal(a, b)
-        assert _rel(to_numpy(sw.gather()["dk"]), dense[1]) < 1e-6
+        # The dense call may split a page's dK/dV over CTAs whose partial sums
+        # meet by fp32 addition; the sparse call does not: the sums agree up to
+        # the order of fp32 rounding.
+        assert _rel(to_numpy(sw.gather()["dk"]), dense[1]) < 1e-5
     finally:
         sw.close()
 
