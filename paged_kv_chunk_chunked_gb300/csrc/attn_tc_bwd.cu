@@ -136,18 +136,24 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     float* stat = reinterpret_cast<float*>(smem + kv_STAT);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // blockIdx.x = page * splits + split: the CTAs that share a page run side
-    // by side, so their gradient additions meet in L2 rather than in DRAM.
+    // Dense: grid (key page * splits + split, KV head); the CTAs that share a
+    // page run side by side, so their gradient additions meet in L2 rather
+    // than in DRAM. Sparse: grid (KV head, position in the chunk's selection
+    // union) -- the union's CTAs are dispatched first, those past its end exit
+    // at once.
     const int n_split = (int)p.kv_splits;
-    // Dense: one CTA (group) per key page. Sparse: per page of the chunk's
-    // selection union, so no CTA is spent on pages no query page lists.
-    int j = (int)blockIdx.x / n_split;               // logical key page
+    int j, split, kvh;
     if (p.pagelist) {
-        if (j >= p.pagelist[0]) return;              // the whole CTA, before any barrier
-        j = p.pagelist[1 + j];
+        const int idx = (int)blockIdx.y;
+        if (idx >= p.pagelist[0]) return;            // the whole CTA, before any barrier
+        j = p.pagelist[1 + idx];
+        split = 0;
+        kvh = (int)blockIdx.x;
+    } else {
+        j = (int)blockIdx.x / n_split;               // logical key page
+        split = (int)blockIdx.x % n_split;
+        kvh = (int)blockIdx.y;
     }
-    const int split = (int)blockIdx.x % n_split;
-    const int kvh = blockIdx.y;
     const int g = p.Hq / p.Hkv;
     const int64_t kfirst = (int64_t)j * 128;
     const int n_qt = (int)((p.n_q + 63) / 64);
@@ -876,7 +882,10 @@ static cudaError_t launch_bwd(const AttnArgs& a, cudaStream_t s) {
     // Key pages the dK/dV grid covers: every page (dense), or at most the
     // selection union's upper bound (its CTAs beyond the union's size exit).
     int64_t grid_pages = n_key_pages;
-    if (a.sel) {
+    // (The union's grid dimension is limited to 65535 pages; beyond that every
+    // key page gets a CTA, as for dense calls.)
+    const bool use_list = a.sel && bwd_pagelist_cap(a) <= 65535;
+    if (use_list) {
         grid_pages = bwd_pagelist_cap(a);
         const size_t fl = (size_t)n_key_pages;
         static size_t attr_u = 0;
@@ -902,10 +911,15 @@ static cudaError_t launch_bwd(const AttnArgs& a, cudaStream_t s) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
     sm_count = std::max(sm_count, 1);
+    // With a selection a page is seen by few query tiles (28 iterations per
+    // page for a local layer with two pages per list): splitting would only
+    // multiply the CTAs' start-up and gradient additions, so only dense calls split.
     const int64_t n_cta = grid_pages * a.Hkv;
-    const int splits = (int)std::min<int64_t>(4, std::max<int64_t>(1, (8 * (int64_t)sm_count + n_cta - 1) / n_cta));
+    const int splits = a.sel ? 1
+        : (int)std::min<int64_t>(4, std::max<int64_t>(1, (8 * (int64_t)sm_count + n_cta - 1) / n_cta));
     p.kv_splits = splits;
-    dim3 g_kv((unsigned)(grid_pages * splits), a.Hkv);
+    const dim3 g_kv = use_list ? dim3(a.Hkv, (unsigned)grid_pages)
+                               : dim3((unsigned)(grid_pages * splits), a.Hkv);
     {
         ProfScope ps("bwd_kv_tc_kernel", s);
         bwd_kv_tc_kernel<D><<<g_kv, kThreads, KVLayout<D>::kSMEM, s>>>(tq64, tdo64, *a.tmap_v, p);

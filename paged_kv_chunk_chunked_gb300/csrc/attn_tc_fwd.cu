@@ -7,9 +7,11 @@
 // on the paged KV cache, gist.science/de §2.B, sciencestack.ai Fig. 3; page
 // selection, gist.science/de §2.D).
 //
-// One CTA per (query tile of 128 rows = one query page, query head); key
-// tiles are whole pages (P = 128), fetched by TMA with the physical page
-// taken from the block table. Head dimension D = 128 or 64 (a template
+// One CTA per (query tile of 128 rows = one query page, query head) -- or,
+// for short page lists (local layers), per (query tile, KV group), looping
+// over the group's query heads with its tensor memory, barriers and page
+// list kept; key tiles are whole pages (P = 128), fetched by TMA with the
+// physical page taken from the block table. Head dimension D = 128 or 64 (a template
 // parameter; a page of one head is D / 64 blocks of 64 columns). Both MMAs take their A operand from tensor
 // memory (an A operand in shared memory costs the tensor core a fixed ~33
 // cycles per instruction on top of the math): Q is placed there once, and
@@ -48,6 +50,7 @@ constexpr int kSoftmaxThreads = 256;
 constexpr uint32_t kHalfBytes = 128 * 128;   // [128 rows][64 bf16] = 16 KB
 constexpr int kKStages = 3, kVStages = 2;
 constexpr float kRescaleThreshold = 8.0f;                         // log2 units
+constexpr int kShortList = 8;            // page lists up to this long: a CTA per (tile, KV group)
 
 // Shared-memory tile offsets (bytes from a 1024-aligned base) and tensor-
 // memory columns for head dimension D.
@@ -67,6 +70,7 @@ template <int D> struct FwdLayout {
 
 struct FwdParams {
     int Hq, Hkv;
+    int heads_per_cta;               // consecutive query heads of one KV group per CTA
     int64_t q_start, n_q;
     const void* q;
     void* o;
@@ -80,6 +84,8 @@ struct FwdParams {
 
 struct __align__(8) FwdBarriers {
     uint64_t q_full;                 // Q in TMEM (256 softmax arrivals)
+    uint64_t q_empty;                // a head's S MMAs done: its Q may be replaced
+    uint64_t o_free;                 // a head's O read by the epilogue (256 arrivals)
     uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
     uint64_t s_full[2];
     uint64_t p_full;
@@ -110,28 +116,36 @@ __device__ __forceinline__ void produce_ring(const FwdParams& p, uint8_t* smem, 
     uint64_t* empty = is_k ? B.k_empty : B.v_empty;
     uint8_t* base = smem + (is_k ? L::kOffK : L::kOffV);
     if (lane == 0) tc::prefetch_tmap(&tmap);
+    // The same pages for every head of the CTA: iteration it = head * nt + tile.
     tc::PageBatch pages;
-    pages.init(p.bt, p.sel ? p.sel + ((size_t)qt * p.Hkv + kvh) * p.kmax : nullptr, nt, lane);
     int issued = 0;
-    for (int j = 0; j < nt; ++j) {
-        const int st = j % nst;
-        if (j >= nst &&
-            !__all_sync(0xffffffffu, tc::mbar_wait(&empty[st], ((j / nst) - 1) & 1, p.err)))
-            break;
-        const int32_t pp = pages.get(j);
-        if (pp < 0 || pp >= p.num_phys) {
-            if (lane == 0) report_error(p.err, kErrBadPage);
-            break;
-        }
-        if (lane == 0) {
-            const int row = (int)(((int64_t)pp * p.Hkv + kvh) * kTile);
-            uint8_t* dst = base + st * (is_k ? L::kTileBytes : L::kVStageBytes);
-            tc::mbar_arrive_expect_tx(&full[st], L::kTileBytes);
+    bool ok = true;
+    for (int hi = 0; ok && hi < p.heads_per_cta; ++hi) {
+        pages.init(p.bt, p.sel ? p.sel + ((size_t)qt * p.Hkv + kvh) * p.kmax : nullptr, nt, lane);
+        for (int j = 0; j < nt; ++j) {
+            const int it = hi * nt + j;
+            const int st = it % nst;
+            if (it >= nst &&
+                !__all_sync(0xffffffffu, tc::mbar_wait(&empty[st], ((it / nst) - 1) & 1, p.err))) {
+                ok = false;
+                break;
+            }
+            const int32_t pp = pages.get(j);
+            if (pp < 0 || pp >= p.num_phys) {
+                if (lane == 0) report_error(p.err, kErrBadPage);
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                const int row = (int)(((int64_t)pp * p.Hkv + kvh) * kTile);
+                uint8_t* dst = base + st * (is_k ? L::kTileBytes : L::kVStageBytes);
+                tc::mbar_arrive_expect_tx(&full[st], L::kTileBytes);
 #pragma unroll
-            for (int b = 0; b < L::kBlocks; ++b)
-                tc::tma_load_2d(dst + b * kHalfBytes, &tmap, &full[st], 64 * b, row);
+                for (int b = 0; b < L::kBlocks; ++b)
+                    tc::tma_load_2d(dst + b * kHalfBytes, &tmap, &full[st], 64 * b, row);
+            }
+            issued = it + 1;
         }
-        issued = j + 1;
     }
     // Make sure none of this CTA's copies is still landing when it exits.
     if (lane == 0)
@@ -153,8 +167,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;        // longest tiles first
-    const int h = blockIdx.y;
-    const int kvh = h / (p.Hq / p.Hkv);
+    const int h0 = (int)blockIdx.y * p.heads_per_cta;           // this CTA's first query head
+    const int kvh = h0 / (p.Hq / p.Hkv);
+    const int nh = p.heads_per_cta;
 
     // The ones block of each V stage: row r holds 1 in column 0, zeros elsewhere
     // (128-byte swizzle: column 0 sits in 16-byte chunk r & 7 of the row).
@@ -167,6 +182,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
     tc::fence_proxy_async_smem();
     if (threadIdx.x == 0) {
         tc::mbar_init(&B.q_full, kSoftmaxThreads);
+        tc::mbar_init(&B.q_empty, 1);
+        tc::mbar_init(&B.o_free, kSoftmaxThreads);
         for (int s = 0; s < kKStages; ++s) {
             tc::mbar_init(&B.k_full[s], 1);
             tc::mbar_init(&B.k_empty[s], 1);
@@ -212,13 +229,18 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
         const uint32_t tmem_o = tmem + kColO, tmem_q = tmem + kColQ;
         const uint64_t dk0 = tc::sdesc(tc::smem_u32(smem + kOffK), 16, 1024);            // K-major
         const uint64_t dv0 = tc::sdesc(tc::smem_u32(smem + kOffV), kHalfBytes, 1024);    // MN-major
-        bool ok = tc::warp_wait(&B.q_full, 0, p.err);
+        bool ok = true;
         // P_i sits over S_i in TMEM; S_{i+2} reuses those columns but is issued
-        // after PV_i, and the tensor core runs MMAs in issue order.
+        // after PV_i, and the tensor core runs MMAs in issue order. Iteration
+        // i = head * nt + tile; a head's first PV overwrites O (accumulate off)
+        // once the epilogue has read the previous head's O (o_free).
         auto issue_pv = [&](int i) -> bool {
             const int vs = i % kVStages;
+            const int hi = i / nt;
+            const bool first = (i % nt) == 0;
             if (!tc::warp_wait(&B.p_full, i & 1, p.err)) return false;
             if (!tc::warp_wait(&B.v_full[vs], (i / kVStages) & 1, p.err)) return false;
+            if (first && hi > 0 && !tc::warp_wait(&B.o_free, (hi - 1) & 1, p.err)) return false;
             tc::tc_fence_after();
             // B = [V 1] [128 keys][D + 16] MN-major: 16 keys = 2 K-groups of 8
             // rows (1024 B apart); columns span 64-column blocks 16 KB apart
@@ -228,32 +250,39 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     tc::mma_bf16_ts(tmem_o, tmem_p + p_col(kk), tc::sdesc_at(dv0, vs * kVStageBytes + kk * 2048),
-                                    idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+                                    idesc_pv, (!first || kk > 0) ? 1u : 0u);
                 tc::mma_commit(&B.o_done);
                 tc::mma_commit(&B.v_empty[vs]);
             }
             __syncwarp();
             return true;
         };
-        for (int j = 0; ok && j < nt; ++j) {
-            const int ks = j % kKStages;
-            if (!tc::warp_wait(&B.k_full[ks], (j / kKStages) & 1, p.err)) { ok = false; break; }
-            tc::tc_fence_after();
-            const uint32_t tmem_s = tmem + (j & 1) * 128;
-            if (leader) {
+        for (int hi = 0; ok && hi < nh; ++hi) {
+            if (!tc::warp_wait(&B.q_full, hi & 1, p.err)) { ok = false; break; }
+            for (int j = 0; ok && j < nt; ++j) {
+                const int it = hi * nt + j;
+                const int ks = it % kKStages;
+                if (!tc::warp_wait(&B.k_full[ks], (it / kKStages) & 1, p.err)) { ok = false; break; }
+                tc::tc_fence_after();
+                const uint32_t tmem_s = tmem + (it & 1) * 128;
+                if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {   // K = d: 16 per MMA, 8 TMEM columns of Q
-                    const uint32_t koff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                    tc::mma_bf16_ts(tmem_s, tmem_q + kk * 8, tc::sdesc_at(dk0, ks * kTileBytes + koff),
-                                    idesc, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {   // K = d: 16 per MMA, 8 TMEM columns of Q
+                        const uint32_t koff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                        tc::mma_bf16_ts(tmem_s, tmem_q + kk * 8, tc::sdesc_at(dk0, ks * kTileBytes + koff),
+                                        idesc, kk > 0 ? 1u : 0u);
+                    }
+                    tc::mma_commit(&B.s_full[it & 1]);
+                    tc::mma_commit(&B.k_empty[ks]);
                 }
-                tc::mma_commit(&B.s_full[j & 1]);
-                tc::mma_commit(&B.k_empty[ks]);
+                __syncwarp();
+                if (j > 0 && !issue_pv(it - 1)) { ok = false; break; }
             }
+            // Every S MMA of this head is issued: Q may be replaced once they finish.
+            if (leader) tc::mma_commit(&B.q_empty);
             __syncwarp();
-            if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
+            if (ok && nt > 0 && !issue_pv(hi * nt + nt - 1)) ok = false;
         }
-        if (ok && nt > 0) issue_pv(nt - 1);
         // Drain: nothing of ours may still run on the tensor core at exit.
         if (leader) {
             tc::mma_commit(&B.drain);
@@ -269,7 +298,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
         const float sl2 = rsqrtf((float)D) * kLog2e;
         const int64_t q_local = (int64_t)qt * kTile + row;
         const bool valid = q_local < p.n_q;
-        {
+        bool ok = true;
+        // Named barrier of the two warps (one per warpgroup) that own rows 32 quad ..
+        const uint32_t pair_bar = 1 + quad;
+        for (int hi = 0; hi < nh; ++hi) {
+        const int h = h0 + hi;
+        // The previous head's S MMAs must be done before its Q is replaced.
+        if (hi > 0 && ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.q_empty, (hi - 1) & 1, p.err));
+        if (ok) {
             // Q row, head dims [D/2 wg, D/2 wg + D/2) -> TMEM columns kColQ + D/4 wg ..
             constexpr int NW = D / 4;                     // 32-bit words per warpgroup
             uint32_t w[NW];
@@ -288,15 +324,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
             else tc::tmem_st16(lane_base + kColQ + wg * 16, w);
             tc::tmem_wait_st();
             tc::tc_fence_before();
-            tc::mbar_arrive(&B.q_full);
         }
+        tc::mbar_arrive(&B.q_full);
         float m = -INFINITY;
-        bool ok = true;
-        // Named barrier of the two warps (one per warpgroup) that own rows 32 quad ..
-        const uint32_t pair_bar = 1 + quad;
         for (int j = 0; j < nt; ++j) {
-            const int st = j & 1;
-            if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.s_full[st], (j >> 1) & 1, p.err));
+            const int it = hi * nt + j;
+            const int st = it & 1;
+            if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.s_full[st], (it >> 1) & 1, p.err));
             // Raw logits q.k of my 64 keys; the scale is folded into the exp2 argument.
             // (After a failed wait the loads just read stale columns: the loop goes
             // on only to keep meeting the partner warp, and writes nothing.)
@@ -353,7 +387,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
             }
             if (j > 0 && __any_sync(0xffffffffu, rescale)) {
                 // PV_{j-1} must be done before O is touched (PV_j waits for this tile's P).
-                ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.o_done, (j - 1) & 1, p.err));
+                ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.o_done, (it - 1) & 1, p.err));
                 if (!ok) continue;
                 tc::tc_fence_after();
                 const float f = rescale ? alpha : 1.f;
@@ -376,7 +410,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
             tc::tc_fence_before();
             tc::mbar_arrive(&B.p_full);
         }
-        if (ok && nt > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.o_done, (nt - 1) & 1, p.err));
+        if (ok && nt > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.o_done, (hi * nt + nt - 1) & 1, p.err));
         if (ok && nt > 0) {
             tc::tc_fence_after();
             // Normalise by the sum of the bf16 weights the tensor core multiplied, so
@@ -403,8 +437,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
             }
             if (valid && wg == 0) p.lse[(size_t)h * p.n_q + q_local] = (m + log2f(l)) * kLn2;
         }
+        // O and l of this head are read: the next head's first PV may overwrite them.
+        tc::tc_fence_before();
+        tc::mbar_arrive(&B.o_free);
+        }
     }
-
     tc::tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -434,7 +471,11 @@ static cudaError_t launch_fwd(const AttnArgs& a, cudaStream_t s) {
     p.Hq = a.Hq; p.Hkv = a.Hkv; p.q_start = a.q_start; p.n_q = a.n_q;
     p.q = a.q; p.o = a.o; p.lse = a.lse; p.bt = a.bt; p.num_phys = a.num_phys;
     p.sel = a.sel; p.kmax = a.kmax; p.err = a.err;
-    dim3 grid((unsigned)((a.n_q + kTile - 1) / kTile), a.Hq);
+    // Short page lists (local layers): one CTA takes every query head of a KV
+    // group, so its start-up (tensor memory, barriers, pipeline fill) is paid
+    // once for the group's g heads instead of once per head.
+    p.heads_per_cta = (a.sel && a.kmax <= kShortList) ? a.Hq / a.Hkv : 1;
+    dim3 grid((unsigned)((a.n_q + kTile - 1) / kTile), a.Hq / p.heads_per_cta);
     ProfScope ps("fwd_tc_kernel", s);
     fwd_tc_kernel<D><<<grid, kThreads, smem, s>>>(*a.tmap_k, *a.tmap_v, p);
     return cudaGetLastError();
