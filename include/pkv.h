@@ -201,8 +201,9 @@ pkv_status pkv_chunk_attn_fwd(pkv_seq* seq, const void* q, int64_t q_start, int6
 /* Recomputes P from LSE; writes dQ [n_q, Hq, d] (pool dtype) and ADDS this
  * chunk's dK/dV into the sequence's fp32 gradient pages (never zeroes them).
  * o and lse are the forward's outputs for the same chunk; dout is dL/dO.
- * Uses a pool-owned scratch buffer of Hq*n_q floats, plus the list of the
- * chunk's selected pages with a selection (grown on demand). */
+ * Uses a pool-owned scratch buffer of Hq*n_q floats, plus, with a selection,
+ * the list of the chunk's selected pages and, per (key page, KV head), a
+ * bitmask of the query pages that list the page (grown on demand). */
 pkv_status pkv_chunk_attn_bwd(pkv_seq* seq, const void* q, const void* o, const void* dout,
                               const float* lse, int64_t q_start, int64_t n_q, void* dq,
                               const pkv_sel* sel, void* stream);
@@ -217,7 +218,10 @@ pkv_status pkv_chunk_attn_bwd(pkv_seq* seq, const void* q, const void* o, const 
  * library until exit; a call needs n_q_heads * n_q floats (with a page
  * selection, plus 1 + min(key pages, n_qp * n_kv_heads * kmax) entries for
  * the list of selected pages) and is rejected
- * with PKV_ERR_INVALID above that. The first call on a device looks up the
+ * with PKV_ERR_INVALID above that. With a selection it also places, when they
+ * fit, the query-page bitmasks (1 + 2 * key pages * n_kv_heads *
+ * ceil(n_qp / 64) entries) there; when they do not, the dK/dV kernel finds
+ * each page's query pages by scanning the selection (the same results). The first call on a device looks up the
  * array's device address (no allocation) and should come before any stream
  * capture. All calls share the array: calls that overlap on the GPU race and
  * must be serialised by the caller. Each call rewrites what it reads, so

@@ -314,9 +314,17 @@ pkv_status pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
         void* vb = host ? p->vslot : p->v;
         const uint64_t rows = (uint64_t)(host ? p->n_slots : np) * desc->n_kv_heads * desc->page_size;
         const uint64_t dd = (uint64_t)desc->head_dim;
+        // The dK/dV kernel adds its page's gradients into the fp32 pool (or
+        // slots) by TMA reduce-add: boxes of 32 columns (128 bytes) x 128 rows.
+        void* dkb = host ? p->dkslot : p->dk;
+        void* dvb = host ? p->dvslot : p->dv;
         if (!make_tmap_2d(&p->tmap_k, kb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dd, rows, dd * 2, 64,
                           128, &why) ||
             !make_tmap_2d(&p->tmap_v, vb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dd, rows, dd * 2, 64,
+                          128, &why) ||
+            !make_tmap_2d(&p->tmap_dk, dkb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dd, rows, dd * 4, 32,
+                          128, &why) ||
+            !make_tmap_2d(&p->tmap_dv, dvb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dd, rows, dd * 4, 32,
                           128, &why)) {
             cleanup();
             return fail(PKV_ERR_CUDA, "pkv_pool_create: " + why);
@@ -562,6 +570,8 @@ pkv_status pkv::attn_common(pkv_seq* s, const void* q, int64_t q_start, int64_t 
     a->err = p->d_err;
     a->tmap_k = p->tmaps_ready ? &p->tmap_k : nullptr;
     a->tmap_v = p->tmaps_ready ? &p->tmap_v : nullptr;
+    a->tmap_dk = p->tmaps_ready ? &p->tmap_dk : nullptr;
+    a->tmap_dv = p->tmaps_ready ? &p->tmap_dv : nullptr;
     if (sel) {
         const int64_t n_qp = (n_q + P - 1) / P;
         if (!sel->pages || sel->kmax <= 0 || sel->n_qp != n_qp)
@@ -614,12 +624,18 @@ pkv_status pkv_chunk_attn_bwd(pkv_seq* s, const void* q, const void* o, const vo
     if (st != PKV_OK) return st;
     if (!o || !dout || !lse || !dq)
         return fail(PKV_ERR_INVALID, "pkv_chunk_attn_bwd: o, dout, lse or dq is NULL");
+    // Scratch: D [Hq * n_q] floats; with a selection, the union's page list
+    // and (8-byte aligned) the per-(page, KV head) query-page masks.
     const size_t n_d = (size_t)a.Hq * n_q;
     const size_t n_list = sel ? 1 + (size_t)bwd_pagelist_cap(a) : 0;
-    st = ensure_scratch(s->pool, n_d + n_list);
+    const size_t n_mask = sel ? 1 + 2 * (size_t)bwd_selmask_words(a) : 0;
+    st = ensure_scratch(s->pool, n_d + n_list + n_mask);
     if (st != PKV_OK) return st;
     a.o_in = o; a.dout = dout; a.lse_in = lse; a.dq = dq; a.Dbuf = s->pool->scratch;
     a.pagelist = sel ? reinterpret_cast<int32_t*>(s->pool->scratch + n_d) : nullptr;
+    a.selmask = sel ? reinterpret_cast<uint64_t*>(
+                          (reinterpret_cast<uintptr_t>(s->pool->scratch + n_d + n_list) + 7) & ~uintptr_t(7))
+                    : nullptr;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_bwd_rowdot(a, cs);
     if (e == cudaSuccess)

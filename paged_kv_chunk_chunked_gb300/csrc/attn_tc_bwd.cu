@@ -70,6 +70,7 @@ struct BwdParams {
     int kmax;
     int kv_splits;             // dK/dV kernel: CTAs per (page, KV head)
     const int32_t* pagelist;   // sparse: [count, pages...] the pages some query page lists
+    const uint64_t* selmask;   // sparse, or null: [key page][KV head][words] query pages listing the page
     int* err;
 };
 
@@ -118,6 +119,7 @@ struct __align__(8) KVBar {
     uint64_t drain[2];
     uint32_t tmem_base;
     int n_i;                         // 64-query tiles per head
+    int epi_bad[2];                  // a warpgroup's epilogue lost a wait: its boxes are not added
     int16_t tiles[2 * kMaxSelQp];    // sparse: the tiles, ascending
     uint8_t sel_flag[kMaxSelQp];
 };
@@ -125,7 +127,8 @@ struct __align__(8) KVBar {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-                 const __grid_constant__ CUtensorMap tm_v, BwdParams p) {
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dk,
+                 const __grid_constant__ CUtensorMap tm_dv, BwdParams p) {
     using L = KVLayout<D>;
     constexpr uint32_t kv_V = L::kV, kv_Q = L::kQ, kv_dO = L::kdO, kv_STAT = L::kSTAT;
     constexpr uint32_t kQS = L::kQStage;
@@ -160,9 +163,90 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int i0 = kfirst > p.q_start ? (int)((kfirst - p.q_start) / 64) : 0;
     const int32_t pp = p.bt[j];
     const bool page_ok = pp >= 0 && pp < p.num_phys;
+
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&B.kv_full, 1);
+        for (int s = 0; s < kv_STAGES; ++s) {
+            tc::mbar_init(&B.qdo_full[s], 32);
+            tc::mbar_init(&B.qdo_empty[s], 1);
+        }
+        tc::mbar_init(&B.k_tmem, kSoftmaxThreads);
+        tc::mbar_init(&B.s_full, 1);
+        tc::mbar_init(&B.s_free, kSoftmaxThreads);
+        tc::mbar_init(&B.p_full, kSoftmaxThreads);
+        tc::mbar_init(&B.p_free, 1);
+        tc::mbar_init(&B.acc_done, 1);
+        tc::mbar_init(&B.drain[0], 1);
+        tc::mbar_init(&B.drain[1], 1);
+        B.epi_bad[0] = B.epi_bad[1] = 0;
+        tc::fence_barrier_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(&B.tmem_base, 512);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    // The page's V streams in while the query tiles are being listed.
+    if (threadIdx.x == 0 && page_ok) {
+        tc::prefetch_tmap(&tm_q);
+        tc::prefetch_tmap(&tm_do);
+        tc::mbar_arrive_expect_tx(&B.kv_full, (D / 64) * 16 * KB);
+#pragma unroll
+        for (int b = 0; b < D / 64; ++b)
+            tc::tma_load_2d(smem + kv_V + b * 16 * KB, &tm_v, &B.kv_full, 64 * b,
+                            (int)(((int64_t)pp * p.Hkv + kvh) * 128));
+    }
+    // Softmax threads: their K row (head dims [D/2 wg, D/2 wg + D/2)) is loaded
+    // now and goes to tensor memory once the tiles are known.
+    constexpr int NW = D / 4;
+    uint32_t kw[NW];
+    if (warp >= 2 && warp < 2 + kSoftmaxThreads / 32 && page_ok) {
+        const int r = (warp & 3) * 32 + lane;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            static_cast<const __nv_bfloat16*>(p.kpool) + (((size_t)pp * p.Hkv + kvh) * 128 + r) * D +
+            ((warp - 2) >> 2) * (D / 2));
+#pragma unroll
+        for (int v = 0; v < NW / 4; ++v) {
+            const uint4 u = __ldg(src + v);
+            kw[4 * v] = u.x; kw[4 * v + 1] = u.y; kw[4 * v + 2] = u.z; kw[4 * v + 3] = u.w;
+        }
+    }
+
     // Query tiles that see this page: dense, every tile from i0 on; sparse, the
-    // two 64-query halves of every query page whose selection lists page j.
-    if (p.sel) {
+    // two 64-query halves of every query page whose selection lists page j --
+    // read from the page's query-page mask when the union kernel wrote one,
+    // else found by scanning the whole selection.
+    if (p.sel && p.selmask) {
+        if (warp == 0) {
+            // Lane l holds mask word l (query pages 64 l ..); set bits in
+            // ascending order, two tiles per query page.
+            const int n_qp = (int)((p.n_q + 127) / 128);
+            const int W = (n_qp + 63) / 64;                      // <= 32 (kMaxSelQp)
+            const uint64_t m = lane < W ? p.selmask[((size_t)j * p.Hkv + kvh) * W + lane] : 0ull;
+            const int c = __popcll(m);
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            int pos = 2 * (incl - c);
+            for (uint64_t mm = m; mm; mm &= mm - 1) {
+                const int qp = lane * 64 + __ffsll((long long)mm) - 1;
+                B.tiles[pos] = (int16_t)(2 * qp);
+                if (2 * qp + 1 < n_qt) B.tiles[pos + 1] = (int16_t)(2 * qp + 1);
+                pos += 2;
+            }
+            // Only the last query page can hold a single 64-query tile (odd n_qt).
+            const int last = n_qp - 1;
+            // (Both shuffles run on every lane, outside the lane-0 store.)
+            const bool last_listed = (__shfl_sync(0xffffffffu, m, last / 64) >> (last % 64)) & 1ull;
+            const int total = __shfl_sync(0xffffffffu, incl, 31);
+            if (lane == 0) B.n_i = 2 * total - (((n_qt & 1) && last_listed) ? 1 : 0);
+        }
+    } else if (p.sel) {
         // Every thread checks a slice of all entries (coalesced, independent loads).
         const int n_qp = (int)((p.n_q + 127) / 128);
         for (int qp = threadIdx.x; qp < n_qp; qp += kThreads) B.sel_flag[qp] = 0;
@@ -193,34 +277,11 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     } else if (threadIdx.x == 0) {
         B.n_i = n_qt - i0;
     }
-
-    if (threadIdx.x == 0) {
-        tc::mbar_init(&B.kv_full, 1);
-        for (int s = 0; s < kv_STAGES; ++s) {
-            tc::mbar_init(&B.qdo_full[s], 32);
-            tc::mbar_init(&B.qdo_empty[s], 1);
-        }
-        tc::mbar_init(&B.k_tmem, kSoftmaxThreads);
-        tc::mbar_init(&B.s_full, 1);
-        tc::mbar_init(&B.s_free, kSoftmaxThreads);
-        tc::mbar_init(&B.p_full, kSoftmaxThreads);
-        tc::mbar_init(&B.p_free, 1);
-        tc::mbar_init(&B.acc_done, 1);
-        tc::mbar_init(&B.drain[0], 1);
-        tc::mbar_init(&B.drain[1], 1);
-        tc::fence_barrier_init();
-        // A page no query tile uses needs no valid slot (sparse, staged pools).
-        if (!page_ok && B.n_i > 0) report_error(p.err, kErrBadPage);
-    }
-    if (warp == 1) {
-        tc::tmem_alloc(&B.tmem_base, 512);
-        tc::tmem_relinquish();
-    }
-    tc::tc_fence_before();
     __syncthreads();
-    tc::tc_fence_after();
     const uint32_t tmem = B.tmem_base;
     const int n_i = B.n_i;
+    // A page no query tile uses needs no valid slot (sparse, staged pools).
+    if (threadIdx.x == 0 && !page_ok && n_i > 0) report_error(p.err, kErrBadPage);
     // Iterations (head, 64-query tile), t = head * n_i + tile; split takes the
     // share [t_base, t_base + T) of them (the gradient epilogue adds, so any
     // partition of the iterations gives the same sums).
@@ -234,18 +295,10 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     auto head_of = [&](int t) -> int { return kvh * g + (t_base + t) / n_i; };
 
     if (!page_ok || T == 0) {
-        // nothing issued: fall through to the common exit
+        // No tile: only V's copy (issued for a valid page) is waited for.
+        if (threadIdx.x == 0 && page_ok) drain_wait(&B.kv_full, 0);
     } else if (warp == 0) {
         // ---------------------------------------------------------------- producer
-        const int row = (int)(((int64_t)pp * p.Hkv + kvh) * 128);
-        if (lane == 0) {
-            tc::prefetch_tmap(&tm_q);
-            tc::prefetch_tmap(&tm_do);
-            tc::mbar_arrive_expect_tx(&B.kv_full, (D / 64) * 16 * KB);
-#pragma unroll
-            for (int b = 0; b < D / 64; ++b)
-                tc::tma_load_2d(smem + kv_V + b * 16 * KB, &tm_v, &B.kv_full, 64 * b, row);
-        }
         // Per-query statistics of tile t (log2e * LSE, +inf past the chunk, and D),
         // two columns per lane; loaded one tile ahead so their latency overlaps
         // the wait for the next free stage.
@@ -387,17 +440,8 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const float sl2 = rsqrtf((float)D) * kLog2e;
         {
             // K row r, head dims [D/2 wg, D/2 wg + D/2) -> TMEM columns kv_TK + D/4 wg ..
-            constexpr int NW = D / 4;
-            const uint4* src = reinterpret_cast<const uint4*>(
-                static_cast<const __nv_bfloat16*>(p.kpool) + (((size_t)pp * p.Hkv + kvh) * 128 + r) * D + wg * (D / 2));
-            uint32_t w[NW];
-#pragma unroll
-            for (int v = 0; v < NW / 4; ++v) {
-                const uint4 u = __ldg(src + v);
-                w[4 * v] = u.x; w[4 * v + 1] = u.y; w[4 * v + 2] = u.z; w[4 * v + 3] = u.w;
-            }
-            if constexpr (D == 128) tc::tmem_st32(lane_base + kv_TK + wg * 32, w);
-            else tc::tmem_st16(lane_base + kv_TK + wg * 16, w);
+            if constexpr (D == 128) tc::tmem_st32(lane_base + kv_TK + wg * 32, kw);
+            else tc::tmem_st16(lane_base + kv_TK + wg * 16, kw);
             tc::tmem_wait_st();
             tc::tc_fence_before();
             tc::mbar_arrive(&B.k_tmem);
@@ -457,29 +501,51 @@ bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tc::tc_fence_before();
             tc::mbar_arrive(&B.p_full);
         }
-        if (ok && T > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.acc_done, 0, p.err));
-        if (ok && T > 0) {
-            // Warpgroup 0 adds dK (scaled), warpgroup 1 adds dV.
+        if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.acc_done, 0, p.err));
+        // Warpgroup 0 adds dK (scaled), warpgroup 1 adds dV into the fp32 pool.
+        // Each 32-column block of the page's 128 rows goes to shared memory (the
+        // Q/dO stages, free once acc_done has completed) in the tensor map's
+        // 128-byte swizzle (16-byte chunk v of row r at chunk v ^ (r % 8)), and
+        // one thread adds the boxes by TMA reduce-add: whole-line reductions at
+        // L2 instead of one 16-byte request per row and vector. Rows past the
+        // sequence's end add zeros. Every softmax thread reaches the
+        // warpgroup's barrier; a warp whose waits failed marks the warpgroup,
+        // whose boxes are then not added (the error is already recorded).
+        const float scale = wg == 0 ? rsqrtf((float)D) : 1.f;
+        const uint32_t col = wg == 0 ? kv_TDK : kv_TDV;
+        uint8_t* stage = smem + kv_Q + wg * (D / 32) * 16 * KB;   // D/32 boxes [128 rows][32 fp32]
+        if (ok) {
             tc::tc_fence_after();
             const bool live = kpos < p.q_start + p.n_q;
-            const size_t off = (((size_t)pp * p.Hkv + kvh) * 128 + r) * D;
-            const float scale = wg == 0 ? rsqrtf((float)D) : 1.f;
-            float* dst = (wg == 0 ? p.dkpool : p.dvpool) + off;
-            const uint32_t col = wg == 0 ? kv_TDK : kv_TDV;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t a[32];
                 tc::tmem_ld32(lane_base + col + c * 32, a);
                 tc::tmem_wait_ld(a);
-                if (live) {
+                uint8_t* row_p = stage + c * 16 * KB + r * 128;
 #pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        red_add_v4(dst + c * 32 + v * 4, __uint_as_float(a[4 * v]) * scale,
-                                   __uint_as_float(a[4 * v + 1]) * scale,
-                                   __uint_as_float(a[4 * v + 2]) * scale,
-                                   __uint_as_float(a[4 * v + 3]) * scale);
+                for (int v = 0; v < 8; ++v) {
+                    const float4 x = live ? make_float4(__uint_as_float(a[4 * v]) * scale,
+                                                        __uint_as_float(a[4 * v + 1]) * scale,
+                                                        __uint_as_float(a[4 * v + 2]) * scale,
+                                                        __uint_as_float(a[4 * v + 3]) * scale)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                    *reinterpret_cast<float4*>(row_p + ((v ^ (r & 7)) << 4)) = x;
                 }
             }
+        } else if (lane == 0) {
+            B.epi_bad[wg] = 1;
+        }
+        tc::fence_proxy_async_smem();
+        if (wg == 0) asm volatile("bar.sync 1, 128;" ::: "memory");   // the warpgroup's rows are written
+        else asm volatile("bar.sync 2, 128;" ::: "memory");
+        if ((warp & 3) == 2 && lane == 0 && !B.epi_bad[wg]) {
+            const CUtensorMap* tm = wg == 0 ? &tm_dk : &tm_dv;
+            const int row0 = (int)(((int64_t)pp * p.Hkv + kvh) * 128);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) tc::tma_reduce_add_2d(tm, stage + c * 16 * KB, 32 * c, row0);
+            tc::bulk_commit();
+            tc::bulk_wait_read();                          // the boxes are read before the CTA exits
         }
     }
 
@@ -811,18 +877,47 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant
 
 // The ascending union of the pages listed in a selection [n_ent entries],
 // out = [count, pages...]. One CTA: flags in shared memory, then an ordered
-// compaction (thread t owns a contiguous run of pages).
+// compaction (thread t owns a contiguous run of pages). With masks, also the
+// query pages listing each (page, KV head), as W 64-bit words per pair.
 constexpr int kUnionThreads = 1024;
 __global__ void __launch_bounds__(kUnionThreads) sel_union_kernel(const int32_t* sel, int64_t n_ent,
-                                                                  int n_pages, int32_t* out) {
-    extern __shared__ uint8_t flag[];
+                                                                  int n_pages, int32_t* out, int Hkv,
+                                                                  int kmax, uint64_t* masks, int W,
+                                                                  int masks_in_smem) {
+    extern __shared__ __align__(16) uint8_t flag[];
     __shared__ int wsum[kUnionThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int i = tid; i < n_pages; i += kUnionThreads) flag[i] = 0;
+    // The masks are built with shared-memory atomics when they fit after the
+    // flags (copied out at the end), else with global ones.
+    const int64_t n_words = (int64_t)n_pages * Hkv * W;
+    uint64_t* mk = masks && masks_in_smem ? reinterpret_cast<uint64_t*>(flag + ((n_pages + 15) & ~15)) : masks;
+    if (mk)
+        for (int64_t i = tid; i < n_words; i += kUnionThreads) mk[i] = 0ull;
     __syncthreads();
-    for (int64_t e = tid; e < n_ent; e += kUnionThreads) {
-        const int32_t pg = sel[e];
-        if (pg >= 0 && pg < n_pages) flag[pg] = 1;
+    // Eight entries are loaded before any is used, so their latencies overlap
+    // (the atomics would otherwise order each load after the previous one).
+    constexpr int kBatch = 8;
+    for (int64_t e0 = tid; e0 < n_ent; e0 += (int64_t)kBatch * kUnionThreads) {
+        int32_t pgs[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int64_t e = e0 + (int64_t)u * kUnionThreads;
+            pgs[u] = e < n_ent ? __ldg(sel + e) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int32_t pg = pgs[u];
+            if (pg < 0 || pg >= n_pages) continue;
+            flag[pg] = 1;
+            if (mk) {
+                // entry e = (query page, KV head, k): bit qp of the page's word qp / 64
+                const int row = (int)((e0 + (int64_t)u * kUnionThreads) / kmax);
+                const int qp = row / Hkv, kvh = row - qp * Hkv;
+                atomicOr(reinterpret_cast<unsigned long long*>(mk + ((int64_t)pg * Hkv + kvh) * W + qp / 64),
+                         1ull << (qp % 64));
+            }
+        }
     }
     __syncthreads();
     const int per = (n_pages + kUnionThreads - 1) / kUnionThreads;
@@ -851,6 +946,8 @@ __global__ void __launch_bounds__(kUnionThreads) sel_union_kernel(const int32_t*
     for (int i = p0; i < p1; ++i)
         if (flag[i]) out[1 + pos++] = i;
     if (tid == 0) out[0] = wsum[kUnionThreads / 32 - 1];
+    if (masks && masks_in_smem)
+        for (int64_t i = tid; i < n_words; i += kUnionThreads) masks[i] = mk[i];
 }
 
 template <int D>
@@ -887,7 +984,14 @@ static cudaError_t launch_bwd(const AttnArgs& a, cudaStream_t s) {
     const bool use_list = a.sel && bwd_pagelist_cap(a) <= 65535;
     if (use_list) {
         grid_pages = bwd_pagelist_cap(a);
-        const size_t fl = (size_t)n_key_pages;
+        // Dynamic shared memory: the page flags, then (16-byte aligned) the
+        // query-page masks when they fit.
+        const int n_qp = (int)((a.n_q + 127) / 128);
+        const int W = (n_qp + 63) / 64;
+        const size_t mask_bytes = (size_t)n_key_pages * a.Hkv * W * sizeof(uint64_t);
+        const size_t flags_bytes = ((size_t)n_key_pages + 15) & ~size_t(15);
+        const int masks_in_smem = a.selmask && flags_bytes + mask_bytes <= 200 * 1024;
+        const size_t fl = masks_in_smem ? flags_bytes + mask_bytes : (size_t)n_key_pages;
         static size_t attr_u = 0;
         if (fl > 48 * 1024 && fl > attr_u) {
             cudaError_t e = cudaFuncSetAttribute(sel_union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -896,11 +1000,13 @@ static cudaError_t launch_bwd(const AttnArgs& a, cudaStream_t s) {
             attr_u = fl;
         }
         ProfScope ps("sel_union_kernel", s);
-        sel_union_kernel<<<1, kUnionThreads, fl, s>>>(a.sel, (int64_t)((a.n_q + 127) / 128) * a.Hkv * a.kmax,
-                                                      (int)n_key_pages, a.pagelist);
+        sel_union_kernel<<<1, kUnionThreads, fl, s>>>(a.sel, (int64_t)n_qp * a.Hkv * a.kmax,
+                                                      (int)n_key_pages, a.pagelist, a.Hkv, a.kmax,
+                                                      a.selmask, W, masks_in_smem);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         p.pagelist = a.pagelist;
+        p.selmask = a.selmask;
     }
     // Small grids (early chunks) leave SMs idle behind a few long CTAs: split
     // each (page, KV head)'s iterations over up to 4 CTAs so that there are
@@ -922,7 +1028,8 @@ static cudaError_t launch_bwd(const AttnArgs& a, cudaStream_t s) {
                                : dim3((unsigned)(grid_pages * splits), a.Hkv);
     {
         ProfScope ps("bwd_kv_tc_kernel", s);
-        bwd_kv_tc_kernel<D><<<g_kv, kThreads, KVLayout<D>::kSMEM, s>>>(tq64, tdo64, *a.tmap_v, p);
+        bwd_kv_tc_kernel<D><<<g_kv, kThreads, KVLayout<D>::kSMEM, s>>>(tq64, tdo64, *a.tmap_v, *a.tmap_dk,
+                                                                       *a.tmap_dv, p);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -939,6 +1046,13 @@ int64_t bwd_pagelist_cap(const AttnArgs& a) {
     const int64_t n_key_pages = (a.q_start + a.n_q + a.P - 1) / a.P;
     const int64_t n_qp = (a.n_q + a.P - 1) / a.P;
     return std::min<int64_t>(n_key_pages, n_qp * a.Hkv * (int64_t)a.kmax);
+}
+
+int64_t bwd_selmask_words(const AttnArgs& a) {
+    if (!a.sel) return 0;
+    const int64_t n_key_pages = (a.q_start + a.n_q + a.P - 1) / a.P;
+    const int64_t n_qp = (a.n_q + a.P - 1) / a.P;
+    return n_key_pages * a.Hkv * ((n_qp + 63) / 64);
 }
 
 cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {

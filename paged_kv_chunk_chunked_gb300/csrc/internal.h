@@ -37,7 +37,7 @@ struct pkv_pool {
     // TMA descriptors over the K and V page pools (2-D: rows x d), with boxes
     // of 64 columns x 128 rows (whole pages). For a PINNED_HOST pool they
     // describe the device slots.
-    CUtensorMap tmap_k{}, tmap_v{};
+    CUtensorMap tmap_k{}, tmap_v{}, tmap_dk{}, tmap_dv{};
     bool tmaps_ready = false;
     // PINNED_HOST pools: k/v/dk/dv above are mapped pinned host pages; the
     // attention kernels read these device slots instead.
@@ -139,6 +139,7 @@ struct AttnArgs {
     void* dq;                        // bwd out
     float* Dbuf;                     // bwd scratch [Hq, n_q]
     int32_t* pagelist;               // bwd scratch with a selection: [1 + bwd_pagelist_cap(a)]
+    uint64_t* selmask;               // bwd scratch with a selection, or null: [bwd_selmask_words(a)]
     const void* kpool;
     const void* vpool;
     float* dkpool;
@@ -150,6 +151,8 @@ struct AttnArgs {
     int* err;
     const CUtensorMap* tmap_k;       // tensor-core path only: whole-page boxes
     const CUtensorMap* tmap_v;
+    const CUtensorMap* tmap_dk;      // tensor-core path only: fp32 gradient rows,
+    const CUtensorMap* tmap_dv;      // boxes of 32 columns x 128 rows (reduce-add)
 };
 
 // Validates the arguments shared by the attention entry points and fills a
@@ -201,6 +204,10 @@ cudaError_t launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t s);
 // Entries of the backward's page-list scratch for a call with a selection:
 // at most every key page, at most every listed entry (0 without a selection).
 int64_t bwd_pagelist_cap(const AttnArgs& a);
+// Words of the backward's per-(key page, KV head) masks of the query pages
+// whose selection lists the page (ceil(n_qp / 64) words each); 0 without a
+// selection. They replace a scan of the whole selection by every dK/dV CTA.
+int64_t bwd_selmask_words(const AttnArgs& a);
 cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s);
 
 // TMA descriptor helpers (driver entry point fetched through the runtime).

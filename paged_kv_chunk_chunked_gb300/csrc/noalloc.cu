@@ -76,7 +76,9 @@ extern "C" pkv_status pkv_chunk_attn_bwd_noalloc(pkv_seq* s, const void* q, cons
     if (!o || !dout || !lse || !dq)
         return fail(PKV_ERR_INVALID, std::string(who) + ": o, dout, lse or dq is NULL");
     const size_t n_d = (size_t)a.Hq * (size_t)n_q;
-    const size_t need = n_d + (sel ? 1 + (size_t)bwd_pagelist_cap(a) : 0);
+    const size_t n_list = sel ? 1 + (size_t)bwd_pagelist_cap(a) : 0;
+    const size_t n_mask = sel ? 1 + 2 * (size_t)bwd_selmask_words(a) : 0;
+    const size_t need = n_d + n_list;
     if (need > kNoAllocMaxFloats)
         return fail(PKV_ERR_INVALID,
                     std::string(who) + ": n_q_heads * n_q" + (sel ? " + the page list" : "") +
@@ -88,6 +90,12 @@ extern "C" pkv_status pkv_chunk_attn_bwd_noalloc(pkv_seq* s, const void* q, cons
     if (st != PKV_OK) return st;
     a.o_in = o; a.dout = dout; a.lse_in = lse; a.dq = dq; a.Dbuf = scratch;
     a.pagelist = sel ? reinterpret_cast<int32_t*>(scratch + n_d) : nullptr;
+    // The query-page masks when they fit too; otherwise the dK/dV kernel finds
+    // each page's query pages by scanning the selection (the same lists).
+    a.selmask = sel && need + n_mask <= kNoAllocMaxFloats
+                    ? reinterpret_cast<uint64_t*>(
+                          (reinterpret_cast<uintptr_t>(scratch + n_d + n_list) + 7) & ~uintptr_t(7))
+                    : nullptr;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_bwd_rowdot(a, cs);
     if (e == cudaSuccess)
