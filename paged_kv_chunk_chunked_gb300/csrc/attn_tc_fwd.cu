@@ -109,7 +109,7 @@ using tc::drain_wait;
 template <int D>
 __device__ __forceinline__ void produce_ring(const FwdParams& p, uint8_t* smem, FwdBarriers& B,
                                              const CUtensorMap& tmap, bool is_k, int qt, int kvh,
-                                             int nt, int lane) {
+                                             int nt, int lane, tc::PageBatch& pages) {
     using L = FwdLayout<D>;
     const int nst = is_k ? kKStages : kVStages;
     uint64_t* full = is_k ? B.k_full : B.v_full;
@@ -117,11 +117,11 @@ __device__ __forceinline__ void produce_ring(const FwdParams& p, uint8_t* smem, 
     uint8_t* base = smem + (is_k ? L::kOffK : L::kOffV);
     if (lane == 0) tc::prefetch_tmap(&tmap);
     // The same pages for every head of the CTA: iteration it = head * nt + tile.
-    tc::PageBatch pages;
+    // `pages` arrives initialised for the first head.
     int issued = 0;
     bool ok = true;
     for (int hi = 0; ok && hi < p.heads_per_cta; ++hi) {
-        pages.init(p.bt, p.sel ? p.sel + ((size_t)qt * p.Hkv + kvh) * p.kmax : nullptr, nt, lane);
+        if (hi > 0) pages.init(p.bt, p.sel ? p.sel + ((size_t)qt * p.Hkv + kvh) * p.kmax : nullptr, nt, lane);
         for (int j = 0; j < nt; ++j) {
             const int it = hi * nt + j;
             const int st = it % nst;
@@ -180,6 +180,36 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
             make_uint4(ch == 0 ? 0x3f80u : 0u, 0u, 0u, 0u);
     }
     tc::fence_proxy_async_smem();
+    // Before the set-up barrier: the producers' tile counts and page indices,
+    // and the softmax threads' Q rows of the first head (their latency overlaps
+    // barrier initialisation and the tensor-memory allocation).
+    const int32_t* sel_row = p.sel ? p.sel + ((size_t)qt * p.Hkv + kvh) * p.kmax : nullptr;
+    tc::PageBatch pages;
+    int n_pre = 0;
+    if (warp == 0 || warp == kThreads / 32 - 1) {
+        n_pre = sel_row ? sel_count_warp(sel_row, p.kmax, lane) : (int)(p.q_start / kTile) + qt + 1;
+        pages.init(p.bt, sel_row, n_pre, lane);
+    }
+    constexpr int NWQ = D / 4;                            // 32-bit words of Q per thread
+    uint32_t qw[NWQ];
+    const bool softmax_warp = warp >= 2 && warp < kThreads / 32 - 1;
+    // Q row of head h, head dims [D/2 wg, D/2 wg + D/2) (rows past the chunk: 0).
+    auto load_q = [&](int h) {
+        const int64_t q_local = (int64_t)qt * kTile + (warp & 3) * 32 + lane;
+#pragma unroll
+        for (int e = 0; e < NWQ; ++e) qw[e] = 0u;
+        if (q_local < p.n_q) {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                static_cast<const __nv_bfloat16*>(p.q) + ((size_t)q_local * p.Hq + h) * D +
+                ((warp - 2) >> 2) * (D / 2));
+#pragma unroll
+            for (int v = 0; v < NWQ / 4; ++v) {
+                const uint4 u = __ldg(src + v);
+                qw[4 * v] = u.x; qw[4 * v + 1] = u.y; qw[4 * v + 2] = u.z; qw[4 * v + 3] = u.w;
+            }
+        }
+    };
+    if (softmax_warp) load_q(h0);
     if (threadIdx.x == 0) {
         tc::mbar_init(&B.q_full, kSoftmaxThreads);
         tc::mbar_init(&B.q_empty, 1);
@@ -203,9 +233,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
         tc::tmem_relinquish();
     } else if (warp == 0) {
         // Key tiles of this CTA: dense, pages 0..own; sparse, the listed pages.
-        const int n = p.sel ? sel_count_warp(p.sel + ((size_t)qt * p.Hkv + kvh) * p.kmax, p.kmax, lane)
-                            : (int)(p.q_start / kTile) + qt + 1;
-        if (lane == 0) B.n_tiles = n;
+        if (lane == 0) B.n_tiles = n_pre;
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -215,10 +243,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
 
     if (warp == 0) {
         // ------------------------------------------------------------ K producer
-        produce_ring<D>(p, smem, B, tmap_k, true, qt, kvh, nt, lane);
+        produce_ring<D>(p, smem, B, tmap_k, true, qt, kvh, nt, lane, pages);
     } else if (warp == kThreads / 32 - 1) {
         // ------------------------------------------------------------ V producer
-        produce_ring<D>(p, smem, B, tmap_v, false, qt, kvh, nt, lane);
+        produce_ring<D>(p, smem, B, tmap_v, false, qt, kvh, nt, lane, pages);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // The whole warp runs the loop (warp-uniform descriptors); one elected
@@ -306,24 +334,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
         // The previous head's S MMAs must be done before its Q is replaced.
         if (hi > 0 && ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.q_empty, (hi - 1) & 1, p.err));
         if (ok) {
-            // Q row, head dims [D/2 wg, D/2 wg + D/2) -> TMEM columns kColQ + D/4 wg ..
-            constexpr int NW = D / 4;                     // 32-bit words per warpgroup
-            uint32_t w[NW];
-#pragma unroll
-            for (int e = 0; e < NW; ++e) w[e] = 0u;          // rows past the chunk: Q = 0
-            if (valid) {
-                const uint4* src = reinterpret_cast<const uint4*>(
-                    static_cast<const __nv_bfloat16*>(p.q) + ((size_t)q_local * p.Hq + h) * D + wg * (D / 2));
-#pragma unroll
-                for (int v = 0; v < NW / 4; ++v) {
-                    const uint4 u = __ldg(src + v);
-                    w[4 * v] = u.x; w[4 * v + 1] = u.y; w[4 * v + 2] = u.z; w[4 * v + 3] = u.w;
-                }
-            }
-            if constexpr (D == 128) tc::tmem_st32(lane_base + kColQ + wg * 32, w);
-            else tc::tmem_st16(lane_base + kColQ + wg * 16, w);
+            // Q row of head h (loaded ahead) -> TMEM columns kColQ + D/4 wg ..;
+            // then the next head's rows start loading, hidden by this head's tiles.
+            if constexpr (D == 128) tc::tmem_st32(lane_base + kColQ + wg * 32, qw);
+            else tc::tmem_st16(lane_base + kColQ + wg * 16, qw);
             tc::tmem_wait_st();
             tc::tc_fence_before();
+            if (hi + 1 < nh) load_q(h + 1);
         }
         tc::mbar_arrive(&B.q_full);
         float m = -INFINITY;
