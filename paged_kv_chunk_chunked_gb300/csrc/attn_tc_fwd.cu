@@ -334,13 +334,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
         // The previous head's S MMAs must be done before its Q is replaced.
         if (hi > 0 && ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.q_empty, (hi - 1) & 1, p.err));
         if (ok) {
-            // Q row of head h (loaded ahead) -> TMEM columns kColQ + D/4 wg ..;
-            // then the next head's rows start loading, hidden by this head's tiles.
+            // Q row of head h (loaded ahead) -> TMEM columns kColQ + D/4 wg ..
             if constexpr (D == 128) tc::tmem_st32(lane_base + kColQ + wg * 32, qw);
             else tc::tmem_st16(lane_base + kColQ + wg * 16, qw);
             tc::tmem_wait_st();
             tc::tc_fence_before();
-            if (hi + 1 < nh) load_q(h + 1);
         }
         tc::mbar_arrive(&B.q_full);
         float m = -INFINITY;
@@ -427,6 +425,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant_
             tc::tc_fence_before();
             tc::mbar_arrive(&B.p_full);
         }
+        // The next head's Q rows load while this head's last PV and epilogue run.
+        // (Loads issued before the tile loop, and left in flight during it, gave
+        // nondeterministic O in a few tiles of multi-head CTAs, for a reason not
+        // found; issued here, repeated calls are bit-identical.)
+        if (hi + 1 < nh) load_q(h + 1);
         if (ok && nt > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.o_done, (hi * nt + nt - 1) & 1, p.err));
         if (ok && nt > 0) {
             tc::tc_fence_after();

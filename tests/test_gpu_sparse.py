@@ -331,3 +331,43 @@ def test_topk_error_against_dense_matches_oracle(K):
             assert abs(got - want) <= 1e-2, (e_gpu, e_ref)
     finally:
         sw.close()
+
+
+@pytest.mark.parametrize("key,n_q", [("qwen7b_local_256k", 9344), ("qwen7b_local_256k", 8192),
+                                     ("gptoss_local_256k", 8192), ("qwen7b_dense_32k", 4096)])
+def test_repeated_calls_are_bit_identical(key, n_q):
+    """The forward, and the backward's dQ, have no atomics: calling them again
+    on the same inputs must reproduce every bit. Local lists put 7 (GPT-OSS
+    shape: 8) query heads in one forward CTA. 73 query pages is the case that
+    once exposed a race there."""
+    w = synth.workload(key, N=16384 + n_q, C=16384)
+    s, e = w.chunk_range(1)
+    n_qp = (e - s + w.P - 1) // w.P
+    sw = ChunkSweep(w).load_inputs()
+    try:
+        sw.reset()
+        for c in range(w.n_chunks):
+            a, b = w.chunk_range(c)
+            B.pkv_append(sw.seq, sw.k[c], sw.v[c], b - a)
+        sel = None
+        if w.local:
+            sel = torch.empty((n_qp, w.Hkv, sum(w.local)), dtype=torch.int32, device="cuda")
+            B.pkv_page_local(sw.seq, s, e - s, *w.local, sel)
+        first = None
+        for rep in range(12):
+            B.pkv_chunk_attn_fwd(sw.seq, sw.q[1], s, e - s, sw.o[1], sw.lse[1], sel)
+            got = (sw.o[1].clone(), sw.lse[1].clone())
+            if first is None:
+                first = got
+            else:
+                assert torch.equal(got[0], first[0]) and torch.equal(got[1], first[1]), rep
+        dq0 = None
+        for rep in range(3):
+            B.pkv_chunk_attn_bwd(sw.seq, sw.q[1], sw.o[1], sw.do[1], sw.lse[1], s, e - s, sw.dq[1], sel)
+            if dq0 is None:
+                dq0 = sw.dq[1].clone()
+            else:
+                assert torch.equal(sw.dq[1], dq0), rep
+        B.pkv_check(sw.pool)
+    finally:
+        sw.close()

@@ -184,3 +184,44 @@ def test_noalloc_rejects_chunks_beyond_the_fixed_scratch():
         B.pkv_check(pool)
     finally:
         B.pkv_pool_destroy(pool)
+
+
+def test_noalloc_scan_fallback_equals_the_mask_path_bit_for_bit():
+    """With a selection, the dK/dV kernel reads each page's query tiles from
+    per-(page, KV head) query-page masks; when those masks do not fit the fixed
+    scratch the no-allocation backward lets the kernel scan the selection
+    instead. Both give the same tile lists in the same order, and every
+    (page, KV head) block of the pool gets one addition per call, so dQ, dK
+    and dV must match pkv_chunk_attn_bwd (the oracle-checked mask path) bit
+    for bit. Sizes: 28 query heads x 9344 queries (73 query pages) after 16384
+    earlier tokens, local lists of 2 pages: D and the page list fit the
+    262144 floats (261834), D, list and masks do not (265051)."""
+    w = synth.workload("qwen7b_local_256k", N=16384 + 9344, C=16384)
+    s, e = w.chunk_range(1)
+    n_q, n_qp, n_key_pages, kmax = e - s, (e - s + w.P - 1) // w.P, (e + w.P - 1) // w.P, 2
+    n_d = w.Hq * n_q
+    n_list = 1 + min(n_key_pages, n_qp * w.Hkv * kmax)
+    n_mask = 1 + 2 * n_key_pages * w.Hkv * ((n_qp + 63) // 64)
+    assert n_d + n_list <= 262144 < n_d + n_list + n_mask
+    outs = []
+    for noalloc in (False, True):
+        sw = ChunkSweep(w).load_inputs()
+        try:
+            sw.reset()
+            for c in range(w.n_chunks):
+                a, b = w.chunk_range(c)
+                B.pkv_append(sw.seq, sw.k[c], sw.v[c], b - a)
+            sel = torch.empty((n_qp, w.Hkv, kmax), dtype=torch.int32, device="cuda")
+            B.pkv_page_local(sw.seq, s, n_q, 0, 2, sel)
+            B.pkv_chunk_attn_fwd(sw.seq, sw.q[1], s, n_q, sw.o[1], sw.lse[1], sel)
+            B.pkv_grad_zero(sw.seq)
+            bwd = B.pkv_chunk_attn_bwd_noalloc if noalloc else B.pkv_chunk_attn_bwd
+            bwd(sw.seq, sw.q[1], sw.o[1], sw.do[1], sw.lse[1], s, n_q, sw.dq[1], sel)
+            g = sw.gather()
+            B.pkv_check(sw.pool)
+            outs.append((sw.dq[1].cpu(), g["dk"].cpu(), g["dv"].cpu()))
+        finally:
+            sw.close()
+    for x, y in zip(outs[0], outs[1]):
+        assert torch.equal(x, y)
+    assert float(outs[0][1].abs().sum()) > 0.0                      # gradients were added
