@@ -605,11 +605,6 @@ def run_sparse(args, world, rank):
     pk, pk_kind = peaks()
     peak_tc, peak_kind = tensor_peak(pk, pk_kind)
     kernels = {k: {"launches": c, "ms_per_step": round(t / args.steps, 3)} for k, (c, t) in prof.items()}
-    # page selection: the page-query kernel reads the chunk's Q once (HBM-bound)
-    q_bytes = w.C * w.Hq * w.d * 2
-    qb_cnt, qb_ms = prof.get("qbar_kernel", (1, float("nan")))
-    qbar_gbs = q_bytes * qb_cnt / (qb_ms * 1e-3) / 1e9
-    sel_cnt, sel_ms = prof.get("select_kernel", (1, float("nan")))
     # Dominant kernel (by device time) with the FLOPs it runs over the attended
     # pairs: dK/dV kernel 8 (S^T, dP^T, dV, dK), dQ kernel 6, forward 4, times d.
     units = {"bwd_kv_tc_kernel": 8, "bwd_q_tc_kernel": 6, "fwd_tc_kernel": 4}
@@ -643,20 +638,11 @@ def run_sparse(args, world, rank):
     sel = selection_record(w, prof, args.steps, pk, pk_kind, K + ns + nl)
     if sel:
         out["selection"] = sel
-    if "qbar_kernel" in prof:
-        # page scoring: the page-query kernel reads the chunk's Q once (HBM-bound)
-        out["page_query_roofline"] = {
-            "bound": "hbm", "kernel": "qbar_kernel", "unit": "GB/s",
-            "achieved": round(qbar_gbs, 1), "peak": pk["hbm_gbs"],
-            "frac": round(qbar_gbs / pk["hbm_gbs"], 4),
-            "bytes_per_launch": q_bytes, "peak_kind": f"{pk_kind} hbm_gbs"}
-        out["select_kernel_us_per_launch"] = round(1e3 * sel_ms / sel_cnt, 2)
     return out
 
 
 # Kernels of the page-selection chain (page queries, scores, top-K).
-SELECTION_KERNELS = ("qbar_kernel", "score_kernel", "select_kernel", "topk_fused_kernel",
-                     "topk_select_kernel")
+SELECTION_KERNELS = ("topk_fused_kernel",)
 
 
 def selection_bytes(w, kmax: int) -> int:
