@@ -637,9 +637,15 @@ pkv_status pkv_chunk_attn_bwd(pkv_seq* s, const void* q, const void* o, const vo
                           (reinterpret_cast<uintptr_t>(s->pool->scratch + n_d + n_list) + 7) & ~uintptr_t(7))
                     : nullptr;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_bwd_rowdot(a, cs);
-    if (e == cudaSuccess)
-        e = use_tc(s->pool, a) ? launch_attn_bwd_tc(a, cs) : launch_attn_bwd_simt(a, cs);
+    // D = rowsum(dO * O): computed inside the tensor-core backward, by its own
+    // kernel before the CUDA-core one.
+    cudaError_t e;
+    if (use_tc(s->pool, a)) {
+        e = launch_attn_bwd_tc(a, cs);
+    } else {
+        e = launch_bwd_rowdot(a, cs);
+        if (e == cudaSuccess) e = launch_attn_bwd_simt(a, cs);
+    }
     if (e == cudaSuccess && s->used) e = cudaEventRecord(s->used, cs);
     if (e != cudaSuccess) return cuda_fail(e, "pkv_chunk_attn_bwd: launch");
     return PKV_OK;

@@ -60,7 +60,7 @@ struct BwdParams {
     const void* q;             // [n_q, Hq, d] bf16
     const void* kpool;         // [pages, Hkv, 128, d] bf16 (the tensor maps' base)
     const float* lse;          // [Hq, n_q]
-    const float* Dbuf;         // [Hq, n_q]
+    float* Dbuf;               // [Hq, n_q]: D = rowsum(dO * O), written by the dQ kernel
     void* dq;                  // [n_q, Hq, d] bf16
     float* dkpool;
     float* dvpool;
@@ -70,6 +70,7 @@ struct BwdParams {
     int kmax;
     int kv_splits;             // dK/dV kernel: CTAs per (page, KV head)
     const int32_t* pagelist;   // sparse: [count, pages...] the pages some query page lists
+    const void* o;             // forward output (the dQ kernel computes D = rowsum(dO * O))
     const uint64_t* selmask;   // sparse, or null: [key page][KV head][words] query pages listing the page
     int* err;
 };
@@ -589,6 +590,7 @@ struct __align__(8) QBar {
     uint64_t acc_done;
     uint64_t drain[2];
     uint32_t tmem_base;
+    float dpart[2][128];             // the two warpgroups' halves of each row's D
 };
 
 template <int D>
@@ -770,7 +772,6 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant
         const int64_t qpos = p.q_start + q_local;
         const bool valid = q_local < p.n_q;
         const float lse2 = valid ? p.lse[(size_t)h * p.n_q + q_local] * kLog2e : INFINITY;
-        const float Dr = valid ? p.Dbuf[(size_t)h * p.n_q + q_local] : 0.f;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         const float sl2 = rsqrtf((float)D) * kLog2e;
         const int64_t first_diag = p.q_start + (int64_t)qt * 128;   // first key of the own page
@@ -795,8 +796,45 @@ bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant
             tc::tc_fence_before();
             tc::mbar_arrive(&B.q_tmem);
         }
+        // D = rowsum(dO * O) of this query row (the backward's D_i): this
+        // warpgroup's half of the head dims, dO from the tile in shared memory
+        // (once it has landed; 128-byte swizzle: 16-byte chunk j of row r at
+        // j ^ (r % 8)) and O from global memory. The halves meet through shared
+        // memory; warpgroup 0 writes D for the dK/dV kernel, which runs after
+        // this one.
         bool ok = true;
-        for (int t = 0; t < T; ++t) {
+        float Dr = 0.f;
+        {
+            constexpr int HC = D / 16;                      // 8-element chunks per half row
+            uint4 ov[HC];
+            if (valid) {
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    static_cast<const __nv_bfloat16*>(p.o) + ((size_t)q_local * p.Hq + h) * D + wg * (D / 2));
+#pragma unroll
+                for (int c = 0; c < HC; ++c) ov[c] = __ldg(src + c);
+            }
+            ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.q_full, 0, p.err));
+            float part = 0.f;
+            if (ok && valid) {
+#pragma unroll
+                for (int c = 0; c < HC; ++c) {
+                    const int d0 = wg * (D / 2) + c * 8;
+                    const int cb = (d0 % 64) / 8;
+                    const uint4 dv4 = *reinterpret_cast<const uint4*>(
+                        smem + q_dO + (d0 / 64) * 16 * KB + r * 128 + ((cb ^ (r & 7)) << 4));
+                    float fo[8], fd[8];
+                    widen16<__nv_bfloat16>(ov[c], fo);
+                    widen16<__nv_bfloat16>(dv4, fd);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) part = fmaf(fd[e], fo[e], part);
+                }
+            }
+            B.dpart[wg][r] = part;
+            asm volatile("bar.sync %0, 64;" :: "r"(1 + quad) : "memory");   // the row's two warps
+            Dr = part + B.dpart[wg ^ 1][r];
+            if (wg == 0 && valid && ok) p.Dbuf[(size_t)h * p.n_q + q_local] = Dr;
+        }
+        for (int t = 0; ok && t < T; ++t) {
             ok = __all_sync(0xffffffffu, tc::mbar_wait(&B.s_full, t & 1, p.err));
             if (!ok) break;
             tc::tc_fence_after();
@@ -972,8 +1010,17 @@ static cudaError_t launch_bwd(const AttnArgs& a, cudaStream_t s) {
     BwdParams p{};
     p.Hq = a.Hq; p.Hkv = a.Hkv; p.q_start = a.q_start; p.n_q = a.n_q; p.q = a.q; p.kpool = a.kpool;
     p.lse = a.lse_in; p.Dbuf = a.Dbuf; p.dq = a.dq; p.dkpool = a.dkpool; p.dvpool = a.dvpool;
+    p.o = a.o_in;
     p.bt = a.bt; p.num_phys = a.num_phys; p.err = a.err;
     p.sel = a.sel; p.kmax = a.kmax;
+    // The dQ kernel first: it computes D = rowsum(dO * O), which the dK/dV kernel reads.
+    {
+        dim3 g_q((unsigned)((a.n_q + 127) / 128), a.Hq);
+        ProfScope ps("bwd_q_tc_kernel", s);
+        bwd_q_tc_kernel<D><<<g_q, kThreads, QLayout<D>::kSMEM, s>>>(tdo128, *a.tmap_k, *a.tmap_v, p);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     const int64_t n_keys = a.q_start + a.n_q;
     const int64_t n_key_pages = (n_keys + 127) / 128;
     // Key pages the dK/dV grid covers: every page (dense), or at most the
@@ -1031,11 +1078,6 @@ static cudaError_t launch_bwd(const AttnArgs& a, cudaStream_t s) {
         bwd_kv_tc_kernel<D><<<g_kv, kThreads, KVLayout<D>::kSMEM, s>>>(tq64, tdo64, *a.tmap_v, *a.tmap_dk,
                                                                        *a.tmap_dv, p);
     }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    dim3 g_q((unsigned)((a.n_q + 127) / 128), a.Hq);
-    ProfScope ps("bwd_q_tc_kernel", s);
-    bwd_q_tc_kernel<D><<<g_q, kThreads, QLayout<D>::kSMEM, s>>>(tdo128, *a.tmap_k, *a.tmap_v, p);
     return cudaGetLastError();
 }
 
@@ -1057,7 +1099,10 @@ int64_t bwd_selmask_words(const AttnArgs& a) {
 
 cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t s) {
     // The sparse dK/dV kernel lists the selecting query pages in shared memory.
-    if (a.sel && (a.n_q + 127) / 128 > kMaxSelQp) return launch_attn_bwd_simt(a, s);
+    if (a.sel && (a.n_q + 127) / 128 > kMaxSelQp) {
+        const cudaError_t e = launch_bwd_rowdot(a, s);
+        return e != cudaSuccess ? e : launch_attn_bwd_simt(a, s);
+    }
     if ((reinterpret_cast<uintptr_t>(a.dout) & 15) || !a.tmap_k || (a.sel && !a.pagelist))
         return cudaErrorInvalidValue;
     return a.d == 64 ? launch_bwd<64>(a, s) : launch_bwd<128>(a, s);
