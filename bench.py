@@ -853,8 +853,12 @@ def run_offload(args, world, rank):
     cache on a side stream: pages already staged by an earlier chunk stay, so
     only the difference crosses the host link; the gradients go back once, at
     the end of the backward sweep, when the step releases the slots (every
-    step starts with an empty cache). The same step on a device-resident pool
-    gives the staging overhead.
+    step starts with an empty cache). Each step first zeroes the gradient
+    pool, as a training step does: on the device-resident pool a write of
+    every gradient page, on the pinned-host pool a per-page record in HBM, so
+    the backward's first staging of a page fills zeros in HBM instead of
+    copying stale host pages. The same step on a device-resident pool gives
+    the staging overhead.
 
     --overlap-proj adds the computations the pages overlap with the transfer
     (gist.science/de §2.C: with sparse attention, the key/value projections
@@ -918,6 +922,7 @@ def run_offload(args, world, rank):
             """rec: dict collecting per-chunk event pairs (main-stream span of
             the chunk from its prefetch to its attention call; side-stream span
             of its staging)."""
+            B.pkv_grad_zero(seq, main_s)      # a training step starts from zero gradients
             for phase, chunks in (("fwd", meas), ("bwd", list(reversed(meas)))):
                 for c in chunks:
                     s, e = w.chunk_range(c)

@@ -134,7 +134,9 @@ pkv_status pkv_pool_free_pages(const pkv_pool* pool, int64_t* n_free);
 
 /* Device addresses of the pool's arrays (layouts above); any may be NULL.
  * For tests and for callers that read pages directly. For PINNED_HOST pools
- * these are host addresses of the pinned pages. */
+ * these are host addresses of the pinned pages; there a gradient page that
+ * was zeroed (pkv_grad_zero, or fresh from pkv_append) holds stale memory
+ * until it is written back or accumulated into (pkv_gather reads it right). */
 pkv_status pkv_pool_arrays(const pkv_pool* pool, void** k, void** v, float** dk,
                            float** dv, float** rep);
 
@@ -232,7 +234,13 @@ pkv_status pkv_chunk_attn_bwd_noalloc(pkv_seq* seq, const void* q, const void* o
                                       const void* dout, const float* lse, int64_t q_start,
                                       int64_t n_q, void* dq, const pkv_sel* sel, void* stream);
 
-/* Zeroes the gradient pages of the sequence's pages. */
+/* Zeroes the gradient pages of the sequence's pages. For a PINNED_HOST pool
+ * nothing is written over the host link: every (page, KV head) of the
+ * sequence is recorded as zero in HBM (staging then fills slots with zeros
+ * instead of copying, pkv_gather reads zeros, pkv_grad_accumulate writes the
+ * whole page), and gradients already staged in the sequence's slots are
+ * zeroed there, after its last prefetch or write-back; later staging waits
+ * for this call. A write-back of the page makes its host memory current. */
 pkv_status pkv_grad_zero(pkv_seq* seq, void* stream);
 
 /* Adds contiguous float32 gradients into the sequence's gradient pages:
@@ -305,8 +313,11 @@ pkv_status pkv_page_local(pkv_seq* seq, int64_t q_start, int64_t n_q, int32_t n_
 /* ---------------------------------------------------------------- host offload (a7)
  * For PINNED_HOST pools the K/V pages and their fp32 gradient pages live in
  * mapped pinned host memory (appends write them there; pkv_gather and
- * pkv_grad_zero work on them) and the pool owns n_device_slots page slots in
- * HBM; page representatives stay in HBM. Attention calls on such a pool read
+ * pkv_grad_accumulate work on them) and the pool owns n_device_slots page
+ * slots in HBM; page representatives stay in HBM. Gradient pages known to be
+ * zero (fresh from an append, or after pkv_grad_zero) are recorded as such in
+ * HBM instead of being written: staging fills their slots with zeros, so they
+ * cross the host link only when written back. Attention calls on such a pool read
  * the slots, so the pages a call needs must be staged first. One sequence
  * of the pool uses the slots at a time (one pool per layer to prefetch layer
  * l+1 while layer l computes).
@@ -329,8 +340,8 @@ pkv_status pkv_page_local(pkv_seq* seq, int64_t q_start, int64_t n_q, int32_t n_
  * pages than slots: the excess is not staged and records
  * PKV_ERR_DEVICE_FAULT for pkv_check. Staged gradients are the authoritative
  * copy until written back: host-side gradient calls (pkv_gather,
- * pkv_grad_accumulate, pkv_grad_zero) see them only after pkv_writeback_grads
- * or pkv_release_slots. Whole-sequence staging (logical_pages NULL, when the
+ * pkv_grad_accumulate) see them only after pkv_writeback_grads or
+ * pkv_release_slots (pkv_grad_zero zeroes them in place). Whole-sequence staging (logical_pages NULL, when the
  * sequence fits the slots) puts page i in slot i and copies with the copy
  * engines; it first writes back gradients still staged.
  * pkv_writeback_grads: on `side`, after the sequence's last attention call,
@@ -354,7 +365,10 @@ pkv_status pkv_wait(pkv_seq* seq, void* main, int64_t timeout_us);
 
 /* Page-heads (one logical page of one KV head) the sequence's staging has
  * moved so far: K/V host-to-device, dK/dV host-to-device, dK/dV
- * device-to-host (write-backs and evictions). Any output may be NULL.
+ * device-to-host (write-backs and evictions). Gradient pages recorded as
+ * zero that the slot cache fills with zeros in HBM are not counted as moved
+ * (whole-sequence staging by the copy engines counts every page it copies).
+ * Any output may be NULL.
  * Synchronizes the device. PINNED_HOST pools only (else PKV_ERR_INVALID). */
 pkv_status pkv_stage_stats(pkv_seq* seq, int64_t* kv_in, int64_t* grads_in, int64_t* grads_out);
 

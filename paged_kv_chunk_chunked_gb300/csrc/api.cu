@@ -255,6 +255,7 @@ pkv_status pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
         if (host) {
             cudaFreeHost(p->k); cudaFreeHost(p->v); cudaFreeHost(p->dk); cudaFreeHost(p->dv);
             cudaFree(p->kslot); cudaFree(p->vslot); cudaFree(p->dkslot); cudaFree(p->dvslot);
+            cudaFree(p->gzero);
         } else {
             cudaFree(p->k); cudaFree(p->v); cudaFree(p->dk); cudaFree(p->dv);
         }
@@ -276,6 +277,8 @@ pkv_status pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
             (e = cudaMalloc(&p->vslot, skv)) != cudaSuccess ||
             (e = cudaMalloc(reinterpret_cast<void**>(&p->dkslot), sg)) != cudaSuccess ||
             (e = cudaMalloc(reinterpret_cast<void**>(&p->dvslot), sg)) != cudaSuccess ||
+            (e = cudaMalloc(reinterpret_cast<void**>(&p->gzero), (size_t)np * desc->n_kv_heads)) != cudaSuccess ||
+            (e = cudaMemset(p->gzero, 0, (size_t)np * desc->n_kv_heads)) != cudaSuccess ||
             (e = cudaMalloc(reinterpret_cast<void**>(&p->rep), rep_bytes)) != cudaSuccess ||
             (e = cudaMalloc(reinterpret_cast<void**>(&p->d_err), sizeof(int))) != cudaSuccess) {
             cleanup();
@@ -348,6 +351,7 @@ void pkv_pool_destroy(pkv_pool* p) {
     if (p->desc.residency == PKV_RES_PINNED_HOST) {
         cudaFreeHost(p->k); cudaFreeHost(p->v); cudaFreeHost(p->dk); cudaFreeHost(p->dv);
         cudaFree(p->kslot); cudaFree(p->vslot); cudaFree(p->dkslot); cudaFree(p->dvslot);
+        cudaFree(p->gzero);
     } else if (is_device(p)) {
         cudaFree(p->k); cudaFree(p->v); cudaFree(p->dk); cudaFree(p->dv);
     }
@@ -532,7 +536,7 @@ pkv_status pkv_append(pkv_seq* s, const void* k, const void* v, int64_t n_tok, v
     a.k_in = k; a.v_in = v;
     a.kpool = p->k; a.vpool = p->v; a.dkpool = p->dk; a.dvpool = p->dv; a.rep = p->rep;
     a.bt = s->d_bt; a.num_phys = p->desc.num_phys_pages;
-    a.old_len = s->len; a.n_tok = n_tok; a.err = p->d_err;
+    a.old_len = s->len; a.n_tok = n_tok; a.gzero = p->gzero; a.err = p->d_err;
     cudaError_t e = launch_append(a, cs);
     if (e == cudaSuccess && s->used) e = cudaEventRecord(s->used, cs);
     if (e != cudaSuccess) return cuda_fail(e, "pkv_append: launch");
@@ -655,8 +659,18 @@ pkv_status pkv_grad_zero(pkv_seq* s, void* stream) {
     if (!s) return fail(PKV_ERR_INVALID, "pkv_grad_zero: seq is NULL");
     if (!is_device(s->pool)) return fail(PKV_ERR_INVALID, "pkv_grad_zero: META pool");
     if (s->bt.empty()) return PKV_OK;
-    cudaError_t e = launch_grad_zero(s->pool, s->d_bt, 0, (int64_t)s->bt.size(),
-                                     static_cast<cudaStream_t>(stream));
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (s->pool->desc.residency == PKV_RES_PINNED_HOST) {
+        // Host pages are recorded as zero, not written; staged gradients are
+        // zeroed in their slots once the last prefetch or write-back is done,
+        // and later staging waits for this call.
+        e = cudaStreamWaitEvent(cs, s->staged, 0);
+        if (e == cudaSuccess) e = launch_grad_zero_staged(s, cs);
+        if (e == cudaSuccess) e = cudaEventRecord(s->used, cs);
+    } else {
+        e = launch_grad_zero(s->pool, s->d_bt, 0, (int64_t)s->bt.size(), cs);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "pkv_grad_zero: launch");
     return PKV_OK;
 }
@@ -810,6 +824,9 @@ static cudaError_t stage_all_dma(const pkv_seq* s, int64_t n, int what, bool to_
         if (e != cudaSuccess) return e;
         i0 = i1;
     }
+    // Gradient pages recorded as zero: their copies were stale, so their slots
+    // get zeros; once written back, the host pages are current.
+    if (what & PKV_STAGE_GRADS) return to_host ? launch_gzero_clear(s, n, cs) : launch_gzero_fill_slots(s, n, cs);
     return cudaSuccess;
 }
 

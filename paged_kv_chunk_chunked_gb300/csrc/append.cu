@@ -51,8 +51,11 @@ __global__ void __launch_bounds__(kAppThreads) append_kernel(AppendArgs a) {
     const size_t page_off = ((size_t)pp * a.Hkv + h) * (size_t)P * D;
 
     if (blockIdx.z == 1) {
-        // A page taken off the free list starts with zero gradient.
-        if (page_start >= a.old_len) {
+        // A page taken off the free list starts with zero gradient (for host
+        // pages only recorded as such, nothing crosses the host link).
+        if (page_start >= a.old_len && a.gzero) {
+            if (tid == 0) a.gzero[(size_t)pp * a.Hkv + h] = 1;
+        } else if (page_start >= a.old_len) {
             float4* g0 = reinterpret_cast<float4*>(a.dkpool + page_off);
             float4* g1 = reinterpret_cast<float4*>(a.dvpool + page_off);
             const int n4 = P * D / 4;
@@ -143,11 +146,12 @@ __global__ void grad_zero_kernel(float* dk, float* dv, const int32_t* bt, int64_
 // pool is paged like the K/V cache and accumulated in place (gist.science/de
 // §2.B, in-place gradient accumulation). 12 bytes of HBM per element: read the
 // delta, read and write the pool. Every thread keeps 4 + 4 loads of each
-// tensor in flight.
+// tensor in flight. A host page recorded as zero (gzero) is written whole
+// instead: the delta rows, zeros elsewhere; then the record is dropped.
 template <int D>
 __global__ void __launch_bounds__(kThreads) grad_accumulate_kernel(float* dkpool, float* dvpool,
         const float* dk, const float* dv, const int32_t* bt, int64_t num_phys, int P, int Hkv,
-        int64_t row0, int64_t row1, int* err) {
+        int64_t row0, int64_t row1, uint8_t* gzero, int* err) {
     constexpr int V4 = D / 4;                        // float4 per row
     const int64_t lp = row0 / P + blockIdx.x;
     const int h = blockIdx.y;
@@ -161,6 +165,23 @@ __global__ void __launch_bounds__(kThreads) grad_accumulate_kernel(float* dkpool
     const size_t page_off = ((size_t)pp * Hkv + h) * (size_t)P * D + (size_t)(r_lo - lp * P) * D;
     const size_t row_stride4 = (size_t)Hkv * V4;     // delta rows are [row, Hkv, D]
     const size_t src0 = (size_t)(r_lo - row0) * row_stride4 + (size_t)h * V4;
+    const size_t tile = (size_t)pp * Hkv + h;
+    if (gzero && gzero[tile]) {
+        const int lo = (int)(r_lo - lp * P) * V4;    // the delta's float4 range in the tile
+        const size_t tile_off = tile * (size_t)P * D;
+        for (int t = 0; t < 2; ++t) {
+            const float4* src = reinterpret_cast<const float4*>(t == 0 ? dk : dv);
+            float4* dst = reinterpret_cast<float4*>((t == 0 ? dkpool : dvpool) + tile_off);
+            for (int i = threadIdx.x; i < P * V4; i += kThreads) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                const int j = i - lo;
+                if (src && j >= 0 && j < n) x = __ldcs(src + src0 + (size_t)(j / V4) * row_stride4 + j % V4);
+                dst[i] = x;
+            }
+        }
+        if (threadIdx.x == 0) gzero[tile] = 0;
+        return;
+    }
     for (int t = 0; t < 2; ++t) {
         const float4* src = reinterpret_cast<const float4*>(t == 0 ? dk : dv);
         if (!src) continue;
@@ -192,7 +213,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) gather_kernel(const T* kpool, const T* vpool,
         const float* dkpool, const float* dvpool, const float* reppool, const int32_t* bt,
         int64_t num_phys, int P, int Hkv, int64_t lp0, int64_t len, T* k, T* v, float* dk,
-        float* dv, float* rep, int* err) {
+        float* dv, float* rep, const uint8_t* gzero, int* err) {
     constexpr int VT = D * (int)sizeof(T) / 16;     // 16-byte vectors per K/V row
     constexpr int VF = D / 4;                       // 16-byte vectors per gradient row
     const int64_t lp = lp0 + blockIdx.x;            // logical page; outputs start at page lp0
@@ -218,11 +239,13 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(const T* kpool, const 
     if (dk || dv) {
         const float4* gk = reinterpret_cast<const float4*>(dkpool + page_off);
         const float4* gv = reinterpret_cast<const float4*>(dvpool + page_off);
+        const bool zero = gzero && gzero[(size_t)pp * Hkv + h];   // recorded zero: memory stale
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int i = threadIdx.x; i < rows * VF; i += kThreads) {
             const int r = i / VF, c = i % VF;
             const size_t dst = ((out_row0 + r) * Hkv + h) * VF + c;
-            if (dk) reinterpret_cast<float4*>(dk)[dst] = gk[i];
-            if (dv) reinterpret_cast<float4*>(dv)[dst] = gv[i];
+            if (dk) reinterpret_cast<float4*>(dk)[dst] = zero ? z : gk[i];
+            if (dv) reinterpret_cast<float4*>(dv)[dst] = zero ? z : gv[i];
         }
     }
     if (rep && threadIdx.x < D)
@@ -246,7 +269,7 @@ cudaError_t gather_dispatch(const pkv_pool* p, const int32_t* bt, int64_t lp0, i
 #define PKV_GATHER_ARGS                                                                      \
     static_cast<const T*>(p->k), static_cast<const T*>(p->v), p->dk, p->dv, p->rep, bt,     \
         p->desc.num_phys_pages, P, Hkv, lp0, len, static_cast<T*>(k), static_cast<T*>(v), dk, \
-        dv, rep, p->d_err
+        dv, rep, p->gzero, p->d_err
     ProfScope ps("gather_kernel", s);
     if (p->desc.head_dim == 128) gather_kernel<T, 128><<<grid, kThreads, 0, s>>>(PKV_GATHER_ARGS);
     else gather_kernel<T, 64><<<grid, kThreads, 0, s>>>(PKV_GATHER_ARGS);
@@ -295,7 +318,8 @@ cudaError_t launch_grad_accumulate(const pkv_pool* p, const int32_t* d_bt, int64
     const int P = p->desc.page_size, Hkv = p->desc.n_kv_heads;
     const int64_t row1 = row0 + n_rows;
     dim3 grid((unsigned)((row1 - 1) / P - row0 / P + 1), Hkv);
-#define PKV_ACC_ARGS p->dk, p->dv, dk, dv, d_bt, p->desc.num_phys_pages, P, Hkv, row0, row1, p->d_err
+#define PKV_ACC_ARGS \
+    p->dk, p->dv, dk, dv, d_bt, p->desc.num_phys_pages, P, Hkv, row0, row1, p->gzero, p->d_err
     ProfScope ps("grad_accumulate_kernel", s);
     if (p->desc.head_dim == 128) grad_accumulate_kernel<128><<<grid, kThreads, 0, s>>>(PKV_ACC_ARGS);
     else grad_accumulate_kernel<64><<<grid, kThreads, 0, s>>>(PKV_ACC_ARGS);

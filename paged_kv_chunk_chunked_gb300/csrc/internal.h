@@ -46,6 +46,11 @@ struct pkv_pool {
     void* vslot = nullptr;
     float* dkslot = nullptr;
     float* dvslot = nullptr;
+    // PINNED_HOST pools: per (physical page, KV head), 1 = the page's dK/dV
+    // are zero and its host memory is stale (set by gradient zeroing and by
+    // appends of fresh pages instead of writing zeros over the host link;
+    // cleared by whatever writes the whole tile: write-backs, accumulation).
+    uint8_t* gzero = nullptr;
 };
 
 struct pkv_seq {
@@ -110,6 +115,7 @@ struct AppendArgs {
     const int32_t* bt;
     int64_t num_phys;
     int64_t old_len, n_tok;
+    uint8_t* gzero;              // PINNED_HOST: record fresh gradient pages as zero
     int* err;
 };
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
@@ -198,6 +204,15 @@ cudaError_t launch_stage_after_writeback(const pkv_seq* s, bool release, cudaStr
 cudaError_t launch_stage_identity(const pkv_seq* s, int64_t n_pages, int want, cudaStream_t st);
 // The partial page lp was extended by an append: its staged K/V is stale.
 cudaError_t launch_stage_invalidate_kv(const pkv_seq* s, int64_t lp, cudaStream_t st);
+// Gradient zeroing of a PINNED_HOST sequence: every (page, KV head) of its
+// block table is recorded as zero, and gradients staged in its slots are zeroed.
+cudaError_t launch_grad_zero_staged(const pkv_seq* s, cudaStream_t st);
+// After the copy engines staged the gradients of logical pages [0, n) into
+// slots 0..n-1: zero the slots of pages recorded as zero.
+cudaError_t launch_gzero_fill_slots(const pkv_seq* s, int64_t n, cudaStream_t st);
+// After the copy engines wrote the gradients of slots 0..n-1 back to logical
+// pages [0, n): those host pages are current again.
+cudaError_t launch_gzero_clear(const pkv_seq* s, int64_t n, cudaStream_t st);
 
 bool tc_supported(const AttnArgs& a);
 cudaError_t launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t s);

@@ -24,6 +24,10 @@
 //             gradients back, then copy the new page's K/V and/or dK/dV from
 //             host memory over NVLink-C2C into the slot, 16-byte accesses;
 //   writeback one CTA per (slot, KV head): copy a dirty slot's dK/dV back.
+// Gradient pages known to be zero (after gradient zeroing, or fresh from an
+// append) are only recorded as such per (page, KV head) in HBM: staging fills
+// their slots with zeros instead of copying, and the record is dropped once a
+// write-back has made the host page current.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -86,9 +90,9 @@ struct PlanArgs {
 
 __global__ void __launch_bounds__(kPlanThreads) stage_plan_kernel(PlanArgs a) {
     __shared__ int sh[kPlanThreads];
-    __shared__ int n_jobs, n_kv, n_g, n_wb;
+    __shared__ int n_jobs, n_kv, n_wb;
     const int tid = threadIdx.x;
-    if (tid == 0) { n_jobs = 0; n_kv = 0; n_g = 0; n_wb = 0; }
+    if (tid == 0) { n_jobs = 0; n_kv = 0; n_wb = 0; }
     for (int64_t p = tid; p < a.n_pages; p += kPlanThreads) a.flags[p] = a.pages ? 0 : 1;
     __syncthreads();
     if (a.pages) {
@@ -161,7 +165,6 @@ __global__ void __launch_bounds__(kPlanThreads) stage_plan_kernel(PlanArgs a) {
             const int j = atomicAdd(&n_jobs, 1);
             a.jobs[j] = make_int4(s, wb, (int)p, need);
             if (need & kSlotKV) atomicAdd(&n_kv, 1);
-            if (need & kSlotG) atomicAdd(&n_g, 1);
             if (wb >= 0) atomicAdd(&n_wb, 1);
         }
         // Staged gradients are about to be added into by a backward call.
@@ -171,8 +174,7 @@ __global__ void __launch_bounds__(kPlanThreads) stage_plan_kernel(PlanArgs a) {
     for (int64_t s = s0; s < s1; ++s) a.slot_state[s] &= ~kSlotKeep;
     if (tid == 0) {
         *a.count_out = n_jobs;
-        atomicAdd(&a.stats[0], (unsigned long long)n_kv * a.Hkv);
-        atomicAdd(&a.stats[1], (unsigned long long)n_g * a.Hkv);
+        atomicAdd(&a.stats[0], (unsigned long long)n_kv * a.Hkv);   // gradients in: by the copies
         atomicAdd(&a.stats[2], (unsigned long long)n_wb * a.Hkv);
     }
 }
@@ -182,6 +184,12 @@ __device__ __forceinline__ void copy16(void* dst, const void* src, size_t bytes)
     uint4* d = static_cast<uint4*>(dst);
     const size_t n = bytes / 16;
     for (size_t i = threadIdx.x; i < n; i += kCopyThreads) d[i] = s[i];
+}
+
+__device__ __forceinline__ void zero16(void* dst, size_t bytes) {
+    uint4* d = static_cast<uint4*>(dst);
+    const size_t n = bytes / 16;
+    for (size_t i = threadIdx.x; i < n; i += kCopyThreads) d[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 struct StageArgs {
@@ -197,6 +205,7 @@ struct StageArgs {
     size_t g_bytes;              // one (page, head) tile of dK or dV
     uint8_t* k; uint8_t* v; uint8_t* dk; uint8_t* dv;        // host pages
     uint8_t* ks; uint8_t* vs; uint8_t* dks; uint8_t* dvs;    // slots
+    uint8_t* gzero;              // [num_phys * Hkv] gradient tiles recorded as zero
     unsigned long long* stats;
     int* err;
 };
@@ -217,6 +226,7 @@ __device__ void stage_copy_job(const StageArgs& a, const int4 job, int h) {
         const size_t dst = (size_t)pp * a.Hkv + h;
         copy16(a.dk + dst * a.g_bytes, a.dks + slot * a.g_bytes, a.g_bytes);
         copy16(a.dv + dst * a.g_bytes, a.dvs + slot * a.g_bytes, a.g_bytes);
+        if (threadIdx.x == 0) a.gzero[dst] = 0;                  // the host page is current
         __syncthreads();                                          // slot read before it is reused
     }
     if (!job.w || !page_ok(a, job.z, &pp)) return;
@@ -226,8 +236,14 @@ __device__ void stage_copy_job(const StageArgs& a, const int4 job, int h) {
         copy16(a.vs + slot * a.kv_bytes, a.v + src * a.kv_bytes, a.kv_bytes);
     }
     if (job.w & kSlotG) {
-        copy16(a.dks + slot * a.g_bytes, a.dk + src * a.g_bytes, a.g_bytes);
-        copy16(a.dvs + slot * a.g_bytes, a.dv + src * a.g_bytes, a.g_bytes);
+        if (a.gzero[src]) {                                       // zero: nothing to copy
+            zero16(a.dks + slot * a.g_bytes, a.g_bytes);
+            zero16(a.dvs + slot * a.g_bytes, a.g_bytes);
+        } else {
+            copy16(a.dks + slot * a.g_bytes, a.dk + src * a.g_bytes, a.g_bytes);
+            copy16(a.dvs + slot * a.g_bytes, a.dv + src * a.g_bytes, a.g_bytes);
+            if (threadIdx.x == 0) atomicAdd(&a.stats[1], 1ull);
+        }
     }
 }
 
@@ -249,7 +265,10 @@ __global__ void __launch_bounds__(kCopyThreads) stage_writeback_kernel(StageArgs
     const size_t src = (size_t)s * a.Hkv + h, dst = (size_t)pp * a.Hkv + h;
     copy16(a.dk + dst * a.g_bytes, a.dks + src * a.g_bytes, a.g_bytes);
     copy16(a.dv + dst * a.g_bytes, a.dvs + src * a.g_bytes, a.g_bytes);
-    if (threadIdx.x == 0) atomicAdd(&a.stats[2], 1ull);
+    if (threadIdx.x == 0) {
+        a.gzero[dst] = 0;                                         // the host page is current
+        atomicAdd(&a.stats[2], 1ull);
+    }
 }
 
 // After a write-back: clear DIRTY (release: empty every slot).
@@ -300,6 +319,7 @@ StageArgs stage_args(const pkv_seq* s) {
     a.dk = reinterpret_cast<uint8_t*>(p->dk); a.dv = reinterpret_cast<uint8_t*>(p->dv);
     a.ks = static_cast<uint8_t*>(p->kslot); a.vs = static_cast<uint8_t*>(p->vslot);
     a.dks = reinterpret_cast<uint8_t*>(p->dkslot); a.dvs = reinterpret_cast<uint8_t*>(p->dvslot);
+    a.gzero = p->gzero;
     a.stats = s->d_stats;
     a.err = p->d_err;
     return a;
@@ -372,6 +392,81 @@ __global__ void stage_invalidate_kv_kernel(const int32_t* slot_of, int32_t* slot
 cudaError_t launch_stage_invalidate_kv(const pkv_seq* s, int64_t lp, cudaStream_t st) {
     stage_invalidate_kv_kernel<<<1, 1, 0, st>>>(s->d_slot_of, s->d_slot_state, lp);
     return cudaGetLastError();
+}
+
+namespace {
+// Sets (value 1) or clears (0) the zero record of (bt[i], h) for logical pages
+// i < n and every KV head.
+__global__ void gzero_set_kernel(const int32_t* bt, int64_t n, int64_t num_phys, int Hkv,
+                                 uint8_t* gzero, uint8_t value, int* err) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n * Hkv; i += stride) {
+        const int32_t pp = bt[i / Hkv];
+        if (pp < 0 || pp >= num_phys) {
+            report_error(err, kErrBadPage);
+            continue;
+        }
+        gzero[(size_t)pp * Hkv + i % Hkv] = value;
+    }
+}
+
+// Zeroes the gradients held by staged slots (state G), KV head blockIdx.y.
+__global__ void __launch_bounds__(kCopyThreads) slot_grad_zero_kernel(StageArgs a) {
+    const int h = blockIdx.y;
+    for (int64_t s = blockIdx.x; s < a.n_slots; s += gridDim.x) {
+        if (a.slot_page[s] < 0 || !(a.slot_state[s] & kSlotG)) continue;
+        const size_t t = (size_t)s * a.Hkv + h;
+        zero16(a.dks + t * a.g_bytes, a.g_bytes);
+        zero16(a.dvs + t * a.g_bytes, a.g_bytes);
+    }
+}
+
+// After the copy engines staged the gradients of logical pages [0, n) into
+// slots 0..n-1: the slots of pages recorded as zero get zeros.
+__global__ void __launch_bounds__(kCopyThreads) gzero_fill_slots_kernel(StageArgs a, int64_t n) {
+    const int h = blockIdx.y;
+    for (int64_t i = blockIdx.x; i < n; i += gridDim.x) {
+        const int32_t pp = a.bt[i];
+        if (pp < 0 || pp >= a.num_phys || !a.gzero[(size_t)pp * a.Hkv + h]) continue;
+        const size_t t = (size_t)i * a.Hkv + h;
+        zero16(a.dks + t * a.g_bytes, a.g_bytes);
+        zero16(a.dvs + t * a.g_bytes, a.g_bytes);
+    }
+}
+
+cudaError_t launch_gzero_set(const pkv_seq* s, int64_t n, uint8_t value, cudaStream_t st) {
+    const pkv_pool* p = s->pool;
+    if (n <= 0) return cudaSuccess;
+    const int Hkv = p->desc.n_kv_heads;
+    const unsigned blocks = (unsigned)std::min<int64_t>(1024, (n * Hkv + 255) / 256);
+    ProfScope ps("gzero_set_kernel", st);
+    gzero_set_kernel<<<blocks, 256, 0, st>>>(s->d_bt, n, p->desc.num_phys_pages, Hkv, p->gzero,
+                                             value, p->d_err);
+    return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_grad_zero_staged(const pkv_seq* s, cudaStream_t st) {
+    const pkv_pool* p = s->pool;
+    cudaError_t e = launch_gzero_set(s, (int64_t)s->bt.size(), 1, st);
+    if (e != cudaSuccess) return e;
+    ProfScope ps("slot_grad_zero_kernel", st);
+    dim3 grid((unsigned)std::min<int64_t>(p->n_slots, 512), p->desc.n_kv_heads);
+    slot_grad_zero_kernel<<<grid, kCopyThreads, 0, st>>>(stage_args(s));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gzero_fill_slots(const pkv_seq* s, int64_t n, cudaStream_t st) {
+    const pkv_pool* p = s->pool;
+    if (n <= 0) return cudaSuccess;
+    ProfScope ps("gzero_fill_slots_kernel", st);
+    dim3 grid((unsigned)std::min<int64_t>(n, 512), p->desc.n_kv_heads);
+    gzero_fill_slots_kernel<<<grid, kCopyThreads, 0, st>>>(stage_args(s), n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gzero_clear(const pkv_seq* s, int64_t n, cudaStream_t st) {
+    return launch_gzero_set(s, n, 0, st);
 }
 
 }  // namespace pkv

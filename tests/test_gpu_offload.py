@@ -342,7 +342,11 @@ def test_slot_cache_with_evictions_matches_oracle_and_moves_fewer_pages():
         afresh = 2 * sum(len(u) for u in unions) * w.Hkv        # forward + backward
         graded = len(np.unique(np.concatenate(unions))) * w.Hkv
         assert st["kv_in"] < afresh, (st, afresh)
-        assert st["grads_in"] >= graded and st["grads_out"] >= graded, (st, graded)
+        # every page staged with gradients went back at least once; gradients
+        # come in over the link only after a write-back (fresh pages are
+        # recorded as zero and zero-filled in HBM)
+        assert st["grads_out"] >= graded, (st, graded)
+        assert st["grads_in"] <= st["grads_out"] - graded, (st, graded)
     finally:
         B.pkv_pool_destroy(pool)
 
@@ -377,5 +381,112 @@ def test_append_into_a_staged_partial_page_restages_it():
         o_ref, lse_ref = oracle.attention_forward(q[128:], k, v, 128)
         assert np.abs(to_numpy(o) - o_ref).max() <= 1e-2
         assert np.abs(to_numpy(lse) - lse_ref).max() <= 1e-2
+    finally:
+        B.pkv_pool_destroy(pool)
+
+
+def _host_grads(pool, w):
+    """numpy views of a PINNED_HOST pool's host gradient pages [n_phys, Hkv, P, d]."""
+    import ctypes
+    arr = B.pkv_pool_arrays(pool)
+    shape = (w.n_phys, w.Hkv, w.P, w.d)
+    n = int(np.prod(shape))
+    return {t: np.ctypeslib.as_array((ctypes.c_float * n).from_address(arr[t])).reshape(shape)
+            for t in ("dk", "dv")}
+
+
+def test_zeroed_gradient_pages_are_recorded_not_written():
+    """Gradient pages of a PINNED_HOST pool that are zero (fresh from an append,
+    or after pkv_grad_zero) are recorded as zero in HBM and not written over the
+    host link: with their host memory poisoned, pkv_gather reads zeros,
+    pkv_grad_accumulate writes whole pages (bit-exact against the oracle's
+    scatter-add onto zeros), staging fills slots with zeros without counting a
+    transfer, and a write-back makes the host memory current -- in the slot
+    cache and in whole-sequence staging."""
+    w = synth.workload("qwen7b_sparse_256k", N=1024, C=512, Hq=4, Hkv=2, extra_pages=2,
+                       topk=(2, 1, 2))
+    bt = synth.block_table(w)
+    pool = B.pkv_pool_create(w.P, w.Hkv, w.Hq, w.d, B.PKV_BF16, w.n_phys,
+                             residency=B.PKV_RES_PINNED_HOST, n_device_slots=w.n_pages)
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    used = np.asarray(bt)[: w.n_pages]
+
+    def gather():
+        dk = torch.empty((w.N, w.Hkv, w.d), dtype=torch.float32, device="cuda")
+        dv = torch.empty_like(dk)
+        B.pkv_gather(seq, None, None, dk, dv, None, main)
+        torch.cuda.synchronize()
+        B.pkv_check(pool)
+        return to_numpy(dk), to_numpy(dv)
+
+    def sync():
+        B.pkv_wait(seq, main, 5_000_000)
+        torch.cuda.synchronize()
+        B.pkv_check(pool)
+
+    try:
+        seq = B.pkv_seq_create(pool)
+        B.pkv_set_block_table(seq, bt)
+        for c in range(w.n_chunks):
+            s, e = w.chunk_range(c)
+            k = to_device(synth.chunk_k(w, c), "bf16")
+            B.pkv_append(seq, k, k, e - s, main)
+        torch.cuda.synchronize()
+        host = _host_grads(pool, w)
+        for t in host:
+            host[t][...] = np.nan                     # nothing may read this memory as data
+        dk, dv = gather()
+        assert not dk.any() and not dv.any()
+        assert np.isnan(host["dk"][used]).all()      # the appends wrote no zeros to the host
+
+        # accumulation onto recorded pages writes them whole
+        ref = {t: np.zeros((w.n_phys, w.Hkv, w.P, w.d), np.float32) for t in ("dk", "dv")}
+        r0, n = 100, 300                              # pages 0..3, partially
+        x = synth.draw_normal(w.seed, "misc", 400, (n, w.Hkv, w.d))
+        y = synth.draw_normal(w.seed, "misc", 401, (n, w.Hkv, w.d))
+        oracle.scatter_rows(ref["dk"], bt, r0, x, w.P, accumulate=True)
+        oracle.scatter_rows(ref["dv"], bt, r0, y, w.P, accumulate=True)
+        B.pkv_grad_accumulate(seq, r0, n, torch.from_numpy(x).cuda(), torch.from_numpy(y).cuda(), main)
+        dk, dv = gather()
+        np.testing.assert_array_equal(dk, oracle.logical_rows(ref["dk"], bt, w.N, w.P))
+        np.testing.assert_array_equal(dv, oracle.logical_rows(ref["dv"], bt, w.N, w.P))
+        np.testing.assert_array_equal(host["dk"][used[:4]], ref["dk"][used[:4]])
+        assert np.isnan(host["dk"][used[4:]]).all()
+
+        # slot cache: recorded pages are zero-filled, the others copied
+        pages = torch.arange(w.n_pages, dtype=torch.int32, device="cuda")
+        st0 = B.pkv_stage_stats(seq)
+        B.pkv_prefetch(seq, pages, w.n_pages, B.PKV_STAGE_KV | B.PKV_STAGE_GRADS, side)
+        B.pkv_writeback_grads(seq, side)
+        sync()
+        st1 = B.pkv_stage_stats(seq)
+        assert st1["grads_in"] - st0["grads_in"] == 4 * w.Hkv
+        assert st1["grads_out"] - st0["grads_out"] == w.n_pages * w.Hkv
+        for t in host:                                # every host page is current now
+            np.testing.assert_array_equal(host[t][used], ref[t][used])
+
+        # zeroing while the gradients are staged zeroes the slots too
+        B.pkv_grad_zero(seq, main)
+        dk, dv = gather()
+        assert not dk.any() and not dv.any()
+        assert np.array_equal(host["dk"][used[:4]], ref["dk"][used[:4]])   # not written
+        B.pkv_prefetch(seq, pages, w.n_pages, B.PKV_STAGE_KV | B.PKV_STAGE_GRADS, side)
+        B.pkv_release_slots(seq, side)
+        sync()
+        assert not host["dk"][used].any() and not host["dv"][used].any()
+
+        # whole-sequence staging by the copy engines
+        B.pkv_grad_accumulate(seq, 0, w.N, torch.from_numpy(np.ones((w.N, w.Hkv, w.d), np.float32)).cuda(),
+                              None, main)
+        for zero_first in (False, True):
+            if zero_first:                            # the cache is empty: host pages recorded
+                B.pkv_grad_zero(seq, main)
+            B.pkv_prefetch(seq, None, 0, B.PKV_STAGE_GRADS, side)   # copies stale host pages
+            B.pkv_release_slots(seq, side)                           # writes the slots back
+            sync()
+            dk, dv = gather()
+            assert (dk == (0.0 if zero_first else 1.0)).all() and not dv.any(), zero_first
+            assert (host["dk"][used] == (0.0 if zero_first else 1.0)).all(), zero_first
     finally:
         B.pkv_pool_destroy(pool)
