@@ -31,7 +31,7 @@ constexpr int kAppThreads = 512;
 constexpr int kAppUnroll = 4;
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kAppThreads) append_kernel(AppendArgs a) {
+__global__ void __launch_bounds__(kAppThreads, 2) append_kernel(AppendArgs a) {
     constexpr int VPR = D * (int)sizeof(T) / 16;   // 16-byte vectors per row
     constexpr int EPV = 16 / (int)sizeof(T);       // elements per vector
     constexpr int RSTEP = kAppThreads / VPR;       // rows handled per pass
