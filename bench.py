@@ -962,6 +962,8 @@ def run_offload(args, world, rank):
         B.pkv_check(pool)
         st0 = B.pkv_stage_stats(seq) if host else None
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        clocks = ClockSampler(torch.cuda.current_device())
+        clocks.start()
         B.pkv_profile_enable(True)
         ev0.record(main_s)
         for _ in range(args.steps):
@@ -970,8 +972,9 @@ def run_offload(args, world, rank):
         torch.cuda.synchronize()
         prof = B.pkv_profile_collect()
         B.pkv_profile_enable(False)
+        clk = clocks.stop()
         B.pkv_check(pool)
-        res[mode] = dict(ms=ev0.elapsed_time(ev1) / args.steps, prof=prof)
+        res[mode] = dict(ms=ev0.elapsed_time(ev1) / args.steps, prof=prof, clocks=clk)
         if host:
             st1 = B.pkv_stage_stats(seq)
             res[mode]["moved"] = {k: (st1[k] - st0[k]) / args.steps for k in st1}
@@ -1063,6 +1066,7 @@ def run_offload(args, world, rank):
         "kernels_pinned_host": {k: {"launches": c, "ms_per_step": round(t / args.steps, 3)}
                                 for k, (c, t) in hp["prof"].items()},
         "data": "synthetic (seeded clustered keys)",
+        "clocks": {"pinned_host": hp["clocks"], "device": res["device"]["clocks"]},
         **extra,
     }
 
@@ -1092,7 +1096,7 @@ def run_offload_dense(args, world, rank):
     lse = torch.empty((w.Hq, e - s), dtype=torch.float32, device="cuda")
     kv = [(to_device(synth.chunk_k(w, i), w.dtype), to_device(synth.chunk_v(w, i), w.dtype))
           for i in range(w.n_chunks)]
-    res = {}
+    res, clk = {}, {}
     for mode in ("pinned_host", "device"):
         host = mode == "pinned_host"
         pools, seqs = [], []
@@ -1130,11 +1134,14 @@ def run_offload_dense(args, world, rank):
         for pool in pools:
             B.pkv_check(pool)
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        clocks = ClockSampler(torch.cuda.current_device())
+        clocks.start()
         ev0.record(main_s)
         for _ in range(args.steps):
             step()
         ev1.record(main_s)
         torch.cuda.synchronize()
+        clk[mode] = clocks.stop()
         for pool in pools:
             B.pkv_check(pool)
         res[mode] = ev0.elapsed_time(ev1) / args.steps
@@ -1156,6 +1163,7 @@ def run_offload_dense(args, world, rank):
         "bytes_moved_per_step": bytes_moved,
         "link_gbs_needed_to_hide": round(bytes_moved / (res["device"] * 1e-3) / 1e9, 1),
         "data": "synthetic (seeded N(0,1) K/V/Q/dO, the same for every layer)",
+        "clocks": clk,
     }
 
 

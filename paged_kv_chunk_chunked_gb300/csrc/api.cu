@@ -537,6 +537,7 @@ pkv_status pkv_append(pkv_seq* s, const void* k, const void* v, int64_t n_tok, v
     a.kpool = p->k; a.vpool = p->v; a.dkpool = p->dk; a.dvpool = p->dv; a.rep = p->rep;
     a.bt = s->d_bt; a.num_phys = p->desc.num_phys_pages;
     a.old_len = s->len; a.n_tok = n_tok; a.gzero = p->gzero; a.err = p->d_err;
+    if (p->gzero) s->gzero_possible = true;              // fresh pages are recorded as zero
     cudaError_t e = launch_append(a, cs);
     if (e == cudaSuccess && s->used) e = cudaEventRecord(s->used, cs);
     if (e != cudaSuccess) return cuda_fail(e, "pkv_append: launch");
@@ -666,6 +667,7 @@ pkv_status pkv_grad_zero(pkv_seq* s, void* stream) {
         // zeroed in their slots once the last prefetch or write-back is done,
         // and later staging waits for this call.
         e = cudaStreamWaitEvent(cs, s->staged, 0);
+        s->gzero_possible = true;
         if (e == cudaSuccess) e = launch_grad_zero_staged(s, cs);
         if (e == cudaSuccess) e = cudaEventRecord(s->used, cs);
     } else {
@@ -799,7 +801,7 @@ static pkv_status host_pool_check(pkv_seq* s, const char* who) {
 // time taken from the attention kernels running meanwhile): logical page i goes
 // to slot i, which is the plan kernel's assignment when every page is staged,
 // in one cudaMemcpyAsync per run of consecutive physical pages per array.
-static cudaError_t stage_all_dma(const pkv_seq* s, int64_t n, int what, bool to_host, cudaStream_t cs) {
+static cudaError_t stage_all_dma(pkv_seq* s, int64_t n, int what, bool to_host, cudaStream_t cs) {
     const pkv_pool* p = s->pool;
     const size_t kv_page = p->page_elems * p->elem, g_page = p->page_elems * sizeof(float);
     for (int64_t i0 = 0; i0 < n;) {
@@ -826,8 +828,11 @@ static cudaError_t stage_all_dma(const pkv_seq* s, int64_t n, int what, bool to_
     }
     // Gradient pages recorded as zero: their copies were stale, so their slots
     // get zeros; once written back, the host pages are current.
-    if (what & PKV_STAGE_GRADS) return to_host ? launch_gzero_clear(s, n, cs) : launch_gzero_fill_slots(s, n, cs);
-    return cudaSuccess;
+    if (!(what & PKV_STAGE_GRADS) || !s->gzero_possible) return cudaSuccess;
+    if (!to_host) return launch_gzero_fill_slots(s, n, cs);
+    cudaError_t e = launch_gzero_clear(s, n, cs);
+    if (n >= (int64_t)s->bt.size()) s->gzero_possible = false;   // every page written back
+    return e;
 }
 
 pkv_status pkv_prefetch(pkv_seq* s, const int32_t* pages, int64_t n, int32_t what, void* side) {

@@ -75,6 +75,8 @@ struct pkv_seq {
     unsigned long long* d_stats = nullptr;   // page-heads moved by kernels: K/V in, grads in, grads out
     int64_t h_stats[3] = {0, 0, 0};  // the same, moved by the copy engines (whole-sequence staging)
     bool dirty_possible = false;     // a prefetch staged gradients since the last write-back
+    bool gzero_possible = false;     // some page may be recorded as zero (pool gzero) since the
+                                     // last whole-sequence write-back
     cudaEvent_t staged = nullptr;    // last event recorded on the side stream
     cudaEvent_t used = nullptr;      // last append/attention call on the sequence's slots
     int64_t staged_all = 0;          // > 0: the last prefetch staged pages [0, staged_all), slot i = page i
