@@ -297,46 +297,25 @@ __device__ void unit_scores(const TopkArgs& a, int kv, int tile, float* smem) {
 // so the compaction's per-thread runs (stride = run length) hit distinct banks.
 __device__ __forceinline__ int padded(int i) { return i + (i >> 5); }
 
-// Keys of the score row: from shared memory when the row was staged there
-// (sm != null, padded layout), else from L2.
-struct RowKeys {
-    const float* g;
-    const float* sm;
+// Keys of the score row: from the copy staged in shared memory (padded
+// layout), or from L2. The source is a template argument, so every loop over
+// the row has a single kind of load.
+template <bool kStaged> struct RowKeys {
+    const float* p;
     __device__ __forceinline__ uint32_t operator[](int i) const {
-        return orderable(sm ? sm[padded(i)] : __ldcg(g + i));
+        return orderable(kStaged ? p[padded(i)] : __ldcg(p + i));
     }
 };
 
-__device__ void unit_select(const TopkArgs& a, int kv, int qp, TopkSmem& S, int* hist2048,
-                            float* rowbuf, int rowbuf_cap) {
+// The row's n_top best candidates (of n; all when n_top == n), then the sink
+// and local pages, into the selection row.
+template <bool kStaged>
+__device__ void select_row(const TopkArgs& a, int kv, int qp, TopkSmem& S, int* hist,
+                           const RowKeys<kStaged> keys, int n, int n_top) {
     const int tid = threadIdx.x;
     const int64_t qpg = a.qp0 + qp;
     const int64_t c_lo = a.n_sink;
-    const int n = (int)max64(0, qpg - a.n_local - c_lo + 1);      // candidates of this row
-    const int n_top = min(a.K, n);
-    const float* row = a.scores + ((size_t)kv * a.n_qp + qp) * a.stride;
     const bool all = n_top == n;
-    RowKeys keys{row, nullptr};
-    if (!all && n_top > 0 && padded(n) <= rowbuf_cap) {
-        // Stage the row (16-byte aligned loads: the stride is a multiple of 4 floats).
-        const int n4 = (n + 3) / 4;
-        for (int i = tid; i < n4; i += 4 * kTkThreads) {
-            float4 v[4];
-#pragma unroll
-            for (int l = 0; l < 4; ++l)
-                if (i + l * kTkThreads < n4) v[l] = __ldcg(reinterpret_cast<const float4*>(row) + i + l * kTkThreads);
-#pragma unroll
-            for (int l = 0; l < 4; ++l) {
-                const int b = 4 * (i + l * kTkThreads);
-                if (b < 4 * n4) {
-                    rowbuf[padded(b)] = v[l].x; rowbuf[padded(b + 1)] = v[l].y;
-                    rowbuf[padded(b + 2)] = v[l].z; rowbuf[padded(b + 3)] = v[l].w;
-                }
-            }
-        }
-        __syncthreads();
-        keys.sm = rowbuf;
-    }
     uint32_t thr = 0;                                             // the n_top-th best key
     int take_eq = 0;                                              // keys == thr to keep
     if (!all && n_top > 0) {
@@ -345,7 +324,6 @@ __device__ void unit_select(const TopkArgs& a, int kv, int qp, TopkSmem& S, int*
         // magnitude spread over many of its 2048 bins.
         uint32_t prefix = 0, mask = 0;
         int krem = n_top;
-        int* hist = hist2048;
         for (int pass = 0; pass < 3; ++pass) {
             const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
             const int width = pass == 2 ? 10 : 11;
@@ -401,7 +379,7 @@ __device__ void unit_select(const TopkArgs& a, int kv, int qp, TopkSmem& S, int*
     const int64_t s_end = min64(a.n_sink, qpg + 1);               // sink pages [0, s_end)
     const int64_t l_beg = max64(s_end, qpg - a.n_local + 1);      // local pages [l_beg, qpg]
     int32_t* out = a.out + ((size_t)qp * a.Hkv + kv) * a.kmax;
-    {
+    if (mine > 0) {
         int pos = (int)s_end + pos0, eq_seen = 0;
         for (int i = i0; i < i1 && pos < a.kmax; ++i) {
             bool keep = all;
@@ -420,6 +398,37 @@ __device__ void unit_select(const TopkArgs& a, int kv, int qp, TopkSmem& S, int*
         else if (i >= n_sel) out[i] = -1;
     }
     if (a.counts && tid == 0) a.counts[(size_t)qp * a.Hkv + kv] = min(n_sel, a.kmax);
+}
+
+__device__ void unit_select(const TopkArgs& a, int kv, int qp, TopkSmem& S, int* hist2048,
+                            float* rowbuf, int rowbuf_cap) {
+    const int tid = threadIdx.x;
+    const int64_t qpg = a.qp0 + qp;
+    const int n = (int)max64(0, qpg - a.n_local - (int64_t)a.n_sink + 1);   // candidates of this row
+    const int n_top = min(a.K, n);
+    const float* row = a.scores + ((size_t)kv * a.n_qp + qp) * a.stride;
+    if (n_top == n || n_top == 0 || padded(n) > rowbuf_cap) {
+        select_row<false>(a, kv, qp, S, hist2048, RowKeys<false>{row}, n, n_top);
+        return;
+    }
+    // Stage the row (16-byte aligned loads: the stride is a multiple of 4 floats).
+    const int n4 = (n + 3) / 4;
+    for (int i = tid; i < n4; i += 4 * kTkThreads) {
+        float4 v[4];
+#pragma unroll
+        for (int l = 0; l < 4; ++l)
+            if (i + l * kTkThreads < n4) v[l] = __ldcg(reinterpret_cast<const float4*>(row) + i + l * kTkThreads);
+#pragma unroll
+        for (int l = 0; l < 4; ++l) {
+            const int b = 4 * (i + l * kTkThreads);
+            if (b < 4 * n4) {
+                rowbuf[padded(b)] = v[l].x; rowbuf[padded(b + 1)] = v[l].y;
+                rowbuf[padded(b + 2)] = v[l].z; rowbuf[padded(b + 3)] = v[l].w;
+            }
+        }
+    }
+    __syncthreads();
+    select_row<true>(a, kv, qp, S, hist2048, RowKeys<true>{rowbuf}, n, n_top);
 }
 
 template <typename T, int D>

@@ -71,8 +71,10 @@ def _check_selection(sel_gpu, q, q_start, k_logical, P, K, n_sink, n_local):
 
 
 @pytest.mark.parametrize("dtype,P,d,K", [("bf16", 128, 128, 3), ("f32", 16, 64, 5),
-                                         ("bf16", 128, 128, 64)])
+                                         ("bf16", 128, 128, 64), ("bf16", 128, 128, 0),
+                                         ("f32", 16, 64, 0)])
 def test_page_topk_matches_oracle(dtype, P, d, K):
+    """K = 0 keeps no scored page: every row is its sink and local pages."""
     w = _w(dtype=dtype, P=P, d=d, N=2048 if P == 128 else 512, C=1024 if P == 128 else 256,
            topk=(K, 1, 2))
     qs, ks, vs, _ = _inputs(w)
